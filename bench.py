@@ -1,0 +1,523 @@
+#!/usr/bin/env python
+"""Benchmark: block-scaled FP4 fake-quantization on GB300.
+
+One step = one pass of the whole hot path over the five synthetic workloads:
+  nvfp4_small   NVFP4 fake-quant (RNE), FP32 [256, 1024]: codes, scales, s_g, FP32 xhat, mask
+  mxfp4_weight  MXFP4 quantize + dequantize (RNE), BF16 [4096, 4096] weight with 0.1% x100
+  nvfp4_act     NVFP4 row 1x16 + column 16x1 on the transpose in one call, BF16 [8192, 8192]
+                activation with 8 outlier channels: both codes/scales, BF16 xhat, STE mask;
+                then the STE backward of a BF16 gradient of the same shape
+  grad_2level   double-block NVFP4 with stochastic rounding, BF16 [16384, 4096] Laplace gradient
+  moe_qat       one QAT step over 32 MoE experts (64 FP32 master matrices [2880, 5760] and
+                [5760, 2880], 1.06 G weights): update + NVFP4 fake-quant + OsciReset
+                statistics, then the OsciReset reset pass over the same weights
+The metric is algorithmic HBM bytes / device time (GB/s); elements/s are
+reported per workload.  Inputs live in HBM before the timed region; the step's
+working set (about 20 GB) is far larger than L2, so every workload starts cold.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "fake-quant HBM GB/s and % of GB300 HBM peak; Gelem/s per format"
+UNIT = "GB/s"
+FALLBACK_HBM_GBS = 6800.0
+
+# Bytes per element each workload must move (reads + writes of its definition;
+# the NVFP4 tensor amax is a second read of x).
+BYTES_PER_ELEM = {
+    "nvfp4_small": 4 + 4 + 0.5 + 1 / 16 + 4 + 1 / 8,
+    "mxfp4_weight": 2 + 0.5 + 1 / 32 + 2 + 1 / 8,
+    "nvfp4_act": 2 + 2 + 0.5 + 1 / 16 + 0.5 + 1 / 16 + 2 + 1 / 8,
+    "ste_backward": 2 + 1 / 8 + 2,
+    "grad_2level": 2 + 0.5 + 1 / 16 + 4 / 128,
+    "osci_update": 20 + (4 + 0.5 + 1 / 16 + 8 + 0.5 + 1 / 16 + 2 + 1 / 8),
+    "osci_reset": 16,
+}
+# Our kernels launched per step (memsets not counted).
+LAUNCHES_PER_STEP = {"nvfp4_small": 2, "mxfp4_weight": 1, "nvfp4_act": 2, "ste_backward": 1,
+                     "grad_2level": 1, "osci_update": 2, "osci_reset": 1}
+# DRAM traffic per launch of the dominant call from an ncu capture, valid only
+# for the kernel source it was taken on (sha256 of k_osci.cu); None: not taken.
+NCU_TRAFFIC = {"osci_update": {"bytes": None, "src_sha256": None}}
+
+
+def log(*a):
+    print(*a, file=sys.stderr, flush=True)
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        try:
+            with open(p) as f:
+                d = json.load(f)
+            for k in ("hbm_gbs", "hbm_GBs", "hbm_gb_s"):
+                if k in d:
+                    return float(d[k]), "measured"
+        except Exception:
+            pass
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+def src_sha(name):
+    with open(os.path.join(ROOT, "fp4_quantization_aware_fq_gb300", "csrc", name), "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()
+
+
+# --------------------------------------------------------------------------- clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4)
+                          if r[5 + i].lower().startswith("active")})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(rows)}
+
+
+# --------------------------------------------------------------------------- workloads
+class Suite:
+    """All five workloads' inputs and outputs, resident on one GPU."""
+
+    def __init__(self, dev, seed_offset=0):
+        import torch
+        from fp4_quantization_aware_fq_gb300 import fq
+        from fp4_quantization_aware_fq_gb300 import workloads as W
+        self.fq, self.torch, self.dev = fq, torch, dev
+        so = seed_offset
+        spec = W.WORKLOADS
+        # nvfp4_small
+        self.x1 = W.nvfp4_small(seed=0 + so, device=dev)
+        self.cfg1 = fq.Config(fq.NVFP4)
+        self.q1 = fq.alloc_qtensor(*self.x1.shape, fq.NVFP4, dev)
+        self.xh1 = torch.empty(self.x1.shape, dtype=torch.float32, device=dev)
+        self.m1 = self._mask(self.x1)
+        self.ws1 = torch.empty(256, dtype=torch.uint8, device=dev)
+        # mxfp4_weight
+        self.x2 = W.mxfp4_weight(seed=1 + so, device=dev)
+        self.cfg2 = fq.Config(fq.MXFP4)
+        self.q2 = fq.alloc_qtensor(*self.x2.shape, fq.MXFP4, dev)
+        self.xh2 = torch.empty(self.x2.shape, dtype=torch.bfloat16, device=dev)
+        self.m2 = self._mask(self.x2)
+        # nvfp4_act + STE backward
+        self.x3 = W.nvfp4_act(seed=2 + so, device=dev)
+        self.cfg3 = fq.Config(fq.NVFP4)
+        r3, c3 = self.x3.shape
+        self.rq3 = fq.alloc_qtensor(r3, c3, fq.NVFP4, dev)
+        self.cq3 = fq.alloc_qtensor(c3, r3, fq.NVFP4, dev)
+        self.xh3 = torch.empty(self.x3.shape, dtype=torch.bfloat16, device=dev)
+        self.m3 = self._mask(self.x3)
+        self.ws3 = torch.empty(256, dtype=torch.uint8, device=dev)
+        self.dy3 = W.normal(self.x3.shape, 1.0, seed=12 + so, dtype=torch.bfloat16, device=dev)
+        self.dx3 = torch.empty_like(self.dy3)
+        # grad_2level
+        self.x4 = W.grad_2level(seed=3 + so, device=dev)
+        self.cfg4 = fq.Config(fq.NVFP4_2LEVEL, fq.SR, 0x5EED, 0)
+        self.q4 = fq.alloc_qtensor(*self.x4.shape, fq.NVFP4_2LEVEL, dev)
+        # moe_qat
+        m = spec["moe_qat"]
+        ws = W.moe_weights(m["experts"], m["up_shape"], m["down_shape"], seed=4 + so, device=dev)
+        self.cfg5 = fq.Config(fq.NVFP4)
+        self.master = [w.float() for w in ws]
+        del ws
+        self.delta = [W.master_update(t.shape, 1, device=dev, seed_base=1000 + so)
+                      for t in self.master]
+        self.dq = [torch.zeros_like(t) for t in self.master]
+        self.dm = [torch.zeros_like(t) for t in self.master]
+        self.prev = [fq.fq_quantize(t, self.cfg5)[0] for t in self.master]
+        self.next = [fq.alloc_qtensor(*t.shape, fq.NVFP4, dev) for t in self.master]
+        self.xh5 = [torch.empty(t.shape, dtype=torch.bfloat16, device=dev) for t in self.master]
+        self.m5 = [self._mask(t) for t in self.master]
+        self.ws5 = torch.empty(fq.fq_osci_workspace_size(len(self.master)), dtype=torch.uint8,
+                               device=dev)
+        self.nreset = torch.zeros(1, dtype=torch.int64, device=dev)
+        self.n5 = sum(t.numel() for t in self.master)
+        self.elems = {"nvfp4_small": self.x1.numel(), "mxfp4_weight": self.x2.numel(),
+                      "nvfp4_act": self.x3.numel(), "ste_backward": self.dy3.numel(),
+                      "grad_2level": self.x4.numel(), "osci_update": self.n5,
+                      "osci_reset": self.n5}
+        self.step_no = 0
+        torch.cuda.synchronize()
+
+    def _mask(self, x):
+        return self.torch.empty(((x.numel() + 7) // 8 + 15) // 16 * 16, dtype=self.torch.uint8,
+                                device=self.dev)
+
+    # each call is one C-ABI entry point; all run on the current stream
+    def nvfp4_small(self):
+        self.fq.fq_fakequant_ste(self.x1, self.cfg1, xhat=self.xh1, mask=self.m1,
+                                 row_out=self.q1, ws=self.ws1)
+
+    def mxfp4_weight(self):
+        self.fq.fq_fakequant_ste(self.x2, self.cfg2, xhat=self.xh2, mask=self.m2,
+                                 row_out=self.q2)
+
+    def nvfp4_act(self):
+        self.fq.fq_fakequant_ste(self.x3, self.cfg3, xhat=self.xh3, mask=self.m3,
+                                 row_out=self.rq3, col_out=self.cq3, ws=self.ws3)
+
+    def ste_backward(self):
+        self.fq.fq_ste_backward(self.dy3, self.m3, self.dx3)
+
+    def grad_2level(self):
+        self.cfg4.offset = self.step_no
+        self.fq.fq_quantize(self.x4, self.cfg4, row_out=self.q4)
+
+    def osci_update(self):
+        self.fq.fq_osci_update(self.cfg5, self.master, self.delta, self.dq, self.dm, self.prev,
+                               self.next, xhat=self.xh5, mask=self.m5, ws=self.ws5)
+        self.prev, self.next = self.next, self.prev
+
+    def osci_reset(self):
+        self.fq.fq_osci_reset(self.cfg5, self.master, self.dq, self.dm, self.prev, 4.0,
+                              n_reset=self.nreset)
+
+    ORDER = ("nvfp4_small", "mxfp4_weight", "nvfp4_act", "ste_backward", "grad_2level",
+             "osci_update", "osci_reset")
+
+
+def bytes_per_step(elems):
+    return {k: BYTES_PER_ELEM[k] * elems[k] for k in elems}
+
+
+# --------------------------------------------------------------------------- device timing
+def run_ours(args, rank, world, dist):
+    import torch
+    dev = torch.device("cuda", torch.cuda.current_device())
+    suite = Suite(dev, seed_offset=0)
+    stream = torch.cuda.current_stream()
+    bps = bytes_per_step(suite.elems)
+    total_bytes = sum(bps.values())
+
+    def step():
+        for name in Suite.ORDER:
+            getattr(suite, name)()
+        suite.step_no += 1
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    ev = {n: [] for n in Suite.ORDER}
+    clocks = ClockSampler(torch.cuda.current_device()) if rank == 0 else None
+    if clocks:
+        clocks.start()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for _ in range(args.steps):
+        for name in Suite.ORDER:
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            getattr(suite, name)()
+            b.record(stream)
+            ev[name].append((a, b))
+        suite.step_no += 1
+    t1.record(stream)
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    clk = clocks.stop() if clocks else None
+    ms = t0.elapsed_time(t1)
+    per_ms = {n: sum(a.elapsed_time(b) for a, b in ev[n]) / args.steps for n in Suite.ORDER}
+    if dist:
+        t = torch.tensor([ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+
+    # end-to-end: pinned host inputs -> device, the same calls, results -> host
+    e2e = run_e2e(args, suite, total_bytes) if not args.no_e2e else None
+    if dist and e2e is not None:
+        t = torch.tensor([e2e["ms_total"]], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e["ms_total"] = float(t.item())
+    return suite, bps, total_bytes, ms, per_ms, clk, e2e
+
+
+def run_e2e(args, suite, total_bytes):
+    import torch
+    stream = torch.cuda.current_stream()
+    h_in = [(suite.x1, suite.x1.cpu().pin_memory()), (suite.x2, suite.x2.cpu().pin_memory()),
+            (suite.x3, suite.x3.cpu().pin_memory()), (suite.dy3, suite.dy3.cpu().pin_memory()),
+            (suite.x4, suite.x4.cpu().pin_memory())]
+    h_in += [(d, d.cpu().pin_memory()) for d in suite.delta]
+    outs = [suite.q1.codes, suite.q1.scales, suite.q2.codes, suite.q2.scales, suite.rq3.codes,
+            suite.rq3.scales, suite.cq3.codes, suite.cq3.scales, suite.q4.codes, suite.q4.scales,
+            suite.q4.tscale, suite.nreset]
+    h_out = [torch.empty(o.shape, dtype=o.dtype).pin_memory() for o in outs]
+    h2d = sum(h.numel() * h.element_size() for _, h in h_in)
+    d2h = sum(o.numel() * o.element_size() for o in outs)
+
+    def step():
+        for d, h in h_in:
+            d.copy_(h, non_blocking=True)
+        for name in Suite.ORDER:
+            getattr(suite, name)()
+        suite.step_no += 1
+        for o, h in zip(outs, h_out):
+            h.copy_(o, non_blocking=True)
+
+    for _ in range(max(1, min(args.warmup, 2))):
+        step()
+    torch.cuda.synchronize()
+    k = max(1, min(args.steps, 5))
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(k):
+        step()
+    b.record(stream)
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b)
+    return {"ms_total": ms, "steps": k, "h2d": h2d, "d2h": d2h, "bytes": total_bytes}
+
+
+# --------------------------------------------------------------------------- oracle timing
+def oracle_sample(max_seconds=None):
+    """Time the oracle on a bounded sample of every workload.  Returns
+    {workload: (elements, seconds)} and a text description."""
+    import numpy as np
+    import oracle
+    from fp4_quantization_aware_fq_gb300 import workloads as W
+    oracle.build()
+    res = {}
+    f32 = lambda t: oracle.bf16_bits_to_f32(W.bf16_bits(t)).reshape(t.shape)  # noqa: E731
+
+    def timed(fn):
+        t = time.perf_counter()
+        fn()
+        return time.perf_counter() - t
+
+    x1 = W.nvfp4_small().numpy()
+    res["nvfp4_small"] = (x1.size, timed(lambda: oracle.quantize(
+        x1, oracle.NVFP4, want_xhat=True, want_mask=True)))
+    x2 = f32(W.mxfp4_weight(shape=(256, 4096), seed=1))
+    res["mxfp4_weight"] = (x2.size, timed(lambda: oracle.quantize(
+        x2, oracle.MXFP4, want_xhat=True, want_mask=True)))
+    x3 = f32(W.nvfp4_act(shape=(256, 8192), seed=2))
+
+    def c3():
+        q = oracle.quantize(x3, oracle.NVFP4, orient=oracle.ROWCOL, want_xhat=True,
+                            want_mask=True)
+        oracle.f32_to_bf16_bits(q["row"]["xhat"])
+        return q
+    q3 = None
+    t = time.perf_counter()
+    q3 = c3()
+    res["nvfp4_act"] = (x3.size, time.perf_counter() - t)
+    dy = W.bf16_bits(W.normal(x3.shape, 1.0, seed=12, dtype=__import__("torch").bfloat16))
+    res["ste_backward"] = (dy.size, timed(lambda: oracle.ste_backward(dy, q3["row"]["mask"])))
+    x4 = f32(W.grad_2level(shape=(256, 4096), seed=3))
+    res["grad_2level"] = (x4.size, timed(lambda: oracle.quantize(
+        x4, oracle.NVFP4_2LEVEL, oracle.SR, 0x5EED)))
+    w = W.normal((512, 5760), 0.02, seed=4).to(__import__("torch").bfloat16)
+    st = oracle.OsciState(f32(w), oracle.NVFP4)
+    d = W.master_update((512, 5760), 1).numpy()
+
+    def upd():
+        out = st.step(d, offset=1)
+        oracle.f32_to_bf16_bits(out["xhat"])
+    res["osci_update"] = (w.numel(), timed(upd))
+    res["osci_reset"] = (w.numel(), timed(lambda: st.reset(4.0)))
+    desc = ("oracle (scalar C, 1 thread) on: nvfp4_small full; mxfp4_weight 256 rows; "
+            "nvfp4_act 256 rows row+col; ste_backward 256x8192; grad_2level 256 rows SR; "
+            "osci update+reset on one [512, 5760] slice; rate scaled to the full step's bytes")
+    return res, desc
+
+
+def oracle_gbs(sample, elems_full):
+    """Suite GB/s of the oracle: full-step bytes / (sum of full-size times at
+    the sampled per-element rates)."""
+    secs = 0.0
+    for k, (n, t) in sample.items():
+        secs += elems_full[k] * (t / n)
+    total = sum(BYTES_PER_ELEM[k] * elems_full[k] for k in elems_full)
+    return total / secs / 1e9, secs
+
+
+FULL_ELEMS = {"nvfp4_small": 256 * 1024, "mxfp4_weight": 4096 * 4096,
+              "nvfp4_act": 8192 * 8192, "ste_backward": 8192 * 8192,
+              "grad_2level": 16384 * 4096, "osci_update": 32 * 2 * 2880 * 5760,
+              "osci_reset": 32 * 2 * 2880 * 5760}
+
+
+def config_block():
+    return {"workload": "fake-quant suite over the five synthetic workloads (one pass each per "
+                        "step): nvfp4_small fp32 256x1024 NVFP4 RNE; mxfp4_weight bf16 "
+                        "4096x4096 MXFP4 RNE quant+dequant; nvfp4_act bf16 8192x8192 NVFP4 "
+                        "row 1x16 + col 16x1 + xhat + STE mask, then STE backward; grad_2level "
+                        "bf16 16384x4096 double-block NVFP4 SR; moe_qat 32 experts x "
+                        "(2880x5760 + 5760x2880) FP32 master: OsciReset update + reset",
+            "elements_per_step": sum(FULL_ELEMS.values()),
+            "l2": "no flush: the step's working set (~20 GB) exceeds L2, inputs are cold",
+            "bytes": "algorithmic (definition reads + writes; NVFP4 amax is a second read)"}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        return main_reference(args, rank, world)
+
+    import torch
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU")
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    from fp4_quantization_aware_fq_gb300 import build as fqbuild
+    fqbuild.build()
+
+    suite, bps, total_bytes, ms, per_ms, clk, e2e = run_ours(args, rank, world, dist)
+    if rank == 0:
+        peak, peak_kind = measured_peaks()
+        ms_step = ms / args.steps
+        value = world * total_bytes * args.steps / (ms / 1e3) / 1e9
+        per = {}
+        for n in Suite.ORDER:
+            t = per_ms[n] / 1e3
+            per[n] = {"gbs": round(bps[n] / t / 1e9, 1),
+                      "gelem_s": round(suite.elems[n] / t / 1e9, 3),
+                      "ms": round(per_ms[n], 4),
+                      "frac_hbm": round(bps[n] / t / 1e9 / peak, 3)}
+        dom = max(Suite.ORDER, key=lambda n: per_ms[n])
+        achieved = bps[dom] / (per_ms[dom] / 1e3) / 1e9
+        tr = NCU_TRAFFIC.get(dom, {})
+        traffic = tr.get("bytes") if tr.get("src_sha256") == src_sha("k_osci.cu") else None
+        line = {
+            "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic (seeded torch generators, shapes/distributions of the five "
+                    "workloads)",
+            "config": config_block(),
+            "per_workload": per,
+            "roofline": {"bound": "hbm", "kernel": dom + (" (osci_pass_a + osci_pass_b)"
+                                                           if dom == "osci_update" else ""),
+                         "achieved": round(achieved, 1), "peak": peak,
+                         "peak_kind": f"{peak_kind} copy bandwidth",
+                         "unit": "GB/s", "frac": round(achieved / peak, 3),
+                         "traffic": traffic,
+                         "algorithmic_bytes_per_launch": int(bps[dom])},
+            "gpu_launches": sum(LAUNCHES_PER_STEP.values()) * args.steps,
+            "clocks": clk,
+        }
+        if e2e is not None:
+            line["e2e"] = {"value": round(world * e2e["bytes"] * e2e["steps"] /
+                                          (e2e["ms_total"] / 1e3) / 1e9, 1),
+                           "unit": UNIT, "h2d_bytes_per_step": e2e["h2d"],
+                           "d2h_bytes_per_step": e2e["d2h"], "steps": e2e["steps"],
+                           "ms_per_step": round(e2e["ms_total"] / e2e["steps"], 3)}
+        if not args.no_cpu_baseline and world == 1:
+            sample, desc = oracle_sample()
+            gbs, secs = oracle_gbs(sample, suite.elems)
+            line["cpu_baseline"] = {"value": round(gbs, 4), "unit": UNIT, "cores": 1,
+                                    "kind": "oracle", "sample": desc,
+                                    "sample_seconds": round(sum(t for _, t in sample.values()), 2),
+                                    "est_seconds_per_step": round(secs, 1)}
+        print(json.dumps(line), flush=True)
+    if dist:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+def main_reference(args, rank, world):
+    """The oracle as it stands, on the host cores: each step times a bounded
+    sample of every workload; value = the suite's bytes at the sampled rates."""
+    if rank != 0:
+        return
+    for _ in range(args.warmup):
+        oracle_sample()
+    vals, secs = [], []
+    desc = ""
+    for _ in range(args.steps):
+        sample, desc = oracle_sample()
+        v, s = oracle_gbs(sample, FULL_ELEMS)
+        vals.append(v)
+        secs.append(sum(t for _, t in sample.values()))
+    value = statistics.median(vals)
+    total = sum(BYTES_PER_ELEM[k] * FULL_ELEMS[k] for k in FULL_ELEMS)
+    line = {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": UNIT,
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(total / (value * 1e9) * 1e3, 1), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic (seeded torch generators)", "config": config_block(),
+            "cpu_baseline": {"kind": "oracle", "cores": 1, "sample": desc,
+                             "value": round(value, 4), "unit": UNIT,
+                             "sample_seconds_per_step": round(statistics.median(secs), 2)},
+            "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

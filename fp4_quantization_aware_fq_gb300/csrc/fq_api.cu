@@ -1,0 +1,403 @@
+// fq_api.cu -- the C ABI declared in include/fq.h: host-side argument
+// checks, workspace handling, and launches on the caller's stream.
+#include <cstring>
+
+#include "fq.h"
+#include "fq_device.cuh"
+#include "fq_internal.h"
+
+using namespace fqk;
+
+namespace {
+
+inline bool aligned16(const void *p)
+{
+    return (reinterpret_cast<uintptr_t>(p) & 15u) == 0;
+}
+
+inline bool valid_cfg(const fq_config *c)
+{
+    return c && (c->format == FQ_NVFP4 || c->format == FQ_MXFP4 || c->format == FQ_NVFP4_2LEVEL) &&
+           (c->rounding == FQ_RNE || c->rounding == FQ_SR);
+}
+
+inline bool valid_dtype(int32_t d)
+{
+    return d == FQ_F32 || d == FQ_BF16;
+}
+
+inline int64_t block_len(int fmt)
+{
+    return fmt == FQ_MXFP4 ? 32 : 16;
+}
+
+// Row-pass block constraint on the last dimension.
+inline int64_t row_multiple(int fmt)
+{
+    return fmt == FQ_NVFP4_2LEVEL ? 128 : block_len(fmt);
+}
+
+inline fq_status cuda_status(cudaError_t e)
+{
+    return e == cudaSuccess ? FQ_OK : FQ_ERR_CUDA;
+}
+
+// Checks a quantized-tensor descriptor that will be written or read.
+fq_status check_q(const fq_qtensor *q, int fmt)
+{
+    if (!q || !q->codes || !q->scales)
+        return FQ_ERR_INVALID_ARG;
+    if (fmt != FQ_MXFP4 && !q->tscale)
+        return FQ_ERR_INVALID_ARG;
+    if (!aligned16(q->codes) || !aligned16(q->scales) || (q->tscale && !aligned16(q->tscale)))
+        return FQ_ERR_ALIGN;
+    return FQ_OK;
+}
+
+constexpr size_t kWsAmaxBytes = 256;
+
+// Shared body of fq_quantize and fq_fakequant_ste.
+fq_status quantize_common(const fq_config *cfg, const void *x, int32_t x_dtype, int64_t rows,
+                          int64_t cols, bool want_row_q, const fq_qtensor *row_out,
+                          const fq_qtensor *col_out, void *xhat, int32_t xhat_dtype,
+                          uint8_t *mask, const float *amax_in, void *ws, size_t ws_bytes,
+                          void *stream)
+{
+    if (!valid_cfg(cfg) || !valid_dtype(x_dtype) || !x)
+        return FQ_ERR_INVALID_ARG;
+    if (rows < 0 || cols < 0)
+        return FQ_ERR_SHAPE;
+    const int fmt = cfg->format;
+    const bool do_row = want_row_q || xhat || mask;
+    const bool do_col = col_out != nullptr;
+    if (do_row && cols % row_multiple(fmt) != 0)
+        return FQ_ERR_SHAPE;
+    if (do_col) {
+        const int64_t rm = fmt == FQ_NVFP4_2LEVEL ? 128 : block_len(fmt);
+        if (rows % rm != 0 || cols % 16 != 0)
+            return FQ_ERR_SHAPE;
+        const int64_t tr = fmt == FQ_NVFP4_2LEVEL ? 128 : 64;
+        if ((rows + tr - 1) / tr > 65535)
+            return FQ_ERR_SHAPE;
+    }
+    if (!aligned16(x) || (xhat && !aligned16(xhat)) || (mask && !aligned16(mask)) ||
+        (amax_in && (reinterpret_cast<uintptr_t>(amax_in) & 3u)))
+        return FQ_ERR_ALIGN;
+    fq_status st;
+    if (want_row_q && (st = check_q(row_out, fmt)) != FQ_OK)
+        return st;
+    if (do_col && (st = check_q(col_out, fmt)) != FQ_OK)
+        return st;
+    if (xhat && !valid_dtype(xhat_dtype))
+        return FQ_ERR_INVALID_ARG;
+    const float *amax = amax_in;
+    if (fmt == FQ_NVFP4 && !amax_in) {
+        if (!ws || ws_bytes < sizeof(float))
+            return FQ_ERR_WORKSPACE;
+        if (!aligned16(ws))
+            return FQ_ERR_ALIGN;
+    }
+    const int64_t n = rows * cols;
+    if (n == 0)
+        return FQ_OK;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const int bf16 = x_dtype == FQ_BF16;
+    if (fmt == FQ_NVFP4 && !amax_in) {
+        cudaError_t e = launch_amax(x, bf16, n, static_cast<float *>(ws), s);
+        if (e != cudaSuccess)
+            return FQ_ERR_CUDA;
+        amax = static_cast<const float *>(ws);
+    }
+    if (!do_col) {
+        RowArgs a{};
+        a.x = x;
+        a.n = n;
+        a.amax = amax;
+        if (want_row_q) {
+            a.codes = row_out->codes;
+            a.scales = row_out->scales;
+            a.tscale = row_out->tscale;
+        }
+        a.xhat = xhat;
+        a.xhat_bf16 = xhat_dtype == FQ_BF16;
+        a.mask = mask;
+        a.seed = cfg->seed;
+        a.offset = cfg->offset;
+        a.stream_id = 0;
+        return cuda_status(launch_row(a, bf16, fmt, cfg->rounding, s));
+    }
+    TileArgs t{};
+    t.x = x;
+    t.rows = rows;
+    t.cols = cols;
+    t.amax = amax;
+    t.do_row = do_row ? 1 : 0;
+    if (want_row_q) {
+        t.rcodes = row_out->codes;
+        t.rscales = row_out->scales;
+        t.rtscale = row_out->tscale;
+    }
+    t.xhat = xhat;
+    t.xhat_bf16 = xhat_dtype == FQ_BF16;
+    t.mask = mask;
+    t.ccodes = col_out->codes;
+    t.cscales = col_out->scales;
+    t.ctscale = col_out->tscale;
+    t.seed = cfg->seed;
+    t.offset = cfg->offset;
+    return cuda_status(launch_tile(t, bf16, fmt, cfg->rounding, s));
+}
+
+fq_status check_group(int32_t ntensors, const int64_t *rows, const int64_t *cols, int fmt)
+{
+    if (ntensors < 0 || (ntensors > 0 && (!rows || !cols)))
+        return FQ_ERR_INVALID_ARG;
+    for (int32_t i = 0; i < ntensors; ++i) {
+        if (rows[i] < 0 || cols[i] < 0)
+            return FQ_ERR_SHAPE;
+        if (cols[i] % row_multiple(fmt) != 0)
+            return FQ_ERR_SHAPE;
+    }
+    return FQ_OK;
+}
+
+// Fills the tile prefix table of one group [i0, i0 + cnt).
+void fill_tiles(OsciArgs &a, const int64_t *rows, const int64_t *cols, int32_t i0, int32_t cnt)
+{
+    a.ntensors = cnt;
+    a.tile_start[0] = 0;
+    for (int32_t j = 0; j < cnt; ++j) {
+        const int64_t n = rows[i0 + j] * cols[i0 + j];
+        a.t[j].n = n;
+        const int64_t nch = n / 4;
+        a.tile_start[j + 1] = a.tile_start[j] + (nch + kOsciTileChunks - 1) / kOsciTileChunks;
+    }
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t fq_workspace_size(const fq_config *cfg, int64_t rows, int64_t cols)
+{
+    (void)rows;
+    (void)cols;
+    if (!valid_cfg(cfg))
+        return 0;
+    return cfg->format == FQ_NVFP4 ? kWsAmaxBytes : 0;
+}
+
+size_t fq_osci_workspace_size(int32_t ntensors)
+{
+    if (ntensors <= 0)
+        return 0;
+    const int32_t g = ntensors < kOsciMaxTensors ? ntensors : kOsciMaxTensors;
+    return ((size_t)g * sizeof(float) + 255) / 256 * 256;
+}
+
+fq_status fq_amax(const void *x, int32_t x_dtype, int64_t n, float *amax_out, void *stream)
+{
+    if (!x || !amax_out || !valid_dtype(x_dtype))
+        return FQ_ERR_INVALID_ARG;
+    if (n < 0 || n % 8 != 0)
+        return FQ_ERR_SHAPE;
+    if (!aligned16(x) || (reinterpret_cast<uintptr_t>(amax_out) & 3u))
+        return FQ_ERR_ALIGN;
+    return cuda_status(launch_amax(x, x_dtype == FQ_BF16, n, amax_out,
+                                   static_cast<cudaStream_t>(stream)));
+}
+
+fq_status fq_quantize(const fq_config *cfg, const void *x, int32_t x_dtype, int64_t rows,
+                      int64_t cols, int32_t orient, const fq_qtensor *row_out,
+                      const fq_qtensor *col_out, const float *amax_in, void *workspace,
+                      size_t workspace_bytes, void *stream)
+{
+    if (orient != FQ_ROW && orient != FQ_COL && orient != FQ_ROWCOL)
+        return FQ_ERR_INVALID_ARG;
+    const bool want_row = (orient & FQ_ROW) != 0;
+    const bool want_col = (orient & FQ_COL) != 0;
+    if ((want_row && !row_out) || (want_col && !col_out))
+        return FQ_ERR_INVALID_ARG;
+    return quantize_common(cfg, x, x_dtype, rows, cols, want_row, row_out,
+                           want_col ? col_out : nullptr, nullptr, FQ_F32, nullptr, amax_in,
+                           workspace, workspace_bytes, stream);
+}
+
+fq_status fq_fakequant_ste(const fq_config *cfg, const void *x, int32_t x_dtype, int64_t rows,
+                           int64_t cols, void *xhat, int32_t xhat_dtype, uint8_t *mask,
+                           const fq_qtensor *row_out, const fq_qtensor *col_out,
+                           const float *amax_in, void *workspace, size_t workspace_bytes,
+                           void *stream)
+{
+    if (!xhat)
+        return FQ_ERR_INVALID_ARG;
+    return quantize_common(cfg, x, x_dtype, rows, cols, row_out != nullptr, row_out, col_out,
+                           xhat, xhat_dtype, mask, amax_in, workspace, workspace_bytes, stream);
+}
+
+fq_status fq_dequantize(const fq_config *cfg, const fq_qtensor *q, int64_t rows, int64_t cols,
+                        void *y, int32_t y_dtype, void *stream)
+{
+    if (!valid_cfg(cfg) || !y || !valid_dtype(y_dtype))
+        return FQ_ERR_INVALID_ARG;
+    if (rows < 0 || cols < 0 || cols % row_multiple(cfg->format) != 0)
+        return FQ_ERR_SHAPE;
+    fq_status st = check_q(q, cfg->format);
+    if (st != FQ_OK)
+        return st;
+    if (!aligned16(y))
+        return FQ_ERR_ALIGN;
+    DequantArgs a{};
+    a.codes = q->codes;
+    a.scales = q->scales;
+    a.tscale = q->tscale;
+    a.n = rows * cols;
+    a.y = y;
+    a.y_bf16 = y_dtype == FQ_BF16;
+    return cuda_status(launch_dequant(a, cfg->format, static_cast<cudaStream_t>(stream)));
+}
+
+fq_status fq_ste_backward(const void *dy, int32_t dtype, const uint8_t *mask, int64_t n,
+                          void *dx, void *stream)
+{
+    if (!dy || !mask || !dx || !valid_dtype(dtype))
+        return FQ_ERR_INVALID_ARG;
+    if (n < 0 || n % 8 != 0)
+        return FQ_ERR_SHAPE;
+    if (!aligned16(dy) || !aligned16(dx))
+        return FQ_ERR_ALIGN;
+    return cuda_status(
+        launch_ste(dy, dtype == FQ_BF16, mask, n, dx, static_cast<cudaStream_t>(stream)));
+}
+
+fq_status fq_osci_update(const fq_config *cfg, int32_t ntensors, const int64_t *rows,
+                         const int64_t *cols, float *const *master, const float *const *delta,
+                         float *const *dist_q, float *const *dist_m, const fq_qtensor *prev,
+                         const fq_qtensor *next, void *const *xhat, int32_t xhat_dtype,
+                         uint8_t *const *mask, void *workspace, size_t workspace_bytes,
+                         void *stream)
+{
+    if (!valid_cfg(cfg))
+        return FQ_ERR_INVALID_ARG;
+    const int fmt = cfg->format;
+    fq_status st = check_group(ntensors, rows, cols, fmt);
+    if (st != FQ_OK)
+        return st;
+    if (ntensors == 0)
+        return FQ_OK;
+    if (!master || !delta || !dist_q || !dist_m || !prev || !next)
+        return FQ_ERR_INVALID_ARG;
+    if (xhat && !valid_dtype(xhat_dtype))
+        return FQ_ERR_INVALID_ARG;
+    for (int32_t i = 0; i < ntensors; ++i) {
+        if (!master[i] || !delta[i] || !dist_q[i] || !dist_m[i])
+            return FQ_ERR_INVALID_ARG;
+        if (!aligned16(master[i]) || !aligned16(delta[i]) || !aligned16(dist_q[i]) ||
+            !aligned16(dist_m[i]) || (xhat && xhat[i] && !aligned16(xhat[i])) ||
+            (mask && mask[i] && !aligned16(mask[i])))
+            return FQ_ERR_ALIGN;
+        if ((st = check_q(&prev[i], fmt)) != FQ_OK || (st = check_q(&next[i], fmt)) != FQ_OK)
+            return st;
+    }
+    if (!workspace || workspace_bytes < fq_osci_workspace_size(ntensors))
+        return FQ_ERR_WORKSPACE;
+    if (!aligned16(workspace))
+        return FQ_ERR_ALIGN;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    static thread_local OsciArgs a;
+    for (int32_t i0 = 0; i0 < ntensors; i0 += kOsciMaxTensors) {
+        const int32_t cnt = ntensors - i0 < kOsciMaxTensors ? ntensors - i0 : kOsciMaxTensors;
+        std::memset(&a, 0, sizeof(a));
+        fill_tiles(a, rows, cols, i0, cnt);
+        a.xhat_bf16 = xhat_dtype == FQ_BF16;
+        a.seed = cfg->seed;
+        a.offset = cfg->offset;
+        a.amax = static_cast<float *>(workspace);
+        for (int32_t j = 0; j < cnt; ++j) {
+            const int32_t i = i0 + j;
+            OsciTensor &t = a.t[j];
+            t.master = master[i];
+            t.delta = delta[i];
+            t.dist_q = dist_q[i];
+            t.dist_m = dist_m[i];
+            t.pcodes = prev[i].codes;
+            t.pscales = prev[i].scales;
+            t.ptscale = prev[i].tscale;
+            t.ncodes = next[i].codes;
+            t.nscales = next[i].scales;
+            t.ntscale = next[i].tscale;
+            t.xhat = xhat ? xhat[i] : nullptr;
+            t.mask = mask ? mask[i] : nullptr;
+        }
+        cudaError_t e = launch_osci_update(a, fmt, cfg->rounding, s);
+        if (e != cudaSuccess)
+            return FQ_ERR_CUDA;
+    }
+    return FQ_OK;
+}
+
+fq_status fq_osci_reset(const fq_config *cfg, int32_t ntensors, const int64_t *rows,
+                        const int64_t *cols, float *const *master, float *const *dist_q,
+                        float *const *dist_m, const fq_qtensor *cur, float threshold,
+                        unsigned long long *n_reset, void *stream)
+{
+    if (!valid_cfg(cfg))
+        return FQ_ERR_INVALID_ARG;
+    const int fmt = cfg->format;
+    fq_status st = check_group(ntensors, rows, cols, fmt);
+    if (st != FQ_OK)
+        return st;
+    if (ntensors > 0 && (!master || !dist_q || !dist_m || !cur))
+        return FQ_ERR_INVALID_ARG;
+    for (int32_t i = 0; i < ntensors; ++i) {
+        if (!master[i] || !dist_q[i] || !dist_m[i])
+            return FQ_ERR_INVALID_ARG;
+        if (!aligned16(master[i]) || !aligned16(dist_q[i]) || !aligned16(dist_m[i]))
+            return FQ_ERR_ALIGN;
+        if ((st = check_q(&cur[i], fmt)) != FQ_OK)
+            return st;
+    }
+    if (n_reset && (reinterpret_cast<uintptr_t>(n_reset) & 7u))
+        return FQ_ERR_ALIGN;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (n_reset && cudaMemsetAsync(n_reset, 0, sizeof(unsigned long long), s) != cudaSuccess)
+        return FQ_ERR_CUDA;
+    static thread_local OsciArgs a;
+    for (int32_t i0 = 0; i0 < ntensors; i0 += kOsciMaxTensors) {
+        const int32_t cnt = ntensors - i0 < kOsciMaxTensors ? ntensors - i0 : kOsciMaxTensors;
+        std::memset(&a, 0, sizeof(a));
+        fill_tiles(a, rows, cols, i0, cnt);
+        a.threshold = threshold;
+        a.n_reset = n_reset;
+        for (int32_t j = 0; j < cnt; ++j) {
+            const int32_t i = i0 + j;
+            OsciTensor &t = a.t[j];
+            t.master = master[i];
+            t.dist_q = dist_q[i];
+            t.dist_m = dist_m[i];
+            t.pcodes = cur[i].codes;
+            t.pscales = cur[i].scales;
+            t.ptscale = cur[i].tscale;
+        }
+        cudaError_t e = launch_osci_reset(a, fmt, s);
+        if (e != cudaSuccess)
+            return FQ_ERR_CUDA;
+    }
+    return FQ_OK;
+}
+
+const char *fq_status_string(fq_status status)
+{
+    switch (status) {
+    case FQ_OK: return "ok";
+    case FQ_ERR_INVALID_ARG: return "invalid argument";
+    case FQ_ERR_SHAPE: return "shape is not a multiple of the block length";
+    case FQ_ERR_ALIGN: return "pointer is not 16-byte aligned";
+    case FQ_ERR_WORKSPACE: return "workspace missing or too small";
+    case FQ_ERR_UNSUPPORTED: return "unsupported combination";
+    case FQ_ERR_CUDA: return "CUDA launch failed";
+    }
+    return "unknown status";
+}
+
+}  // extern "C"

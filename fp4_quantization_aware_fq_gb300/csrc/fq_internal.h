@@ -1,0 +1,101 @@
+// fq_internal.h -- argument blocks and launchers shared between the C ABI
+// (fq_api.cu) and the kernel translation units.  Host-side only types.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace fqk {
+
+// Row-wise quantization of a dense tensor seen as a flat array of n elements
+// (n a multiple of the block length).
+struct RowArgs {
+    const void *x;
+    int64_t n;
+    const float *amax;  // NVFP4: device pointer to the tensor amax
+    uint8_t *codes;
+    uint8_t *scales;
+    float *tscale;      // NVFP4: s_g (1 float); double block: one per 128 elements
+    void *xhat;         // optional fake-quantized output
+    int xhat_bf16;
+    uint8_t *mask;      // optional STE mask (1 bit per element)
+    uint64_t seed;
+    uint32_t offset;
+    uint32_t stream_id;
+};
+
+// Tiled quantization producing the column-wise (transposed) output and,
+// optionally, the row-wise outputs from the same read of x.
+struct TileArgs {
+    const void *x;
+    int64_t rows, cols;
+    const float *amax;
+    int do_row;
+    uint8_t *rcodes;
+    uint8_t *rscales;
+    float *rtscale;
+    void *xhat;
+    int xhat_bf16;
+    uint8_t *mask;
+    uint8_t *ccodes;
+    uint8_t *cscales;
+    float *ctscale;
+    uint64_t seed;
+    uint32_t offset;
+};
+
+struct DequantArgs {
+    const uint8_t *codes;
+    const uint8_t *scales;
+    const float *tscale;
+    int64_t n;
+    void *y;
+    int y_bf16;
+};
+
+// Grouped OsciReset passes: up to kOsciMaxTensors tensors per launch.  Tiles
+// of kOsciTileChunks 16-byte chunks are numbered across the group; tile_start
+// holds the prefix sums (tile_start[i] = first tile of tensor i).
+constexpr int kOsciMaxTensors = 64;
+constexpr int kOsciTileChunks = 1024;
+
+struct OsciTensor {
+    float *master;
+    const float *delta;
+    float *dist_q;
+    float *dist_m;
+    const uint8_t *pcodes;
+    const uint8_t *pscales;
+    const float *ptscale;
+    uint8_t *ncodes;
+    uint8_t *nscales;
+    float *ntscale;
+    void *xhat;
+    uint8_t *mask;
+    int64_t n;
+};
+
+struct OsciArgs {
+    int ntensors;
+    int xhat_bf16;
+    uint64_t seed;
+    uint32_t offset;
+    float threshold;
+    float *amax;                       // one float per tensor (workspace)
+    unsigned long long *n_reset;
+    int64_t tile_start[kOsciMaxTensors + 1];
+    OsciTensor t[kOsciMaxTensors];
+};
+
+int sm_count();
+
+cudaError_t launch_amax(const void *x, int bf16, int64_t n, float *out, cudaStream_t s);
+cudaError_t launch_row(const RowArgs &a, int bf16, int fmt, int rnd, cudaStream_t s);
+cudaError_t launch_tile(const TileArgs &a, int bf16, int fmt, int rnd, cudaStream_t s);
+cudaError_t launch_dequant(const DequantArgs &a, int fmt, cudaStream_t s);
+cudaError_t launch_ste(const void *dy, int bf16, const uint8_t *mask, int64_t n, void *dx,
+                       cudaStream_t s);
+cudaError_t launch_osci_update(const OsciArgs &a, int fmt, int rnd, cudaStream_t s);
+cudaError_t launch_osci_reset(const OsciArgs &a, int fmt, cudaStream_t s);
+
+}  // namespace fqk

@@ -1,0 +1,113 @@
+// k_aux.cu -- dequantization and the straight-through-estimator backward.
+//
+// Dequantization is the "dequantize" half of the quantize/dequantize operator
+// of fake quantization ("Como o Treinamento com Quantização Detecta e Recupera
+// Precisão em Inferência de Baixa Precisão", "Detalhes técnicos"); the STE
+// backward lets the gradient through where the element was inside the
+// block's representable range and zeroes it where it was clipped.
+#include "fq_device.cuh"
+#include "fq_internal.h"
+
+namespace fqk {
+
+constexpr int kAuxThreads = 256;
+
+// One thread = 8 consecutive elements (4 code bytes).
+template <int FMT>
+__global__ void __launch_bounds__(kAuxThreads) dequant_kernel(DequantArgs a)
+{
+    constexpr int B = FmtInfo<FMT>::B;
+    const int64_t ng = a.n / 8;
+    const int64_t stride = (int64_t)gridDim.x * kAuxThreads;
+    for (int64_t g = (int64_t)blockIdx.x * kAuxThreads + threadIdx.x; g < ng; g += stride) {
+        const uint32_t q = __ldg(reinterpret_cast<const uint32_t *>(a.codes) + g);
+        const int64_t e0 = g * 8;
+        const uint32_t sc = __ldg(a.scales + e0 / B);
+        float s_outer = 0.0f;
+        if (FMT == NVFP4)
+            s_outer = __ldg(a.tscale);
+        else if (FMT == NV2L)
+            s_outer = __ldg(a.tscale + e0 / 128);
+        const float s_eff = stored_s_eff<FMT>(sc, s_outer);
+        float xh[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+            xh[i] = __fmul_rn(e2m1_value(q >> (4 * i)), s_eff);
+        if (a.y_bf16) {
+            uint4 o = make_uint4(bf16x2_rn(xh[0], xh[1]), bf16x2_rn(xh[2], xh[3]),
+                                 bf16x2_rn(xh[4], xh[5]), bf16x2_rn(xh[6], xh[7]));
+            reinterpret_cast<uint4 *>(a.y)[g] = o;
+        } else {
+            float4 *dst = reinterpret_cast<float4 *>(a.y) + 2 * g;
+            dst[0] = make_float4(xh[0], xh[1], xh[2], xh[3]);
+            dst[1] = make_float4(xh[4], xh[5], xh[6], xh[7]);
+        }
+    }
+}
+
+// One thread = one 16-byte vector of dy.
+template <typename T>
+__global__ void __launch_bounds__(kAuxThreads) ste_kernel(const void *__restrict__ dy,
+                                                          const uint8_t *__restrict__ mask,
+                                                          int64_t nch, void *__restrict__ dx)
+{
+    constexpr int E = VecInfo<T>::E;
+    const int64_t stride = (int64_t)gridDim.x * kAuxThreads;
+    for (int64_t ch = (int64_t)blockIdx.x * kAuxThreads + threadIdx.x; ch < nch; ch += stride) {
+        uint4 v = ld16((const char *)dy + ch * 16);
+        uint32_t m = __ldg(mask + (ch * E) / 8);
+        if (E == 4)
+            m >>= (ch & 1) * 4;
+        uint32_t w[4] = {v.x, v.y, v.z, v.w};
+        if (E == 8) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const uint32_t keep = ((m >> (2 * i)) & 1u ? 0x0000FFFFu : 0u) |
+                                      ((m >> (2 * i + 1)) & 1u ? 0xFFFF0000u : 0u);
+                w[i] &= keep;
+            }
+        } else {
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+                w[i] = ((m >> i) & 1u) ? w[i] : 0u;
+        }
+        reinterpret_cast<uint4 *>(dx)[ch] = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+}
+
+static int grid_for(int64_t items, int ctas_per_sm)
+{
+    const int64_t need = (items + kAuxThreads - 1) / kAuxThreads;
+    const int64_t cap = (int64_t)sm_count() * ctas_per_sm;
+    return (int)(need < cap ? (need > 0 ? need : 1) : cap);
+}
+
+cudaError_t launch_dequant(const DequantArgs &a, int fmt, cudaStream_t s)
+{
+    if (a.n == 0)
+        return cudaSuccess;
+    const int grid = grid_for(a.n / 8, 8);
+    if (fmt == NVFP4)
+        dequant_kernel<NVFP4><<<grid, kAuxThreads, 0, s>>>(a);
+    else if (fmt == MXFP4)
+        dequant_kernel<MXFP4><<<grid, kAuxThreads, 0, s>>>(a);
+    else
+        dequant_kernel<NV2L><<<grid, kAuxThreads, 0, s>>>(a);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_ste(const void *dy, int bf16, const uint8_t *mask, int64_t n, void *dx,
+                       cudaStream_t s)
+{
+    if (n == 0)
+        return cudaSuccess;
+    const int64_t nch = n / (bf16 ? 8 : 4);
+    const int grid = grid_for(nch, 8);
+    if (bf16)
+        ste_kernel<__nv_bfloat16><<<grid, kAuxThreads, 0, s>>>(dy, mask, nch, dx);
+    else
+        ste_kernel<float><<<grid, kAuxThreads, 0, s>>>(dy, mask, nch, dx);
+    return cudaGetLastError();
+}
+
+}  // namespace fqk

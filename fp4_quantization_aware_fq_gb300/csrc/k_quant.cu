@@ -1,0 +1,411 @@
+// k_quant.cu -- tensor amax, row-wise quantization and the tiled row +
+// column-wise quantization kernels.
+//
+// Row-wise ("Resumo Técnico: TetraJet-v2" §2A, 1x16 groups; MXFP4 1x32 as
+// named on "Aprimorando gpt-oss ...", "O que há de novo"): each thread owns
+// one 16-byte vector of the input (8 BF16 or 4 FP32 values); the lanes that
+// share a block combine their partial amax with warp shuffles, derive the
+// scale in registers, and write packed codes, scales, the fake-quantized
+// values and the STE mask with coalesced stores.
+//
+// Column-wise (§2A, the transposed 1x16 groups of the backward pass): a CTA
+// stages a tile of x in shared memory while doing the row-wise pass on it,
+// then quantizes 16x1 column blocks out of shared memory and writes the
+// transposed codes through a shared-memory staging buffer.
+#include "fq_device.cuh"
+#include "fq_internal.h"
+
+namespace fqk {
+
+constexpr int kThreads = 256;
+
+// ------------------------------------------------------------------ amax
+template <typename T>
+__global__ void __launch_bounds__(kThreads) amax_kernel(const void *__restrict__ x, int64_t nch,
+                                                        unsigned *__restrict__ out)
+{
+    constexpr int E = VecInfo<T>::E;
+    constexpr int U = 4;
+    float m = 0.0f;
+    const int64_t stride = (int64_t)gridDim.x * kThreads * U;
+    for (int64_t base = (int64_t)blockIdx.x * kThreads * U; base < nch; base += stride) {
+        uint4 raw[U];
+#pragma unroll
+        for (int k = 0; k < U; ++k) {
+            const int64_t ch = base + k * kThreads + threadIdx.x;
+            raw[k] = ch < nch ? ld16((const char *)x + ch * 16) : make_uint4(0, 0, 0, 0);
+        }
+#pragma unroll
+        for (int k = 0; k < U; ++k) {
+            float v[E];
+            unpack16<T>(raw[k], v);
+#pragma unroll
+            for (int i = 0; i < E; ++i)
+                m = fmaxf(m, fabsf(v[i]));
+        }
+    }
+    m = group_max<32>(m);
+    __shared__ float wm[kThreads / 32];
+    if ((threadIdx.x & 31) == 0)
+        wm[threadIdx.x >> 5] = m;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        float b = wm[0];
+#pragma unroll
+        for (int w = 1; w < kThreads / 32; ++w)
+            b = fmaxf(b, wm[w]);
+        atomicMax(out, __float_as_uint(b));  // non-negative floats order like their bits
+    }
+}
+
+// ------------------------------------------------------------------ row-wise core
+// Quantize one 16-byte vector (E values) of a row-wise block.  `ch` is the
+// flat vector index in the tensor, so the flat element index is ch * E.  All
+// 32 lanes of the warp must call this together (block amax uses shuffles).
+template <typename T, int FMT, int RND>
+__device__ __forceinline__ void row_vector(const uint4 &raw, int64_t ch, bool valid, float s_g,
+                                           uint8_t *__restrict__ codes,
+                                           uint8_t *__restrict__ scales,
+                                           float *__restrict__ tscale, void *__restrict__ xhat,
+                                           int xhat_bf16, uint8_t *__restrict__ mask,
+                                           uint64_t seed, uint32_t offset, uint32_t stream_id)
+{
+    constexpr int E = VecInfo<T>::E;
+    constexpr int L = FmtInfo<FMT>::B / E;
+    constexpr int LO = 128 / E;
+    const VecQ<E> r = quant_vec<T, FMT, RND>(raw, ch, s_g, seed, offset, stream_id);
+    const uint32_t q = r.q, mbits = r.mbits;
+    const Scale sc = r.sc;
+    const float s_o = r.s_o;
+    const int lane = threadIdx.x & 31;
+    uint32_t mpair = 0;
+    if (E == 4)
+        mpair = __shfl_down_sync(0xFFFFFFFFu, mbits, 1);
+    if (!valid)
+        return;
+    if (codes) {
+        if (E == 8)
+            *reinterpret_cast<uint32_t *>(codes + ch * 4) = q;
+        else
+            *reinterpret_cast<uint16_t *>(codes + ch * 2) = (uint16_t)q;
+        if ((lane % L) == 0)
+            scales[ch / L] = (uint8_t)sc.code;
+        if (FMT == NV2L && (lane % LO) == 0)
+            tscale[ch / LO] = s_o;
+    }
+    if (xhat) {
+        float xh[E];
+#pragma unroll
+        for (int i = 0; i < E; ++i)
+            xh[i] = __fmul_rn(e2m1_value(q >> (4 * i)), sc.s_eff);
+        if (xhat_bf16) {
+            if (E == 8) {
+                uint4 o = make_uint4(bf16x2_rn(xh[0], xh[1]), bf16x2_rn(xh[2], xh[3]),
+                                     bf16x2_rn(xh[4], xh[5]), bf16x2_rn(xh[6], xh[7]));
+                *reinterpret_cast<uint4 *>((char *)xhat + ch * 16) = o;
+            } else {
+                uint2 o = make_uint2(bf16x2_rn(xh[0], xh[1]), bf16x2_rn(xh[2], xh[3]));
+                *reinterpret_cast<uint2 *>((char *)xhat + ch * 8) = o;
+            }
+        } else {
+            float4 *dst = reinterpret_cast<float4 *>((char *)xhat + ch * E * 4);
+            dst[0] = make_float4(xh[0], xh[1], xh[2], xh[3]);
+            if (E == 8)
+                dst[1] = make_float4(xh[4], xh[5], xh[6], xh[7]);
+        }
+    }
+    if (mask) {
+        if (E == 8)
+            mask[ch] = (uint8_t)mbits;
+        else if ((lane & 1) == 0)
+            mask[ch >> 1] = (uint8_t)(mbits | (mpair << 4));
+    }
+}
+
+template <typename T, int FMT, int RND>
+__global__ void __launch_bounds__(kThreads) row_kernel(RowArgs a)
+{
+    constexpr int E = VecInfo<T>::E;
+    constexpr int U = 4;
+    const int64_t nch = a.n / E;
+    float s_g = 0.0f;
+    if (FMT == NVFP4) {
+        s_g = outer_scale(*a.amax);
+        if (blockIdx.x == 0 && threadIdx.x == 0 && a.tscale)
+            a.tscale[0] = s_g;
+    }
+    const int64_t stride = (int64_t)gridDim.x * kThreads * U;
+    for (int64_t base = (int64_t)blockIdx.x * kThreads * U; base < nch; base += stride) {
+        uint4 raw[U];
+#pragma unroll
+        for (int k = 0; k < U; ++k) {
+            const int64_t ch = base + k * kThreads + threadIdx.x;
+            raw[k] = ch < nch ? ld16((const char *)a.x + ch * 16) : make_uint4(0, 0, 0, 0);
+        }
+#pragma unroll
+        for (int k = 0; k < U; ++k) {
+            const int64_t ch = base + k * kThreads + threadIdx.x;
+            row_vector<T, FMT, RND>(raw[k], ch, ch < nch, s_g, a.codes, a.scales, a.tscale,
+                                    a.xhat, a.xhat_bf16, a.mask, a.seed, a.offset, a.stream_id);
+        }
+    }
+}
+
+// ------------------------------------------------------------------ tiled row + column
+template <int FMT>
+struct TileShape {
+    static constexpr int TR = (FMT == NV2L) ? 128 : 64;  // tile rows
+    static constexpr int TC = (FMT == NV2L) ? 128 : 64;  // tile cols
+    static constexpr int BC = FmtInfo<FMT>::B;           // column block (rows)
+};
+
+template <typename T, int FMT>
+constexpr size_t tile_smem_bytes()
+{
+    using S = TileShape<FMT>;
+    return (size_t)S::TR * S::TC * sizeof(T)          // x tile
+           + (size_t)S::TC * (S::TR / 2)              // staged column codes
+           + (size_t)S::TC * (S::TR / S::BC)          // staged column scales
+           + (FMT == NV2L ? (size_t)S::TC * (S::TR / S::BC) * 4 : 0);  // inner amax
+}
+
+template <typename T, int FMT, int RND>
+__global__ void __launch_bounds__(kThreads) tile_kernel(TileArgs a)
+{
+    using S = TileShape<FMT>;
+    constexpr int E = VecInfo<T>::E;
+    constexpr int TR = S::TR, TC = S::TC, BC = S::BC;
+    constexpr int VPR = TC / E;  // 16-byte vectors per tile row
+    constexpr int NRB = TR / BC;  // column blocks per tile column
+    extern __shared__ __align__(16) unsigned char smem[];
+    T *tile = reinterpret_cast<T *>(smem);
+    uint8_t *ccs = smem + (size_t)TR * TC * sizeof(T);   // [TC][TR/2]
+    uint8_t *css = ccs + (size_t)TC * (TR / 2);          // [TC][NRB]
+    float *am16 = reinterpret_cast<float *>(css + (size_t)TC * NRB);  // [NRB][TC] (double block)
+
+    const int64_t r0 = (int64_t)blockIdx.y * TR;
+    const int64_t c0 = (int64_t)blockIdx.x * TC;
+    const int64_t rows = a.rows, cols = a.cols;
+    float s_g = 0.0f;
+    if (FMT == NVFP4) {
+        s_g = outer_scale(*a.amax);
+        if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) {
+            if (a.ctscale)
+                a.ctscale[0] = s_g;
+            if (a.do_row && a.rtscale)
+                a.rtscale[0] = s_g;
+        }
+    }
+
+    // Phase 1: load the tile (coalesced 16-byte vectors along rows), stage it,
+    // and run the row-wise pass on the registers.
+    constexpr int NV = TR * VPR / kThreads;
+    uint4 raw[NV];
+#pragma unroll
+    for (int k = 0; k < NV; ++k) {
+        const int q = k * kThreads + threadIdx.x;
+        const int tr = q / VPR, tv = q % VPR;
+        const int64_t gr = r0 + tr, gc = c0 + (int64_t)tv * E;
+        raw[k] = (gr < rows && gc < cols)
+                     ? ld16((const char *)a.x + (gr * cols + gc) * (int64_t)sizeof(T))
+                     : make_uint4(0, 0, 0, 0);
+    }
+#pragma unroll
+    for (int k = 0; k < NV; ++k) {
+        const int q = k * kThreads + threadIdx.x;
+        const int tr = q / VPR, tv = q % VPR;
+        *reinterpret_cast<uint4 *>(tile + tr * TC + tv * E) = raw[k];
+        if (a.do_row) {
+            const int64_t gr = r0 + tr, gc = c0 + (int64_t)tv * E;
+            const bool valid = gr < rows && gc < cols;
+            const int64_t ch = (gr * cols + gc) / E;
+            row_vector<T, FMT, RND>(raw[k], ch, valid, s_g, a.rcodes, a.rscales, a.rtscale,
+                                    a.xhat, a.xhat_bf16, a.mask, a.seed, a.offset, 0u);
+        }
+    }
+    __syncthreads();
+
+    // Phase 2: column blocks (BC rows x 1 column) out of shared memory.
+    if (FMT == NV2L) {
+        for (int task = threadIdx.x; task < TC * NRB; task += kThreads) {
+            const int c = task % TC, rb = task / TC;
+            float m = 0.0f;
+#pragma unroll
+            for (int i = 0; i < BC; ++i)
+                m = fmaxf(m, fabsf(static_cast<float>(tile[(rb * BC + i) * TC + c])));
+            am16[rb * TC + c] = m;
+        }
+        __syncthreads();
+    }
+    for (int task = threadIdx.x; task < TC * NRB; task += kThreads) {
+        const int c = task % TC, rb = task / TC;
+        const int64_t gc = c0 + c, gr0 = r0 + (int64_t)rb * BC;
+        if (gc >= cols || gr0 >= rows)
+            continue;
+        float v[BC];
+        float m = 0.0f;
+#pragma unroll
+        for (int i = 0; i < BC; ++i) {
+            v[i] = static_cast<float>(tile[(rb * BC + i) * TC + c]);
+            m = fmaxf(m, fabsf(v[i]));
+        }
+        Scale sc;
+        if (FMT == MXFP4) {
+            sc = mx_scale(m);
+        } else if (FMT == NVFP4) {
+            sc = nv_scale(m, s_g);
+        } else {
+            float mo = 0.0f;
+#pragma unroll
+            for (int j = 0; j < NRB; ++j)
+                mo = fmaxf(mo, am16[j * TC + c]);
+            const float s_o = outer_scale(mo);
+            sc = nv_scale(m, s_o);
+            if (rb == 0)
+                a.ctscale[gc * (rows / 128) + r0 / 128] = s_o;
+        }
+        uint32_t *dst = reinterpret_cast<uint32_t *>(ccs + c * (TR / 2) + rb * (BC / 2));
+#pragma unroll
+        for (int w = 0; w < BC / 8; ++w) {
+            float y[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+                y[i] = __fmul_rn(v[w * 8 + i], sc.r);
+            uint32_t q;
+            if (RND == RNE) {
+                q = e2m1_rn_pack8(y);
+            } else {
+                // flat index in X^T of this group of 8
+                const uint64_t e0 = (uint64_t)gc * (uint64_t)rows + (uint64_t)(gr0 + w * 8);
+                const uint4 rbits = sr_bits8(a.seed, e0 >> 3, 1u, a.offset);
+                q = 0;
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+                    q |= e2m1_sr(y[i], u16_of(rbits, i)) << (4 * i);
+            }
+            dst[w] = q;
+        }
+        css[c * NRB + rb] = (uint8_t)sc.code;
+    }
+    __syncthreads();
+
+    // Phase 3: write the staged column outputs (rows of X^T).
+    constexpr int U8 = TR / 16;  // 8-byte units of codes per tile column
+    for (int u = threadIdx.x; u < TC * U8; u += kThreads) {
+        const int c = u / U8, j = u % U8;
+        const int64_t gc = c0 + c, gr = r0 + (int64_t)j * 16;
+        if (gc < cols && gr < rows)
+            *reinterpret_cast<uint2 *>(a.ccodes + gc * (rows / 2) + gr / 2) =
+                *reinterpret_cast<const uint2 *>(ccs + c * (TR / 2) + j * 8);
+    }
+    for (int u = threadIdx.x; u < TC * NRB; u += kThreads) {
+        const int c = u / NRB, j = u % NRB;
+        const int64_t gc = c0 + c, gr = r0 + (int64_t)j * BC;
+        if (gc < cols && gr < rows)
+            a.cscales[gc * (rows / BC) + gr / BC] = css[c * NRB + j];
+    }
+}
+
+// ------------------------------------------------------------------ launchers
+int sm_count()
+{
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess)
+        return 132;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+        return 132;
+    return n;
+}
+
+static int persistent_grid(int64_t work_items, int per_cta, int ctas_per_sm)
+{
+    const int64_t need = (work_items + per_cta - 1) / per_cta;
+    const int64_t cap = (int64_t)sm_count() * ctas_per_sm;
+    return (int)(need < cap ? (need > 0 ? need : 1) : cap);
+}
+
+cudaError_t launch_amax(const void *x, int bf16, int64_t n, float *out, cudaStream_t s)
+{
+    cudaError_t e = cudaMemsetAsync(out, 0, sizeof(float), s);
+    if (e != cudaSuccess)
+        return e;
+    if (n == 0)
+        return cudaSuccess;
+    const int E = bf16 ? 8 : 4;
+    const int64_t nch = n / E;
+    const int grid = persistent_grid(nch, kThreads * 4, 4);
+    if (bf16)
+        amax_kernel<__nv_bfloat16><<<grid, kThreads, 0, s>>>(x, nch, (unsigned *)out);
+    else
+        amax_kernel<float><<<grid, kThreads, 0, s>>>(x, nch, (unsigned *)out);
+    return cudaGetLastError();
+}
+
+template <typename T, int FMT, int RND>
+static cudaError_t row_go(const RowArgs &a, cudaStream_t s)
+{
+    constexpr int E = VecInfo<T>::E;
+    const int64_t nch = a.n / E;
+    if (nch == 0)
+        return cudaSuccess;
+    const int grid = persistent_grid(nch, kThreads * 4, 4);
+    row_kernel<T, FMT, RND><<<grid, kThreads, 0, s>>>(a);
+    return cudaGetLastError();
+}
+
+template <typename T>
+static cudaError_t row_fmt(const RowArgs &a, int fmt, int rnd, cudaStream_t s)
+{
+    switch (fmt * 2 + rnd) {
+    case NVFP4 * 2 + RNE: return row_go<T, NVFP4, RNE>(a, s);
+    case NVFP4 * 2 + SR: return row_go<T, NVFP4, SR>(a, s);
+    case MXFP4 * 2 + RNE: return row_go<T, MXFP4, RNE>(a, s);
+    case MXFP4 * 2 + SR: return row_go<T, MXFP4, SR>(a, s);
+    case NV2L * 2 + RNE: return row_go<T, NV2L, RNE>(a, s);
+    default: return row_go<T, NV2L, SR>(a, s);
+    }
+}
+
+cudaError_t launch_row(const RowArgs &a, int bf16, int fmt, int rnd, cudaStream_t s)
+{
+    return bf16 ? row_fmt<__nv_bfloat16>(a, fmt, rnd, s) : row_fmt<float>(a, fmt, rnd, s);
+}
+
+template <typename T, int FMT, int RND>
+static cudaError_t tile_go(const TileArgs &a, cudaStream_t s)
+{
+    using S = TileShape<FMT>;
+    if (a.rows == 0 || a.cols == 0)
+        return cudaSuccess;
+    constexpr size_t smem = tile_smem_bytes<T, FMT>();
+    if (smem > 48 * 1024) {
+        cudaError_t e = cudaFuncSetAttribute(tile_kernel<T, FMT, RND>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)smem);
+        if (e != cudaSuccess)
+            return e;
+    }
+    dim3 grid((unsigned)((a.cols + S::TC - 1) / S::TC), (unsigned)((a.rows + S::TR - 1) / S::TR));
+    tile_kernel<T, FMT, RND><<<grid, kThreads, smem, s>>>(a);
+    return cudaGetLastError();
+}
+
+template <typename T>
+static cudaError_t tile_fmt(const TileArgs &a, int fmt, int rnd, cudaStream_t s)
+{
+    switch (fmt * 2 + rnd) {
+    case NVFP4 * 2 + RNE: return tile_go<T, NVFP4, RNE>(a, s);
+    case NVFP4 * 2 + SR: return tile_go<T, NVFP4, SR>(a, s);
+    case MXFP4 * 2 + RNE: return tile_go<T, MXFP4, RNE>(a, s);
+    case MXFP4 * 2 + SR: return tile_go<T, MXFP4, SR>(a, s);
+    case NV2L * 2 + RNE: return tile_go<T, NV2L, RNE>(a, s);
+    default: return tile_go<T, NV2L, SR>(a, s);
+    }
+}
+
+cudaError_t launch_tile(const TileArgs &a, int bf16, int fmt, int rnd, cudaStream_t s)
+{
+    return bf16 ? tile_fmt<__nv_bfloat16>(a, fmt, rnd, s) : tile_fmt<float>(a, fmt, rnd, s);
+}
+
+}  // namespace fqk

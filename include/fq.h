@@ -1,0 +1,208 @@
+/*
+ * fq.h -- C ABI of the GB300 block-scaled FP4 fake-quantization library.
+ *
+ * The library quantizes FP32 or BF16 tensors to 4-bit E2M1 codes under
+ * per-block scales, packs them, dequantizes them, produces the
+ * straight-through-estimator mask of fake quantization, and keeps the
+ * OsciReset oscillation statistics of quantization-aware training.
+ *
+ * Sources (web pages on FP4 quantization-aware training):
+ *  [GPTOSS] "Aprimorando gpt-oss para Precisão e Desempenho com Treinamento
+ *           Consciente à Quantização" -- TL;DR, "O que há de novo": MXFP4 and
+ *           NVFP4, NVFP4 with FP8 E4M3 block scales.
+ *  [QATREC] "Como o Treinamento com Quantização Detecta e Recupera Precisão em
+ *           Inferência de Baixa Precisão" -- "Detalhes técnicos": fake
+ *           quantization (quantize/dequantize in a high-precision type) with a
+ *           straight-through estimator exposing rounding and clipping.
+ *  [TJV2]   "Resumo Técnico: TetraJet-v2" -- §2A double-block NVFP4 (FP32 scale
+ *           per 128-element outer block, 8-bit scale per 16-element inner
+ *           block), stochastic rounding with E[round(x)] = x, 1x16 groups and
+ *           the transposed weight; §2B OsciReset (dist_Q / dist_M).
+ *
+ * Numeric definitions (the pages leave these open; this library's readings):
+ *  E2M1 code: bit 3 sign, bits 2..1 exponent (bias 1), bit 0 mantissa;
+ *    magnitudes {0, 0.5, 1, 1.5, 2, 3, 4, 6}.  Nearest-even rounding with
+ *    saturation to +-6; the sign bit is kept for zero results.
+ *  E4M3 scale: OCP "FN" byte (bias 7, max 448), nearest-even, saturating.
+ *  E8M0 scale: value 2^(code - 127).
+ *  NVFP4 (FQ_NVFP4): s_g = amax(tensor) / 2688 (FP32, 2688 = 6 * 448);
+ *    per 1x16 block s_b = (block_amax / 6) / s_g -> E4M3 code c;
+ *    s_eff = E4M3(c) * s_g; r = 1 / s_eff (0 when s_eff = 0).
+ *  Double block (FQ_NVFP4_2LEVEL, [TJV2] §2A): as NVFP4 with s_g replaced by
+ *    s_o = amax(1x128 block) / 2688, stored per outer block.
+ *  MXFP4 (FQ_MXFP4): per 1x32 block k = floor(log2 block_amax) - 2 clamped to
+ *    [-127, 127], E8M0 code k + 127, s_eff = 2^k, r = 2^-k.
+ *  Element: y = x * r (FP32); code = E2M1(y) (nearest-even, or stochastic:
+ *    round up iff u16 < frac * 65536); xhat = E2M1value(code) * s_eff (FP32,
+ *    then nearest-even to BF16 when a BF16 output is asked for).
+ *  STE mask ([QATREC] clipped straight-through estimator): bit = 1 iff
+ *    |x| <= 6 * s_eff, i.e. x is inside the block's representable range.
+ *  Stochastic rounding draw: Philox4x32-10 (Salmon et al., SC'11) with key =
+ *    (seed low, seed high) and counter = (g low, g high, stream, offset),
+ *    g = flat element index / 8 in the tensor being quantized (the transpose
+ *    for the column-wise pass), stream 0 row-wise / 1 column-wise; element
+ *    j = index % 8 takes 16-bit half (j % 2) of output word j / 2.
+ *
+ * Layouts (all dense, row-major, no padding):
+ *  x        [rows, cols] FP32 or BF16.
+ *  codes    [rows, cols/2] bytes; element 2j in the low nibble of byte j.
+ *  scales   [rows, cols/B] bytes, B = 16 (NVFP4, double block) or 32 (MXFP4).
+ *  tscale   NVFP4: 1 float (s_g); double block: [rows, cols/128] floats;
+ *           MXFP4: not used (may be NULL).
+ *  column-wise outputs describe the transpose X^T [cols, rows]:
+ *           codes [cols, rows/2], scales [cols, rows/B], tscale as above.
+ *  mask     ceil(rows*cols/8) bytes: bit (e % 8) of byte e / 8 holds flat
+ *           element e (equivalently bit e % 32 of little-endian word e / 32).
+ *
+ * Conventions:
+ *  - Every pointer argument to tensor data is a DEVICE pointer unless said
+ *    otherwise; the caller allocates all of them.  Pointers to tensor data
+ *    must be 16-byte aligned (FQ_ERR_ALIGN otherwise).
+ *  - `stream` is a cudaStream_t passed as void*; NULL is the legacy default
+ *    stream.  Calls are asynchronous on that stream: they never synchronise,
+ *    never allocate device memory, and may return before the GPU finishes.
+ *  - Argument errors are detected on the host and returned before any launch;
+ *    nothing is written then.  A failed launch returns FQ_ERR_CUDA.
+ *  - Inputs must be finite.  For NVFP4 the tensor amax (for the double block:
+ *    each 1x128 block amax) must be 0 or at least 2^-100, so that every
+ *    effective scale is a normal FP32 number; smaller non-zero ranges are
+ *    outside the contract.
+ *  - Calls keep no state between them and may run concurrently on different
+ *    streams with different workspaces.
+ */
+#ifndef FQ_H
+#define FQ_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define FQ_API __attribute__((visibility("default")))
+#else
+#define FQ_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    FQ_OK = 0,
+    FQ_ERR_INVALID_ARG = 1, /* NULL where a pointer is required, unknown enum value */
+    FQ_ERR_SHAPE = 2,       /* dimension not a multiple of the block length, negative size */
+    FQ_ERR_ALIGN = 3,       /* a tensor pointer is not 16-byte aligned */
+    FQ_ERR_WORKSPACE = 4,   /* workspace NULL or smaller than fq_workspace_size() */
+    FQ_ERR_UNSUPPORTED = 5, /* valid but not implemented combination */
+    FQ_ERR_CUDA = 6         /* a CUDA launch or memset failed */
+} fq_status;
+
+typedef enum { FQ_NVFP4 = 0, FQ_MXFP4 = 1, FQ_NVFP4_2LEVEL = 2 } fq_format;
+typedef enum { FQ_RNE = 0, FQ_SR = 1 } fq_rounding;
+typedef enum { FQ_ROW = 1, FQ_COL = 2, FQ_ROWCOL = 3 } fq_orient;
+typedef enum { FQ_F32 = 0, FQ_BF16 = 1 } fq_dtype;
+
+/* Quantizer configuration.  seed and offset matter only for FQ_SR. */
+typedef struct {
+    int32_t format;   /* fq_format */
+    int32_t rounding; /* fq_rounding */
+    uint64_t seed;    /* Philox key */
+    uint32_t offset;  /* Philox counter word 3, e.g. the training step */
+    uint32_t reserved;
+} fq_config;
+
+/* A quantized tensor: device pointers, layouts as described above. */
+typedef struct {
+    uint8_t *codes;
+    uint8_t *scales;
+    float *tscale;
+} fq_qtensor;
+
+/* Bytes of device workspace that fq_quantize / fq_fakequant_ste need for a
+ * [rows, cols] tensor in this configuration (NVFP4 keeps its tensor amax
+ * there; the other formats need none and get 0).  Pure host function. */
+FQ_API size_t fq_workspace_size(const fq_config *cfg, int64_t rows, int64_t cols);
+
+/* Bytes of device workspace that fq_osci_update needs for `ntensors` tensors. */
+FQ_API size_t fq_osci_workspace_size(int32_t ntensors);
+
+/* Tensor amax ([TJV2] §2A names the per-tensor max|x| that NVFP4 needs):
+ * amax_out[0] = max |x| over n elements (device float).  n must be a multiple
+ * of 8.  The result is order-independent, hence identical to any sequential
+ * evaluation. */
+FQ_API fq_status fq_amax(const void *x, int32_t x_dtype, int64_t n, float *amax_out, void *stream);
+
+/* Quantize x ([rows, cols]) -- [GPTOSS] NVFP4/MXFP4, [TJV2] §2A double block
+ * and stochastic rounding.  orient selects the row-wise output (row_out), the
+ * column-wise output on the transpose (col_out, [TJV2] §2A transposed 1x16
+ * groups), or both from one read of x.  Shapes: cols % B == 0 for the row
+ * pass (cols % 128 for the double block); rows % B == 0 for the column pass
+ * (rows % 128 for the double block).  amax_in: optional device float holding
+ * the tensor amax to use for NVFP4 (NULL: computed here into the workspace).
+ * NVFP4 uses the same s_g for both orientations. */
+FQ_API fq_status fq_quantize(const fq_config *cfg, const void *x, int32_t x_dtype, int64_t rows,
+                      int64_t cols, int32_t orient, const fq_qtensor *row_out,
+                      const fq_qtensor *col_out, const float *amax_in, void *workspace,
+                      size_t workspace_bytes, void *stream);
+
+/* Fake quantization with the straight-through-estimator mask ([QATREC]
+ * "Detalhes técnicos"): xhat = dequant(quant(x)) in xhat_dtype, mask as
+ * defined above (NULL: not written), both from the row-wise pass.  row_out
+ * and col_out (NULL: not written) additionally receive the packed tensors,
+ * so one call does the whole forward/backward quantization of an activation. */
+FQ_API fq_status fq_fakequant_ste(const fq_config *cfg, const void *x, int32_t x_dtype, int64_t rows,
+                           int64_t cols, void *xhat, int32_t xhat_dtype, uint8_t *mask,
+                           const fq_qtensor *row_out, const fq_qtensor *col_out,
+                           const float *amax_in, void *workspace, size_t workspace_bytes,
+                           void *stream);
+
+/* Dequantize a row-wise quantized [rows, cols] tensor: y = E2M1value(code) *
+ * s_eff, in y_dtype.  Bit-identical to the xhat of fq_fakequant_ste. */
+FQ_API fq_status fq_dequantize(const fq_config *cfg, const fq_qtensor *q, int64_t rows, int64_t cols,
+                        void *y, int32_t y_dtype, void *stream);
+
+/* Straight-through-estimator backward ([QATREC]): dx = dy where the mask bit
+ * is set, +0 elsewhere.  n elements, n % 8 == 0; dy/dx share dtype. */
+FQ_API fq_status fq_ste_backward(const void *dy, int32_t dtype, const uint8_t *mask, int64_t n,
+                          void *dx, void *stream);
+
+/* One optimizer step with OsciReset statistics ([TJV2] §2B), over a group of
+ * tensors (e.g. every expert matrix of an MoE layer).  Host arrays of length
+ * ntensors hold the shapes and the device pointers of each tensor:
+ *   master[i]   FP32 [rows, cols], updated in place: w_t = w_{t-1} + delta
+ *   delta[i]    FP32 update for this step
+ *   dist_m[i]   FP32, += |w_t - w_{t-1}|
+ *   dist_q[i]   FP32, += |xhat_t - xhat_{t-1}|
+ *   prev[i]     quantized w_{t-1} (read), next[i] quantized w_t (written);
+ *               the caller swaps them between steps.  Initialise prev with
+ *               fq_quantize of the initial master.
+ *   xhat[i]     fake-quantized w_t in xhat_dtype (NULL array or entry: skip)
+ *   mask[i]     STE mask of w_t (NULL array or entry: skip)
+ * Quantization follows cfg (NVFP4 takes s_g from amax(w_t)).  cols must be a
+ * multiple of the block length.  The workspace holds one float per tensor
+ * (fq_osci_workspace_size). */
+FQ_API fq_status fq_osci_update(const fq_config *cfg, int32_t ntensors, const int64_t *rows,
+                         const int64_t *cols, float *const *master, const float *const *delta,
+                         float *const *dist_q, float *const *dist_m, const fq_qtensor *prev,
+                         const fq_qtensor *next, void *const *xhat, int32_t xhat_dtype,
+                         uint8_t *const *mask, void *workspace, size_t workspace_bytes,
+                         void *stream);
+
+/* End of an OsciReset window ([TJV2] §2B): where dist_Q > threshold * dist_M
+ * (FP32 product, strict), the master weight is set to xhat_t decoded from cur
+ * (the quantized value of its current bin); dist_Q and dist_M are then zeroed
+ * for every weight.  n_reset (device uint64, may be NULL) receives the number
+ * of weights reset.  Deciding when the learning rate is low enough to call
+ * this is the caller's schedule. */
+FQ_API fq_status fq_osci_reset(const fq_config *cfg, int32_t ntensors, const int64_t *rows,
+                        const int64_t *cols, float *const *master, float *const *dist_q,
+                        float *const *dist_m, const fq_qtensor *cur, float threshold,
+                        unsigned long long *n_reset, void *stream);
+
+/* Static description of a status code. */
+FQ_API const char *fq_status_string(fq_status status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FQ_H */

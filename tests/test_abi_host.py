@@ -1,0 +1,126 @@
+"""Host-side checks of the C ABI (no GPU): the library builds, loads and
+exports every entry point include/fq.h declares, and argument errors come back
+as the documented status codes before anything is launched."""
+import ctypes
+
+import pytest
+
+from fp4_quantization_aware_fq_gb300 import build as fqbuild
+from fp4_quantization_aware_fq_gb300 import fq
+
+
+@pytest.fixture(scope="module")
+def L():
+    fqbuild.build()
+    return fq.lib()
+
+
+def test_header_declares_the_boundary():
+    names = set(fq.declared_symbols())
+    for n in ("fq_quantize", "fq_dequantize", "fq_fakequant_ste", "fq_osci_update",
+              "fq_osci_reset", "fq_ste_backward", "fq_amax", "fq_workspace_size",
+              "fq_osci_workspace_size", "fq_status_string"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(L):
+    for n in fq.declared_symbols():
+        assert hasattr(L, n), n
+
+
+def test_status_strings(L):
+    assert fq.fq_status_string(0) == "ok"
+    for s in range(1, 7):
+        assert fq.fq_status_string(s) not in ("ok", "unknown status")
+    assert fq.fq_status_string(99) == "unknown status"
+
+
+def test_workspace_sizes(L):
+    assert fq.fq_workspace_size(fq.Config(fq.NVFP4), 256, 1024) >= 4
+    assert fq.fq_workspace_size(fq.Config(fq.MXFP4), 256, 1024) == 0
+    assert fq.fq_workspace_size(fq.Config(fq.NVFP4_2LEVEL), 256, 1024) == 0
+    assert fq.fq_osci_workspace_size(64) >= 64 * 4
+    assert fq.fq_osci_workspace_size(0) == 0
+
+
+FAKE = 0x10000  # 16-byte aligned, never dereferenced: every case fails validation first
+
+
+def _qt(codes=FAKE, scales=FAKE, tscale=FAKE):
+    return fq._QT(codes, scales, tscale)
+
+
+def _quant(L, cfg, x=FAKE, dtype=fq.BF16, rows=64, cols=64, orient=fq.ROW, row=None, col=None,
+           ws=FAKE, wsb=256):
+    r = ctypes.byref(row) if row is not None else None
+    c = ctypes.byref(col) if col is not None else None
+    return L.fq_quantize(ctypes.byref(cfg), x, dtype, rows, cols, orient, r, c, None, ws, wsb,
+                         None)
+
+
+def test_quantize_argument_errors(L):
+    ok = fq.Config(fq.NVFP4)
+    assert _quant(L, fq.Config(7)) == 1                                    # unknown format
+    assert _quant(L, fq.Config(fq.NVFP4, 5)) == 1                          # unknown rounding
+    assert _quant(L, ok, dtype=9, row=_qt()) == 1                          # unknown dtype
+    assert _quant(L, ok, x=0, row=_qt()) == 1                              # NULL input
+    assert _quant(L, ok, orient=0, row=_qt()) == 1                         # bad orientation
+    assert _quant(L, ok, orient=fq.ROW, row=None) == 1                     # missing output
+    assert _quant(L, ok, cols=40, row=_qt()) == 2                          # cols % 16
+    assert _quant(L, fq.Config(fq.MXFP4), cols=48, row=_qt()) == 2         # cols % 32
+    assert _quant(L, fq.Config(fq.NVFP4_2LEVEL), cols=64, row=_qt()) == 2  # cols % 128
+    assert _quant(L, ok, rows=40, orient=fq.COL, col=_qt()) == 2           # rows % 16
+    assert _quant(L, fq.Config(fq.NVFP4_2LEVEL), rows=64, cols=128, orient=fq.COL,
+                  col=_qt()) == 2                                          # rows % 128
+    assert _quant(L, ok, rows=-1, row=_qt()) == 2
+    assert _quant(L, ok, x=FAKE + 8, row=_qt()) == 3                       # misaligned input
+    assert _quant(L, ok, row=_qt(codes=FAKE + 4)) == 3                     # misaligned codes
+    assert _quant(L, ok, row=_qt(tscale=0)) == 1                           # NVFP4 needs tscale
+    assert _quant(L, ok, row=_qt(), ws=0) == 4                             # no workspace
+    assert _quant(L, ok, row=_qt(), wsb=2) == 4                            # workspace too small
+
+
+def test_fakequant_dequant_ste_amax_errors(L):
+    cfg = fq.Config(fq.NVFP4)
+    f = L.fq_fakequant_ste
+    assert f(ctypes.byref(cfg), FAKE, fq.BF16, 64, 64, None, fq.BF16, None, None, None, None,
+             FAKE, 256, None) == 1                                         # xhat required
+    assert f(ctypes.byref(cfg), FAKE, fq.BF16, 64, 64, FAKE + 2, fq.BF16, None, None, None, None,
+             FAKE, 256, None) == 3
+    assert f(ctypes.byref(cfg), FAKE, fq.BF16, 64, 64, FAKE, 5, None, None, None, None,
+             FAKE, 256, None) == 1
+    q = _qt()
+    assert L.fq_dequantize(ctypes.byref(cfg), ctypes.byref(q), 64, 24, FAKE, fq.F32, None) == 2
+    assert L.fq_dequantize(ctypes.byref(cfg), None, 64, 64, FAKE, fq.F32, None) == 1
+    assert L.fq_dequantize(ctypes.byref(cfg), ctypes.byref(q), 64, 64, FAKE + 1, fq.F32,
+                           None) == 3
+    assert L.fq_ste_backward(FAKE, fq.BF16, FAKE, 12, FAKE, None) == 2
+    assert L.fq_ste_backward(FAKE, fq.BF16, None, 16, FAKE, None) == 1
+    assert L.fq_ste_backward(FAKE + 2, fq.BF16, FAKE, 16, FAKE, None) == 3
+    assert L.fq_amax(FAKE, fq.F32, 12, FAKE, None) == 2
+    assert L.fq_amax(FAKE, fq.F32, 16, None, None) == 1
+
+
+def test_osci_argument_errors(L):
+    cfg = fq.Config(fq.NVFP4)
+    vp, i64 = ctypes.c_void_p, ctypes.c_int64
+    rows = (i64 * 2)(64, 64)
+    cols = (i64 * 2)(64, 40)
+    ptrs = (vp * 2)(FAKE, FAKE)
+    qs = (fq._QT * 2)(_qt(), _qt())
+    u = L.fq_osci_update
+    assert u(ctypes.byref(cfg), 2, rows, cols, ptrs, ptrs, ptrs, ptrs, qs, qs, None, fq.BF16,
+             None, FAKE, 256, None) == 2                                   # 40 % 16 != 0
+    cols[1] = 64
+    assert u(ctypes.byref(cfg), 2, rows, cols, ptrs, ptrs, ptrs, ptrs, qs, qs, None, fq.BF16,
+             None, None, 0, None) == 4                                     # no workspace
+    assert u(ctypes.byref(cfg), 2, rows, cols, None, ptrs, ptrs, ptrs, qs, qs, None, fq.BF16,
+             None, FAKE, 256, None) == 1
+    bad = (vp * 2)(FAKE, FAKE + 4)
+    assert u(ctypes.byref(cfg), 2, rows, cols, bad, ptrs, ptrs, ptrs, qs, qs, None, fq.BF16,
+             None, FAKE, 256, None) == 3
+    assert u(ctypes.byref(cfg), -1, rows, cols, ptrs, ptrs, ptrs, ptrs, qs, qs, None, fq.BF16,
+             None, FAKE, 256, None) == 1
+    r = L.fq_osci_reset
+    assert r(ctypes.byref(cfg), 2, rows, cols, ptrs, ptrs, ptrs, None, 4.0, None, None) == 1
+    assert r(ctypes.byref(cfg), 2, rows, cols, ptrs, ptrs, ptrs, qs, 4.0, FAKE + 4, None) == 3

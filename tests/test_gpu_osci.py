@@ -1,0 +1,148 @@
+"""OsciReset update / reset on the GPU vs the oracle, bit for bit."""
+import json
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from fp4_quantization_aware_fq_gb300 import fq
+from fp4_quantization_aware_fq_gb300 import workloads as W
+from gpu_common import FMT_O, assert_eq, bits, npy
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+class GpuOsci:
+    """Device-side state of a group of tensors (ping-pong quantized buffers)."""
+
+    def __init__(self, ws_bf16, cfg):
+        self.cfg = cfg
+        self.master = [w.float().to(DEV).contiguous() for w in ws_bf16]
+        self.dq = [torch.zeros_like(m) for m in self.master]
+        self.dm = [torch.zeros_like(m) for m in self.master]
+        init_cfg = fq.Config(cfg.format, cfg.rounding, cfg.seed, 0)
+        self.prev = [fq.fq_quantize(m, init_cfg)[0] for m in self.master]
+        self.next = [fq.alloc_qtensor(*m.shape, cfg.format, DEV) for m in self.master]
+        self.xhat = [torch.empty(m.shape, dtype=torch.bfloat16, device=DEV) for m in self.master]
+        self.mask = [torch.empty(((m.numel() + 7) // 8 + 15) // 16 * 16, dtype=torch.uint8,
+                                 device=DEV) for m in self.master]
+
+    def step(self, deltas, t):
+        cfg = fq.Config(self.cfg.format, self.cfg.rounding, self.cfg.seed, t)
+        fq.fq_osci_update(cfg, self.master, deltas, self.dq, self.dm, self.prev, self.next,
+                          xhat=self.xhat, mask=self.mask)
+        self.prev, self.next = self.next, self.prev
+
+    def reset(self, thr):
+        cnt = torch.zeros(1, dtype=torch.int64, device=DEV)
+        fq.fq_osci_reset(self.cfg, self.master, self.dq, self.dm, self.prev, thr, n_reset=cnt)
+        return cnt
+
+
+def _compare(name, g: GpuOsci, i, st: oracle.OsciState, out=None):
+    assert_eq(f"{name}.master", bits(g.master[i]), st.master.view(np.uint32))
+    assert_eq(f"{name}.dist_q", bits(g.dq[i]), st.dist_q.view(np.uint32))
+    assert_eq(f"{name}.dist_m", bits(g.dm[i]), st.dist_m.view(np.uint32))
+    assert_eq(f"{name}.codes", npy(g.prev[i].codes), st.codes)
+    assert_eq(f"{name}.scales", npy(g.prev[i].scales), st.scales)
+    if g.cfg.format == fq.NVFP4:
+        assert_eq(f"{name}.tscale", npy(g.prev[i].tscale)[:1].view(np.uint32),
+                  st.tscale.reshape(-1)[:1].view(np.uint32))
+    if out is not None:
+        assert_eq(f"{name}.xhat", bits(g.xhat[i]), oracle.f32_to_bf16_bits(out["xhat"]))
+        n = g.master[i].numel()
+        assert_eq(f"{name}.mask", npy(g.mask[i])[: (n + 7) // 8],
+                  out["mask"].view(np.uint8)[: (n + 7) // 8])
+
+
+@pytest.mark.parametrize("fmt,rnd", [(fq.NVFP4, fq.RNE), (fq.NVFP4, fq.SR), (fq.MXFP4, fq.RNE),
+                                     (fq.NVFP4_2LEVEL, fq.SR)])
+def test_osci_group_matches_oracle(fmt, rnd):
+    shapes = [(96, 256), (256, 128), (48, 384), (128, 128)]
+    ws = [W.normal(s, 0.02, seed=40 + i).to(torch.bfloat16) for i, s in enumerate(shapes)]
+    cfg = fq.Config(fmt, rnd, seed=77)
+    g = GpuOsci(ws, cfg)
+    sts = [oracle.OsciState(w.float().numpy(), FMT_O[fmt], rnd, seed=77) for w in ws]
+    for t in range(1, 4):
+        deltas = [W.master_update(s, t, std=3e-3) for s in shapes]   # large enough to flip bins
+        g.step([d.to(DEV) for d in deltas], t)
+        torch.cuda.synchronize()
+        for i, (st, d) in enumerate(zip(sts, deltas)):
+            out = st.step(d.numpy(), offset=t)
+            _compare(f"t{t}.{i}", g, i, st, out)
+    cnt = g.reset(4.0)
+    torch.cuda.synchronize()
+    total = sum(st.reset(4.0) for st in sts)
+    assert int(cnt.item()) == total
+    assert total > 0
+    for i, st in enumerate(sts):
+        _compare(f"reset.{i}", g, i, st)
+
+
+def test_osci_flip_example():
+    with open(os.path.join(os.path.dirname(__file__), "golden", "osci_flip_e4.json")) as f:
+        gd = json.load(f)
+    w0 = torch.zeros((gd["rows"], gd["cols"]), dtype=torch.float32)
+    for k, v in gd["w0"].items():
+        w0[0, int(k)] = v
+    g = GpuOsci([w0], fq.Config(fq.NVFP4))
+    for t in range(1, gd["steps"] + 1):
+        d = torch.zeros_like(w0)
+        d[0, 1] = gd["delta_watched"] if t % 2 == 1 else -gd["delta_watched"]
+        d[0, 2] = gd["delta_control"]
+        g.step([d.to(DEV)], t)
+    torch.cuda.synchronize()
+    assert float(g.dq[0][0, 1]) == gd["expected_dist_q_watched"]
+    assert abs(float(g.dm[0][0, 1]) - gd["expected_dist_m_watched_approx"]) < 1e-5
+    assert float(g.dq[0][0, 2]) == gd["expected_dist_q_control"]
+    cnt = g.reset(gd["threshold"])
+    torch.cuda.synchronize()
+    assert int(cnt.item()) == gd["expected_resets"]
+    assert float(g.master[0][0, 1]) == gd["expected_master_watched_after_reset"]
+    assert float(g.master[0][0, 16]) == 2688.0
+
+
+@pytest.mark.slow
+def test_osci_full_moe_two_steps():
+    """The 32-expert MoE workload at full size (64 matrices, 1.06 G weights):
+    two update steps through the grouped launch; the first and last matrices
+    are checked against the oracle bit for bit, every matrix for invariants."""
+    spec = W.WORKLOADS["moe_qat"]
+    E, up, down = spec["experts"], spec["up_shape"], spec["down_shape"]
+    shapes = [up, down] * E
+    checked = {0: None, len(shapes) - 1: None}
+    gen = torch.Generator(device=DEV)
+    gen.manual_seed(1234)
+    ws = []
+    for i, s in enumerate(shapes):
+        if i in checked:
+            w = W.normal(s, 0.02, seed=500 + i).to(torch.bfloat16)
+            checked[i] = w
+            ws.append(w)
+        else:
+            ws.append((torch.randn(s, generator=gen, device=DEV) * 0.02).to(torch.bfloat16))
+    cfg = fq.Config(fq.NVFP4, fq.RNE)
+    g = GpuOsci(ws, cfg)
+    del ws
+    sts = {i: oracle.OsciState(w.float().numpy(), oracle.NVFP4) for i, w in checked.items()}
+    for t in (1, 2):
+        deltas, host = [], {}
+        for i, s in enumerate(shapes):
+            if i in checked:
+                d = W.master_update(s, t)
+                host[i] = d
+                deltas.append(d.to(DEV))
+            else:
+                deltas.append(torch.randn(s, generator=gen, device=DEV) * 1e-4)
+        g.step(deltas, t)
+        torch.cuda.synchronize()
+        del deltas
+        for i, st in sts.items():
+            out = st.step(host[i].numpy(), offset=t)
+            _compare(f"t{t}.{i}", g, i, st, out)
+    for i in range(len(shapes)):
+        assert torch.isfinite(g.dq[i]).all() and (g.dq[i] >= 0).all()
+        assert (g.dm[i] > 0).float().mean() > 0.99

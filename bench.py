@@ -96,7 +96,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", "50"],
                 stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
         except Exception:
             self.proc = None
@@ -130,71 +130,91 @@ class ClockSampler:
 
 # --------------------------------------------------------------------------- workloads
 class Suite:
-    """All five workloads' inputs and outputs, resident on one GPU."""
+    """The workloads' inputs and outputs, resident on one GPU.  `only` limits
+    the suite to some workloads; `experts` scales the MoE workload down (for
+    profiling a smaller case of the same kernels)."""
 
-    def __init__(self, dev, seed_offset=0):
+    ORDER = ("nvfp4_small", "mxfp4_weight", "nvfp4_act", "ste_backward", "grad_2level",
+             "osci_update", "osci_reset")
+
+    def __init__(self, dev, only=None, experts=None):
         import torch
         from fp4_quantization_aware_fq_gb300 import fq
         from fp4_quantization_aware_fq_gb300 import workloads as W
-        self.fq, self.torch, self.dev = fq, torch, dev
-        so = seed_offset
-        spec = W.WORKLOADS
-        # nvfp4_small
-        self.x1 = W.nvfp4_small(seed=0 + so, device=dev)
-        self.cfg1 = fq.Config(fq.NVFP4)
-        self.q1 = fq.alloc_qtensor(*self.x1.shape, fq.NVFP4, dev)
-        self.xh1 = torch.empty(self.x1.shape, dtype=torch.float32, device=dev)
-        self.m1 = self._mask(self.x1)
-        self.ws1 = torch.empty(256, dtype=torch.uint8, device=dev)
-        # mxfp4_weight
-        self.x2 = W.mxfp4_weight(seed=1 + so, device=dev)
-        self.cfg2 = fq.Config(fq.MXFP4)
-        self.q2 = fq.alloc_qtensor(*self.x2.shape, fq.MXFP4, dev)
-        self.xh2 = torch.empty(self.x2.shape, dtype=torch.bfloat16, device=dev)
-        self.m2 = self._mask(self.x2)
-        # nvfp4_act + STE backward
-        self.x3 = W.nvfp4_act(seed=2 + so, device=dev)
-        self.cfg3 = fq.Config(fq.NVFP4)
-        r3, c3 = self.x3.shape
-        self.rq3 = fq.alloc_qtensor(r3, c3, fq.NVFP4, dev)
-        self.cq3 = fq.alloc_qtensor(c3, r3, fq.NVFP4, dev)
-        self.xh3 = torch.empty(self.x3.shape, dtype=torch.bfloat16, device=dev)
-        self.m3 = self._mask(self.x3)
-        self.ws3 = torch.empty(256, dtype=torch.uint8, device=dev)
-        self.dy3 = W.normal(self.x3.shape, 1.0, seed=12 + so, dtype=torch.bfloat16, device=dev)
-        self.dx3 = torch.empty_like(self.dy3)
-        # grad_2level
-        self.x4 = W.grad_2level(seed=3 + so, device=dev)
-        self.cfg4 = fq.Config(fq.NVFP4_2LEVEL, fq.SR, 0x5EED, 0)
-        self.q4 = fq.alloc_qtensor(*self.x4.shape, fq.NVFP4_2LEVEL, dev)
-        # moe_qat
-        m = spec["moe_qat"]
-        ws = W.moe_weights(m["experts"], m["up_shape"], m["down_shape"], seed=4 + so, device=dev)
-        self.cfg5 = fq.Config(fq.NVFP4)
-        self.master = [w.float() for w in ws]
-        del ws
-        self.delta = [W.master_update(t.shape, 1, device=dev, seed_base=1000 + so)
-                      for t in self.master]
-        self.dq = [torch.zeros_like(t) for t in self.master]
-        self.dm = [torch.zeros_like(t) for t in self.master]
-        self.prev = [fq.fq_quantize(t, self.cfg5)[0] for t in self.master]
-        self.next = [fq.alloc_qtensor(*t.shape, fq.NVFP4, dev) for t in self.master]
-        self.xh5 = [torch.empty(t.shape, dtype=torch.bfloat16, device=dev) for t in self.master]
-        self.m5 = [self._mask(t) for t in self.master]
-        self.ws5 = torch.empty(fq.fq_osci_workspace_size(len(self.master)), dtype=torch.uint8,
-                               device=dev)
-        self.nreset = torch.zeros(1, dtype=torch.int64, device=dev)
-        self.n5 = sum(t.numel() for t in self.master)
-        self.elems = {"nvfp4_small": self.x1.numel(), "mxfp4_weight": self.x2.numel(),
-                      "nvfp4_act": self.x3.numel(), "ste_backward": self.dy3.numel(),
-                      "grad_2level": self.x4.numel(), "osci_update": self.n5,
-                      "osci_reset": self.n5}
+        self.fq, self.torch, self.W, self.dev = fq, torch, W, dev
+        self.names = [n for n in self.ORDER if not only or n in only]
+        self.elems = {}
         self.step_no = 0
+        want = set(self.names)
+        if "nvfp4_small" in want:
+            self.x1 = W.nvfp4_small(device=dev)
+            self.cfg1 = fq.Config(fq.NVFP4)
+            self.q1 = fq.alloc_qtensor(*self.x1.shape, fq.NVFP4, dev)
+            self.xh1 = torch.empty(self.x1.shape, dtype=torch.float32, device=dev)
+            self.m1 = self._mask(self.x1)
+            self.ws1 = torch.empty(256, dtype=torch.uint8, device=dev)
+            self.elems["nvfp4_small"] = self.x1.numel()
+        if "mxfp4_weight" in want:
+            self.x2 = W.mxfp4_weight(device=dev)
+            self.cfg2 = fq.Config(fq.MXFP4)
+            self.q2 = fq.alloc_qtensor(*self.x2.shape, fq.MXFP4, dev)
+            self.xh2 = torch.empty(self.x2.shape, dtype=torch.bfloat16, device=dev)
+            self.m2 = self._mask(self.x2)
+            self.elems["mxfp4_weight"] = self.x2.numel()
+        if want & {"nvfp4_act", "ste_backward"}:
+            self.x3 = W.nvfp4_act(device=dev)
+            self.cfg3 = fq.Config(fq.NVFP4)
+            r3, c3 = self.x3.shape
+            self.rq3 = fq.alloc_qtensor(r3, c3, fq.NVFP4, dev)
+            self.cq3 = fq.alloc_qtensor(c3, r3, fq.NVFP4, dev)
+            self.xh3 = torch.empty(self.x3.shape, dtype=torch.bfloat16, device=dev)
+            self.m3 = self._mask(self.x3)
+            self.ws3 = torch.empty(256, dtype=torch.uint8, device=dev)
+            self.elems["nvfp4_act"] = self.x3.numel()
+            if "ste_backward" in want:
+                self.nvfp4_act()          # the backward consumes this call's mask
+                self.dy3 = W.normal(self.x3.shape, 1.0, seed=12, dtype=torch.bfloat16,
+                                    device=dev)
+                self.dx3 = torch.empty_like(self.dy3)
+                self.elems["ste_backward"] = self.dy3.numel()
+        if "grad_2level" in want:
+            self.x4 = W.grad_2level(device=dev)
+            self.cfg4 = fq.Config(fq.NVFP4_2LEVEL, fq.SR, 0x5EED, 0)
+            self.q4 = fq.alloc_qtensor(*self.x4.shape, fq.NVFP4_2LEVEL, dev)
+            self.elems["grad_2level"] = self.x4.numel()
+        if want & {"osci_update", "osci_reset"}:
+            m = W.WORKLOADS["moe_qat"]
+            ws = W.moe_weights(experts or m["experts"], m["up_shape"], m["down_shape"],
+                               seed=4, device=dev)
+            self.cfg5 = fq.Config(fq.NVFP4)
+            self.master = [w.float() for w in ws]
+            del ws
+            self.delta = [W.master_update(t.shape, 1, device=dev) for t in self.master]
+            self.dq = [torch.zeros_like(t) for t in self.master]
+            self.dm = [torch.zeros_like(t) for t in self.master]
+            self.prev = [fq.fq_quantize(t, self.cfg5)[0] for t in self.master]
+            self.next = [fq.alloc_qtensor(*t.shape, fq.NVFP4, dev) for t in self.master]
+            self.xh5 = [torch.empty(t.shape, dtype=torch.bfloat16, device=dev)
+                        for t in self.master]
+            self.m5 = [self._mask(t) for t in self.master]
+            self.ws5 = torch.empty(fq.fq_osci_workspace_size(len(self.master)),
+                                   dtype=torch.uint8, device=dev)
+            self.nreset = torch.zeros(1, dtype=torch.int64, device=dev)
+            n5 = sum(t.numel() for t in self.master)
+            for k in ("osci_update", "osci_reset"):
+                if k in want:
+                    self.elems[k] = n5
+        self.elems = {k: v for k, v in self.elems.items() if k in want}
         torch.cuda.synchronize()
 
     def _mask(self, x):
         return self.torch.empty(((x.numel() + 7) // 8 + 15) // 16 * 16, dtype=self.torch.uint8,
                                 device=self.dev)
+
+    def step(self):
+        for name in self.names:
+            getattr(self, name)()
+        self.step_no += 1
 
     # each call is one C-ABI entry point; all run on the current stream
     def nvfp4_small(self):
@@ -225,9 +245,6 @@ class Suite:
         self.fq.fq_osci_reset(self.cfg5, self.master, self.dq, self.dm, self.prev, 4.0,
                               n_reset=self.nreset)
 
-    ORDER = ("nvfp4_small", "mxfp4_weight", "nvfp4_act", "ste_backward", "grad_2level",
-             "osci_update", "osci_reset")
-
 
 def bytes_per_step(elems):
     return {k: BYTES_PER_ELEM[k] * elems[k] for k in elems}
@@ -237,23 +254,18 @@ def bytes_per_step(elems):
 def run_ours(args, rank, world, dist):
     import torch
     dev = torch.device("cuda", torch.cuda.current_device())
-    suite = Suite(dev, seed_offset=0)
+    suite = Suite(dev, only=args.only, experts=args.experts)
     stream = torch.cuda.current_stream()
     bps = bytes_per_step(suite.elems)
     total_bytes = sum(bps.values())
 
-    def step():
-        for name in Suite.ORDER:
-            getattr(suite, name)()
-        suite.step_no += 1
-
     for _ in range(args.warmup):
-        step()
+        suite.step()
     torch.cuda.synchronize()
     if dist:
         dist.barrier()
     torch.cuda.synchronize()
-    ev = {n: [] for n in Suite.ORDER}
+    ev = {n: [] for n in suite.names}
     clocks = ClockSampler(torch.cuda.current_device()) if rank == 0 else None
     if clocks:
         clocks.start()
@@ -261,7 +273,7 @@ def run_ours(args, rank, world, dist):
     t1 = torch.cuda.Event(enable_timing=True)
     t0.record(stream)
     for _ in range(args.steps):
-        for name in Suite.ORDER:
+        for name in suite.names:
             a = torch.cuda.Event(enable_timing=True)
             b = torch.cuda.Event(enable_timing=True)
             a.record(stream)
@@ -275,7 +287,7 @@ def run_ours(args, rank, world, dist):
         dist.barrier()
     clk = clocks.stop() if clocks else None
     ms = t0.elapsed_time(t1)
-    per_ms = {n: sum(a.elapsed_time(b) for a, b in ev[n]) / args.steps for n in Suite.ORDER}
+    per_ms = {n: sum(a.elapsed_time(b) for a, b in ev[n]) / args.steps for n in suite.names}
     if dist:
         t = torch.tensor([ms], dtype=torch.float64, device=dev)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
@@ -290,16 +302,37 @@ def run_ours(args, rank, world, dist):
     return suite, bps, total_bytes, ms, per_ms, clk, e2e
 
 
+def e2e_buffers(suite):
+    """Device tensors that each step takes from the host (its inputs) and the
+    results it hands back (packed codes and scales, the reset count)."""
+    ins, outs = [], []
+    if "nvfp4_small" in suite.names:
+        ins.append(suite.x1)
+        outs += [suite.q1.codes, suite.q1.scales, suite.q1.tscale]
+    if "mxfp4_weight" in suite.names:
+        ins.append(suite.x2)
+        outs += [suite.q2.codes, suite.q2.scales]
+    if "nvfp4_act" in suite.names:
+        ins.append(suite.x3)
+        outs += [suite.rq3.codes, suite.rq3.scales, suite.cq3.codes, suite.cq3.scales]
+    if "ste_backward" in suite.names:
+        ins.append(suite.dy3)
+        outs.append(suite.dx3)
+    if "grad_2level" in suite.names:
+        ins.append(suite.x4)
+        outs += [suite.q4.codes, suite.q4.scales, suite.q4.tscale]
+    if "osci_update" in suite.names:
+        ins += list(suite.delta)
+    if "osci_reset" in suite.names:
+        outs.append(suite.nreset)
+    return ins, outs
+
+
 def run_e2e(args, suite, total_bytes):
     import torch
     stream = torch.cuda.current_stream()
-    h_in = [(suite.x1, suite.x1.cpu().pin_memory()), (suite.x2, suite.x2.cpu().pin_memory()),
-            (suite.x3, suite.x3.cpu().pin_memory()), (suite.dy3, suite.dy3.cpu().pin_memory()),
-            (suite.x4, suite.x4.cpu().pin_memory())]
-    h_in += [(d, d.cpu().pin_memory()) for d in suite.delta]
-    outs = [suite.q1.codes, suite.q1.scales, suite.q2.codes, suite.q2.scales, suite.rq3.codes,
-            suite.rq3.scales, suite.cq3.codes, suite.cq3.scales, suite.q4.codes, suite.q4.scales,
-            suite.q4.tscale, suite.nreset]
+    ins, outs = e2e_buffers(suite)
+    h_in = [(d, d.cpu().pin_memory()) for d in ins]
     h_out = [torch.empty(o.shape, dtype=o.dtype).pin_memory() for o in outs]
     h2d = sum(h.numel() * h.element_size() for _, h in h_in)
     d2h = sum(o.numel() * o.element_size() for o in outs)
@@ -307,16 +340,14 @@ def run_e2e(args, suite, total_bytes):
     def step():
         for d, h in h_in:
             d.copy_(h, non_blocking=True)
-        for name in Suite.ORDER:
-            getattr(suite, name)()
-        suite.step_no += 1
+        suite.step()
         for o, h in zip(outs, h_out):
             h.copy_(o, non_blocking=True)
 
     for _ in range(max(1, min(args.warmup, 2))):
         step()
     torch.cuda.synchronize()
-    k = max(1, min(args.steps, 5))
+    k = max(1, min(args.steps, 10))
     a = torch.cuda.Event(enable_timing=True)
     b = torch.cuda.Event(enable_timing=True)
     a.record(stream)
@@ -347,10 +378,10 @@ def oracle_sample(max_seconds=None):
     x1 = W.nvfp4_small().numpy()
     res["nvfp4_small"] = (x1.size, timed(lambda: oracle.quantize(
         x1, oracle.NVFP4, want_xhat=True, want_mask=True)))
-    x2 = f32(W.mxfp4_weight(shape=(256, 4096), seed=1))
+    x2 = f32(W.mxfp4_weight(shape=(2048, 4096), seed=1))
     res["mxfp4_weight"] = (x2.size, timed(lambda: oracle.quantize(
         x2, oracle.MXFP4, want_xhat=True, want_mask=True)))
-    x3 = f32(W.nvfp4_act(shape=(256, 8192), seed=2))
+    x3 = f32(W.nvfp4_act(shape=(1024, 8192), seed=2))
 
     def c3():
         q = oracle.quantize(x3, oracle.NVFP4, orient=oracle.ROWCOL, want_xhat=True,
@@ -363,21 +394,22 @@ def oracle_sample(max_seconds=None):
     res["nvfp4_act"] = (x3.size, time.perf_counter() - t)
     dy = W.bf16_bits(W.normal(x3.shape, 1.0, seed=12, dtype=__import__("torch").bfloat16))
     res["ste_backward"] = (dy.size, timed(lambda: oracle.ste_backward(dy, q3["row"]["mask"])))
-    x4 = f32(W.grad_2level(shape=(256, 4096), seed=3))
+    x4 = f32(W.grad_2level(shape=(2048, 4096), seed=3))
     res["grad_2level"] = (x4.size, timed(lambda: oracle.quantize(
         x4, oracle.NVFP4_2LEVEL, oracle.SR, 0x5EED)))
-    w = W.normal((512, 5760), 0.02, seed=4).to(__import__("torch").bfloat16)
+    w = W.normal((2880, 5760), 0.02, seed=4).to(__import__("torch").bfloat16)
     st = oracle.OsciState(f32(w), oracle.NVFP4)
-    d = W.master_update((512, 5760), 1).numpy()
+    d = W.master_update((2880, 5760), 1).numpy()
 
     def upd():
         out = st.step(d, offset=1)
         oracle.f32_to_bf16_bits(out["xhat"])
     res["osci_update"] = (w.numel(), timed(upd))
     res["osci_reset"] = (w.numel(), timed(lambda: st.reset(4.0)))
-    desc = ("oracle (scalar C, 1 thread) on: nvfp4_small full; mxfp4_weight 256 rows; "
-            "nvfp4_act 256 rows row+col; ste_backward 256x8192; grad_2level 256 rows SR; "
-            "osci update+reset on one [512, 5760] slice; rate scaled to the full step's bytes")
+    desc = ("oracle (scalar C, 1 thread) on: nvfp4_small full; mxfp4_weight 2048 rows; "
+            "nvfp4_act 1024 rows row+col; ste_backward 1024x8192; grad_2level 2048 rows SR; "
+            "osci update+reset on one full [2880, 5760] matrix; per-element rates scaled to "
+            "the full step's elements")
     return res, desc
 
 
@@ -397,7 +429,11 @@ FULL_ELEMS = {"nvfp4_small": 256 * 1024, "mxfp4_weight": 4096 * 4096,
               "osci_reset": 32 * 2 * 2880 * 5760}
 
 
-def config_block():
+def config_block(names=None, experts=None):
+    if names is not None and (list(names) != list(Suite.ORDER) or experts):
+        return {"workload": "subset: " + ",".join(names) + (f"; moe experts={experts}"
+                                                           if experts else ""),
+                "l2": "no flush between steps", "bytes": "algorithmic"}
     return {"workload": "fake-quant suite over the five synthetic workloads (one pass each per "
                         "step): nvfp4_small fp32 256x1024 NVFP4 RNE; mxfp4_weight bf16 "
                         "4096x4096 MXFP4 RNE quant+dequant; nvfp4_act bf16 8192x8192 NVFP4 "
@@ -412,11 +448,15 @@ def config_block():
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--only", nargs="*", choices=Suite.ORDER, default=None,
+                    help="run only these workloads (profiling a single kernel)")
+    ap.add_argument("--experts", type=int, default=None,
+                    help="MoE experts in moe_qat (default: the full 32)")
     args = ap.parse_args()
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -443,13 +483,13 @@ def main():
         ms_step = ms / args.steps
         value = world * total_bytes * args.steps / (ms / 1e3) / 1e9
         per = {}
-        for n in Suite.ORDER:
+        for n in suite.names:
             t = per_ms[n] / 1e3
             per[n] = {"gbs": round(bps[n] / t / 1e9, 1),
                       "gelem_s": round(suite.elems[n] / t / 1e9, 3),
                       "ms": round(per_ms[n], 4),
                       "frac_hbm": round(bps[n] / t / 1e9 / peak, 3)}
-        dom = max(Suite.ORDER, key=lambda n: per_ms[n])
+        dom = max(suite.names, key=lambda n: per_ms[n])
         achieved = bps[dom] / (per_ms[dom] / 1e3) / 1e9
         tr = NCU_TRAFFIC.get(dom, {})
         traffic = tr.get("bytes") if tr.get("src_sha256") == src_sha("k_osci.cu") else None
@@ -459,7 +499,7 @@ def main():
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
             "data": "synthetic (seeded torch generators, shapes/distributions of the five "
                     "workloads)",
-            "config": config_block(),
+            "config": config_block(suite.names, args.experts),
             "per_workload": per,
             "roofline": {"bound": "hbm", "kernel": dom + (" (osci_pass_a + osci_pass_b)"
                                                            if dom == "osci_update" else ""),
@@ -468,7 +508,7 @@ def main():
                          "unit": "GB/s", "frac": round(achieved / peak, 3),
                          "traffic": traffic,
                          "algorithmic_bytes_per_launch": int(bps[dom])},
-            "gpu_launches": sum(LAUNCHES_PER_STEP.values()) * args.steps,
+            "gpu_launches": sum(LAUNCHES_PER_STEP[n] for n in suite.names) * args.steps,
             "clocks": clk,
         }
         if e2e is not None:
@@ -477,7 +517,7 @@ def main():
                            "unit": UNIT, "h2d_bytes_per_step": e2e["h2d"],
                            "d2h_bytes_per_step": e2e["d2h"], "steps": e2e["steps"],
                            "ms_per_step": round(e2e["ms_total"] / e2e["steps"], 3)}
-        if not args.no_cpu_baseline and world == 1:
+        if not args.no_cpu_baseline and world == 1 and not args.only and not args.experts:
             sample, desc = oracle_sample()
             gbs, secs = oracle_gbs(sample, suite.elems)
             line["cpu_baseline"] = {"value": round(gbs, 4), "unit": UNIT, "cores": 1,

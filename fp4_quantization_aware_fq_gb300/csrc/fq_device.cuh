@@ -89,22 +89,6 @@ __device__ __forceinline__ uint32_t e2m1_rn_pack8(const float *y)
     return out;
 }
 
-__device__ __forceinline__ uint32_t e2m1_rn_pack4(const float *y)
-{
-    uint32_t out;
-    asm("{\n\t"
-        ".reg .b8 q0, q1;\n\t"
-        ".reg .b16 h;\n\t"
-        "cvt.rn.satfinite.e2m1x2.f32 q0, %2, %1;\n\t"
-        "cvt.rn.satfinite.e2m1x2.f32 q1, %4, %3;\n\t"
-        "mov.b16 h, {q0, q1};\n\t"
-        "cvt.u32.u16 %0, h;\n\t"
-        "}"
-        : "=r"(out)
-        : "f"(y[0]), "f"(y[1]), "f"(y[2]), "f"(y[3]));
-    return out;
-}
-
 // E2M1 magnitude of code bits 0..2 as an FP32 bit pattern: 0, 0.5, then
 // (1 + m/2) * 2^(e-1) for exponent e >= 1.
 __device__ __forceinline__ float e2m1_value(uint32_t code)
@@ -113,26 +97,6 @@ __device__ __forceinline__ float e2m1_value(uint32_t code)
     uint32_t bits = (mag >= 2u) ? ((mag + 252u) << 22) : (mag ? 0x3F000000u : 0u);
     bits |= (code & 8u) << 28;
     return __uint_as_float(bits);
-}
-
-// Stochastic rounding of one value given a 16-bit uniform u: with lo the
-// largest grid magnitude <= |y|, round up iff u < frac * 65536.  In each
-// binade of the grid the scaled value z = |y| * {2, 1, 1/2} has unit spacing,
-// so lo and frac come from floor(z) exactly.
-__device__ __forceinline__ uint32_t e2m1_sr(float y, uint32_t u)
-{
-    const uint32_t sign = (__float_as_uint(y) >> 28) & 8u;
-    const float a = fabsf(y);
-    if (!(a < 6.0f))
-        return sign | 7u;
-    const bool lo2 = a < 2.0f, lo4 = a < 4.0f;
-    const float s = lo2 ? 2.0f : (lo4 ? 1.0f : 0.5f);
-    const uint32_t base = lo2 ? 0u : (lo4 ? 2u : 4u);
-    const float z = __fmul_rn(a, s);
-    const float f = floorf(z);
-    const float t = __fmul_rn(__fsub_rn(z, f), 65536.0f);
-    const uint32_t up = (__uint2float_rn(u) < t) ? 1u : 0u;
-    return sign | (base + (uint32_t)f + up);
 }
 
 // ---------------------------------------------------------------- E4M3
@@ -256,72 +220,99 @@ __device__ __forceinline__ uint32_t bf16x2_rn(float lo, float hi)
     return *reinterpret_cast<uint32_t *>(&h);
 }
 
-// ---------------------------------------------------------------- per-vector core
-// Result of quantizing one 16-byte input vector (E values) of a row-wise block.
-template <int E>
-struct VecQ {
-    float v[E];       // the input values (FP32)
-    uint32_t q;       // packed codes, element i in nibble i
-    uint32_t mbits;   // STE mask bits, element i in bit i
-    Scale sc;         // inner block scale
-    float s_o;        // outer scale (double block only)
-};
+// ---------------------------------------------------------------- per-block core
+// Dequantize 8 packed E2M1 codes to their grid values (exact in FP16, then
+// widened): element 2j comes from the low nibble of byte j.
+__device__ __forceinline__ void e2m1_decode8(uint32_t q, float *out)
+{
+    uint32_t h[4];
+    asm("{\n\t"
+        ".reg .b8 q0, q1, q2, q3;\n\t"
+        "mov.b32 {q0, q1, q2, q3}, %4;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %0, q0;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %1, q1;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %2, q2;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %3, q3;\n\t"
+        "}"
+        : "=r"(h[0]), "=r"(h[1]), "=r"(h[2]), "=r"(h[3])
+        : "r"(q));
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&h[i]));
+        out[2 * i] = f.x;
+        out[2 * i + 1] = f.y;
+    }
+}
 
-// Quantize the vector `raw` whose flat vector index in the tensor is `ch`
-// (flat element index ch * E).  All 32 lanes of the warp must call this
-// together: the block amax is combined with shuffles over the lanes that hold
-// the block.  s_g is the NVFP4 tensor scale (unused for the other formats).
-template <typename T, int FMT, int RND>
-__device__ __forceinline__ VecQ<VecInfo<T>::E> quant_vec(const uint4 &raw, int64_t ch, float s_g,
-                                                        uint64_t seed, uint32_t offset,
-                                                        uint32_t stream_id)
+// Stochastic rounding of y to the E2M1 grid given a 16-bit uniform u, as an
+// FP32 value on the grid (values at or above 6 come out >= 6 and saturate in
+// the final conversion).  With lo the grid magnitude at or below |y| and frac
+// its position in the gap, the result rounds up iff u < frac * 65536.
+//  |y| >= 1: the grid keeps one mantissa bit, frac * 65536 is the 22 dropped
+//    mantissa bits / 64, so adding 2^22 - 1 - 64u below the kept bit and
+//    truncating rounds up exactly when those bits exceed 64u.
+//  |y| < 1: the grid steps are 0.5, so with D = ceil(|y| * 2^17) the number of
+//    steps is (D + 65535 - u) >> 16 (D is exact: a power-of-two scaling).
+__device__ __forceinline__ float e2m1_sr_value(float y, uint32_t u)
+{
+    const uint32_t b = __float_as_uint(y);
+    const float a = fabsf(y);
+    const uint32_t hi = (b + (0x3FFFFFu - (u << 6))) & 0xFFC00000u;
+    const uint32_t d = __float2uint_ru(__fmul_rn(a, 131072.0f));
+    const uint32_t n = (d + 65535u - u) >> 16;
+    const uint32_t lo = (n ? (0x3E800000u + (n << 23)) : 0u) | (b & 0x80000000u);
+    return __uint_as_float(a < 1.0f ? lo : hi);
+}
+
+// Encode B values (already loaded as FP32) of one block under scale sc into
+// B/8 words of packed codes, and the block's STE mask bits (bit i = element i
+// inside [-6 s_eff, 6 s_eff]).  e0 is the flat index of the block's first
+// element in the tensor being quantized (Philox counter for SR).
+template <int B, int RND>
+__device__ __forceinline__ void encode_block(const float *v, const Scale &sc, uint64_t seed,
+                                             uint64_t e0, uint32_t stream_id, uint32_t offset,
+                                             uint32_t *q, uint32_t &mask)
+{
+#pragma unroll
+    for (int w = 0; w < B / 8; ++w) {
+        float y[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+            y[i] = __fmul_rn(v[w * 8 + i], sc.r);
+        if (RND == SR) {
+            const uint4 rb = sr_bits8(seed, (e0 >> 3) + w, stream_id, offset);
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+                y[i] = e2m1_sr_value(y[i], u16_of(rb, i));
+        }
+        q[w] = e2m1_rn_pack8(y);
+    }
+    // clip bit = sign of (lim - |x|): exact, since a non-zero difference of two
+    // floats never rounds to zero without flush-to-zero.
+    uint32_t clip = 0;
+#pragma unroll
+    for (int i = 0; i < B; ++i)
+        clip |= (__float_as_uint(__fsub_rn(sc.lim, fabsf(v[i]))) >> 31) << i;
+    mask = (B == 32) ? ~clip : (~clip & ((1u << B) - 1u));
+}
+
+// Block scale for one block; for the double block, s_outer is the outer scale.
+template <int FMT>
+__device__ __forceinline__ Scale block_scale(float amax_b, float s_outer)
+{
+    if (FMT == MXFP4)
+        return mx_scale(amax_b);
+    return nv_scale(amax_b, s_outer);
+}
+
+template <typename T, int N>
+__device__ __forceinline__ void load_block(const void *src, float *v)
 {
     constexpr int E = VecInfo<T>::E;
-    constexpr int L = FmtInfo<FMT>::B / E;  // lanes per inner block
-    constexpr int LO = 128 / E;             // lanes per outer block (double block)
-    VecQ<E> r;
-    unpack16<T>(raw, r.v);
-    float am = 0.0f;
 #pragma unroll
-    for (int i = 0; i < E; ++i)
-        am = fmaxf(am, fabsf(r.v[i]));
-    const float amb = group_max<L>(am);
-    r.s_o = 0.0f;
-    if (FMT == MXFP4) {
-        r.sc = mx_scale(amb);
-    } else if (FMT == NVFP4) {
-        r.sc = nv_scale(amb, s_g);
-    } else {
-        r.s_o = outer_scale(group_max<LO>(amb));
-        r.sc = nv_scale(amb, r.s_o);
-    }
-    float y[E];
-    r.mbits = 0;
-#pragma unroll
-    for (int i = 0; i < E; ++i) {
-        y[i] = __fmul_rn(r.v[i], r.sc.r);
-        r.mbits |= (fabsf(r.v[i]) <= r.sc.lim ? 1u : 0u) << i;
-    }
-    if (RND == RNE) {
-        r.q = (E == 8) ? e2m1_rn_pack8(y) : e2m1_rn_pack4(y);
-    } else {
-        const int64_t e0 = ch * E;
-        const uint4 rb = sr_bits8(seed, (uint64_t)e0 >> 3, stream_id, offset);
-        uint32_t q = 0;
-        if (E == 8) {
-#pragma unroll
-            for (int i = 0; i < E; ++i)
-                q |= e2m1_sr(y[i], u16_of(rb, i)) << (4 * i);
-        } else {
-            const bool hi = (e0 & 7) != 0;
-            const uint4 h = hi ? make_uint4(rb.z, rb.w, 0, 0) : make_uint4(rb.x, rb.y, 0, 0);
-#pragma unroll
-            for (int i = 0; i < E; ++i)
-                q |= e2m1_sr(y[i], u16_of(h, i)) << (4 * i);
-        }
-        r.q = q;
-    }
-    return r;
+    for (int k = 0; k < N / E; ++k)
+        unpack16<T>(ld16((const char *)src + 16 * k), v + k * E);
 }
 
 }  // namespace fqk
+

@@ -30,9 +30,10 @@ __global__ void __launch_bounds__(kAuxThreads) dequant_kernel(DequantArgs a)
             s_outer = __ldg(a.tscale + e0 / 128);
         const float s_eff = stored_s_eff<FMT>(sc, s_outer);
         float xh[8];
+        e2m1_decode8(q, xh);
 #pragma unroll
         for (int i = 0; i < 8; ++i)
-            xh[i] = __fmul_rn(e2m1_value(q >> (4 * i)), s_eff);
+            xh[i] = __fmul_rn(xh[i], s_eff);
         if (a.y_bf16) {
             uint4 o = make_uint4(bf16x2_rn(xh[0], xh[1]), bf16x2_rn(xh[2], xh[3]),
                                  bf16x2_rn(xh[4], xh[5]), bf16x2_rn(xh[6], xh[7]));

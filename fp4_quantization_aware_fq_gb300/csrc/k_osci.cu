@@ -93,12 +93,12 @@ __global__ void __launch_bounds__(kOsciThreads) osci_pass_a(const __grid_constan
     }
 }
 
+// Pass B: one thread per block of 16 (32 for MXFP4) master weights.
 template <int FMT, int RND>
 __global__ void __launch_bounds__(kOsciThreads) osci_pass_b(const __grid_constant__ OsciArgs a)
 {
-    constexpr int E = 4;
-    constexpr int L = FmtInfo<FMT>::B / E;
-    constexpr int LO = 128 / E;
+    constexpr int B = FmtInfo<FMT>::B;
+    constexpr int BPTILE = kOsciTileChunks * 4 / B;  // blocks per tile
     const int64_t ntiles = a.tile_start[a.ntensors];
     int t = 0;
     const int lane = threadIdx.x & 31;
@@ -106,69 +106,115 @@ __global__ void __launch_bounds__(kOsciThreads) osci_pass_b(const __grid_constan
         while (a.tile_start[t + 1] <= tile)
             ++t;
         const OsciTensor &T = a.t[t];
-        const int64_t nch = T.n / 4;
-        const int64_t cbeg = (tile - a.tile_start[t]) * kOsciTileChunks;
+        const int64_t nblk = T.n / B;
+        const int64_t bbeg = (tile - a.tile_start[t]) * BPTILE;
         float s_g = 0.0f, s_gp = 0.0f;
         if (FMT == NVFP4) {
             s_g = outer_scale(__ldg(a.amax + t));
             s_gp = __ldg(T.ptscale);
-            if (cbeg == 0 && threadIdx.x == 0)
+            if (bbeg == 0 && threadIdx.x == 0)
                 T.ntscale[0] = s_g;
         }
-        for (int k0 = 0; k0 < kOsciTileChunks; k0 += kOsciThreads * kOsciU) {
-            uint4 raw[kOsciU];
+        for (int k = 0; k < BPTILE; k += kOsciThreads) {
+            const int64_t blk = bbeg + k + threadIdx.x;
+            const bool valid = k + (int)threadIdx.x < BPTILE && blk < nblk;
+            float v[B];
+            if (valid) {
 #pragma unroll
-            for (int k = 0; k < kOsciU; ++k) {
-                const int64_t ch = cbeg + k0 + k * kOsciThreads + threadIdx.x;
-                raw[k] = ch < nch ? *reinterpret_cast<const uint4 *>(T.master + ch * 4)
-                                  : make_uint4(0, 0, 0, 0);
+                for (int j = 0; j < B / 4; ++j) {
+                    const float4 w = ldf4_rw(T.master + blk * B + 4 * j);
+                    v[4 * j] = w.x;
+                    v[4 * j + 1] = w.y;
+                    v[4 * j + 2] = w.z;
+                    v[4 * j + 3] = w.w;
+                }
+            } else {
+#pragma unroll
+                for (int i = 0; i < B; ++i)
+                    v[i] = 0.0f;
             }
+            float am = 0.0f;
 #pragma unroll
-            for (int k = 0; k < kOsciU; ++k) {
-                const int64_t ch = cbeg + k0 + k * kOsciThreads + threadIdx.x;
-                const bool valid = ch < nch;
-                const VecQ<E> r = quant_vec<float, FMT, RND>(raw[k], ch, s_g, a.seed, a.offset, 0u);
-                const uint32_t mpair = __shfl_down_sync(0xFFFFFFFFu, r.mbits, 1);
-                if (!valid)
-                    continue;
-                // previous quantized value of these 4 weights
-                const uint32_t qp = __ldg(reinterpret_cast<const uint16_t *>(T.pcodes) + ch);
-                const uint32_t scp = __ldg(T.pscales + ch / L);
-                float so_p = s_gp;
-                if (FMT == NV2L)
-                    so_p = __ldg(T.ptscale + ch / LO);
-                const float seff_p = stored_s_eff<FMT>(scp, so_p);
-                float xh[E], xp[E];
+            for (int i = 0; i < B; ++i)
+                am = fmaxf(am, fabsf(v[i]));
+            float s_o = s_g;
+            if (FMT == NV2L)
+                s_o = outer_scale(group_max<8>(am));
+            const Scale sc = block_scale<FMT>(am, s_o);
+            uint32_t q[B / 8];
+            uint32_t mask;
+            encode_block<B, RND>(v, sc, a.seed, (uint64_t)blk * B, 0u, a.offset, q, mask);
+            if (!valid)
+                continue;
+            // previous quantized value of this block
+            uint32_t qp[B / 8];
+            if (B == 16) {
+                const uint2 p2 = __ldg(reinterpret_cast<const uint2 *>(T.pcodes) + blk);
+                qp[0] = p2.x;
+                qp[1] = p2.y;
+            } else {
+                const uint4 p4 = __ldg(reinterpret_cast<const uint4 *>(T.pcodes) + blk);
+                qp[0] = p4.x;
+                qp[1] = p4.y;
+                qp[2] = p4.z;
+                qp[3] = p4.w;
+            }
+            float so_p = s_gp;
+            if (FMT == NV2L)
+                so_p = __ldg(T.ptscale + (blk >> 3));
+            const float seff_p = stored_s_eff<FMT>(__ldg(T.pscales + blk), so_p);
 #pragma unroll
-                for (int i = 0; i < E; ++i) {
-                    xh[i] = __fmul_rn(e2m1_value(r.q >> (4 * i)), r.sc.s_eff);
-                    xp[i] = __fmul_rn(e2m1_value(qp >> (4 * i)), seff_p);
+            for (int w = 0; w < B / 8; ++w) {
+                float xh[8], xp[8];
+                e2m1_decode8(q[w], xh);
+                e2m1_decode8(qp[w], xp);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    xh[i] = __fmul_rn(xh[i], sc.s_eff);
+                    xp[i] = __fmul_rn(xp[i], seff_p);
                 }
-                float4 dq = ldf4_rw(T.dist_q + ch * 4);
-                dq.x = __fadd_rn(dq.x, fabsf(__fsub_rn(xh[0], xp[0])));
-                dq.y = __fadd_rn(dq.y, fabsf(__fsub_rn(xh[1], xp[1])));
-                dq.z = __fadd_rn(dq.z, fabsf(__fsub_rn(xh[2], xp[2])));
-                dq.w = __fadd_rn(dq.w, fabsf(__fsub_rn(xh[3], xp[3])));
-                stf4(T.dist_q + ch * 4, dq);
-                reinterpret_cast<uint16_t *>(T.ncodes)[ch] = (uint16_t)r.q;
-                if ((lane % L) == 0)
-                    T.nscales[ch / L] = (uint8_t)r.sc.code;
-                if (FMT == NV2L && (lane % LO) == 0)
-                    T.ntscale[ch / LO] = r.s_o;
+                float *dqp = T.dist_q + blk * B + w * 8;
+                float4 d0 = ldf4_rw(dqp), d1 = ldf4_rw(dqp + 4);
+                d0.x = __fadd_rn(d0.x, fabsf(__fsub_rn(xh[0], xp[0])));
+                d0.y = __fadd_rn(d0.y, fabsf(__fsub_rn(xh[1], xp[1])));
+                d0.z = __fadd_rn(d0.z, fabsf(__fsub_rn(xh[2], xp[2])));
+                d0.w = __fadd_rn(d0.w, fabsf(__fsub_rn(xh[3], xp[3])));
+                d1.x = __fadd_rn(d1.x, fabsf(__fsub_rn(xh[4], xp[4])));
+                d1.y = __fadd_rn(d1.y, fabsf(__fsub_rn(xh[5], xp[5])));
+                d1.z = __fadd_rn(d1.z, fabsf(__fsub_rn(xh[6], xp[6])));
+                d1.w = __fadd_rn(d1.w, fabsf(__fsub_rn(xh[7], xp[7])));
+                stf4(dqp, d0);
+                stf4(dqp + 4, d1);
                 if (T.xhat) {
-                    if (a.xhat_bf16)
-                        reinterpret_cast<uint2 *>(T.xhat)[ch] =
-                            make_uint2(bf16x2_rn(xh[0], xh[1]), bf16x2_rn(xh[2], xh[3]));
-                    else
-                        reinterpret_cast<float4 *>(T.xhat)[ch] = make_float4(xh[0], xh[1], xh[2], xh[3]);
+                    if (a.xhat_bf16) {
+                        *reinterpret_cast<uint4 *>((char *)T.xhat + (blk * B + w * 8) * 2) =
+                            make_uint4(bf16x2_rn(xh[0], xh[1]), bf16x2_rn(xh[2], xh[3]),
+                                       bf16x2_rn(xh[4], xh[5]), bf16x2_rn(xh[6], xh[7]));
+                    } else {
+                        float *xo = reinterpret_cast<float *>(T.xhat) + blk * B + w * 8;
+                        stf4(xo, make_float4(xh[0], xh[1], xh[2], xh[3]));
+                        stf4(xo + 4, make_float4(xh[4], xh[5], xh[6], xh[7]));
+                    }
                 }
-                if (T.mask && (lane & 1) == 0)
-                    T.mask[ch >> 1] = (uint8_t)(r.mbits | (mpair << 4));
+            }
+            if (B == 16)
+                reinterpret_cast<uint2 *>(T.ncodes)[blk] = make_uint2(q[0], q[1]);
+            else
+                reinterpret_cast<uint4 *>(T.ncodes)[blk] = make_uint4(q[0], q[1], q[2], q[3]);
+            T.nscales[blk] = (uint8_t)sc.code;
+            if (FMT == NV2L && (lane & 7) == 0)
+                T.ntscale[blk >> 3] = s_o;
+            if (T.mask) {
+                if (B == 16)
+                    reinterpret_cast<uint16_t *>(T.mask)[blk] = (uint16_t)mask;
+                else
+                    reinterpret_cast<uint32_t *>(T.mask)[blk] = mask;
             }
         }
     }
 }
 
+// Reset: one thread per 16-byte chunk, four chunks in flight per thread.
 template <int FMT>
 __global__ void __launch_bounds__(kOsciThreads) osci_reset_kernel(const __grid_constant__ OsciArgs a)
 {
@@ -186,33 +232,43 @@ __global__ void __launch_bounds__(kOsciThreads) osci_reset_kernel(const __grid_c
         float s_g = 0.0f;
         if (FMT == NVFP4)
             s_g = __ldg(T.ptscale);
-        for (int k = 0; k < kOsciTileChunks; k += kOsciThreads) {
-            const int64_t ch = cbeg + k + threadIdx.x;
-            if (ch >= nch)
-                continue;
-            const float4 dq = ldf4_rw(T.dist_q + ch * 4);
-            const float4 dm = ldf4_rw(T.dist_m + ch * 4);
-            const float q4[4] = {dq.x, dq.y, dq.z, dq.w};
-            const float m4[4] = {dm.x, dm.y, dm.z, dm.w};
-            uint32_t hit = 0;
+        for (int k0 = 0; k0 < kOsciTileChunks; k0 += kOsciThreads * kOsciU) {
+            float4 dq[kOsciU], dm[kOsciU];
 #pragma unroll
-            for (int i = 0; i < 4; ++i)
-                hit |= (q4[i] > __fmul_rn(a.threshold, m4[i]) ? 1u : 0u) << i;
-            if (hit) {
-                const uint32_t q = __ldg(reinterpret_cast<const uint16_t *>(T.pcodes) + ch);
-                const uint32_t sc = __ldg(T.pscales + ch / L);
-                float so = s_g;
-                if (FMT == NV2L)
-                    so = __ldg(T.ptscale + ch / LO);
-                const float s_eff = stored_s_eff<FMT>(sc, so);
+            for (int k = 0; k < kOsciU; ++k) {
+                const int64_t ch = cbeg + k0 + k * kOsciThreads + threadIdx.x;
+                if (ch < nch) {
+                    dq[k] = ldf4_rw(T.dist_q + ch * 4);
+                    dm[k] = ldf4_rw(T.dist_m + ch * 4);
+                }
+            }
+#pragma unroll
+            for (int k = 0; k < kOsciU; ++k) {
+                const int64_t ch = cbeg + k0 + k * kOsciThreads + threadIdx.x;
+                if (ch >= nch)
+                    continue;
+                const float q4[4] = {dq[k].x, dq[k].y, dq[k].z, dq[k].w};
+                const float m4[4] = {dm[k].x, dm[k].y, dm[k].z, dm[k].w};
+                uint32_t hit = 0;
 #pragma unroll
                 for (int i = 0; i < 4; ++i)
-                    if ((hit >> i) & 1u)
-                        T.master[ch * 4 + i] = __fmul_rn(e2m1_value(q >> (4 * i)), s_eff);
-                cnt += __popc(hit);
+                    hit |= (q4[i] > __fmul_rn(a.threshold, m4[i]) ? 1u : 0u) << i;
+                if (hit) {
+                    const uint32_t q = __ldg(reinterpret_cast<const uint16_t *>(T.pcodes) + ch);
+                    const uint32_t sc = __ldg(T.pscales + ch / L);
+                    float so = s_g;
+                    if (FMT == NV2L)
+                        so = __ldg(T.ptscale + ch / LO);
+                    const float s_eff = stored_s_eff<FMT>(sc, so);
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+                        if ((hit >> i) & 1u)
+                            T.master[ch * 4 + i] = __fmul_rn(e2m1_value(q >> (4 * i)), s_eff);
+                    cnt += __popc(hit);
+                }
+                stf4(T.dist_q + ch * 4, make_float4(0.f, 0.f, 0.f, 0.f));
+                stf4(T.dist_m + ch * 4, make_float4(0.f, 0.f, 0.f, 0.f));
             }
-            stf4(T.dist_q + ch * 4, make_float4(0.f, 0.f, 0.f, 0.f));
-            stf4(T.dist_m + ch * 4, make_float4(0.f, 0.f, 0.f, 0.f));
         }
     }
     if (a.n_reset) {

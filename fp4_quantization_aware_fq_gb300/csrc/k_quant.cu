@@ -59,94 +59,108 @@ __global__ void __launch_bounds__(kThreads) amax_kernel(const void *__restrict__
 }
 
 // ------------------------------------------------------------------ row-wise core
-// Quantize one 16-byte vector (E values) of a row-wise block.  `ch` is the
-// flat vector index in the tensor, so the flat element index is ch * E.  All
-// 32 lanes of the warp must call this together (block amax uses shuffles).
-template <typename T, int FMT, int RND>
-__device__ __forceinline__ void row_vector(const uint4 &raw, int64_t ch, bool valid, float s_g,
-                                           uint8_t *__restrict__ codes,
-                                           uint8_t *__restrict__ scales,
-                                           float *__restrict__ tscale, void *__restrict__ xhat,
-                                           int xhat_bf16, uint8_t *__restrict__ mask,
-                                           uint64_t seed, uint32_t offset, uint32_t stream_id)
+// Outputs of the row-wise pass (any pointer may be NULL: not written).
+struct RowOut {
+    uint8_t *codes;
+    uint8_t *scales;
+    float *tscale;
+    void *xhat;
+    int xhat_bf16;
+    uint8_t *mask;
+};
+
+// Quantize one row-wise block of B values held by this thread.  `blk` is the
+// flat block index in the tensor (flat element index blk * B).  For the double
+// block, the 8 inner blocks of an outer block sit on 8 consecutive lanes, and
+// all 32 lanes of the warp must call this together.
+template <int FMT, int RND>
+__device__ __forceinline__ void row_block(const float *v, int64_t blk, bool valid, float s_g,
+                                          const RowOut &o, uint64_t seed, uint32_t offset,
+                                          uint32_t stream_id)
 {
-    constexpr int E = VecInfo<T>::E;
-    constexpr int L = FmtInfo<FMT>::B / E;
-    constexpr int LO = 128 / E;
-    const VecQ<E> r = quant_vec<T, FMT, RND>(raw, ch, s_g, seed, offset, stream_id);
-    const uint32_t q = r.q, mbits = r.mbits;
-    const Scale sc = r.sc;
-    const float s_o = r.s_o;
-    const int lane = threadIdx.x & 31;
-    uint32_t mpair = 0;
-    if (E == 4)
-        mpair = __shfl_down_sync(0xFFFFFFFFu, mbits, 1);
+    constexpr int B = FmtInfo<FMT>::B;
+    float am = 0.0f;
+#pragma unroll
+    for (int i = 0; i < B; ++i)
+        am = fmaxf(am, fabsf(v[i]));
+    float s_o = s_g;
+    if (FMT == NV2L)
+        s_o = outer_scale(group_max<8>(am));
+    const Scale sc = block_scale<FMT>(am, s_o);
+    uint32_t q[B / 8];
+    uint32_t mask;
+    encode_block<B, RND>(v, sc, seed, (uint64_t)blk * B, stream_id, offset, q, mask);
     if (!valid)
         return;
-    if (codes) {
-        if (E == 8)
-            *reinterpret_cast<uint32_t *>(codes + ch * 4) = q;
+    const int lane = threadIdx.x & 31;
+    if (o.codes) {
+        if (B == 16)
+            *reinterpret_cast<uint2 *>(o.codes + blk * 8) = make_uint2(q[0], q[1]);
         else
-            *reinterpret_cast<uint16_t *>(codes + ch * 2) = (uint16_t)q;
-        if ((lane % L) == 0)
-            scales[ch / L] = (uint8_t)sc.code;
-        if (FMT == NV2L && (lane % LO) == 0)
-            tscale[ch / LO] = s_o;
+            *reinterpret_cast<uint4 *>(o.codes + blk * 16) = make_uint4(q[0], q[1], q[2], q[3]);
+        o.scales[blk] = (uint8_t)sc.code;
+        if (FMT == NV2L && (lane & 7) == 0)
+            o.tscale[blk >> 3] = s_o;
     }
-    if (xhat) {
-        float xh[E];
+    if (o.xhat) {
 #pragma unroll
-        for (int i = 0; i < E; ++i)
-            xh[i] = __fmul_rn(e2m1_value(q >> (4 * i)), sc.s_eff);
-        if (xhat_bf16) {
-            if (E == 8) {
-                uint4 o = make_uint4(bf16x2_rn(xh[0], xh[1]), bf16x2_rn(xh[2], xh[3]),
-                                     bf16x2_rn(xh[4], xh[5]), bf16x2_rn(xh[6], xh[7]));
-                *reinterpret_cast<uint4 *>((char *)xhat + ch * 16) = o;
+        for (int w = 0; w < B / 8; ++w) {
+            float xh[8];
+            e2m1_decode8(q[w], xh);
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+                xh[i] = __fmul_rn(xh[i], sc.s_eff);
+            if (o.xhat_bf16) {
+                *reinterpret_cast<uint4 *>((char *)o.xhat + (blk * B + w * 8) * 2) =
+                    make_uint4(bf16x2_rn(xh[0], xh[1]), bf16x2_rn(xh[2], xh[3]),
+                               bf16x2_rn(xh[4], xh[5]), bf16x2_rn(xh[6], xh[7]));
             } else {
-                uint2 o = make_uint2(bf16x2_rn(xh[0], xh[1]), bf16x2_rn(xh[2], xh[3]));
-                *reinterpret_cast<uint2 *>((char *)xhat + ch * 8) = o;
-            }
-        } else {
-            float4 *dst = reinterpret_cast<float4 *>((char *)xhat + ch * E * 4);
-            dst[0] = make_float4(xh[0], xh[1], xh[2], xh[3]);
-            if (E == 8)
+                float4 *dst = reinterpret_cast<float4 *>((char *)o.xhat + (blk * B + w * 8) * 4);
+                dst[0] = make_float4(xh[0], xh[1], xh[2], xh[3]);
                 dst[1] = make_float4(xh[4], xh[5], xh[6], xh[7]);
+            }
         }
     }
-    if (mask) {
-        if (E == 8)
-            mask[ch] = (uint8_t)mbits;
-        else if ((lane & 1) == 0)
-            mask[ch >> 1] = (uint8_t)(mbits | (mpair << 4));
+    if (o.mask) {
+        if (B == 16)
+            reinterpret_cast<uint16_t *>(o.mask)[blk] = (uint16_t)mask;
+        else
+            reinterpret_cast<uint32_t *>(o.mask)[blk] = mask;
     }
 }
 
+// One thread per block; each iteration a thread holds BPT blocks' loads in
+// flight (about 64 bytes).
 template <typename T, int FMT, int RND>
 __global__ void __launch_bounds__(kThreads) row_kernel(RowArgs a)
 {
-    constexpr int E = VecInfo<T>::E;
-    constexpr int U = 4;
-    const int64_t nch = a.n / E;
+    constexpr int B = FmtInfo<FMT>::B;
+    constexpr int BPT = (B * sizeof(T) >= 64) ? 1 : 2;
+    const int64_t nblk = a.n / B;
     float s_g = 0.0f;
     if (FMT == NVFP4) {
         s_g = outer_scale(*a.amax);
         if (blockIdx.x == 0 && threadIdx.x == 0 && a.tscale)
             a.tscale[0] = s_g;
     }
-    const int64_t stride = (int64_t)gridDim.x * kThreads * U;
-    for (int64_t base = (int64_t)blockIdx.x * kThreads * U; base < nch; base += stride) {
-        uint4 raw[U];
+    const RowOut o{a.codes, a.scales, a.tscale, a.xhat, a.xhat_bf16, a.mask};
+    const int64_t stride = (int64_t)gridDim.x * kThreads * BPT;
+    for (int64_t base = (int64_t)blockIdx.x * kThreads * BPT; base < nblk; base += stride) {
+        float v[BPT][B];
 #pragma unroll
-        for (int k = 0; k < U; ++k) {
-            const int64_t ch = base + k * kThreads + threadIdx.x;
-            raw[k] = ch < nch ? ld16((const char *)a.x + ch * 16) : make_uint4(0, 0, 0, 0);
+        for (int k = 0; k < BPT; ++k) {
+            const int64_t blk = base + k * kThreads + threadIdx.x;
+            if (blk < nblk)
+                load_block<T, B>((const char *)a.x + blk * B * (int64_t)sizeof(T), v[k]);
+            else
+#pragma unroll
+                for (int i = 0; i < B; ++i)
+                    v[k][i] = 0.0f;
         }
 #pragma unroll
-        for (int k = 0; k < U; ++k) {
-            const int64_t ch = base + k * kThreads + threadIdx.x;
-            row_vector<T, FMT, RND>(raw[k], ch, ch < nch, s_g, a.codes, a.scales, a.tscale,
-                                    a.xhat, a.xhat_bf16, a.mask, a.seed, a.offset, a.stream_id);
+        for (int k = 0; k < BPT; ++k) {
+            const int64_t blk = base + k * kThreads + threadIdx.x;
+            row_block<FMT, RND>(v[k], blk, blk < nblk, s_g, o, a.seed, a.offset, a.stream_id);
         }
     }
 }
@@ -157,6 +171,7 @@ struct TileShape {
     static constexpr int TR = (FMT == NV2L) ? 128 : 64;  // tile rows
     static constexpr int TC = (FMT == NV2L) ? 128 : 64;  // tile cols
     static constexpr int BC = FmtInfo<FMT>::B;           // column block (rows)
+    static constexpr int CP = TR / 2 + 8;                // staged code bytes per column (padded)
 };
 
 template <typename T, int FMT>
@@ -164,7 +179,7 @@ constexpr size_t tile_smem_bytes()
 {
     using S = TileShape<FMT>;
     return (size_t)S::TR * S::TC * sizeof(T)          // x tile
-           + (size_t)S::TC * (S::TR / 2)              // staged column codes
+           + (size_t)S::TC * S::CP                    // staged column codes
            + (size_t)S::TC * (S::TR / S::BC)          // staged column scales
            + (FMT == NV2L ? (size_t)S::TC * (S::TR / S::BC) * 4 : 0);  // inner amax
 }
@@ -174,14 +189,15 @@ __global__ void __launch_bounds__(kThreads) tile_kernel(TileArgs a)
 {
     using S = TileShape<FMT>;
     constexpr int E = VecInfo<T>::E;
-    constexpr int TR = S::TR, TC = S::TC, BC = S::BC;
-    constexpr int VPR = TC / E;  // 16-byte vectors per tile row
-    constexpr int NRB = TR / BC;  // column blocks per tile column
+    constexpr int TR = S::TR, TC = S::TC, BC = S::BC, CP = S::CP;
+    constexpr int BR = FmtInfo<FMT>::B;  // row block
+    constexpr int RBPR = TC / BR;         // row blocks per tile row
+    constexpr int NRB = TR / BC;          // column blocks per tile column
     extern __shared__ __align__(16) unsigned char smem[];
     T *tile = reinterpret_cast<T *>(smem);
-    uint8_t *ccs = smem + (size_t)TR * TC * sizeof(T);   // [TC][TR/2]
-    uint8_t *css = ccs + (size_t)TC * (TR / 2);          // [TC][NRB]
-    float *am16 = reinterpret_cast<float *>(css + (size_t)TC * NRB);  // [NRB][TC] (double block)
+    uint8_t *ccs = smem + (size_t)TR * TC * sizeof(T);   // [TC][CP]
+    uint8_t *css = ccs + (size_t)TC * CP;                // [TC][NRB]
+    float *am16 = reinterpret_cast<float *>(css + (size_t)TC * NRB);  // [NRB][TC]
 
     const int64_t r0 = (int64_t)blockIdx.y * TR;
     const int64_t c0 = (int64_t)blockIdx.x * TC;
@@ -197,31 +213,26 @@ __global__ void __launch_bounds__(kThreads) tile_kernel(TileArgs a)
         }
     }
 
-    // Phase 1: load the tile (coalesced 16-byte vectors along rows), stage it,
-    // and run the row-wise pass on the registers.
-    constexpr int NV = TR * VPR / kThreads;
-    uint4 raw[NV];
+    // Phase 1: each thread loads whole row blocks (16-byte vectors), stages
+    // them in shared memory and, when asked, runs the row-wise pass on them.
+    const RowOut o{a.rcodes, a.rscales, a.rtscale, a.xhat, a.xhat_bf16, a.mask};
+    for (int t = threadIdx.x; t < TR * RBPR; t += kThreads) {
+        const int tr = t / RBPR, tb = t % RBPR;
+        const int64_t gr = r0 + tr, gc = c0 + (int64_t)tb * BR;
+        const bool valid = gr < rows && gc < cols;
+        float v[BR];
+        uint4 raw[BR / E];
 #pragma unroll
-    for (int k = 0; k < NV; ++k) {
-        const int q = k * kThreads + threadIdx.x;
-        const int tr = q / VPR, tv = q % VPR;
-        const int64_t gr = r0 + tr, gc = c0 + (int64_t)tv * E;
-        raw[k] = (gr < rows && gc < cols)
-                     ? ld16((const char *)a.x + (gr * cols + gc) * (int64_t)sizeof(T))
-                     : make_uint4(0, 0, 0, 0);
-    }
+        for (int k = 0; k < BR / E; ++k)
+            raw[k] = valid ? ld16((const char *)a.x + ((gr * cols + gc) + k * E) * (int64_t)sizeof(T))
+                           : make_uint4(0, 0, 0, 0);
 #pragma unroll
-    for (int k = 0; k < NV; ++k) {
-        const int q = k * kThreads + threadIdx.x;
-        const int tr = q / VPR, tv = q % VPR;
-        *reinterpret_cast<uint4 *>(tile + tr * TC + tv * E) = raw[k];
-        if (a.do_row) {
-            const int64_t gr = r0 + tr, gc = c0 + (int64_t)tv * E;
-            const bool valid = gr < rows && gc < cols;
-            const int64_t ch = (gr * cols + gc) / E;
-            row_vector<T, FMT, RND>(raw[k], ch, valid, s_g, a.rcodes, a.rscales, a.rtscale,
-                                    a.xhat, a.xhat_bf16, a.mask, a.seed, a.offset, 0u);
+        for (int k = 0; k < BR / E; ++k) {
+            *reinterpret_cast<uint4 *>(tile + tr * TC + tb * BR + k * E) = raw[k];
+            unpack16<T>(raw[k], v + k * E);
         }
+        if (a.do_row)
+            row_block<FMT, RND>(v, (gr * cols + gc) / BR, valid, s_g, o, a.seed, a.offset, 0u);
     }
     __syncthreads();
 
@@ -249,42 +260,26 @@ __global__ void __launch_bounds__(kThreads) tile_kernel(TileArgs a)
             v[i] = static_cast<float>(tile[(rb * BC + i) * TC + c]);
             m = fmaxf(m, fabsf(v[i]));
         }
-        Scale sc;
-        if (FMT == MXFP4) {
-            sc = mx_scale(m);
-        } else if (FMT == NVFP4) {
-            sc = nv_scale(m, s_g);
-        } else {
+        float s_o = s_g;
+        if (FMT == NV2L) {
             float mo = 0.0f;
 #pragma unroll
             for (int j = 0; j < NRB; ++j)
                 mo = fmaxf(mo, am16[j * TC + c]);
-            const float s_o = outer_scale(mo);
-            sc = nv_scale(m, s_o);
+            s_o = outer_scale(mo);
             if (rb == 0)
                 a.ctscale[gc * (rows / 128) + r0 / 128] = s_o;
         }
-        uint32_t *dst = reinterpret_cast<uint32_t *>(ccs + c * (TR / 2) + rb * (BC / 2));
+        const Scale sc = block_scale<FMT>(m, s_o);
+        uint32_t q[BC / 8];
+        uint32_t unused_mask;
+        // flat index in X^T of the block's first element
+        encode_block<BC, RND>(v, sc, a.seed, (uint64_t)gc * (uint64_t)rows + (uint64_t)gr0, 1u,
+                              a.offset, q, unused_mask);
+        uint32_t *dst = reinterpret_cast<uint32_t *>(ccs + c * CP + rb * (BC / 2));
 #pragma unroll
-        for (int w = 0; w < BC / 8; ++w) {
-            float y[8];
-#pragma unroll
-            for (int i = 0; i < 8; ++i)
-                y[i] = __fmul_rn(v[w * 8 + i], sc.r);
-            uint32_t q;
-            if (RND == RNE) {
-                q = e2m1_rn_pack8(y);
-            } else {
-                // flat index in X^T of this group of 8
-                const uint64_t e0 = (uint64_t)gc * (uint64_t)rows + (uint64_t)(gr0 + w * 8);
-                const uint4 rbits = sr_bits8(a.seed, e0 >> 3, 1u, a.offset);
-                q = 0;
-#pragma unroll
-                for (int i = 0; i < 8; ++i)
-                    q |= e2m1_sr(y[i], u16_of(rbits, i)) << (4 * i);
-            }
-            dst[w] = q;
-        }
+        for (int w = 0; w < BC / 8; ++w)
+            dst[w] = q[w];
         css[c * NRB + rb] = (uint8_t)sc.code;
     }
     __syncthreads();
@@ -296,7 +291,7 @@ __global__ void __launch_bounds__(kThreads) tile_kernel(TileArgs a)
         const int64_t gc = c0 + c, gr = r0 + (int64_t)j * 16;
         if (gc < cols && gr < rows)
             *reinterpret_cast<uint2 *>(a.ccodes + gc * (rows / 2) + gr / 2) =
-                *reinterpret_cast<const uint2 *>(ccs + c * (TR / 2) + j * 8);
+                *reinterpret_cast<const uint2 *>(ccs + c * CP + j * 8);
     }
     for (int u = threadIdx.x; u < TC * NRB; u += kThreads) {
         const int c = u / NRB, j = u % NRB;
@@ -344,11 +339,12 @@ cudaError_t launch_amax(const void *x, int bf16, int64_t n, float *out, cudaStre
 template <typename T, int FMT, int RND>
 static cudaError_t row_go(const RowArgs &a, cudaStream_t s)
 {
-    constexpr int E = VecInfo<T>::E;
-    const int64_t nch = a.n / E;
-    if (nch == 0)
+    constexpr int B = FmtInfo<FMT>::B;
+    constexpr int BPT = (B * sizeof(T) >= 64) ? 1 : 2;
+    const int64_t nblk = a.n / B;
+    if (nblk == 0)
         return cudaSuccess;
-    const int grid = persistent_grid(nch, kThreads * 4, 4);
+    const int grid = persistent_grid(nblk, kThreads * BPT, 8);
     row_kernel<T, FMT, RND><<<grid, kThreads, 0, s>>>(a);
     return cudaGetLastError();
 }

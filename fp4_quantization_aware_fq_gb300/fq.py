@@ -120,8 +120,11 @@ def lib():
                                      P(_QT), P(_QT), P(vp), i32, P(vp), vp, sz, vp]
         L.fq_osci_reset.argtypes = [P(Config), i32, P(i64), P(i64), P(vp), P(vp), P(vp), P(_QT),
                                     ctypes.c_float, vp, vp]
+        L.fq_osci_update_noalloc.argtypes = [P(Config), i32, P(i64), P(i64), P(vp), P(vp), P(vp),
+                                             P(vp), P(_QT), P(_QT), P(vp), i32, P(vp), vp]
         for name in ("fq_amax", "fq_quantize", "fq_fakequant_ste", "fq_dequantize",
-                     "fq_ste_backward", "fq_osci_update", "fq_osci_reset"):
+                     "fq_ste_backward", "fq_osci_update", "fq_osci_reset",
+                     "fq_osci_update_noalloc"):
             getattr(L, name).restype = ctypes.c_int
         L.fq_status_string.argtypes = [ctypes.c_int]
         L.fq_status_string.restype = ctypes.c_char_p
@@ -285,6 +288,32 @@ def fq_osci_update(cfg: Config, master: Sequence[torch.Tensor], delta: Sequence[
         None if mask is None else _arr(vp, [t.data_ptr() for t in mask]),
         ws.data_ptr(), ws.numel(), _stream(stream))
     _check(st, "fq_osci_update")
+
+
+def fq_osci_update_noalloc(cfg: Config, master: Sequence[torch.Tensor],
+                           delta: Sequence[torch.Tensor], dist_q: Sequence[torch.Tensor],
+                           dist_m: Sequence[torch.Tensor], prev: Sequence[QTensor],
+                           nxt: Sequence[QTensor], xhat: Optional[Sequence[torch.Tensor]] = None,
+                           xhat_dtype=torch.bfloat16,
+                           mask: Optional[Sequence[torch.Tensor]] = None, stream=None):
+    """fq_osci_update for callers that cannot allocate: no workspace argument;
+    the library's own static device scratch holds the per-tensor amax (at most
+    FQ_NOALLOC_MAX_TENSORS tensors per call; concurrent calls on the GPU race
+    on that scratch).  This wrapper allocates nothing either."""
+    n = len(master)
+    vp, i64 = ctypes.c_void_p, ctypes.c_int64
+    rows = _arr(i64, [m.shape[0] for m in master])
+    cols = _arr(i64, [m.shape[1] for m in master])
+    pq = (_QT * max(n, 1))(*[q._c() for q in prev])
+    nq = (_QT * max(n, 1))(*[q._c() for q in nxt])
+    st = lib().fq_osci_update_noalloc(
+        ctypes.byref(cfg), n, rows, cols, _arr(vp, [t.data_ptr() for t in master]),
+        _arr(vp, [t.data_ptr() for t in delta]), _arr(vp, [t.data_ptr() for t in dist_q]),
+        _arr(vp, [t.data_ptr() for t in dist_m]), pq, nq,
+        None if xhat is None else _arr(vp, [t.data_ptr() for t in xhat]),
+        BF16 if xhat_dtype == torch.bfloat16 else F32,
+        None if mask is None else _arr(vp, [t.data_ptr() for t in mask]), _stream(stream))
+    _check(st, "fq_osci_update_noalloc")
 
 
 def fq_osci_reset(cfg: Config, master: Sequence[torch.Tensor], dist_q: Sequence[torch.Tensor],

@@ -187,6 +187,32 @@ FQ_API fq_status fq_osci_update(const fq_config *cfg, int32_t ntensors, const in
                          uint8_t *const *mask, void *workspace, size_t workspace_bytes,
                          void *stream);
 
+/* fq_osci_update without a workspace argument.  The pages have no counterpart
+ * to this entry point; it exists for callers that cannot allocate device
+ * memory where they run the optimizer step (a framework whose allocator owns
+ * all device memory, a plugin that only receives its tensors, a process that
+ * forbids cudaMalloc after start-up).  The per-tensor amax scratch lives in a
+ * file-scope device array of FQ_NOALLOC_MAX_TENSORS floats (256 bytes) that
+ * every GPU which loads the library keeps until the process exits; the caller
+ * still passes all inputs and outputs, and nothing here allocates.
+ *  - At most FQ_NOALLOC_MAX_TENSORS tensors per call; more returns
+ *    FQ_ERR_WORKSPACE before anything runs.  Otherwise arguments, results and
+ *    errors are those of fq_osci_update.
+ *  - The first call on each device looks up the array's device address with
+ *    that device current (cudaGetSymbolAddress); make that first call before
+ *    any stream capture.
+ *  - Every call shares the one array; each call clears the slots it uses on
+ *    its stream before using them, but calls that overlap on the GPU (other
+ *    streams, other threads) race on it. */
+#define FQ_NOALLOC_MAX_TENSORS 64
+FQ_API fq_status fq_osci_update_noalloc(const fq_config *cfg, int32_t ntensors,
+                                        const int64_t *rows, const int64_t *cols,
+                                        float *const *master, const float *const *delta,
+                                        float *const *dist_q, float *const *dist_m,
+                                        const fq_qtensor *prev, const fq_qtensor *next,
+                                        void *const *xhat, int32_t xhat_dtype,
+                                        uint8_t *const *mask, void *stream);
+
 /* End of an OsciReset window ([TJV2] §2B): where dist_Q > threshold * dist_M
  * (FP32 product, strict), the master weight is set to xhat_t decoded from cur
  * (the quantized value of its current bin); dist_Q and dist_M are then zeroed

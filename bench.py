@@ -250,6 +250,22 @@ def bytes_per_step(elems):
     return {k: BYTES_PER_ELEM[k] * elems[k] for k in elems}
 
 
+# --------------------------------------------------------------------------- ranks
+def max_over_ranks(value: float, dist, device) -> float:
+    """The largest value over all ranks (the job's time is its slowest rank's)."""
+    if dist is None:
+        return value
+    import torch
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(world: int, bytes_per_step: float, steps: int, ms: float) -> float:
+    """Whole-job GB/s: every rank moves bytes_per_step per step (weak scaling)."""
+    return world * bytes_per_step * steps / (ms / 1e3) / 1e9
+
+
 # --------------------------------------------------------------------------- device timing
 def run_ours(args, rank, world, dist):
     import torch
@@ -288,17 +304,12 @@ def run_ours(args, rank, world, dist):
     clk = clocks.stop() if clocks else None
     ms = t0.elapsed_time(t1)
     per_ms = {n: sum(a.elapsed_time(b) for a, b in ev[n]) / args.steps for n in suite.names}
-    if dist:
-        t = torch.tensor([ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(ms, dist, dev)
 
     # end-to-end: pinned host inputs -> device, the same calls, results -> host
     e2e = run_e2e(args, suite, total_bytes) if not args.no_e2e else None
-    if dist and e2e is not None:
-        t = torch.tensor([e2e["ms_total"]], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e["ms_total"] = float(t.item())
+    if e2e is not None:
+        e2e["ms_total"] = max_over_ranks(e2e["ms_total"], dist, dev)
     return suite, bps, total_bytes, ms, per_ms, clk, e2e
 
 
@@ -481,7 +492,7 @@ def main():
     if rank == 0:
         peak, peak_kind = measured_peaks()
         ms_step = ms / args.steps
-        value = world * total_bytes * args.steps / (ms / 1e3) / 1e9
+        value = job_throughput(world, total_bytes, args.steps, ms)
         per = {}
         for n in suite.names:
             t = per_ms[n] / 1e3
@@ -512,8 +523,8 @@ def main():
             "clocks": clk,
         }
         if e2e is not None:
-            line["e2e"] = {"value": round(world * e2e["bytes"] * e2e["steps"] /
-                                          (e2e["ms_total"] / 1e3) / 1e9, 1),
+            line["e2e"] = {"value": round(job_throughput(world, e2e["bytes"], e2e["steps"],
+                                                         e2e["ms_total"]), 1),
                            "unit": UNIT, "h2d_bytes_per_step": e2e["h2d"],
                            "d2h_bytes_per_step": e2e["d2h"], "steps": e2e["steps"],
                            "ms_per_step": round(e2e["ms_total"] / e2e["steps"], 3)}

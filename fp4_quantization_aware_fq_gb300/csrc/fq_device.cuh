@@ -173,29 +173,41 @@ __device__ __forceinline__ float stored_s_eff(uint32_t code, float s_outer)
 // Salmon, Moraes, Dror, Shaw, "Parallel Random Numbers: As Easy as 1, 2, 3"
 // (SC'11): ten rounds; each round multiplies counter words 0 and 2 by the two
 // round multipliers, mixes the high halves with words 1 / 3 and the key, and
-// the key is bumped by the two Weyl constants between rounds.
-__device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1)
+// the key is bumped by the two Weyl constants between rounds.  The round keys
+// (the key plus r times the Weyl constants) are computed once per thread.
+struct PhiloxKey {
+    uint32_t k0[10], k1[10];
+};
+
+__device__ __forceinline__ PhiloxKey philox_key(uint64_t seed)
+{
+    PhiloxKey k;
+#pragma unroll
+    for (int r = 0; r < 10; ++r) {
+        k.k0[r] = (uint32_t)seed + 0x9E3779B9u * (uint32_t)r;
+        k.k1[r] = (uint32_t)(seed >> 32) + 0xBB67AE85u * (uint32_t)r;
+    }
+    return k;
+}
+
+__device__ __forceinline__ uint4 philox4x32_10(uint4 c, const PhiloxKey &k)
 {
 #pragma unroll
-    for (int round = 0; round < 10; ++round) {
-        const uint32_t lo0 = 0xD2511F53u * c.x;
-        const uint32_t hi0 = __umulhi(0xD2511F53u, c.x);
-        const uint32_t lo1 = 0xCD9E8D57u * c.z;
-        const uint32_t hi1 = __umulhi(0xCD9E8D57u, c.z);
-        c = make_uint4(hi1 ^ c.y ^ k0, lo1, hi0 ^ c.w ^ k1, lo0);
-        k0 += 0x9E3779B9u;
-        k1 += 0xBB67AE85u;
+    for (int r = 0; r < 10; ++r) {
+        const uint64_t p0 = (uint64_t)0xD2511F53u * c.x;
+        const uint64_t p1 = (uint64_t)0xCD9E8D57u * c.z;
+        c = make_uint4((uint32_t)(p1 >> 32) ^ c.y ^ k.k0[r], (uint32_t)p1,
+                       (uint32_t)(p0 >> 32) ^ c.w ^ k.k1[r], (uint32_t)p0);
     }
     return c;
 }
 
 // Eight 16-bit uniforms for elements 8g .. 8g+7 of a tensor, in element order
 // (element j: half j % 2 of word j / 2).
-__device__ __forceinline__ uint4 sr_bits8(uint64_t seed, uint64_t g, uint32_t stream,
+__device__ __forceinline__ uint4 sr_bits8(const PhiloxKey &k, uint64_t g, uint32_t stream,
                                           uint32_t offset)
 {
-    return philox4x32_10(make_uint4((uint32_t)g, (uint32_t)(g >> 32), stream, offset),
-                         (uint32_t)seed, (uint32_t)(seed >> 32));
+    return philox4x32_10(make_uint4((uint32_t)g, (uint32_t)(g >> 32), stream, offset), k);
 }
 
 __device__ __forceinline__ uint32_t u16_of(const uint4 &w, int j)
@@ -258,9 +270,12 @@ __device__ __forceinline__ float e2m1_sr_value(float y, uint32_t u)
     const uint32_t b = __float_as_uint(y);
     const float a = fabsf(y);
     const uint32_t hi = (b + (0x3FFFFFu - (u << 6))) & 0xFFC00000u;
-    const uint32_t d = __float2uint_ru(__fmul_rn(a, 131072.0f));
-    const uint32_t n = (d + 65535u - u) >> 16;
-    const uint32_t lo = (n ? (0x3E800000u + (n << 23)) : 0u) | (b & 0x80000000u);
+    // 2^23 + ceil(|y| * 2^17): an exact product, one upward rounding in the add
+    const uint32_t cb = __float_as_uint(__fmaf_ru(a, 131072.0f, 8388608.0f));
+    const uint32_t n = (cb - 0x4B000000u + 65535u - u) >> 16;
+    // n half-steps as a value: 0.5 n, except that n = 0 gives 0.25, which the
+    // final nearest-even conversion sends to (signed) zero
+    const uint32_t lo = ((n << 23) + 0x3E800000u) | (b & 0x80000000u);
     return __uint_as_float(a < 1.0f ? lo : hi);
 }
 
@@ -269,9 +284,9 @@ __device__ __forceinline__ float e2m1_sr_value(float y, uint32_t u)
 // inside [-6 s_eff, 6 s_eff]).  e0 is the flat index of the block's first
 // element in the tensor being quantized (Philox counter for SR).
 template <int B, int RND>
-__device__ __forceinline__ void encode_block(const float *v, const Scale &sc, uint64_t seed,
+__device__ __forceinline__ void encode_block(const float *v, const Scale &sc, const PhiloxKey &key,
                                              uint64_t e0, uint32_t stream_id, uint32_t offset,
-                                             uint32_t *q, uint32_t &mask)
+                                             uint32_t *q)
 {
 #pragma unroll
     for (int w = 0; w < B / 8; ++w) {
@@ -280,20 +295,26 @@ __device__ __forceinline__ void encode_block(const float *v, const Scale &sc, ui
         for (int i = 0; i < 8; ++i)
             y[i] = __fmul_rn(v[w * 8 + i], sc.r);
         if (RND == SR) {
-            const uint4 rb = sr_bits8(seed, (e0 >> 3) + w, stream_id, offset);
+            const uint4 rb = sr_bits8(key, (e0 >> 3) + w, stream_id, offset);
 #pragma unroll
             for (int i = 0; i < 8; ++i)
                 y[i] = e2m1_sr_value(y[i], u16_of(rb, i));
         }
         q[w] = e2m1_rn_pack8(y);
     }
-    // clip bit = sign of (lim - |x|): exact, since a non-zero difference of two
-    // floats never rounds to zero without flush-to-zero.
+}
+
+// STE mask bits of a block: bit i = element i inside [-6 s_eff, 6 s_eff].
+// The clip bit is the sign of (lim - |x|): exact, since a non-zero difference
+// of two floats never rounds to zero without flush-to-zero.
+template <int B>
+__device__ __forceinline__ uint32_t block_mask(const float *v, float lim)
+{
     uint32_t clip = 0;
 #pragma unroll
     for (int i = 0; i < B; ++i)
-        clip |= (__float_as_uint(__fsub_rn(sc.lim, fabsf(v[i]))) >> 31) << i;
-    mask = (B == 32) ? ~clip : (~clip & ((1u << B) - 1u));
+        clip |= (__float_as_uint(__fsub_rn(lim, fabsf(v[i]))) >> 31) << i;
+    return (B == 32) ? ~clip : (~clip & ((1u << B) - 1u));
 }
 
 // Block scale for one block; for the double block, s_outer is the outer scale.

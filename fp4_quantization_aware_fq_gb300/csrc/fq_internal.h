@@ -57,7 +57,7 @@ struct DequantArgs {
 // of kOsciTileChunks 16-byte chunks are numbered across the group; tile_start
 // holds the prefix sums (tile_start[i] = first tile of tensor i).
 constexpr int kOsciMaxTensors = 64;
-constexpr int kOsciTileChunks = 1024;
+constexpr int kOsciTileChunks = 2048;
 
 struct OsciTensor {
     float *master;

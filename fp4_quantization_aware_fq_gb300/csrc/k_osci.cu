@@ -93,13 +93,17 @@ __global__ void __launch_bounds__(kOsciThreads) osci_pass_a(const __grid_constan
     }
 }
 
-// Pass B: one thread per block of 16 (32 for MXFP4) master weights.
+// Pass B: one thread per block of 16 (32 for MXFP4) master weights, NB blocks
+// per thread per iteration with all their loads issued before any compute.
 template <int FMT, int RND>
 __global__ void __launch_bounds__(kOsciThreads) osci_pass_b(const __grid_constant__ OsciArgs a)
 {
     constexpr int B = FmtInfo<FMT>::B;
     constexpr int BPTILE = kOsciTileChunks * 4 / B;  // blocks per tile
+    constexpr int NB = BPTILE >= 2 * kOsciThreads ? 2 : 1;
+    static_assert(BPTILE % (NB * kOsciThreads) == 0, "tile must split evenly");
     const int64_t ntiles = a.tile_start[a.ntensors];
+    const PhiloxKey key = philox_key(a.seed);
     int t = 0;
     const int lane = threadIdx.x & 31;
     for (int64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
@@ -115,100 +119,112 @@ __global__ void __launch_bounds__(kOsciThreads) osci_pass_b(const __grid_constan
             if (bbeg == 0 && threadIdx.x == 0)
                 T.ntscale[0] = s_g;
         }
-        for (int k = 0; k < BPTILE; k += kOsciThreads) {
-            const int64_t blk = bbeg + k + threadIdx.x;
-            const bool valid = k + (int)threadIdx.x < BPTILE && blk < nblk;
-            float v[B];
-            if (valid) {
+        for (int k = 0; k < BPTILE; k += NB * kOsciThreads) {
+            float v[NB][B], dq[NB][B];
+            uint32_t qp[NB][B / 8];
+            uint32_t scp[NB];
+            float so_p[NB];
 #pragma unroll
-                for (int j = 0; j < B / 4; ++j) {
-                    const float4 w = ldf4_rw(T.master + blk * B + 4 * j);
-                    v[4 * j] = w.x;
-                    v[4 * j + 1] = w.y;
-                    v[4 * j + 2] = w.z;
-                    v[4 * j + 3] = w.w;
+            for (int j = 0; j < NB; ++j) {
+                const int64_t blk = bbeg + k + j * kOsciThreads + threadIdx.x;
+                if (blk < nblk) {
+#pragma unroll
+                    for (int i = 0; i < B / 4; ++i) {
+                        const float4 w = ldf4_rw(T.master + blk * B + 4 * i);
+                        v[j][4 * i] = w.x;
+                        v[j][4 * i + 1] = w.y;
+                        v[j][4 * i + 2] = w.z;
+                        v[j][4 * i + 3] = w.w;
+                        const float4 d = ldf4_rw(T.dist_q + blk * B + 4 * i);
+                        dq[j][4 * i] = d.x;
+                        dq[j][4 * i + 1] = d.y;
+                        dq[j][4 * i + 2] = d.z;
+                        dq[j][4 * i + 3] = d.w;
+                    }
+                    if (B == 16) {
+                        const uint2 p2 = __ldg(reinterpret_cast<const uint2 *>(T.pcodes) + blk);
+                        qp[j][0] = p2.x;
+                        qp[j][1] = p2.y;
+                    } else {
+                        const uint4 p4 = __ldg(reinterpret_cast<const uint4 *>(T.pcodes) + blk);
+                        qp[j][0] = p4.x;
+                        qp[j][1] = p4.y;
+                        qp[j][2] = p4.z;
+                        qp[j][3] = p4.w;
+                    }
+                    scp[j] = __ldg(T.pscales + blk);
+                    so_p[j] = (FMT == NV2L) ? __ldg(T.ptscale + (blk >> 3)) : s_gp;
+                } else {
+#pragma unroll
+                    for (int i = 0; i < B; ++i)
+                        v[j][i] = dq[j][i] = 0.0f;
+#pragma unroll
+                    for (int w = 0; w < B / 8; ++w)
+                        qp[j][w] = 0;
+                    scp[j] = 0;
+                    so_p[j] = 0.0f;
                 }
-            } else {
+            }
+#pragma unroll
+            for (int j = 0; j < NB; ++j) {
+                const int64_t blk = bbeg + k + j * kOsciThreads + threadIdx.x;
+                const bool valid = blk < nblk;
+                float am = 0.0f;
 #pragma unroll
                 for (int i = 0; i < B; ++i)
-                    v[i] = 0.0f;
-            }
-            float am = 0.0f;
+                    am = fmaxf(am, fabsf(v[j][i]));
+                float s_o = s_g;
+                if (FMT == NV2L)
+                    s_o = outer_scale(group_max<8>(am));
+                const Scale sc = block_scale<FMT>(am, s_o);
+                uint32_t q[B / 8];
+                encode_block<B, RND>(v[j], sc, key, (uint64_t)blk * B, 0u, a.offset, q);
+                if (!valid)
+                    continue;
+                const float seff_p = stored_s_eff<FMT>(scp[j], so_p[j]);
 #pragma unroll
-            for (int i = 0; i < B; ++i)
-                am = fmaxf(am, fabsf(v[i]));
-            float s_o = s_g;
-            if (FMT == NV2L)
-                s_o = outer_scale(group_max<8>(am));
-            const Scale sc = block_scale<FMT>(am, s_o);
-            uint32_t q[B / 8];
-            uint32_t mask;
-            encode_block<B, RND>(v, sc, a.seed, (uint64_t)blk * B, 0u, a.offset, q, mask);
-            if (!valid)
-                continue;
-            // previous quantized value of this block
-            uint32_t qp[B / 8];
-            if (B == 16) {
-                const uint2 p2 = __ldg(reinterpret_cast<const uint2 *>(T.pcodes) + blk);
-                qp[0] = p2.x;
-                qp[1] = p2.y;
-            } else {
-                const uint4 p4 = __ldg(reinterpret_cast<const uint4 *>(T.pcodes) + blk);
-                qp[0] = p4.x;
-                qp[1] = p4.y;
-                qp[2] = p4.z;
-                qp[3] = p4.w;
-            }
-            float so_p = s_gp;
-            if (FMT == NV2L)
-                so_p = __ldg(T.ptscale + (blk >> 3));
-            const float seff_p = stored_s_eff<FMT>(__ldg(T.pscales + blk), so_p);
+                for (int w = 0; w < B / 8; ++w) {
+                    float xh[8], xp[8];
+                    e2m1_decode8(q[w], xh);
+                    e2m1_decode8(qp[j][w], xp);
 #pragma unroll
-            for (int w = 0; w < B / 8; ++w) {
-                float xh[8], xp[8];
-                e2m1_decode8(q[w], xh);
-                e2m1_decode8(qp[w], xp);
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    xh[i] = __fmul_rn(xh[i], sc.s_eff);
-                    xp[i] = __fmul_rn(xp[i], seff_p);
-                }
-                float *dqp = T.dist_q + blk * B + w * 8;
-                float4 d0 = ldf4_rw(dqp), d1 = ldf4_rw(dqp + 4);
-                d0.x = __fadd_rn(d0.x, fabsf(__fsub_rn(xh[0], xp[0])));
-                d0.y = __fadd_rn(d0.y, fabsf(__fsub_rn(xh[1], xp[1])));
-                d0.z = __fadd_rn(d0.z, fabsf(__fsub_rn(xh[2], xp[2])));
-                d0.w = __fadd_rn(d0.w, fabsf(__fsub_rn(xh[3], xp[3])));
-                d1.x = __fadd_rn(d1.x, fabsf(__fsub_rn(xh[4], xp[4])));
-                d1.y = __fadd_rn(d1.y, fabsf(__fsub_rn(xh[5], xp[5])));
-                d1.z = __fadd_rn(d1.z, fabsf(__fsub_rn(xh[6], xp[6])));
-                d1.w = __fadd_rn(d1.w, fabsf(__fsub_rn(xh[7], xp[7])));
-                stf4(dqp, d0);
-                stf4(dqp + 4, d1);
-                if (T.xhat) {
-                    if (a.xhat_bf16) {
-                        *reinterpret_cast<uint4 *>((char *)T.xhat + (blk * B + w * 8) * 2) =
-                            make_uint4(bf16x2_rn(xh[0], xh[1]), bf16x2_rn(xh[2], xh[3]),
-                                       bf16x2_rn(xh[4], xh[5]), bf16x2_rn(xh[6], xh[7]));
-                    } else {
-                        float *xo = reinterpret_cast<float *>(T.xhat) + blk * B + w * 8;
-                        stf4(xo, make_float4(xh[0], xh[1], xh[2], xh[3]));
-                        stf4(xo + 4, make_float4(xh[4], xh[5], xh[6], xh[7]));
+                    for (int i = 0; i < 8; ++i) {
+                        xh[i] = __fmul_rn(xh[i], sc.s_eff);
+                        xp[i] = __fmul_rn(xp[i], seff_p);
+                        dq[j][w * 8 + i] =
+                            __fadd_rn(dq[j][w * 8 + i], fabsf(__fsub_rn(xh[i], xp[i])));
+                    }
+                    if (T.xhat) {
+                        if (a.xhat_bf16) {
+                            *reinterpret_cast<uint4 *>((char *)T.xhat + (blk * B + w * 8) * 2) =
+                                make_uint4(bf16x2_rn(xh[0], xh[1]), bf16x2_rn(xh[2], xh[3]),
+                                           bf16x2_rn(xh[4], xh[5]), bf16x2_rn(xh[6], xh[7]));
+                        } else {
+                            float *xo = reinterpret_cast<float *>(T.xhat) + blk * B + w * 8;
+                            stf4(xo, make_float4(xh[0], xh[1], xh[2], xh[3]));
+                            stf4(xo + 4, make_float4(xh[4], xh[5], xh[6], xh[7]));
+                        }
                     }
                 }
-            }
-            if (B == 16)
-                reinterpret_cast<uint2 *>(T.ncodes)[blk] = make_uint2(q[0], q[1]);
-            else
-                reinterpret_cast<uint4 *>(T.ncodes)[blk] = make_uint4(q[0], q[1], q[2], q[3]);
-            T.nscales[blk] = (uint8_t)sc.code;
-            if (FMT == NV2L && (lane & 7) == 0)
-                T.ntscale[blk >> 3] = s_o;
-            if (T.mask) {
+#pragma unroll
+                for (int i = 0; i < B / 4; ++i)
+                    stf4(T.dist_q + blk * B + 4 * i,
+                         make_float4(dq[j][4 * i], dq[j][4 * i + 1], dq[j][4 * i + 2],
+                                     dq[j][4 * i + 3]));
                 if (B == 16)
-                    reinterpret_cast<uint16_t *>(T.mask)[blk] = (uint16_t)mask;
+                    reinterpret_cast<uint2 *>(T.ncodes)[blk] = make_uint2(q[0], q[1]);
                 else
-                    reinterpret_cast<uint32_t *>(T.mask)[blk] = mask;
+                    reinterpret_cast<uint4 *>(T.ncodes)[blk] = make_uint4(q[0], q[1], q[2], q[3]);
+                T.nscales[blk] = (uint8_t)sc.code;
+                if (FMT == NV2L && (lane & 7) == 0)
+                    T.ntscale[blk >> 3] = s_o;
+                if (T.mask) {
+                    const uint32_t mask = block_mask<B>(v[j], sc.lim);
+                    if (B == 16)
+                        reinterpret_cast<uint16_t *>(T.mask)[blk] = (uint16_t)mask;
+                    else
+                        reinterpret_cast<uint32_t *>(T.mask)[blk] = mask;
+                }
             }
         }
     }
@@ -282,7 +298,7 @@ __global__ void __launch_bounds__(kOsciThreads) osci_reset_kernel(const __grid_c
 
 static int osci_grid(int64_t ntiles)
 {
-    const int64_t cap = (int64_t)sm_count() * 4;
+    const int64_t cap = (int64_t)sm_count() * 8;
     return (int)(ntiles < cap ? (ntiles > 0 ? ntiles : 1) : cap);
 }
 

@@ -75,7 +75,7 @@ struct RowOut {
 // all 32 lanes of the warp must call this together.
 template <int FMT, int RND>
 __device__ __forceinline__ void row_block(const float *v, int64_t blk, bool valid, float s_g,
-                                          const RowOut &o, uint64_t seed, uint32_t offset,
+                                          const RowOut &o, const PhiloxKey &key, uint32_t offset,
                                           uint32_t stream_id)
 {
     constexpr int B = FmtInfo<FMT>::B;
@@ -88,8 +88,7 @@ __device__ __forceinline__ void row_block(const float *v, int64_t blk, bool vali
         s_o = outer_scale(group_max<8>(am));
     const Scale sc = block_scale<FMT>(am, s_o);
     uint32_t q[B / 8];
-    uint32_t mask;
-    encode_block<B, RND>(v, sc, seed, (uint64_t)blk * B, stream_id, offset, q, mask);
+    encode_block<B, RND>(v, sc, key, (uint64_t)blk * B, stream_id, offset, q);
     if (!valid)
         return;
     const int lane = threadIdx.x & 31;
@@ -122,6 +121,7 @@ __device__ __forceinline__ void row_block(const float *v, int64_t blk, bool vali
         }
     }
     if (o.mask) {
+        const uint32_t mask = block_mask<B>(v, sc.lim);
         if (B == 16)
             reinterpret_cast<uint16_t *>(o.mask)[blk] = (uint16_t)mask;
         else
@@ -144,6 +144,7 @@ __global__ void __launch_bounds__(kThreads) row_kernel(RowArgs a)
             a.tscale[0] = s_g;
     }
     const RowOut o{a.codes, a.scales, a.tscale, a.xhat, a.xhat_bf16, a.mask};
+    const PhiloxKey key = philox_key(a.seed);
     const int64_t stride = (int64_t)gridDim.x * kThreads * BPT;
     for (int64_t base = (int64_t)blockIdx.x * kThreads * BPT; base < nblk; base += stride) {
         float v[BPT][B];
@@ -160,7 +161,7 @@ __global__ void __launch_bounds__(kThreads) row_kernel(RowArgs a)
 #pragma unroll
         for (int k = 0; k < BPT; ++k) {
             const int64_t blk = base + k * kThreads + threadIdx.x;
-            row_block<FMT, RND>(v[k], blk, blk < nblk, s_g, o, a.seed, a.offset, a.stream_id);
+            row_block<FMT, RND>(v[k], blk, blk < nblk, s_g, o, key, a.offset, a.stream_id);
         }
     }
 }
@@ -216,6 +217,7 @@ __global__ void __launch_bounds__(kThreads) tile_kernel(TileArgs a)
     // Phase 1: each thread loads whole row blocks (16-byte vectors), stages
     // them in shared memory and, when asked, runs the row-wise pass on them.
     const RowOut o{a.rcodes, a.rscales, a.rtscale, a.xhat, a.xhat_bf16, a.mask};
+    const PhiloxKey key = philox_key(a.seed);
     for (int t = threadIdx.x; t < TR * RBPR; t += kThreads) {
         const int tr = t / RBPR, tb = t % RBPR;
         const int64_t gr = r0 + tr, gc = c0 + (int64_t)tb * BR;
@@ -232,7 +234,7 @@ __global__ void __launch_bounds__(kThreads) tile_kernel(TileArgs a)
             unpack16<T>(raw[k], v + k * E);
         }
         if (a.do_row)
-            row_block<FMT, RND>(v, (gr * cols + gc) / BR, valid, s_g, o, a.seed, a.offset, 0u);
+            row_block<FMT, RND>(v, (gr * cols + gc) / BR, valid, s_g, o, key, a.offset, 0u);
     }
     __syncthreads();
 
@@ -248,39 +250,48 @@ __global__ void __launch_bounds__(kThreads) tile_kernel(TileArgs a)
         }
         __syncthreads();
     }
-    for (int task = threadIdx.x; task < TC * NRB; task += kThreads) {
-        const int c = task % TC, rb = task / TC;
-        const int64_t gc = c0 + c, gr0 = r0 + (int64_t)rb * BC;
-        if (gc >= cols || gr0 >= rows)
+    // Two adjacent columns per task: one 4- or 8-byte shared-memory read
+    // serves both.
+    for (int task = threadIdx.x; task < (TC / 2) * NRB; task += kThreads) {
+        const int cp = task % (TC / 2), rb = task / (TC / 2);
+        const int64_t gr0 = r0 + (int64_t)rb * BC;
+        if (c0 + 2 * cp >= cols || gr0 >= rows)
             continue;
-        float v[BC];
-        float m = 0.0f;
+        float v[2][BC];
+        float m0 = 0.0f, m1 = 0.0f;
 #pragma unroll
         for (int i = 0; i < BC; ++i) {
-            v[i] = static_cast<float>(tile[(rb * BC + i) * TC + c]);
-            m = fmaxf(m, fabsf(v[i]));
+            const T *p = tile + (rb * BC + i) * TC + 2 * cp;
+            v[0][i] = static_cast<float>(p[0]);
+            v[1][i] = static_cast<float>(p[1]);
+            m0 = fmaxf(m0, fabsf(v[0][i]));
+            m1 = fmaxf(m1, fabsf(v[1][i]));
         }
-        float s_o = s_g;
-        if (FMT == NV2L) {
-            float mo = 0.0f;
 #pragma unroll
-            for (int j = 0; j < NRB; ++j)
-                mo = fmaxf(mo, am16[j * TC + c]);
-            s_o = outer_scale(mo);
-            if (rb == 0)
-                a.ctscale[gc * (rows / 128) + r0 / 128] = s_o;
+        for (int h = 0; h < 2; ++h) {
+            const int c = 2 * cp + h;
+            const int64_t gc = c0 + c;
+            float s_o = s_g;
+            if (FMT == NV2L) {
+                float mo = 0.0f;
+#pragma unroll
+                for (int j = 0; j < NRB; ++j)
+                    mo = fmaxf(mo, am16[j * TC + c]);
+                s_o = outer_scale(mo);
+                if (rb == 0)
+                    a.ctscale[gc * (rows / 128) + r0 / 128] = s_o;
+            }
+            const Scale sc = block_scale<FMT>(h ? m1 : m0, s_o);
+            uint32_t q[BC / 8];
+            // flat index in X^T of the block's first element
+            encode_block<BC, RND>(v[h], sc, key, (uint64_t)gc * (uint64_t)rows + (uint64_t)gr0,
+                                  1u, a.offset, q);
+            uint32_t *dst = reinterpret_cast<uint32_t *>(ccs + c * CP + rb * (BC / 2));
+#pragma unroll
+            for (int w = 0; w < BC / 8; ++w)
+                dst[w] = q[w];
+            css[c * NRB + rb] = (uint8_t)sc.code;
         }
-        const Scale sc = block_scale<FMT>(m, s_o);
-        uint32_t q[BC / 8];
-        uint32_t unused_mask;
-        // flat index in X^T of the block's first element
-        encode_block<BC, RND>(v, sc, a.seed, (uint64_t)gc * (uint64_t)rows + (uint64_t)gr0, 1u,
-                              a.offset, q, unused_mask);
-        uint32_t *dst = reinterpret_cast<uint32_t *>(ccs + c * CP + rb * (BC / 2));
-#pragma unroll
-        for (int w = 0; w < BC / 8; ++w)
-            dst[w] = q[w];
-        css[c * NRB + rb] = (uint8_t)sc.code;
     }
     __syncthreads();
 

@@ -45,15 +45,14 @@ BYTES_PER_ELEM = {
     "nvfp4_act": 2 + 2 + 0.5 + 1 / 16 + 0.5 + 1 / 16 + 2 + 1 / 8,
     "ste_backward": 2 + 1 / 8 + 2,
     "grad_2level": 2 + 0.5 + 1 / 16 + 4 / 128,
-    "osci_update": 20 + (4 + 0.5 + 1 / 16 + 8 + 0.5 + 1 / 16 + 2 + 1 / 8),
-    "osci_reset": 16,
+    "osci_update_reset": 20 + (4 + 0.5 + 1 / 16 + 8 + 8 + 0.5 + 1 / 16 + 2 + 1 / 8),
 }
 # Our kernels launched per step (memsets not counted).
 LAUNCHES_PER_STEP = {"nvfp4_small": 2, "mxfp4_weight": 1, "nvfp4_act": 2, "ste_backward": 1,
-                     "grad_2level": 1, "osci_update": 2, "osci_reset": 1}
+                     "grad_2level": 1, "osci_update_reset": 2}
 # DRAM traffic per launch of the dominant call from an ncu capture, valid only
 # for the kernel source it was taken on (sha256 of k_osci.cu); None: not taken.
-NCU_TRAFFIC = {"osci_update": {"bytes": None, "src_sha256": None}}
+NCU_TRAFFIC = {"osci_update_reset": {"bytes": None, "src_sha256": None}}
 
 
 def log(*a):
@@ -135,7 +134,7 @@ class Suite:
     profiling a smaller case of the same kernels)."""
 
     ORDER = ("nvfp4_small", "mxfp4_weight", "nvfp4_act", "ste_backward", "grad_2level",
-             "osci_update", "osci_reset")
+             "osci_update_reset")
 
     def __init__(self, dev, only=None, experts=None):
         import torch
@@ -182,7 +181,7 @@ class Suite:
             self.cfg4 = fq.Config(fq.NVFP4_2LEVEL, fq.SR, 0x5EED, 0)
             self.q4 = fq.alloc_qtensor(*self.x4.shape, fq.NVFP4_2LEVEL, dev)
             self.elems["grad_2level"] = self.x4.numel()
-        if want & {"osci_update", "osci_reset"}:
+        if "osci_update_reset" in want:
             m = W.WORKLOADS["moe_qat"]
             ws = W.moe_weights(experts or m["experts"], m["up_shape"], m["down_shape"],
                                seed=4, device=dev)
@@ -200,10 +199,7 @@ class Suite:
             self.ws5 = torch.empty(fq.fq_osci_workspace_size(len(self.master)),
                                    dtype=torch.uint8, device=dev)
             self.nreset = torch.zeros(1, dtype=torch.int64, device=dev)
-            n5 = sum(t.numel() for t in self.master)
-            for k in ("osci_update", "osci_reset"):
-                if k in want:
-                    self.elems[k] = n5
+            self.elems["osci_update_reset"] = sum(t.numel() for t in self.master)
         self.elems = {k: v for k, v in self.elems.items() if k in want}
         torch.cuda.synchronize()
 
@@ -236,14 +232,12 @@ class Suite:
         self.cfg4.offset = self.step_no
         self.fq.fq_quantize(self.x4, self.cfg4, row_out=self.q4)
 
-    def osci_update(self):
-        self.fq.fq_osci_update(self.cfg5, self.master, self.delta, self.dq, self.dm, self.prev,
-                               self.next, xhat=self.xh5, mask=self.m5, ws=self.ws5)
+    def osci_update_reset(self):
+        # one QAT step that also ends the OsciReset window (reset fused in)
+        self.fq.fq_osci_update_reset(self.cfg5, self.master, self.delta, self.dq, self.dm,
+                                     self.prev, self.next, 4.0, n_reset=self.nreset,
+                                     xhat=self.xh5, mask=self.m5, ws=self.ws5)
         self.prev, self.next = self.next, self.prev
-
-    def osci_reset(self):
-        self.fq.fq_osci_reset(self.cfg5, self.master, self.dq, self.dm, self.prev, 4.0,
-                              n_reset=self.nreset)
 
 
 def bytes_per_step(elems):
@@ -332,9 +326,8 @@ def e2e_buffers(suite):
     if "grad_2level" in suite.names:
         ins.append(suite.x4)
         outs += [suite.q4.codes, suite.q4.scales, suite.q4.tscale]
-    if "osci_update" in suite.names:
+    if "osci_update_reset" in suite.names:
         ins += list(suite.delta)
-    if "osci_reset" in suite.names:
         outs.append(suite.nreset)
     return ins, outs
 
@@ -415,8 +408,8 @@ def oracle_sample(max_seconds=None):
     def upd():
         out = st.step(d, offset=1)
         oracle.f32_to_bf16_bits(out["xhat"])
-    res["osci_update"] = (w.numel(), timed(upd))
-    res["osci_reset"] = (w.numel(), timed(lambda: st.reset(4.0)))
+    t_upd = timed(upd)
+    res["osci_update_reset"] = (w.numel(), t_upd + timed(lambda: st.reset(4.0)))
     desc = ("oracle (scalar C, 1 thread) on: nvfp4_small full; mxfp4_weight 2048 rows; "
             "nvfp4_act 1024 rows row+col; ste_backward 1024x8192; grad_2level 2048 rows SR; "
             "osci update+reset on one full [2880, 5760] matrix; per-element rates scaled to "
@@ -436,8 +429,7 @@ def oracle_gbs(sample, elems_full):
 
 FULL_ELEMS = {"nvfp4_small": 256 * 1024, "mxfp4_weight": 4096 * 4096,
               "nvfp4_act": 8192 * 8192, "ste_backward": 8192 * 8192,
-              "grad_2level": 16384 * 4096, "osci_update": 32 * 2 * 2880 * 5760,
-              "osci_reset": 32 * 2 * 2880 * 5760}
+              "grad_2level": 16384 * 4096, "osci_update_reset": 32 * 2 * 2880 * 5760}
 
 
 def config_block(names=None, experts=None):
@@ -450,7 +442,8 @@ def config_block(names=None, experts=None):
                         "4096x4096 MXFP4 RNE quant+dequant; nvfp4_act bf16 8192x8192 NVFP4 "
                         "row 1x16 + col 16x1 + xhat + STE mask, then STE backward; grad_2level "
                         "bf16 16384x4096 double-block NVFP4 SR; moe_qat 32 experts x "
-                        "(2880x5760 + 5760x2880) FP32 master: OsciReset update + reset",
+                        "(2880x5760 + 5760x2880) FP32 master: one QAT step with OsciReset "
+                        "statistics and the window-end reset fused in",
             "elements_per_step": sum(FULL_ELEMS.values()),
             "l2": "no flush: the step's working set (~20 GB) exceeds L2, inputs are cold",
             "bytes": "algorithmic (definition reads + writes; NVFP4 amax is a second read)"}
@@ -512,8 +505,8 @@ def main():
                     "workloads)",
             "config": config_block(suite.names, args.experts),
             "per_workload": per,
-            "roofline": {"bound": "hbm", "kernel": dom + (" (osci_pass_a + osci_pass_b)"
-                                                           if dom == "osci_update" else ""),
+            "roofline": {"bound": "hbm", "kernel": dom + (" (osci_pass_a + osci_pass_b<reset>)"
+                                                           if dom == "osci_update_reset" else ""),
                          "achieved": round(achieved, 1), "peak": peak,
                          "peak_kind": f"{peak_kind} copy bandwidth",
                          "unit": "GB/s", "frac": round(achieved / peak, 3),

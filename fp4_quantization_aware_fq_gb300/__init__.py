@@ -7,10 +7,11 @@ not load the library; the first call does, and fails loudly if it is absent.
 """
 from .fq import (BF16, COL, F32, MXFP4, NVFP4, NVFP4_2LEVEL, RNE, ROW, ROWCOL, SR, Config,
                  FqError, QTensor, alloc_qtensor, fq_amax, fq_dequantize, fq_fakequant_ste,
-                 fq_osci_reset, fq_osci_update, fq_osci_workspace_size, fq_quantize,
+                 fq_osci_reset, fq_osci_update, fq_osci_update_reset,
+                 fq_osci_workspace_size, fq_quantize,
                  fq_status_string, fq_ste_backward, fq_workspace_size)
 
 __all__ = ["BF16", "COL", "F32", "MXFP4", "NVFP4", "NVFP4_2LEVEL", "RNE", "ROW", "ROWCOL", "SR",
            "Config", "FqError", "QTensor", "alloc_qtensor", "fq_amax", "fq_dequantize",
-           "fq_fakequant_ste", "fq_osci_reset", "fq_osci_update", "fq_osci_workspace_size",
+           "fq_fakequant_ste", "fq_osci_reset", "fq_osci_update", "fq_osci_update_reset", "fq_osci_workspace_size",
            "fq_quantize", "fq_status_string", "fq_ste_backward", "fq_workspace_size"]

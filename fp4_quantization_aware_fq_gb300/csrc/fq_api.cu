@@ -176,6 +176,80 @@ void fill_tiles(OsciArgs &a, const int64_t *rows, const int64_t *cols, int32_t i
 
 }  // namespace
 
+static fq_status osci_update_impl(const fq_config *cfg, int32_t ntensors, const int64_t *rows,
+                         const int64_t *cols, float *const *master, const float *const *delta,
+                         float *const *dist_q, float *const *dist_m, const fq_qtensor *prev,
+                         const fq_qtensor *next, void *const *xhat, int32_t xhat_dtype,
+                         uint8_t *const *mask, void *workspace, size_t workspace_bytes,
+                         void *stream, int reset, float threshold, unsigned long long *n_reset)
+{
+    if (!valid_cfg(cfg))
+        return FQ_ERR_INVALID_ARG;
+    const int fmt = cfg->format;
+    fq_status st = check_group(ntensors, rows, cols, fmt);
+    if (st != FQ_OK)
+        return st;
+    if (ntensors == 0)
+        return FQ_OK;
+    if (!master || !delta || !dist_q || !dist_m || !prev || !next)
+        return FQ_ERR_INVALID_ARG;
+    if (xhat && !valid_dtype(xhat_dtype))
+        return FQ_ERR_INVALID_ARG;
+    for (int32_t i = 0; i < ntensors; ++i) {
+        if (!master[i] || !delta[i] || !dist_q[i] || !dist_m[i])
+            return FQ_ERR_INVALID_ARG;
+        if (!aligned16(master[i]) || !aligned16(delta[i]) || !aligned16(dist_q[i]) ||
+            !aligned16(dist_m[i]) || (xhat && xhat[i] && !aligned16(xhat[i])) ||
+            (mask && mask[i] && !aligned16(mask[i])))
+            return FQ_ERR_ALIGN;
+        if ((st = check_q(&prev[i], fmt)) != FQ_OK || (st = check_q(&next[i], fmt)) != FQ_OK)
+            return st;
+    }
+    if (!workspace || workspace_bytes < fq_osci_workspace_size(ntensors))
+        return FQ_ERR_WORKSPACE;
+    if (!aligned16(workspace))
+        return FQ_ERR_ALIGN;
+    if (n_reset && (reinterpret_cast<uintptr_t>(n_reset) & 7u))
+        return FQ_ERR_ALIGN;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (reset && n_reset && cudaMemsetAsync(n_reset, 0, sizeof(unsigned long long), s) != cudaSuccess)
+        return FQ_ERR_CUDA;
+    static thread_local OsciArgs a;
+    for (int32_t i0 = 0; i0 < ntensors; i0 += kOsciMaxTensors) {
+        const int32_t cnt = ntensors - i0 < kOsciMaxTensors ? ntensors - i0 : kOsciMaxTensors;
+        std::memset(&a, 0, sizeof(a));
+        fill_tiles(a, rows, cols, i0, cnt);
+        a.xhat_bf16 = xhat_dtype == FQ_BF16;
+        a.reset = reset;
+        a.threshold = threshold;
+        a.n_reset = reset ? n_reset : nullptr;
+        a.seed = cfg->seed;
+        a.offset = cfg->offset;
+        a.amax = static_cast<float *>(workspace);
+        for (int32_t j = 0; j < cnt; ++j) {
+            const int32_t i = i0 + j;
+            OsciTensor &t = a.t[j];
+            t.master = master[i];
+            t.delta = delta[i];
+            t.dist_q = dist_q[i];
+            t.dist_m = dist_m[i];
+            t.pcodes = prev[i].codes;
+            t.pscales = prev[i].scales;
+            t.ptscale = prev[i].tscale;
+            t.ncodes = next[i].codes;
+            t.nscales = next[i].scales;
+            t.ntscale = next[i].tscale;
+            t.xhat = xhat ? xhat[i] : nullptr;
+            t.mask = mask ? mask[i] : nullptr;
+        }
+        cudaError_t e = launch_osci_update(a, fmt, cfg->rounding, s);
+        if (e != cudaSuccess)
+            return FQ_ERR_CUDA;
+    }
+    return FQ_OK;
+}
+
+
 extern "C" {
 
 size_t fq_workspace_size(const fq_config *cfg, int64_t rows, int64_t cols)
@@ -277,63 +351,23 @@ fq_status fq_osci_update(const fq_config *cfg, int32_t ntensors, const int64_t *
                          uint8_t *const *mask, void *workspace, size_t workspace_bytes,
                          void *stream)
 {
-    if (!valid_cfg(cfg))
-        return FQ_ERR_INVALID_ARG;
-    const int fmt = cfg->format;
-    fq_status st = check_group(ntensors, rows, cols, fmt);
-    if (st != FQ_OK)
-        return st;
-    if (ntensors == 0)
-        return FQ_OK;
-    if (!master || !delta || !dist_q || !dist_m || !prev || !next)
-        return FQ_ERR_INVALID_ARG;
-    if (xhat && !valid_dtype(xhat_dtype))
-        return FQ_ERR_INVALID_ARG;
-    for (int32_t i = 0; i < ntensors; ++i) {
-        if (!master[i] || !delta[i] || !dist_q[i] || !dist_m[i])
-            return FQ_ERR_INVALID_ARG;
-        if (!aligned16(master[i]) || !aligned16(delta[i]) || !aligned16(dist_q[i]) ||
-            !aligned16(dist_m[i]) || (xhat && xhat[i] && !aligned16(xhat[i])) ||
-            (mask && mask[i] && !aligned16(mask[i])))
-            return FQ_ERR_ALIGN;
-        if ((st = check_q(&prev[i], fmt)) != FQ_OK || (st = check_q(&next[i], fmt)) != FQ_OK)
-            return st;
-    }
-    if (!workspace || workspace_bytes < fq_osci_workspace_size(ntensors))
-        return FQ_ERR_WORKSPACE;
-    if (!aligned16(workspace))
-        return FQ_ERR_ALIGN;
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
-    static thread_local OsciArgs a;
-    for (int32_t i0 = 0; i0 < ntensors; i0 += kOsciMaxTensors) {
-        const int32_t cnt = ntensors - i0 < kOsciMaxTensors ? ntensors - i0 : kOsciMaxTensors;
-        std::memset(&a, 0, sizeof(a));
-        fill_tiles(a, rows, cols, i0, cnt);
-        a.xhat_bf16 = xhat_dtype == FQ_BF16;
-        a.seed = cfg->seed;
-        a.offset = cfg->offset;
-        a.amax = static_cast<float *>(workspace);
-        for (int32_t j = 0; j < cnt; ++j) {
-            const int32_t i = i0 + j;
-            OsciTensor &t = a.t[j];
-            t.master = master[i];
-            t.delta = delta[i];
-            t.dist_q = dist_q[i];
-            t.dist_m = dist_m[i];
-            t.pcodes = prev[i].codes;
-            t.pscales = prev[i].scales;
-            t.ptscale = prev[i].tscale;
-            t.ncodes = next[i].codes;
-            t.nscales = next[i].scales;
-            t.ntscale = next[i].tscale;
-            t.xhat = xhat ? xhat[i] : nullptr;
-            t.mask = mask ? mask[i] : nullptr;
-        }
-        cudaError_t e = launch_osci_update(a, fmt, cfg->rounding, s);
-        if (e != cudaSuccess)
-            return FQ_ERR_CUDA;
-    }
-    return FQ_OK;
+    return osci_update_impl(cfg, ntensors, rows, cols, master, delta, dist_q, dist_m, prev, next,
+                            xhat, xhat_dtype, mask, workspace, workspace_bytes, stream, 0, 0.0f,
+                            nullptr);
+}
+
+fq_status fq_osci_update_reset(const fq_config *cfg, int32_t ntensors, const int64_t *rows,
+                               const int64_t *cols, float *const *master,
+                               const float *const *delta, float *const *dist_q,
+                               float *const *dist_m, const fq_qtensor *prev,
+                               const fq_qtensor *next, void *const *xhat, int32_t xhat_dtype,
+                               uint8_t *const *mask, float threshold,
+                               unsigned long long *n_reset, void *workspace,
+                               size_t workspace_bytes, void *stream)
+{
+    return osci_update_impl(cfg, ntensors, rows, cols, master, delta, dist_q, dist_m, prev, next,
+                            xhat, xhat_dtype, mask, workspace, workspace_bytes, stream, 1,
+                            threshold, n_reset);
 }
 
 fq_status fq_osci_reset(const fq_config *cfg, int32_t ntensors, const int64_t *rows,

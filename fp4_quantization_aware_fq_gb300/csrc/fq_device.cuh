@@ -127,16 +127,69 @@ struct Scale {
     uint32_t code;
 };
 
+// 1 / (6 s_outer), rounded; 0 when s_outer = 0.  Used to find block scale
+// codes without dividing (nv_scale_code).
+__device__ __forceinline__ float nv_inv6(float s_outer)
+{
+    return (s_outer == 0.0f) ? 0.0f : __frcp_rn(__fmul_rn(6.0f, s_outer));
+}
+
+// E4M3 code of the block scale s_b = (amax_b / 6) / s_outer (two IEEE
+// divisions, in that order).  amax_b * inv6 is within 5 ulps of s_b (three
+// roundings on each side), so both round to the same E4M3 code unless the
+// product lies within 64 ulps of an E4M3 rounding boundary -- in the E4M3
+// normal range every boundary has FP32 mantissa bits 19..0 equal to 0x80000
+// -- or below 2^-6, where E4M3 is subnormal.  Those rare blocks take the
+// exact divisions.
+__device__ __forceinline__ uint32_t nv_scale_code(float amax_b, float s_outer, float inv6)
+{
+    float sb = __fmul_rn(amax_b, inv6);
+    const uint32_t low = __float_as_uint(sb) & 0xFFFFFu;
+    const bool near = amax_b != 0.0f && ((low - 0x7FFC0u) < 128u || sb < 0.0157f);
+    if (near)
+        sb = (s_outer == 0.0f) ? 0.0f : __fdiv_rn(__fdiv_rn(amax_b, 6.0f), s_outer);
+    return e4m3_rn_sat(sb);
+}
+
 // NVFP4-style inner scale under an outer scale s_outer (the tensor scale s_g
 // for NVFP4, the 1x128 block scale for the double block).
-__device__ __forceinline__ Scale nv_scale(float amax_b, float s_outer)
+__device__ __forceinline__ Scale nv_scale(float amax_b, float s_outer, float inv6)
 {
     Scale s;
-    const float sb = (s_outer == 0.0f) ? 0.0f : __fdiv_rn(__fdiv_rn(amax_b, 6.0f), s_outer);
-    s.code = e4m3_rn_sat(sb);
+    s.code = nv_scale_code(amax_b, s_outer, inv6);
     s.s_eff = __fmul_rn(e4m3_value(s.code), s_outer);
     s.r = (s.s_eff == 0.0f) ? 0.0f : __frcp_rn(s.s_eff);
     s.lim = __fmul_rn(6.0f, s.s_eff);
+    return s;
+}
+
+// Per-code tables of one tensor scale s_g (NVFP4): the effective scale, its
+// reciprocal and 6 s_eff for each of the 127 finite non-negative E4M3 codes.
+// Built once per CTA in shared memory (fill with all threads, then sync).
+struct NvTables {
+    float s_eff[128];
+    float r[128];
+    float lim[128];
+};
+
+__device__ __forceinline__ void nv_tables_fill(NvTables &t, float s_g)
+{
+    for (int c = threadIdx.x; c < 128; c += blockDim.x) {
+        const float se = (c < 0x7F) ? __fmul_rn(e4m3_value(c), s_g) : 0.0f;
+        t.s_eff[c] = se;
+        t.r[c] = (se == 0.0f) ? 0.0f : __frcp_rn(se);
+        t.lim[c] = __fmul_rn(6.0f, se);
+    }
+}
+
+__device__ __forceinline__ Scale nv_scale_tab(float amax_b, float s_g, float inv6,
+                                              const NvTables &t)
+{
+    Scale s;
+    s.code = nv_scale_code(amax_b, s_g, inv6);
+    s.s_eff = t.s_eff[s.code];
+    s.r = t.r[s.code];
+    s.lim = t.lim[s.code];
     return s;
 }
 
@@ -317,13 +370,17 @@ __device__ __forceinline__ uint32_t block_mask(const float *v, float lim)
     return (B == 32) ? ~clip : (~clip & ((1u << B) - 1u));
 }
 
-// Block scale for one block; for the double block, s_outer is the outer scale.
+// Block scale for one block.  NVFP4 reads the per-code tables of its tensor
+// scale; the double block derives its scale from the outer scale s_o.
 template <int FMT>
-__device__ __forceinline__ Scale block_scale(float amax_b, float s_outer)
+__device__ __forceinline__ Scale block_scale(float amax_b, float s_outer, float inv6,
+                                             const NvTables *tab)
 {
     if (FMT == MXFP4)
         return mx_scale(amax_b);
-    return nv_scale(amax_b, s_outer);
+    if (FMT == NVFP4)
+        return nv_scale_tab(amax_b, s_outer, inv6, *tab);
+    return nv_scale(amax_b, s_outer, inv6);
 }
 
 template <typename T, int N>

@@ -78,6 +78,7 @@ struct OsciTensor {
 struct OsciArgs {
     int ntensors;
     int xhat_bf16;
+    int reset;                         // update: also end the OsciReset window
     uint64_t seed;
     uint32_t offset;
     float threshold;

@@ -95,32 +95,46 @@ __global__ void __launch_bounds__(kOsciThreads) osci_pass_a(const __grid_constan
 
 // Pass B: one thread per block of 16 (32 for MXFP4) master weights, NB blocks
 // per thread per iteration with all their loads issued before any compute.
-template <int FMT, int RND>
+// With RESET, this step also ends the OsciReset window: where the new
+// dist_Q exceeds threshold * dist_M, the master weight becomes xhat_t, and
+// both accumulators are written back as zero (the same bits as the separate
+// reset pass after this update).
+template <int FMT, int RND, bool RESET>
 __global__ void __launch_bounds__(kOsciThreads) osci_pass_b(const __grid_constant__ OsciArgs a)
 {
     constexpr int B = FmtInfo<FMT>::B;
     constexpr int BPTILE = kOsciTileChunks * 4 / B;  // blocks per tile
-    constexpr int NB = BPTILE >= 2 * kOsciThreads ? 2 : 1;
+    // two blocks in flight per thread, one when dist_M is read as well
+    constexpr int NB = (!RESET && BPTILE >= 2 * kOsciThreads) ? 2 : 1;
     static_assert(BPTILE % (NB * kOsciThreads) == 0, "tile must split evenly");
+    __shared__ NvTables tab, tabp;  // NVFP4: this step's and the previous step's tensor scale
     const int64_t ntiles = a.tile_start[a.ntensors];
     const PhiloxKey key = philox_key(a.seed);
-    int t = 0;
+    int t = 0, t_tab = -1;
     const int lane = threadIdx.x & 31;
+    unsigned long long cnt = 0;
     for (int64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
         while (a.tile_start[t + 1] <= tile)
             ++t;
         const OsciTensor &T = a.t[t];
         const int64_t nblk = T.n / B;
         const int64_t bbeg = (tile - a.tile_start[t]) * BPTILE;
-        float s_g = 0.0f, s_gp = 0.0f;
+        float s_g = 0.0f, inv6 = 0.0f;
         if (FMT == NVFP4) {
             s_g = outer_scale(__ldg(a.amax + t));
-            s_gp = __ldg(T.ptscale);
+            inv6 = nv_inv6(s_g);
+            if (t != t_tab) {  // uniform across the CTA: rebuild the tables
+                __syncthreads();
+                nv_tables_fill(tab, s_g);
+                nv_tables_fill(tabp, __ldg(T.ptscale));
+                __syncthreads();
+                t_tab = t;
+            }
             if (bbeg == 0 && threadIdx.x == 0)
                 T.ntscale[0] = s_g;
         }
         for (int k = 0; k < BPTILE; k += NB * kOsciThreads) {
-            float v[NB][B], dq[NB][B];
+            float v[NB][B], dq[NB][B], dm[NB][B];
             uint32_t qp[NB][B / 8];
             uint32_t scp[NB];
             float so_p[NB];
@@ -140,6 +154,13 @@ __global__ void __launch_bounds__(kOsciThreads) osci_pass_b(const __grid_constan
                         dq[j][4 * i + 1] = d.y;
                         dq[j][4 * i + 2] = d.z;
                         dq[j][4 * i + 3] = d.w;
+                        if (RESET) {
+                            const float4 e = ldf4_rw(T.dist_m + blk * B + 4 * i);
+                            dm[j][4 * i] = e.x;
+                            dm[j][4 * i + 1] = e.y;
+                            dm[j][4 * i + 2] = e.z;
+                            dm[j][4 * i + 3] = e.w;
+                        }
                     }
                     if (B == 16) {
                         const uint2 p2 = __ldg(reinterpret_cast<const uint2 *>(T.pcodes) + blk);
@@ -153,11 +174,11 @@ __global__ void __launch_bounds__(kOsciThreads) osci_pass_b(const __grid_constan
                         qp[j][3] = p4.w;
                     }
                     scp[j] = __ldg(T.pscales + blk);
-                    so_p[j] = (FMT == NV2L) ? __ldg(T.ptscale + (blk >> 3)) : s_gp;
+                    so_p[j] = (FMT == NV2L) ? __ldg(T.ptscale + (blk >> 3)) : 0.0f;
                 } else {
 #pragma unroll
                     for (int i = 0; i < B; ++i)
-                        v[j][i] = dq[j][i] = 0.0f;
+                        v[j][i] = dq[j][i] = dm[j][i] = 0.0f;
 #pragma unroll
                     for (int w = 0; w < B / 8; ++w)
                         qp[j][w] = 0;
@@ -173,15 +194,19 @@ __global__ void __launch_bounds__(kOsciThreads) osci_pass_b(const __grid_constan
 #pragma unroll
                 for (int i = 0; i < B; ++i)
                     am = fmaxf(am, fabsf(v[j][i]));
-                float s_o = s_g;
-                if (FMT == NV2L)
+                float s_o = s_g, inv6b = inv6;
+                if (FMT == NV2L) {
                     s_o = outer_scale(group_max<8>(am));
-                const Scale sc = block_scale<FMT>(am, s_o);
+                    inv6b = nv_inv6(s_o);
+                }
+                const Scale sc = block_scale<FMT>(am, s_o, inv6b, &tab);
                 uint32_t q[B / 8];
                 encode_block<B, RND>(v[j], sc, key, (uint64_t)blk * B, 0u, a.offset, q);
                 if (!valid)
                     continue;
-                const float seff_p = stored_s_eff<FMT>(scp[j], so_p[j]);
+                const float seff_p = (FMT == NVFP4) ? tabp.s_eff[scp[j] & 127u]
+                                                    : stored_s_eff<FMT>(scp[j], so_p[j]);
+                uint32_t hit = 0;
 #pragma unroll
                 for (int w = 0; w < B / 8; ++w) {
                     float xh[8], xp[8];
@@ -191,8 +216,18 @@ __global__ void __launch_bounds__(kOsciThreads) osci_pass_b(const __grid_constan
                     for (int i = 0; i < 8; ++i) {
                         xh[i] = __fmul_rn(xh[i], sc.s_eff);
                         xp[i] = __fmul_rn(xp[i], seff_p);
-                        dq[j][w * 8 + i] =
+                        const float dn =
                             __fadd_rn(dq[j][w * 8 + i], fabsf(__fsub_rn(xh[i], xp[i])));
+                        if (RESET) {
+                            const int e = w * 8 + i;
+                            if (dn > __fmul_rn(a.threshold, dm[j][e])) {
+                                T.master[blk * B + e] = xh[i];
+                                hit |= 1u << e;
+                            }
+                            dq[j][e] = 0.0f;
+                        } else {
+                            dq[j][w * 8 + i] = dn;
+                        }
                     }
                     if (T.xhat) {
                         if (a.xhat_bf16) {
@@ -207,10 +242,14 @@ __global__ void __launch_bounds__(kOsciThreads) osci_pass_b(const __grid_constan
                     }
                 }
 #pragma unroll
-                for (int i = 0; i < B / 4; ++i)
+                for (int i = 0; i < B / 4; ++i) {
                     stf4(T.dist_q + blk * B + 4 * i,
                          make_float4(dq[j][4 * i], dq[j][4 * i + 1], dq[j][4 * i + 2],
                                      dq[j][4 * i + 3]));
+                    if (RESET)
+                        stf4(T.dist_m + blk * B + 4 * i, make_float4(0.f, 0.f, 0.f, 0.f));
+                }
+                cnt += __popc(hit);
                 if (B == 16)
                     reinterpret_cast<uint2 *>(T.ncodes)[blk] = make_uint2(q[0], q[1]);
                 else
@@ -227,6 +266,13 @@ __global__ void __launch_bounds__(kOsciThreads) osci_pass_b(const __grid_constan
                 }
             }
         }
+    }
+    if (RESET && a.n_reset) {
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1)
+            cnt += __shfl_xor_sync(0xFFFFFFFFu, cnt, o);
+        if (lane == 0 && cnt)
+            atomicAdd(a.n_reset, cnt);
     }
 }
 
@@ -312,13 +358,20 @@ cudaError_t launch_osci_update(const OsciArgs &a, int fmt, int rnd, cudaStream_t
     osci_pass_a<<<grid, kOsciThreads, 0, s>>>(a);
     if ((e = cudaGetLastError()) != cudaSuccess)
         return e;
-    switch (fmt * 2 + rnd) {
-    case NVFP4 * 2 + RNE: osci_pass_b<NVFP4, RNE><<<grid, kOsciThreads, 0, s>>>(a); break;
-    case NVFP4 * 2 + SR: osci_pass_b<NVFP4, SR><<<grid, kOsciThreads, 0, s>>>(a); break;
-    case MXFP4 * 2 + RNE: osci_pass_b<MXFP4, RNE><<<grid, kOsciThreads, 0, s>>>(a); break;
-    case MXFP4 * 2 + SR: osci_pass_b<MXFP4, SR><<<grid, kOsciThreads, 0, s>>>(a); break;
-    case NV2L * 2 + RNE: osci_pass_b<NV2L, RNE><<<grid, kOsciThreads, 0, s>>>(a); break;
-    default: osci_pass_b<NV2L, SR><<<grid, kOsciThreads, 0, s>>>(a); break;
+    const int key = (fmt * 2 + rnd) * 2 + (a.reset ? 1 : 0);
+    switch (key) {
+    case (NVFP4 * 2 + RNE) * 2: osci_pass_b<NVFP4, RNE, false><<<grid, kOsciThreads, 0, s>>>(a); break;
+    case (NVFP4 * 2 + RNE) * 2 + 1: osci_pass_b<NVFP4, RNE, true><<<grid, kOsciThreads, 0, s>>>(a); break;
+    case (NVFP4 * 2 + SR) * 2: osci_pass_b<NVFP4, SR, false><<<grid, kOsciThreads, 0, s>>>(a); break;
+    case (NVFP4 * 2 + SR) * 2 + 1: osci_pass_b<NVFP4, SR, true><<<grid, kOsciThreads, 0, s>>>(a); break;
+    case (MXFP4 * 2 + RNE) * 2: osci_pass_b<MXFP4, RNE, false><<<grid, kOsciThreads, 0, s>>>(a); break;
+    case (MXFP4 * 2 + RNE) * 2 + 1: osci_pass_b<MXFP4, RNE, true><<<grid, kOsciThreads, 0, s>>>(a); break;
+    case (MXFP4 * 2 + SR) * 2: osci_pass_b<MXFP4, SR, false><<<grid, kOsciThreads, 0, s>>>(a); break;
+    case (MXFP4 * 2 + SR) * 2 + 1: osci_pass_b<MXFP4, SR, true><<<grid, kOsciThreads, 0, s>>>(a); break;
+    case (NV2L * 2 + RNE) * 2: osci_pass_b<NV2L, RNE, false><<<grid, kOsciThreads, 0, s>>>(a); break;
+    case (NV2L * 2 + RNE) * 2 + 1: osci_pass_b<NV2L, RNE, true><<<grid, kOsciThreads, 0, s>>>(a); break;
+    case (NV2L * 2 + SR) * 2: osci_pass_b<NV2L, SR, false><<<grid, kOsciThreads, 0, s>>>(a); break;
+    default: osci_pass_b<NV2L, SR, true><<<grid, kOsciThreads, 0, s>>>(a); break;
     }
     return cudaGetLastError();
 }

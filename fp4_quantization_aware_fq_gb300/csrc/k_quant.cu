@@ -75,7 +75,8 @@ struct RowOut {
 // all 32 lanes of the warp must call this together.
 template <int FMT, int RND>
 __device__ __forceinline__ void row_block(const float *v, int64_t blk, bool valid, float s_g,
-                                          const RowOut &o, const PhiloxKey &key, uint32_t offset,
+                                          float inv6, const NvTables *tab, const RowOut &o,
+                                          const PhiloxKey &key, uint32_t offset,
                                           uint32_t stream_id)
 {
     constexpr int B = FmtInfo<FMT>::B;
@@ -84,9 +85,11 @@ __device__ __forceinline__ void row_block(const float *v, int64_t blk, bool vali
     for (int i = 0; i < B; ++i)
         am = fmaxf(am, fabsf(v[i]));
     float s_o = s_g;
-    if (FMT == NV2L)
+    if (FMT == NV2L) {
         s_o = outer_scale(group_max<8>(am));
-    const Scale sc = block_scale<FMT>(am, s_o);
+        inv6 = nv_inv6(s_o);
+    }
+    const Scale sc = block_scale<FMT>(am, s_o, inv6, tab);
     uint32_t q[B / 8];
     encode_block<B, RND>(v, sc, key, (uint64_t)blk * B, stream_id, offset, q);
     if (!valid)
@@ -137,9 +140,13 @@ __global__ void __launch_bounds__(kThreads) row_kernel(RowArgs a)
     constexpr int B = FmtInfo<FMT>::B;
     constexpr int BPT = (B * sizeof(T) >= 64) ? 1 : 2;
     const int64_t nblk = a.n / B;
-    float s_g = 0.0f;
+    __shared__ NvTables tab;
+    float s_g = 0.0f, inv6 = 0.0f;
     if (FMT == NVFP4) {
         s_g = outer_scale(*a.amax);
+        inv6 = nv_inv6(s_g);
+        nv_tables_fill(tab, s_g);
+        __syncthreads();
         if (blockIdx.x == 0 && threadIdx.x == 0 && a.tscale)
             a.tscale[0] = s_g;
     }
@@ -161,7 +168,8 @@ __global__ void __launch_bounds__(kThreads) row_kernel(RowArgs a)
 #pragma unroll
         for (int k = 0; k < BPT; ++k) {
             const int64_t blk = base + k * kThreads + threadIdx.x;
-            row_block<FMT, RND>(v[k], blk, blk < nblk, s_g, o, key, a.offset, a.stream_id);
+            row_block<FMT, RND>(v[k], blk, blk < nblk, s_g, inv6, &tab, o, key, a.offset,
+                                a.stream_id);
         }
     }
 }
@@ -203,9 +211,13 @@ __global__ void __launch_bounds__(kThreads) tile_kernel(TileArgs a)
     const int64_t r0 = (int64_t)blockIdx.y * TR;
     const int64_t c0 = (int64_t)blockIdx.x * TC;
     const int64_t rows = a.rows, cols = a.cols;
-    float s_g = 0.0f;
+    __shared__ NvTables tab;
+    float s_g = 0.0f, inv6 = 0.0f;
     if (FMT == NVFP4) {
         s_g = outer_scale(*a.amax);
+        inv6 = nv_inv6(s_g);
+        nv_tables_fill(tab, s_g);
+        __syncthreads();
         if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) {
             if (a.ctscale)
                 a.ctscale[0] = s_g;
@@ -234,7 +246,8 @@ __global__ void __launch_bounds__(kThreads) tile_kernel(TileArgs a)
             unpack16<T>(raw[k], v + k * E);
         }
         if (a.do_row)
-            row_block<FMT, RND>(v, (gr * cols + gc) / BR, valid, s_g, o, key, a.offset, 0u);
+            row_block<FMT, RND>(v, (gr * cols + gc) / BR, valid, s_g, inv6, &tab, o, key,
+                                a.offset, 0u);
     }
     __syncthreads();
 
@@ -250,48 +263,39 @@ __global__ void __launch_bounds__(kThreads) tile_kernel(TileArgs a)
         }
         __syncthreads();
     }
-    // Two adjacent columns per task: one 4- or 8-byte shared-memory read
-    // serves both.
-    for (int task = threadIdx.x; task < (TC / 2) * NRB; task += kThreads) {
-        const int cp = task % (TC / 2), rb = task / (TC / 2);
-        const int64_t gr0 = r0 + (int64_t)rb * BC;
-        if (c0 + 2 * cp >= cols || gr0 >= rows)
+    for (int task = threadIdx.x; task < TC * NRB; task += kThreads) {
+        const int c = task % TC, rb = task / TC;
+        const int64_t gc = c0 + c, gr0 = r0 + (int64_t)rb * BC;
+        if (gc >= cols || gr0 >= rows)
             continue;
-        float v[2][BC];
-        float m0 = 0.0f, m1 = 0.0f;
+        float v[BC];
+        float m = 0.0f;
 #pragma unroll
         for (int i = 0; i < BC; ++i) {
-            const T *p = tile + (rb * BC + i) * TC + 2 * cp;
-            v[0][i] = static_cast<float>(p[0]);
-            v[1][i] = static_cast<float>(p[1]);
-            m0 = fmaxf(m0, fabsf(v[0][i]));
-            m1 = fmaxf(m1, fabsf(v[1][i]));
+            v[i] = static_cast<float>(tile[(rb * BC + i) * TC + c]);
+            m = fmaxf(m, fabsf(v[i]));
         }
+        float s_o = s_g, inv6c = inv6;
+        if (FMT == NV2L) {
+            float mo = 0.0f;
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            const int c = 2 * cp + h;
-            const int64_t gc = c0 + c;
-            float s_o = s_g;
-            if (FMT == NV2L) {
-                float mo = 0.0f;
-#pragma unroll
-                for (int j = 0; j < NRB; ++j)
-                    mo = fmaxf(mo, am16[j * TC + c]);
-                s_o = outer_scale(mo);
-                if (rb == 0)
-                    a.ctscale[gc * (rows / 128) + r0 / 128] = s_o;
-            }
-            const Scale sc = block_scale<FMT>(h ? m1 : m0, s_o);
-            uint32_t q[BC / 8];
-            // flat index in X^T of the block's first element
-            encode_block<BC, RND>(v[h], sc, key, (uint64_t)gc * (uint64_t)rows + (uint64_t)gr0,
-                                  1u, a.offset, q);
-            uint32_t *dst = reinterpret_cast<uint32_t *>(ccs + c * CP + rb * (BC / 2));
-#pragma unroll
-            for (int w = 0; w < BC / 8; ++w)
-                dst[w] = q[w];
-            css[c * NRB + rb] = (uint8_t)sc.code;
+            for (int j = 0; j < NRB; ++j)
+                mo = fmaxf(mo, am16[j * TC + c]);
+            s_o = outer_scale(mo);
+            inv6c = nv_inv6(s_o);
+            if (rb == 0)
+                a.ctscale[gc * (rows / 128) + r0 / 128] = s_o;
         }
+        const Scale sc = block_scale<FMT>(m, s_o, inv6c, &tab);
+        uint32_t q[BC / 8];
+        // flat index in X^T of the block's first element
+        encode_block<BC, RND>(v, sc, key, (uint64_t)gc * (uint64_t)rows + (uint64_t)gr0, 1u,
+                              a.offset, q);
+        uint32_t *dst = reinterpret_cast<uint32_t *>(ccs + c * CP + rb * (BC / 2));
+#pragma unroll
+        for (int w = 0; w < BC / 8; ++w)
+            dst[w] = q[w];
+        css[c * NRB + rb] = (uint8_t)sc.code;
     }
     __syncthreads();
 

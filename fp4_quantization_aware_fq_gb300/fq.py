@@ -122,9 +122,12 @@ def lib():
                                     ctypes.c_float, vp, vp]
         L.fq_osci_update_noalloc.argtypes = [P(Config), i32, P(i64), P(i64), P(vp), P(vp), P(vp),
                                              P(vp), P(_QT), P(_QT), P(vp), i32, P(vp), vp]
+        L.fq_osci_update_reset.argtypes = [P(Config), i32, P(i64), P(i64), P(vp), P(vp), P(vp),
+                                           P(vp), P(_QT), P(_QT), P(vp), i32, P(vp),
+                                           ctypes.c_float, vp, vp, sz, vp]
         for name in ("fq_amax", "fq_quantize", "fq_fakequant_ste", "fq_dequantize",
                      "fq_ste_backward", "fq_osci_update", "fq_osci_reset",
-                     "fq_osci_update_noalloc"):
+                     "fq_osci_update_noalloc", "fq_osci_update_reset"):
             getattr(L, name).restype = ctypes.c_int
         L.fq_status_string.argtypes = [ctypes.c_int]
         L.fq_status_string.restype = ctypes.c_char_p
@@ -288,6 +291,36 @@ def fq_osci_update(cfg: Config, master: Sequence[torch.Tensor], delta: Sequence[
         None if mask is None else _arr(vp, [t.data_ptr() for t in mask]),
         ws.data_ptr(), ws.numel(), _stream(stream))
     _check(st, "fq_osci_update")
+
+
+def fq_osci_update_reset(cfg: Config, master: Sequence[torch.Tensor],
+                         delta: Sequence[torch.Tensor], dist_q: Sequence[torch.Tensor],
+                         dist_m: Sequence[torch.Tensor], prev: Sequence[QTensor],
+                         nxt: Sequence[QTensor], threshold: float = 4.0,
+                         n_reset: Optional[torch.Tensor] = None,
+                         xhat: Optional[Sequence[torch.Tensor]] = None, xhat_dtype=torch.bfloat16,
+                         mask: Optional[Sequence[torch.Tensor]] = None,
+                         ws: Optional[torch.Tensor] = None, stream=None):
+    """The window's last update step with the OsciReset reset fused in."""
+    n = len(master)
+    vp, i64 = ctypes.c_void_p, ctypes.c_int64
+    rows = _arr(i64, [m.shape[0] for m in master])
+    cols = _arr(i64, [m.shape[1] for m in master])
+    if ws is None:
+        ws = torch.empty(max(fq_osci_workspace_size(n), 16), dtype=torch.uint8,
+                         device=master[0].device)
+    pq = (_QT * max(n, 1))(*[q._c() for q in prev])
+    nq = (_QT * max(n, 1))(*[q._c() for q in nxt])
+    st = lib().fq_osci_update_reset(
+        ctypes.byref(cfg), n, rows, cols, _arr(vp, [t.data_ptr() for t in master]),
+        _arr(vp, [t.data_ptr() for t in delta]), _arr(vp, [t.data_ptr() for t in dist_q]),
+        _arr(vp, [t.data_ptr() for t in dist_m]), pq, nq,
+        None if xhat is None else _arr(vp, [t.data_ptr() for t in xhat]),
+        BF16 if xhat_dtype == torch.bfloat16 else F32,
+        None if mask is None else _arr(vp, [t.data_ptr() for t in mask]), float(threshold),
+        _ptr(n_reset), ws.data_ptr(), ws.numel(), _stream(stream))
+    _check(st, "fq_osci_update_reset")
+    return n_reset
 
 
 def fq_osci_update_noalloc(cfg: Config, master: Sequence[torch.Tensor],

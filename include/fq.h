@@ -187,6 +187,24 @@ FQ_API fq_status fq_osci_update(const fq_config *cfg, int32_t ntensors, const in
                          uint8_t *const *mask, void *workspace, size_t workspace_bytes,
                          void *stream);
 
+/* fq_osci_update for the last step of an OsciReset window ([TJV2] §2B): the
+ * update, then in the same pass over the weights the reset that
+ * fq_osci_reset would apply to this step's result -- where the new
+ * dist_Q > threshold * dist_M (FP32 product, strict) the master weight becomes
+ * xhat_t (FP32), and dist_Q and dist_M are left at zero for every weight.
+ * Bit-identical to fq_osci_update followed by fq_osci_reset(cur = next), but
+ * it reads dist_M once more instead of making a separate pass over both
+ * accumulators.  Outputs (next, xhat, mask) describe w_t before the reset.
+ * n_reset (device uint64, may be NULL) receives the number of weights reset. */
+FQ_API fq_status fq_osci_update_reset(const fq_config *cfg, int32_t ntensors, const int64_t *rows,
+                                      const int64_t *cols, float *const *master,
+                                      const float *const *delta, float *const *dist_q,
+                                      float *const *dist_m, const fq_qtensor *prev,
+                                      const fq_qtensor *next, void *const *xhat,
+                                      int32_t xhat_dtype, uint8_t *const *mask, float threshold,
+                                      unsigned long long *n_reset, void *workspace,
+                                      size_t workspace_bytes, void *stream);
+
 /* fq_osci_update without a workspace argument.  The pages have no counterpart
  * to this entry point; it exists for callers that cannot allocate device
  * memory where they run the optimizer step (a framework whose allocator owns

@@ -82,6 +82,34 @@ def test_osci_group_matches_oracle(fmt, rnd):
         _compare(f"reset.{i}", g, i, st)
 
 
+@pytest.mark.parametrize("fmt,rnd", [(fq.NVFP4, fq.RNE), (fq.NVFP4_2LEVEL, fq.SR),
+                                     (fq.MXFP4, fq.RNE)])
+def test_fused_window_end_reset_matches_update_then_reset(fmt, rnd):
+    """fq_osci_update_reset == fq_osci_update followed by fq_osci_reset, and
+    both equal the oracle's step + reset."""
+    shapes = [(64, 256), (128, 384), (32, 128)]
+    ws = [W.normal(s, 0.02, seed=80 + i).to(torch.bfloat16) for i, s in enumerate(shapes)]
+    cfg = fq.Config(fmt, rnd, seed=5)
+    g = GpuOsci(ws, cfg)
+    sts = [oracle.OsciState(w.float().numpy(), FMT_O[fmt], rnd, seed=5) for w in ws]
+    for t in range(1, 4):
+        deltas = [W.master_update(s, t, std=3e-3) for s in shapes]
+        c = fq.Config(fmt, rnd, 5, t)
+        if t < 3:
+            g.step([d.to(DEV) for d in deltas], t)
+        else:
+            cnt = torch.zeros(1, dtype=torch.int64, device=DEV)
+            fq.fq_osci_update_reset(c, g.master, [d.to(DEV) for d in deltas], g.dq, g.dm,
+                                    g.prev, g.next, 4.0, n_reset=cnt, xhat=g.xhat, mask=g.mask)
+            g.prev, g.next = g.next, g.prev
+        torch.cuda.synchronize()
+        outs = [st.step(d.numpy(), offset=t) for st, d in zip(sts, deltas)]
+    total = sum(st.reset(4.0) for st in sts)
+    assert int(cnt.item()) == total and total > 0
+    for i, st in enumerate(sts):
+        _compare(f"fused.{i}", g, i, st, outs[i])
+
+
 def test_osci_flip_example():
     with open(os.path.join(os.path.dirname(__file__), "golden", "osci_flip_e4.json")) as f:
         gd = json.load(f)

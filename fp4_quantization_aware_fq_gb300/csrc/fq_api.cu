@@ -76,9 +76,7 @@ fq_status quantize_common(const fq_config *cfg, const void *x, int32_t x_dtype, 
         const int64_t rm = fmt == FQ_NVFP4_2LEVEL ? 128 : block_len(fmt);
         if (rows % rm != 0 || cols % 16 != 0)
             return FQ_ERR_SHAPE;
-        const int64_t tr = fmt == FQ_NVFP4_2LEVEL ? 128 : 64;
-        if ((rows + tr - 1) / tr > 65535)
-            return FQ_ERR_SHAPE;
+
     }
     if (!aligned16(x) || (xhat && !aligned16(xhat)) || (mask && !aligned16(mask)) ||
         (amax_in && (reinterpret_cast<uintptr_t>(amax_in) & 3u)))

@@ -208,8 +208,6 @@ __global__ void __launch_bounds__(kThreads) tile_kernel(TileArgs a)
     uint8_t *css = ccs + (size_t)TC * CP;                // [TC][NRB]
     float *am16 = reinterpret_cast<float *>(css + (size_t)TC * NRB);  // [NRB][TC]
 
-    const int64_t r0 = (int64_t)blockIdx.y * TR;
-    const int64_t c0 = (int64_t)blockIdx.x * TC;
     const int64_t rows = a.rows, cols = a.cols;
     __shared__ NvTables tab;
     float s_g = 0.0f, inv6 = 0.0f;
@@ -218,18 +216,25 @@ __global__ void __launch_bounds__(kThreads) tile_kernel(TileArgs a)
         inv6 = nv_inv6(s_g);
         nv_tables_fill(tab, s_g);
         __syncthreads();
-        if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) {
+        if (blockIdx.x == 0 && threadIdx.x == 0) {
             if (a.ctscale)
                 a.ctscale[0] = s_g;
             if (a.do_row && a.rtscale)
                 a.rtscale[0] = s_g;
         }
     }
+    const RowOut o{a.rcodes, a.rscales, a.rtscale, a.xhat, a.xhat_bf16, a.mask};
+    const PhiloxKey key = philox_key(a.seed);
+    const int64_t ntc = (cols + TC - 1) / TC;
+    const int64_t ntiles = ntc * ((rows + TR - 1) / TR);
+
+    // Persistent CTAs walk the tiles in row-major order.
+    for (int64_t tile_id = blockIdx.x; tile_id < ntiles; tile_id += gridDim.x) {
+    const int64_t r0 = (tile_id / ntc) * TR;
+    const int64_t c0 = (tile_id % ntc) * TC;
 
     // Phase 1: each thread loads whole row blocks (16-byte vectors), stages
     // them in shared memory and, when asked, runs the row-wise pass on them.
-    const RowOut o{a.rcodes, a.rscales, a.rtscale, a.xhat, a.xhat_bf16, a.mask};
-    const PhiloxKey key = philox_key(a.seed);
     for (int t = threadIdx.x; t < TR * RBPR; t += kThreads) {
         const int tr = t / RBPR, tb = t % RBPR;
         const int64_t gr = r0 + tr, gc = c0 + (int64_t)tb * BR;
@@ -314,6 +319,8 @@ __global__ void __launch_bounds__(kThreads) tile_kernel(TileArgs a)
         if (gc < cols && gr < rows)
             a.cscales[gc * (rows / BC) + gr / BC] = css[c * NRB + j];
     }
+    __syncthreads();  // the next tile overwrites the tile and staging buffers
+    }
 }
 
 // ------------------------------------------------------------------ launchers
@@ -396,7 +403,13 @@ static cudaError_t tile_go(const TileArgs &a, cudaStream_t s)
         if (e != cudaSuccess)
             return e;
     }
-    dim3 grid((unsigned)((a.cols + S::TC - 1) / S::TC), (unsigned)((a.rows + S::TR - 1) / S::TR));
+    const int64_t ntiles = ((a.cols + S::TC - 1) / S::TC) * ((a.rows + S::TR - 1) / S::TR);
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, tile_kernel<T, FMT, RND>, kThreads,
+                                                      smem) != cudaSuccess || per_sm < 1)
+        per_sm = 1;
+    const int64_t cap = (int64_t)sm_count() * per_sm;
+    const unsigned grid = (unsigned)(ntiles < cap ? ntiles : cap);
     tile_kernel<T, FMT, RND><<<grid, kThreads, smem, s>>>(a);
     return cudaGetLastError();
 }

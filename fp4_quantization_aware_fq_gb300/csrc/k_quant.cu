@@ -228,27 +228,57 @@ __global__ void __launch_bounds__(kThreads) tile_kernel(TileArgs a)
     const int64_t ntc = (cols + TC - 1) / TC;
     const int64_t ntiles = ntc * ((rows + TR - 1) / TR);
 
+    // Each thread owns RPT row blocks of a tile.  The loads of the next tile
+    // are issued before the current tile is processed, so they overlap its
+    // column pass and write-out.
+    constexpr int RPT = (TR * RBPR + kThreads - 1) / kThreads;
+    uint4 nxt[RPT][BR / E];
+    auto load_tile = [&](int64_t id) {
+        const int64_t lr0 = (id / ntc) * TR, lc0 = (id % ntc) * TC;
+#pragma unroll
+        for (int j = 0; j < RPT; ++j) {
+            const int t = threadIdx.x + j * kThreads;
+            const int tr = t / RBPR, tb = t % RBPR;
+            const int64_t gr = lr0 + tr, gc = lc0 + (int64_t)tb * BR;
+            const bool valid = t < TR * RBPR && gr < rows && gc < cols;
+#pragma unroll
+            for (int k = 0; k < BR / E; ++k)
+                nxt[j][k] = valid ? ld16((const char *)a.x +
+                                         ((gr * cols + gc) + k * E) * (int64_t)sizeof(T))
+                                  : make_uint4(0, 0, 0, 0);
+        }
+    };
+    if ((int64_t)blockIdx.x < ntiles)
+        load_tile(blockIdx.x);
+
     // Persistent CTAs walk the tiles in row-major order.
     for (int64_t tile_id = blockIdx.x; tile_id < ntiles; tile_id += gridDim.x) {
     const int64_t r0 = (tile_id / ntc) * TR;
     const int64_t c0 = (tile_id % ntc) * TC;
+    uint4 cur[RPT][BR / E];
+#pragma unroll
+    for (int j = 0; j < RPT; ++j)
+#pragma unroll
+        for (int k = 0; k < BR / E; ++k)
+            cur[j][k] = nxt[j][k];
+    if (tile_id + gridDim.x < ntiles)
+        load_tile(tile_id + gridDim.x);
 
-    // Phase 1: each thread loads whole row blocks (16-byte vectors), stages
-    // them in shared memory and, when asked, runs the row-wise pass on them.
-    for (int t = threadIdx.x; t < TR * RBPR; t += kThreads) {
+    // Phase 1: stage the tile's row blocks in shared memory and, when asked,
+    // run the row-wise pass on them.
+#pragma unroll
+    for (int j = 0; j < RPT; ++j) {
+        const int t = threadIdx.x + j * kThreads;
+        if (RPT * kThreads > TR * RBPR && t >= TR * RBPR)
+            break;
         const int tr = t / RBPR, tb = t % RBPR;
         const int64_t gr = r0 + tr, gc = c0 + (int64_t)tb * BR;
         const bool valid = gr < rows && gc < cols;
         float v[BR];
-        uint4 raw[BR / E];
-#pragma unroll
-        for (int k = 0; k < BR / E; ++k)
-            raw[k] = valid ? ld16((const char *)a.x + ((gr * cols + gc) + k * E) * (int64_t)sizeof(T))
-                           : make_uint4(0, 0, 0, 0);
 #pragma unroll
         for (int k = 0; k < BR / E; ++k) {
-            *reinterpret_cast<uint4 *>(tile + tr * TC + tb * BR + k * E) = raw[k];
-            unpack16<T>(raw[k], v + k * E);
+            *reinterpret_cast<uint4 *>(tile + tr * TC + tb * BR + k * E) = cur[j][k];
+            unpack16<T>(cur[j][k], v + k * E);
         }
         if (a.do_row)
             row_block<FMT, RND>(v, (gr * cols + gc) / BR, valid, s_g, inv6, &tab, o, key,

@@ -386,10 +386,10 @@ def oracle_sample(max_seconds=None):
     x1 = W.nvfp4_small().numpy()
     res["nvfp4_small"] = (x1.size, timed(lambda: oracle.quantize(
         x1, oracle.NVFP4, want_xhat=True, want_mask=True)))
-    x2 = f32(W.mxfp4_weight(shape=(2048, 4096), seed=1))
+    x2 = f32(W.mxfp4_weight(shape=(4096, 4096), seed=1))
     res["mxfp4_weight"] = (x2.size, timed(lambda: oracle.quantize(
         x2, oracle.MXFP4, want_xhat=True, want_mask=True)))
-    x3 = f32(W.nvfp4_act(shape=(1024, 8192), seed=2))
+    x3 = f32(W.nvfp4_act(shape=(4096, 8192), seed=2))
 
     def c3():
         q = oracle.quantize(x3, oracle.NVFP4, orient=oracle.ROWCOL, want_xhat=True,
@@ -402,22 +402,22 @@ def oracle_sample(max_seconds=None):
     res["nvfp4_act"] = (x3.size, time.perf_counter() - t)
     dy = W.bf16_bits(W.normal(x3.shape, 1.0, seed=12, dtype=__import__("torch").bfloat16))
     res["ste_backward"] = (dy.size, timed(lambda: oracle.ste_backward(dy, q3["row"]["mask"])))
-    x4 = f32(W.grad_2level(shape=(2048, 4096), seed=3))
+    x4 = f32(W.grad_2level(shape=(8192, 4096), seed=3))
     res["grad_2level"] = (x4.size, timed(lambda: oracle.quantize(
         x4, oracle.NVFP4_2LEVEL, oracle.SR, 0x5EED)))
-    w = W.normal((2880, 5760), 0.02, seed=4).to(__import__("torch").bfloat16)
+    w = W.normal((5760, 5760), 0.02, seed=4).to(__import__("torch").bfloat16)
     st = oracle.OsciState(f32(w), oracle.NVFP4)
-    d = W.master_update((2880, 5760), 1).numpy()
+    d = W.master_update((5760, 5760), 1).numpy()
 
     def upd():
         out = st.step(d, offset=1)
         oracle.f32_to_bf16_bits(out["xhat"])
     t_upd = timed(upd)
     res["osci_update_reset"] = (w.numel(), t_upd + timed(lambda: st.reset(4.0)))
-    desc = ("oracle (scalar C, 1 thread) on: nvfp4_small full; mxfp4_weight 2048 rows; "
-            "nvfp4_act 1024 rows row+col; ste_backward 1024x8192; grad_2level 2048 rows SR; "
-            "osci update+reset on one full [2880, 5760] matrix; per-element rates scaled to "
-            "the full step's elements")
+    desc = ("oracle (scalar C, 1 thread) on: nvfp4_small full; mxfp4_weight full; "
+            "nvfp4_act 4096 rows row+col; ste_backward 4096x8192; grad_2level 8192 rows SR; "
+            "osci update+reset on a [5760, 5760] matrix (one expert's weights); per-element "
+            "rates scaled to the full step's elements")
     return res, desc
 
 

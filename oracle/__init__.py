@@ -72,6 +72,9 @@ def _load():
         lib.fqo_philox4x32_10.argtypes = [vp, vp, vp]; lib.fqo_philox4x32_10.restype = None
         lib.fqo_sr_draw.argtypes = [u64, u64, u32, u32]; lib.fqo_sr_draw.restype = ctypes.c_uint
         lib.fqo_amax.argtypes = [vp, i64]; lib.fqo_amax.restype = f32
+        lib.fqo_rht_signs.argtypes = [u32, u32]; lib.fqo_rht_signs.restype = ctypes.c_uint
+        lib.fqo_rht16.argtypes = [vp, ctypes.c_uint]; lib.fqo_rht16.restype = None
+        lib.fqo_rht_rows.argtypes = [vp, i64, i64, u32, u32]; lib.fqo_rht_rows.restype = None
         lib.fqo_quantize_rows.argtypes = [i32, i32, u64, u32, u32, vp, i64, i64, f32,
                                           vp, vp, vp, vp, vp]
         lib.fqo_quantize_rows.restype = i32
@@ -157,6 +160,25 @@ def f32_to_bf16_bits(x: np.ndarray) -> np.ndarray:
     return out.reshape(np.shape(x))
 
 
+def rht_signs(rht_seed: int, offset: int = 0) -> int:
+    return _load().fqo_rht_signs(rht_seed, offset)
+
+
+def rht16(block, signs: int) -> np.ndarray:
+    z = np.ascontiguousarray(block, dtype=np.float32).copy()
+    assert z.size == 16
+    _load().fqo_rht16(_ptr(z), signs)
+    return z
+
+
+def rht_rows(x: np.ndarray, rht_seed: int, offset: int = 0) -> np.ndarray:
+    """The 16-point randomized Hadamard transform of every 1x16 block (a copy)."""
+    z = np.ascontiguousarray(x, dtype=np.float32).copy()
+    rows, cols = z.shape
+    _load().fqo_rht_rows(_ptr(z), rows, cols, rht_seed, offset)
+    return z
+
+
 def amax(x: np.ndarray) -> float:
     x = np.ascontiguousarray(x, dtype=np.float32)
     return _load().fqo_amax(_ptr(x), x.size)
@@ -199,22 +221,32 @@ def _quantize_rows(x, fmt, rounding, seed, offset, stream, tensor_amax,
 
 
 def quantize(x, fmt=NVFP4, rounding=RNE, seed=0, offset=0, orient=ROW,
-             want_xhat=False, want_mask=False, amax_in=None):
+             want_xhat=False, want_mask=False, amax_in=None, rht_seed=0):
     """Quantize a float32 [rows, cols] array.
 
     Row-wise outputs under "row"; for the column-wise orientation the row-wise
     definition is applied to the transpose (stream 1), with the same tensor
     amax (NVFP4), and returned under "col" (codes [cols, rows/2] etc.).
     xhat and mask are produced by the row-wise pass only.
+    rht_seed != 0: each orientation first applies the 16-point randomized
+    Hadamard transform to its own 1x16 blocks, and the NVFP4 tensor amax is
+    that of the transformed tensor of the orientation.
     """
     x = np.ascontiguousarray(x, dtype=np.float32)
-    t_amax = amax(x) if amax_in is None else float(amax_in)
-    res = {"amax": np.float32(t_amax)}
+    res = {}
     if orient & ROW:
-        res["row"] = _quantize_rows(x, fmt, rounding, seed, offset, 0, t_amax,
+        xr = rht_rows(x, rht_seed, offset) if rht_seed else x
+        t_amax = amax(xr) if amax_in is None else float(amax_in)
+        res["amax"] = np.float32(t_amax)
+        res["row"] = _quantize_rows(xr, fmt, rounding, seed, offset, 0, t_amax,
                                     want_xhat, want_mask)
     if orient & COL:
         xt = np.ascontiguousarray(x.T)
+        if rht_seed:
+            xt = rht_rows(xt, rht_seed, offset)
+        t_amax = amax(xt) if amax_in is None else float(amax_in)
+        res.setdefault("amax", np.float32(t_amax))
+        res["col_amax"] = np.float32(t_amax)
         res["col"] = _quantize_rows(xt, fmt, rounding, seed, offset, 1, t_amax, False, False)
     return res
 

@@ -237,6 +237,53 @@ unsigned fqo_sr_draw(uint64_t seed, uint64_t idx, uint32_t stream, uint32_t offs
 }
 
 /* ------------------------------------------------------------------------ */
+/* Random Hadamard transform ("Resumo Técnico: TetraJet-v2", §2C: RHT on the  */
+/* backward operands spreads outlier energy across channels).  Reading: a     */
+/* 16-point transform along each quantization block, z = (1/4) H16 (d . x),   */
+/* with the random signs d shared by every block of the call.  The butterfly  */
+/* order is fixed (strides 1, 2, 4, 8; a, b -> a + b, a - b), each step one    */
+/* FP32 addition, then the exact scaling by 1/4.                              */
+/* ------------------------------------------------------------------------ */
+
+/* The 16 sign bits: bit i set means d_i = -1.  Drawn from Philox with key
+ * (rht_seed, 0) and counter (0, 0, 2, offset); the low 16 bits of word 0. */
+unsigned fqo_rht_signs(uint32_t rht_seed, uint32_t offset)
+{
+    uint32_t ctr[4] = {0, 0, 2, offset};
+    uint32_t key[2] = {rht_seed, 0};
+    uint32_t out[4];
+    fqo_philox4x32_10(ctr, key, out);
+    return out[0] & 0xFFFFu;
+}
+
+void fqo_rht16(float *z, unsigned signs)
+{
+    for (int i = 0; i < 16; i++)
+        if ((signs >> i) & 1u)
+            z[i] = -z[i];
+    for (int h = 1; h < 16; h *= 2) {
+        for (int i = 0; i < 16; i++) {
+            if (i & h)
+                continue;
+            float a = z[i], b = z[i + h];
+            z[i] = a + b;
+            z[i + h] = a - b;
+        }
+    }
+    for (int i = 0; i < 16; i++)
+        z[i] = z[i] * 0.25f;
+}
+
+/* Applies fqo_rht16 to every 1x16 block of a dense [rows, cols] array in place. */
+void fqo_rht_rows(float *x, int64_t rows, int64_t cols, uint32_t rht_seed, uint32_t offset)
+{
+    unsigned signs = fqo_rht_signs(rht_seed, offset);
+    for (int64_t r = 0; r < rows; r++)
+        for (int64_t c = 0; c + 16 <= cols; c += 16)
+            fqo_rht16(x + r * cols + c, signs);
+}
+
+/* ------------------------------------------------------------------------ */
 /* Tensor operations.                                                         */
 /* ------------------------------------------------------------------------ */
 float fqo_amax(const float *x, int64_t n)

@@ -8,6 +8,8 @@ One step = one pass of the whole hot path over the five synthetic workloads:
                 activation with 8 outlier channels: both codes/scales, BF16 xhat, STE mask;
                 then the STE backward of a BF16 gradient of the same shape
   grad_2level   double-block NVFP4 with stochastic rounding, BF16 [16384, 4096] Laplace gradient
+  grad_rht_rowcol  the same kind of gradient as a backward-GEMM operand: 16-point random
+                Hadamard transform + double-block SR, row 1x16 and column 16x1 in one call
   moe_qat       one QAT step over 32 MoE experts (64 FP32 master matrices [2880, 5760] and
                 [5760, 2880], 1.06 G weights): update + NVFP4 fake-quant + OsciReset
                 statistics, then the OsciReset reset pass over the same weights
@@ -45,11 +47,12 @@ BYTES_PER_ELEM = {
     "nvfp4_act": 2 + 2 + 0.5 + 1 / 16 + 0.5 + 1 / 16 + 2 + 1 / 8,
     "ste_backward": 2 + 1 / 8 + 2,
     "grad_2level": 2 + 0.5 + 1 / 16 + 4 / 128,
+    "grad_rht_rowcol": 2 + 2 * (0.5 + 1 / 16 + 4 / 128),
     "osci_update_reset": 20 + (4 + 0.5 + 1 / 16 + 8 + 8 + 0.5 + 1 / 16 + 2 + 1 / 8),
 }
 # Our kernels launched per step (memsets not counted).
 LAUNCHES_PER_STEP = {"nvfp4_small": 2, "mxfp4_weight": 1, "nvfp4_act": 2, "ste_backward": 1,
-                     "grad_2level": 1, "osci_update_reset": 2}
+                     "grad_2level": 1, "grad_rht_rowcol": 1, "osci_update_reset": 2}
 # DRAM traffic per launch of the dominant call from an ncu capture, valid only
 # for the kernel source it was taken on (sha256 of k_osci.cu).  Captured on the
 # 2-expert case (66.4 M weights: pass A + pass B read+write 2852.8 MB) and
@@ -138,7 +141,7 @@ class Suite:
     profiling a smaller case of the same kernels)."""
 
     ORDER = ("nvfp4_small", "mxfp4_weight", "nvfp4_act", "ste_backward", "grad_2level",
-             "osci_update_reset")
+             "grad_rht_rowcol", "osci_update_reset")
 
     def __init__(self, dev, only=None, experts=None):
         import torch
@@ -185,6 +188,13 @@ class Suite:
             self.cfg4 = fq.Config(fq.NVFP4_2LEVEL, fq.SR, 0x5EED, 0)
             self.q4 = fq.alloc_qtensor(*self.x4.shape, fq.NVFP4_2LEVEL, dev)
             self.elems["grad_2level"] = self.x4.numel()
+        if "grad_rht_rowcol" in want:
+            self.x6 = W.grad_2level(seed=6, device=dev)
+            self.cfg6 = fq.Config(fq.NVFP4_2LEVEL, fq.SR, 0x5EED, 0, rht_seed=0xB00F)
+            r6, c6 = self.x6.shape
+            self.rq6 = fq.alloc_qtensor(r6, c6, fq.NVFP4_2LEVEL, dev)
+            self.cq6 = fq.alloc_qtensor(c6, r6, fq.NVFP4_2LEVEL, dev)
+            self.elems["grad_rht_rowcol"] = self.x6.numel()
         if "osci_update_reset" in want:
             m = W.WORKLOADS["moe_qat"]
             ws = W.moe_weights(experts or m["experts"], m["up_shape"], m["down_shape"],
@@ -235,6 +245,12 @@ class Suite:
     def grad_2level(self):
         self.cfg4.offset = self.step_no
         self.fq.fq_quantize(self.x4, self.cfg4, row_out=self.q4)
+
+    def grad_rht_rowcol(self):
+        # backward operand: Hadamard transform + double-block SR, both orientations
+        self.cfg6.offset = self.step_no
+        self.fq.fq_quantize(self.x6, self.cfg6, orient=self.fq.ROWCOL, row_out=self.rq6,
+                            col_out=self.cq6)
 
     def osci_update_reset(self):
         # one QAT step that also ends the OsciReset window (reset fused in)
@@ -330,6 +346,10 @@ def e2e_buffers(suite):
     if "grad_2level" in suite.names:
         ins.append(suite.x4)
         outs += [suite.q4.codes, suite.q4.scales, suite.q4.tscale]
+    if "grad_rht_rowcol" in suite.names:
+        ins.append(suite.x6)
+        outs += [suite.rq6.codes, suite.rq6.scales, suite.rq6.tscale, suite.cq6.codes,
+                 suite.cq6.scales, suite.cq6.tscale]
     if "osci_update_reset" in suite.names:
         ins += list(suite.delta)
         outs.append(suite.nreset)
@@ -405,6 +425,9 @@ def oracle_sample(max_seconds=None):
     x4 = f32(W.grad_2level(shape=(8192, 4096), seed=3))
     res["grad_2level"] = (x4.size, timed(lambda: oracle.quantize(
         x4, oracle.NVFP4_2LEVEL, oracle.SR, 0x5EED)))
+    x6 = f32(W.grad_2level(shape=(2048, 4096), seed=6))
+    res["grad_rht_rowcol"] = (x6.size, timed(lambda: oracle.quantize(
+        x6, oracle.NVFP4_2LEVEL, oracle.SR, 0x5EED, orient=oracle.ROWCOL, rht_seed=0xB00F)))
     w = W.normal((5760, 5760), 0.02, seed=4).to(__import__("torch").bfloat16)
     st = oracle.OsciState(f32(w), oracle.NVFP4)
     d = W.master_update((5760, 5760), 1).numpy()
@@ -416,6 +439,7 @@ def oracle_sample(max_seconds=None):
     res["osci_update_reset"] = (w.numel(), t_upd + timed(lambda: st.reset(4.0)))
     desc = ("oracle (scalar C, 1 thread) on: nvfp4_small full; mxfp4_weight full; "
             "nvfp4_act 4096 rows row+col; ste_backward 4096x8192; grad_2level 8192 rows SR; "
+            "grad_rht_rowcol 2048 rows; "
             "osci update+reset on a [5760, 5760] matrix (one expert's weights); per-element "
             "rates scaled to the full step's elements")
     return res, desc
@@ -433,7 +457,8 @@ def oracle_gbs(sample, elems_full):
 
 FULL_ELEMS = {"nvfp4_small": 256 * 1024, "mxfp4_weight": 4096 * 4096,
               "nvfp4_act": 8192 * 8192, "ste_backward": 8192 * 8192,
-              "grad_2level": 16384 * 4096, "osci_update_reset": 32 * 2 * 2880 * 5760}
+              "grad_2level": 16384 * 4096, "grad_rht_rowcol": 16384 * 4096,
+              "osci_update_reset": 32 * 2 * 2880 * 5760}
 
 
 def config_block(names=None, experts=None):
@@ -445,7 +470,9 @@ def config_block(names=None, experts=None):
                         "step): nvfp4_small fp32 256x1024 NVFP4 RNE; mxfp4_weight bf16 "
                         "4096x4096 MXFP4 RNE quant+dequant; nvfp4_act bf16 8192x8192 NVFP4 "
                         "row 1x16 + col 16x1 + xhat + STE mask, then STE backward; grad_2level "
-                        "bf16 16384x4096 double-block NVFP4 SR; moe_qat 32 experts x "
+                        "bf16 16384x4096 double-block NVFP4 SR; grad_rht_rowcol the same "
+                        "gradient with the 16-point Hadamard transform, both orientations; "
+                        "moe_qat 32 experts x "
                         "(2880x5760 + 5760x2880) FP32 master: one QAT step with OsciReset "
                         "statistics and the window-end reset fused in",
             "elements_per_step": sum(FULL_ELEMS.values()),

@@ -68,6 +68,8 @@ fq_status quantize_common(const fq_config *cfg, const void *x, int32_t x_dtype, 
     if (rows < 0 || cols < 0)
         return FQ_ERR_SHAPE;
     const int fmt = cfg->format;
+    if (cfg->rht_seed && fmt == FQ_NVFP4)
+        return FQ_ERR_UNSUPPORTED;
     const bool do_row = want_row_q || xhat || mask;
     const bool do_col = col_out != nullptr;
     if (do_row && cols % row_multiple(fmt) != 0)
@@ -122,6 +124,7 @@ fq_status quantize_common(const fq_config *cfg, const void *x, int32_t x_dtype, 
         a.seed = cfg->seed;
         a.offset = cfg->offset;
         a.stream_id = 0;
+        a.rht_seed = cfg->rht_seed;
         return cuda_status(launch_row(a, bf16, fmt, cfg->rounding, s));
     }
     TileArgs t{};
@@ -143,6 +146,7 @@ fq_status quantize_common(const fq_config *cfg, const void *x, int32_t x_dtype, 
     t.ctscale = col_out->tscale;
     t.seed = cfg->seed;
     t.offset = cfg->offset;
+    t.rht_seed = cfg->rht_seed;
     return cuda_status(launch_tile(t, bf16, fmt, cfg->rounding, s));
 }
 
@@ -183,6 +187,8 @@ static fq_status osci_update_impl(const fq_config *cfg, int32_t ntensors, const 
 {
     if (!valid_cfg(cfg))
         return FQ_ERR_INVALID_ARG;
+    if (cfg->rht_seed)
+        return FQ_ERR_UNSUPPORTED;
     const int fmt = cfg->format;
     fq_status st = check_group(ntensors, rows, cols, fmt);
     if (st != FQ_OK)

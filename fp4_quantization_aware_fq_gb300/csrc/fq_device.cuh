@@ -263,6 +263,39 @@ __device__ __forceinline__ uint4 sr_bits8(const PhiloxKey &k, uint64_t g, uint32
     return philox4x32_10(make_uint4((uint32_t)g, (uint32_t)(g >> 32), stream, offset), k);
 }
 
+// ---------------------------------------------------------------- Hadamard transform
+// Random Hadamard transform of the backward operands ("Resumo Técnico:
+// TetraJet-v2", §2C): z = (1/4) H16 (d . x) on each 16-element block, H16 the
+// Sylvester Hadamard matrix as butterflies of strides 1, 2, 4, 8 (one FP32
+// addition each), d the signs of bits 0..15 of Philox word 0 at counter
+// (0, 0, 2, offset) under key (rht_seed, 0).
+__device__ __forceinline__ uint32_t rht_signs(uint32_t rht_seed, uint32_t offset)
+{
+    const uint4 o = philox4x32_10(make_uint4(0u, 0u, 2u, offset), philox_key(rht_seed));
+    return o.x & 0xFFFFu;
+}
+
+__device__ __forceinline__ void rht16(float *z, uint32_t signs)
+{
+#pragma unroll
+    for (int i = 0; i < 16; ++i)
+        z[i] = __uint_as_float(__float_as_uint(z[i]) ^ (((signs >> i) & 1u) << 31));
+#pragma unroll
+    for (int h = 1; h < 16; h *= 2) {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            if (i & h)
+                continue;
+            const float a = z[i], b = z[i + h];
+            z[i] = __fadd_rn(a, b);
+            z[i + h] = __fsub_rn(a, b);
+        }
+    }
+#pragma unroll
+    for (int i = 0; i < 16; ++i)
+        z[i] = __fmul_rn(z[i], 0.25f);
+}
+
 __device__ __forceinline__ uint32_t u16_of(const uint4 &w, int j)
 {
     const uint32_t word = (j >> 1) == 0 ? w.x : (j >> 1) == 1 ? w.y : (j >> 1) == 2 ? w.z : w.w;

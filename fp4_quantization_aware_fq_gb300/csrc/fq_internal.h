@@ -22,6 +22,7 @@ struct RowArgs {
     uint64_t seed;
     uint32_t offset;
     uint32_t stream_id;
+    uint32_t rht_seed;  // 0: no Hadamard transform
 };
 
 // Tiled quantization producing the column-wise (transposed) output and,
@@ -42,6 +43,7 @@ struct TileArgs {
     float *ctscale;
     uint64_t seed;
     uint32_t offset;
+    uint32_t rht_seed;  // 0: no Hadamard transform
 };
 
 struct DequantArgs {

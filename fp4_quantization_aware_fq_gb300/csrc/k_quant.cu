@@ -74,12 +74,17 @@ struct RowOut {
 // block, the 8 inner blocks of an outer block sit on 8 consecutive lanes, and
 // all 32 lanes of the warp must call this together.
 template <int FMT, int RND>
-__device__ __forceinline__ void row_block(const float *v, int64_t blk, bool valid, float s_g,
+__device__ __forceinline__ void row_block(float *v, int64_t blk, bool valid, float s_g,
                                           float inv6, const NvTables *tab, const RowOut &o,
                                           const PhiloxKey &key, uint32_t offset,
-                                          uint32_t stream_id)
+                                          uint32_t stream_id, bool rht, uint32_t signs)
 {
     constexpr int B = FmtInfo<FMT>::B;
+    if (FMT != NVFP4 && rht) {
+#pragma unroll
+        for (int j = 0; j < B / 16; ++j)
+            rht16(v + 16 * j, signs);
+    }
     float am = 0.0f;
 #pragma unroll
     for (int i = 0; i < B; ++i)
@@ -152,6 +157,8 @@ __global__ void __launch_bounds__(kThreads) row_kernel(RowArgs a)
     }
     const RowOut o{a.codes, a.scales, a.tscale, a.xhat, a.xhat_bf16, a.mask};
     const PhiloxKey key = philox_key(a.seed);
+    const bool rht = a.rht_seed != 0;
+    const uint32_t signs = rht ? rht_signs(a.rht_seed, a.offset) : 0u;
     const int64_t stride = (int64_t)gridDim.x * kThreads * BPT;
     for (int64_t base = (int64_t)blockIdx.x * kThreads * BPT; base < nblk; base += stride) {
         float v[BPT][B];
@@ -169,7 +176,7 @@ __global__ void __launch_bounds__(kThreads) row_kernel(RowArgs a)
         for (int k = 0; k < BPT; ++k) {
             const int64_t blk = base + k * kThreads + threadIdx.x;
             row_block<FMT, RND>(v[k], blk, blk < nblk, s_g, inv6, &tab, o, key, a.offset,
-                                a.stream_id);
+                                a.stream_id, rht, signs);
         }
     }
 }
@@ -225,6 +232,8 @@ __global__ void __launch_bounds__(kThreads) tile_kernel(TileArgs a)
     }
     const RowOut o{a.rcodes, a.rscales, a.rtscale, a.xhat, a.xhat_bf16, a.mask};
     const PhiloxKey key = philox_key(a.seed);
+    const bool rht = a.rht_seed != 0;
+    const uint32_t signs = rht ? rht_signs(a.rht_seed, a.offset) : 0u;
     const int64_t ntc = (cols + TC - 1) / TC;
     const int64_t ntiles = ntc * ((rows + TR - 1) / TR);
 
@@ -282,7 +291,7 @@ __global__ void __launch_bounds__(kThreads) tile_kernel(TileArgs a)
         }
         if (a.do_row)
             row_block<FMT, RND>(v, (gr * cols + gc) / BR, valid, s_g, inv6, &tab, o, key,
-                                a.offset, 0u);
+                                a.offset, 0u, rht, signs);
     }
     __syncthreads();
 
@@ -290,10 +299,19 @@ __global__ void __launch_bounds__(kThreads) tile_kernel(TileArgs a)
     if (FMT == NV2L) {
         for (int task = threadIdx.x; task < TC * NRB; task += kThreads) {
             const int c = task % TC, rb = task / TC;
+            float w[BC];
+#pragma unroll
+            for (int i = 0; i < BC; ++i)
+                w[i] = static_cast<float>(tile[(rb * BC + i) * TC + c]);
+            if (rht) {
+#pragma unroll
+                for (int j = 0; j < BC / 16; ++j)
+                    rht16(w + 16 * j, signs);
+            }
             float m = 0.0f;
 #pragma unroll
             for (int i = 0; i < BC; ++i)
-                m = fmaxf(m, fabsf(static_cast<float>(tile[(rb * BC + i) * TC + c])));
+                m = fmaxf(m, fabsf(w[i]));
             am16[rb * TC + c] = m;
         }
         __syncthreads();
@@ -304,12 +322,18 @@ __global__ void __launch_bounds__(kThreads) tile_kernel(TileArgs a)
         if (gc >= cols || gr0 >= rows)
             continue;
         float v[BC];
+#pragma unroll
+        for (int i = 0; i < BC; ++i)
+            v[i] = static_cast<float>(tile[(rb * BC + i) * TC + c]);
+        if (FMT != NVFP4 && rht) {
+#pragma unroll
+            for (int j = 0; j < BC / 16; ++j)
+                rht16(v + 16 * j, signs);
+        }
         float m = 0.0f;
 #pragma unroll
-        for (int i = 0; i < BC; ++i) {
-            v[i] = static_cast<float>(tile[(rb * BC + i) * TC + c]);
+        for (int i = 0; i < BC; ++i)
             m = fmaxf(m, fabsf(v[i]));
-        }
         float s_o = s_g, inv6c = inv6;
         if (FMT == NV2L) {
             float mo = 0.0f;

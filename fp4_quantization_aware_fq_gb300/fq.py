@@ -41,10 +41,10 @@ class FqError(RuntimeError):
 class Config(ctypes.Structure):
     _fields_ = [("format", ctypes.c_int32), ("rounding", ctypes.c_int32),
                 ("seed", ctypes.c_uint64), ("offset", ctypes.c_uint32),
-                ("reserved", ctypes.c_uint32)]
+                ("rht_seed", ctypes.c_uint32)]
 
-    def __init__(self, format=NVFP4, rounding=RNE, seed=0, offset=0):
-        super().__init__(format, rounding, seed, offset, 0)
+    def __init__(self, format=NVFP4, rounding=RNE, seed=0, offset=0, rht_seed=0):
+        super().__init__(format, rounding, seed, offset, rht_seed)
 
 
 class _QT(ctypes.Structure):

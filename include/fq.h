@@ -101,13 +101,25 @@ typedef enum { FQ_RNE = 0, FQ_SR = 1 } fq_rounding;
 typedef enum { FQ_ROW = 1, FQ_COL = 2, FQ_ROWCOL = 3 } fq_orient;
 typedef enum { FQ_F32 = 0, FQ_BF16 = 1 } fq_dtype;
 
-/* Quantizer configuration.  seed and offset matter only for FQ_SR. */
+/* Quantizer configuration.  seed matters only for FQ_SR; offset for FQ_SR and
+ * the Hadamard transform.
+ * rht_seed != 0 turns on the random Hadamard transform of the backward
+ * operands ([TJV2] §2C, OutControl): every 1x16 block along the quantization
+ * direction (each 16x1 block for the column-wise output) becomes
+ * z = (1/4) H16 (d . x) before it is quantized -- H16 the Sylvester Hadamard
+ * matrix applied as butterflies of strides 1, 2, 4, 8 in FP32, d random signs
+ * shared by all blocks: bit i of Philox4x32-10(key (rht_seed, 0), counter
+ * (0, 0, 2, offset)) word 0 set means d_i = -1.  Operands quantized with the
+ * same rht_seed and offset share one orthogonal transform, so their product
+ * is unchanged.  Outputs (codes, scales, xhat, mask) describe z.  Supported
+ * for FQ_MXFP4 and FQ_NVFP4_2LEVEL (no tensor-wide amax to transform first);
+ * FQ_NVFP4 returns FQ_ERR_UNSUPPORTED. */
 typedef struct {
-    int32_t format;   /* fq_format */
-    int32_t rounding; /* fq_rounding */
-    uint64_t seed;    /* Philox key */
-    uint32_t offset;  /* Philox counter word 3, e.g. the training step */
-    uint32_t reserved;
+    int32_t format;    /* fq_format */
+    int32_t rounding;  /* fq_rounding */
+    uint64_t seed;     /* Philox key of stochastic rounding */
+    uint32_t offset;   /* Philox counter word 3, e.g. the training step */
+    uint32_t rht_seed; /* 0: no Hadamard transform */
 } fq_config;
 
 /* A quantized tensor: device pointers, layouts as described above. */

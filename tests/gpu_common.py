@@ -50,11 +50,12 @@ def check_q(name, q: fq.QTensor, ref: dict, fmt: int):
 
 
 def fakequant_parity(x: torch.Tensor, fmt: int, rnd: int = fq.RNE, seed: int = 0,
-                     offset: int = 0, orient: int = fq.ROW, xhat_dtype=None, check_col=True):
+                     offset: int = 0, orient: int = fq.ROW, xhat_dtype=None, check_col=True,
+                     rht_seed: int = 0):
     """Run fq_fakequant_ste (with row codes, optional column codes) on the GPU
     and the oracle; assert everything matches bit for bit."""
     rows, cols = x.shape
-    cfg = fq.Config(fmt, rnd, seed, offset)
+    cfg = fq.Config(fmt, rnd, seed, offset, rht_seed)
     xhat_dtype = xhat_dtype or x.dtype
     xhat, mask, rq, cq = fq.fq_fakequant_ste(x, cfg, xhat_dtype=xhat_dtype, want_mask=True,
                                              want_row_q=True,
@@ -63,7 +64,7 @@ def fakequant_parity(x: torch.Tensor, fmt: int, rnd: int = fq.RNE, seed: int = 0
     xo = as_oracle_input(x)
     ref = oracle.quantize(xo, FMT_O[fmt], rnd, seed, offset,
                           orient=(oracle.ROWCOL if orient & fq.COL else oracle.ROW),
-                          want_xhat=True, want_mask=True)
+                          want_xhat=True, want_mask=True, rht_seed=rht_seed)
     r = ref["row"]
     check_q("row", rq, r, fmt)
     if xhat_dtype == torch.bfloat16:

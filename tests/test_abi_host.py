@@ -80,6 +80,17 @@ def test_quantize_argument_errors(L):
     assert _quant(L, ok, row=_qt(), wsb=2) == 4                            # workspace too small
 
 
+def test_hadamard_transform_needs_block_local_scales(L):
+    cfg = fq.Config(fq.NVFP4, fq.SR, 1, 0, rht_seed=7)
+    assert _quant(L, cfg, row=_qt()) == 5                                  # unsupported
+    vp, i64 = ctypes.c_void_p, ctypes.c_int64
+    rows, cols = (i64 * 1)(64), (i64 * 1)(64)
+    ptrs = (vp * 1)(FAKE)
+    qs = (fq._QT * 1)(_qt())
+    assert L.fq_osci_update(ctypes.byref(cfg), 1, rows, cols, ptrs, ptrs, ptrs, ptrs, qs, qs,
+                            None, fq.BF16, None, FAKE, 256, None) == 5
+
+
 def test_fakequant_dequant_ste_amax_errors(L):
     cfg = fq.Config(fq.NVFP4)
     f = L.fq_fakequant_ste

@@ -149,6 +149,25 @@ def test_saturation_near_six_and_subnormals():
     fakequant_parity(_dev(y), fq.NVFP4, rnd=fq.SR, seed=1, orient=fq.ROWCOL)
 
 
+# ------------------------------------------------------------------ Hadamard transform
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+@pytest.mark.parametrize("fmt,rnd", [(fq.NVFP4_2LEVEL, fq.SR), (fq.NVFP4_2LEVEL, fq.RNE),
+                                     (fq.MXFP4, fq.SR), (fq.MXFP4, fq.RNE)])
+def test_rht_row_and_column(dtype, fmt, rnd):
+    rows, cols = 256, 384
+    x = W.grad_2level(shape=(rows, cols), seed=31).to(dtype)
+    x[:, 5] *= 200.0                      # an outlier channel for the transform to spread
+    fakequant_parity(_dev(x), fmt, rnd, seed=17, offset=4, orient=fq.ROWCOL, rht_seed=0xC0FFEE)
+    fakequant_parity(_dev(x), fmt, rnd, seed=17, offset=4, orient=fq.ROW, rht_seed=99)
+
+
+def test_rht_rejected_for_per_tensor_nvfp4():
+    x = _dev(W.grad_2level(shape=(64, 128), seed=1))
+    with pytest.raises(fq.FqError) as e:
+        fq.fq_quantize(x, fq.Config(fq.NVFP4, fq.SR, 1, 0, rht_seed=5))
+    assert e.value.status == 5
+
+
 # ------------------------------------------------------------------ full-size workloads
 @pytest.mark.slow
 def test_full_nvfp4_small_fp32():

@@ -82,6 +82,12 @@ def _load():
         lib.fqo_dequantize_rows.restype = i32
         lib.fqo_ste_backward.argtypes = [vp, vp, i64, i32, vp]
         lib.fqo_ste_backward.restype = None
+        lib.fqo_channel_amax.argtypes = [vp, i64, i64, vp]; lib.fqo_channel_amax.restype = None
+        lib.fqo_select_channels.argtypes = [vp, i64, i64, vp, vp, vp]
+        lib.fqo_select_channels.restype = i32
+        lib.fqo_quantize_outliers.argtypes = [i32, i32, u64, u32, vp, i64, i64, vp, i64, vp, vp,
+                                              vp, vp, vp, vp, vp, vp]
+        lib.fqo_quantize_outliers.restype = i32
         lib.fqo_osci_step.argtypes = [i32, i32, u64, u32, vp, vp, vp, vp, vp, vp, vp,
                                       vp, vp, vp, i64, i64, vp, vp, vp]
         lib.fqo_osci_step.restype = i32
@@ -270,6 +276,55 @@ def ste_backward(dy: np.ndarray, mask: np.ndarray) -> np.ndarray:
     dx = np.empty_like(dy)
     _load().fqo_ste_backward(_ptr(dy), _ptr(mask), dy.size, dy.itemsize, _ptr(dx))
     return dx
+
+
+def channel_amax(x: np.ndarray, amax_in=None) -> np.ndarray:
+    """Running per-column max |x| (start from zeros when amax_in is None)."""
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    rows, cols = x.shape
+    a = (np.zeros(cols, np.float32) if amax_in is None
+         else np.ascontiguousarray(amax_in, dtype=np.float32).copy())
+    _load().fqo_channel_amax(_ptr(x), rows, cols, _ptr(a))
+    return a
+
+
+def select_channels(amax_c: np.ndarray, k: int):
+    amax_c = np.ascontiguousarray(amax_c, dtype=np.float32)
+    cols = amax_c.size
+    idx = np.zeros(max(k, 1), np.int32)
+    bitmap = np.zeros((cols + 31) // 32, np.uint32)
+    scale = np.zeros(max(k, 1), np.float32)
+    _check(_load().fqo_select_channels(_ptr(amax_c), cols, k, _ptr(idx), _ptr(bitmap),
+                                       _ptr(scale)), "select_channels")
+    return {"idx": idx[:k], "bitmap": bitmap, "fp8_scale": scale[:k]}
+
+
+def quantize_outliers(x, idx, fp8_scale, fmt=NVFP4, rounding=RNE, seed=0, offset=0):
+    """Split fake-quantization: FP4 for the tensor with the retained columns
+    zeroed, FP8 E4M3 (static per-channel scales) for the retained columns."""
+    lib = _load()
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    rows, cols = x.shape
+    idx = np.ascontiguousarray(idx, dtype=np.int32)
+    fp8_scale = np.ascontiguousarray(fp8_scale, dtype=np.float32)
+    k = idx.size
+    B = BLOCK[fmt]
+    codes = np.zeros((rows, cols // 2), np.uint8)
+    scales = np.zeros((rows, cols // B), np.uint8)
+    tscale = (np.zeros((rows, max(cols // 128, 1)), np.float32) if fmt == NVFP4_2LEVEL
+              else np.zeros(1, np.float32))
+    fp8 = np.zeros((rows, max(k, 1)), np.uint8)
+    xhat = np.zeros((rows, cols), np.float32)
+    mask = np.zeros((rows * cols + 31) // 32, np.uint32)
+    scratch = np.zeros_like(x)
+    st = lib.fqo_quantize_outliers(fmt, rounding, seed, offset, _ptr(x), rows, cols,
+                                   _ptr(idx), k, _ptr(fp8_scale), _ptr(scratch), _ptr(codes),
+                                   _ptr(scales), _ptr(tscale), _ptr(fp8), _ptr(xhat), _ptr(mask))
+    _check(st, "quantize_outliers")
+    out = {"codes": codes, "scales": scales, "fp8": fp8[:, :k], "xhat": xhat, "mask": mask}
+    if fmt != MXFP4:
+        out["tscale"] = tscale
+    return out
 
 
 class OsciState:

@@ -445,6 +445,100 @@ void fqo_ste_backward(const void *dy, const uint32_t *mask, int64_t n, int elem_
 }
 
 /* ------------------------------------------------------------------------ */
+/* Static outlier retention ("Resumo Técnico: TetraJet-v2", §2C, OutControl:  */
+/* the top p% channels by norm, found in a short calibration window, stay in  */
+/* higher precision -- e.g. FP8 -- in both passes; the rest stays FP4).       */
+/* Readings: channel = column of an activation [tokens, channels]; the norm   */
+/* is the L-infinity norm (max |x|) over the calibration window; ties go to   */
+/* the lower channel index; the retained channels use FP8 E4M3 with a static  */
+/* per-channel scale s_c = amax_c / 448; the FP4 part quantizes the tensor    */
+/* with the retained columns set to +0.                                       */
+/* ------------------------------------------------------------------------ */
+
+/* amax[c] = max(amax[c], max over rows |x[r, c]|): a running maximum. */
+void fqo_channel_amax(const float *x, int64_t rows, int64_t cols, float *amax)
+{
+    for (int64_t r = 0; r < rows; r++)
+        for (int64_t c = 0; c < cols; c++) {
+            float a = fabsf(x[r * cols + c]);
+            if (a > amax[c])
+                amax[c] = a;
+        }
+}
+
+/* The k channels with the largest amax (ties: lower index first), returned in
+ * ascending index order, plus the bitmap (bit c % 32 of word c / 32) and the
+ * FP8 scale amax_c / 448 of each selected channel. */
+int fqo_select_channels(const float *amax, int64_t cols, int64_t k, int32_t *idx,
+                        uint32_t *bitmap, float *fp8_scale)
+{
+    if (k < 0 || k > cols)
+        return FQO_ERR_ARG;
+    memset(bitmap, 0, (size_t)((cols + 31) / 32) * 4);
+    for (int64_t j = 0; j < k; j++) {
+        int64_t best = -1;
+        for (int64_t c = 0; c < cols; c++) {
+            if ((bitmap[c / 32] >> (c % 32)) & 1u)
+                continue;
+            if (best < 0 || amax[c] > amax[best])
+                best = c;
+        }
+        bitmap[best / 32] |= 1u << (best % 32);
+    }
+    int64_t j = 0;
+    for (int64_t c = 0; c < cols; c++)
+        if ((bitmap[c / 32] >> (c % 32)) & 1u) {
+            idx[j] = (int32_t)c;
+            fp8_scale[j] = amax[c] / 448.0f;
+            j++;
+        }
+    return FQO_OK;
+}
+
+/* Split fake-quantization.  The FP4 part is fqo_quantize_rows of x with the
+ * retained columns zeroed (NVFP4: tensor amax of that tensor).  Retained
+ * column c (the j-th selected) gets y = x * r_j, r_j = 1 / s_j (0 if s_j = 0),
+ * code = sign | E4M3 nearest-even saturating of |y| into fp8[r, j],
+ * xhat = E4M3value(code) * s_j, mask bit = |x| <= 448 * s_j. */
+int fqo_quantize_outliers(int fmt, int rounding, uint64_t seed, uint32_t offset,
+                          const float *x, int64_t rows, int64_t cols, const int32_t *idx,
+                          int64_t k, const float *fp8_scale, float *xz_scratch,
+                          uint8_t *codes, uint8_t *scales, float *tscale, uint8_t *fp8,
+                          float *xhat, uint32_t *mask)
+{
+    int64_t n = rows * cols;
+    memcpy(xz_scratch, x, (size_t)n * 4);
+    for (int64_t r = 0; r < rows; r++)
+        for (int64_t j = 0; j < k; j++)
+            xz_scratch[r * cols + idx[j]] = 0.0f;
+    float amax = fqo_amax(xz_scratch, n);
+    int st = fqo_quantize_rows(fmt, rounding, seed, offset, 0, xz_scratch, rows, cols, amax,
+                               codes, scales, tscale, xhat, mask);
+    if (st != FQO_OK)
+        return st;
+    for (int64_t j = 0; j < k; j++) {
+        float s = fp8_scale[j];
+        float rcp = (s == 0.0f) ? 0.0f : 1.0f / s;
+        float lim = 448.0f * s;
+        for (int64_t r = 0; r < rows; r++) {
+            int64_t e = r * cols + idx[j];
+            float y = x[e] * rcp;
+            int code = fqo_e4m3_encode(fabsf(y)) | (signbit(y) ? 0x80 : 0);
+            fp8[r * k + j] = (uint8_t)code;
+            if (xhat)
+                xhat[e] = fqo_e4m3_value(code) * s;
+            if (mask) {
+                if (fabsf(x[e]) <= lim)
+                    mask[e / 32] |= 1u << (e % 32);
+                else
+                    mask[e / 32] &= ~(1u << (e % 32));
+            }
+        }
+    }
+    return FQO_OK;
+}
+
+/* ------------------------------------------------------------------------ */
 /* OsciReset ("Resumo Técnico: TetraJet-v2", §2B).                            */
 /* ------------------------------------------------------------------------ */
 

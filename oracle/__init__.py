@@ -11,7 +11,8 @@ pass, which is the row-wise definition applied to the transpose).
 
 Parity status: pinned.  See tests/test_oracle_*.py: exact-rational format
 tables, torch's float8/bfloat16 casts, cuRAND's host Philox4x32-10 generator,
-hand-worked blocks and invariants.
+hand-worked blocks and invariants; for the distillation loss, the Bernoulli
+closed form, scipy's relative entropy, finite differences and invariants.
 """
 from __future__ import annotations
 
@@ -93,6 +94,9 @@ def _load():
         lib.fqo_osci_step.restype = i32
         lib.fqo_osci_reset.argtypes = [i32, vp, vp, vp, vp, vp, vp, i64, i64, f32, vp]
         lib.fqo_osci_reset.restype = i64
+        lib.fqo_qad_kl.argtypes = [vp, vp, i64, i64, ctypes.c_double, ctypes.c_double, vp, vp,
+                                   vp, vp]
+        lib.fqo_qad_kl.restype = i32
         _lib = lib
         return lib
 
@@ -370,3 +374,24 @@ class OsciState:
         if cnt < 0:
             raise ValueError("oracle osci_reset failed")
         return int(cnt)
+
+
+def qad_kl(zt: np.ndarray, zs: np.ndarray, temperature: float = 1.0, grad_scale=None,
+           want_grad: bool = True):
+    """QAD distillation loss of [rows, vocab] teacher / student logits (FP32
+    values; widen BF16 first): per-row KL(softmax(zt/T) || softmax(zs/T)),
+    their mean, and dz = g (q - p) / T with g = grad_scale (default 1/rows,
+    the gradient of the mean).  All results in float64."""
+    zt = np.ascontiguousarray(zt, dtype=np.float32)
+    zs = np.ascontiguousarray(zs, dtype=np.float32)
+    assert zt.shape == zs.shape and zt.ndim == 2
+    rows, vocab = zt.shape
+    g = (1.0 / rows if rows else 0.0) if grad_scale is None else float(grad_scale)
+    loss = np.zeros(rows, np.float64)
+    dz = np.zeros((rows, vocab), np.float64) if want_grad else None
+    mean = np.zeros(1, np.float64)
+    scratch = np.zeros(2 * vocab, np.float64)
+    _check(_load().fqo_qad_kl(_ptr(zt), _ptr(zs), rows, vocab, float(temperature), g,
+                              _ptr(loss), _ptr(mean), _ptr(dz) if want_grad else None,
+                              _ptr(scratch)), "qad_kl")
+    return {"loss_rows": loss, "loss_mean": float(mean[0]), "dz": dz}

@@ -600,3 +600,59 @@ int64_t fqo_osci_reset(int fmt, float *master, float *dist_q, float *dist_m,
     }
     return count;
 }
+
+/* ------------------------------------------------------------------------ */
+/* QAD distillation loss ("Quantization-Aware Distillation for NVFP4         */
+/* Inference Accuracy Recovery", §2 Metodologia: KL divergence between the   */
+/* BF16 teacher's and the NVFP4 student's output distributions, softmax      */
+/* temperature T = 1).  Double precision throughout.                        */
+/* ------------------------------------------------------------------------ */
+
+/* log of the sum of exp over n values, shifted by their maximum */
+static double fqo_logsumexp(const double *v, int64_t n)
+{
+    double m = v[0];
+    for (int64_t i = 1; i < n; i++)
+        if (v[i] > m)
+            m = v[i];
+    double s = 0.0;
+    for (int64_t i = 0; i < n; i++)
+        s += exp(v[i] - m);
+    return m + log(s);
+}
+
+/* For each row r of the [rows, vocab] teacher logits zt and student logits
+ * zs: p = softmax(zt / T), q = softmax(zs / T),
+ *   loss_rows[r] = KL(p || q) = sum_v p_v (log p_v - log q_v),
+ *   dz[r, v]     = g * (q_v - p_v) / T   (the gradient of g * loss_rows[r]
+ *                                         with respect to zs[r, v]).
+ * and *loss_mean = the mean of loss_rows over the rows (0 for no rows).
+ * dz may be NULL.  scratch holds 2 * vocab doubles. */
+int fqo_qad_kl(const float *zt, const float *zs, int64_t rows, int64_t vocab, double temperature,
+               double g, double *loss_rows, double *loss_mean, double *dz, double *scratch)
+{
+    if (vocab <= 0 || !(temperature > 0.0))
+        return FQO_ERR_ARG;
+    double *a = scratch, *b = scratch + vocab;
+    for (int64_t r = 0; r < rows; r++) {
+        for (int64_t v = 0; v < vocab; v++) {
+            a[v] = (double)zt[r * vocab + v] / temperature;
+            b[v] = (double)zs[r * vocab + v] / temperature;
+        }
+        double lse_t = fqo_logsumexp(a, vocab), lse_s = fqo_logsumexp(b, vocab);
+        double kl = 0.0;
+        for (int64_t v = 0; v < vocab; v++) {
+            double log_p = a[v] - lse_t, log_q = b[v] - lse_s;
+            double p = exp(log_p), q = exp(log_q);
+            kl += p * (log_p - log_q);
+            if (dz)
+                dz[r * vocab + v] = g * (q - p) / temperature;
+        }
+        loss_rows[r] = kl;
+    }
+    double sum = 0.0;
+    for (int64_t r = 0; r < rows; r++)
+        sum += loss_rows[r];
+    *loss_mean = rows ? sum / (double)rows : 0.0;
+    return FQO_OK;
+}

@@ -1,7 +1,7 @@
 #!/usr/bin/env python
 """Benchmark: block-scaled FP4 fake-quantization on GB300.
 
-One step = one pass of the whole hot path over the five synthetic workloads:
+One step = one pass of the whole hot path over the synthetic workloads:
   nvfp4_small   NVFP4 fake-quant (RNE), FP32 [256, 1024]: codes, scales, s_g, FP32 xhat, mask
   mxfp4_weight  MXFP4 quantize + dequantize (RNE), BF16 [4096, 4096] weight with 0.1% x100
   nvfp4_act     NVFP4 row 1x16 + column 16x1 on the transpose in one call, BF16 [8192, 8192]
@@ -10,6 +10,10 @@ One step = one pass of the whole hot path over the five synthetic workloads:
   grad_2level   double-block NVFP4 with stochastic rounding, BF16 [16384, 4096] Laplace gradient
   grad_rht_rowcol  the same kind of gradient as a backward-GEMM operand: 16-point random
                 Hadamard transform + double-block SR, row 1x16 and column 16x1 in one call
+  act_outliers  static outlier retention: BF16 [8192, 8192] activation with 64 outlier
+                channels x50; the 10% of channels (819) with the largest calibration amax
+                (two earlier batches, selected once before timing) go to FP8 E4M3, the rest
+                to NVFP4: codes, scales, s_g, FP8 columns, BF16 xhat, STE mask
   moe_qat       one QAT step over 32 MoE experts (64 FP32 master matrices [2880, 5760] and
                 [5760, 2880], 1.06 G weights): update + NVFP4 fake-quant + OsciReset
                 statistics, then the OsciReset reset pass over the same weights
@@ -48,11 +52,13 @@ BYTES_PER_ELEM = {
     "ste_backward": 2 + 1 / 8 + 2,
     "grad_2level": 2 + 0.5 + 1 / 16 + 4 / 128,
     "grad_rht_rowcol": 2 + 2 * (0.5 + 1 / 16 + 4 / 128),
+    "act_outliers": 2 + 2 + 0.5 + 1 / 16 + 819 / 8192 + 2 + 1 / 8,
     "osci_update_reset": 20 + (4 + 0.5 + 1 / 16 + 8 + 8 + 0.5 + 1 / 16 + 2 + 1 / 8),
 }
 # Our kernels launched per step (memsets not counted).
 LAUNCHES_PER_STEP = {"nvfp4_small": 2, "mxfp4_weight": 1, "nvfp4_act": 2, "ste_backward": 1,
-                     "grad_2level": 1, "grad_rht_rowcol": 1, "osci_update_reset": 2}
+                     "grad_2level": 1, "grad_rht_rowcol": 1, "act_outliers": 2,
+                     "osci_update_reset": 2}
 # DRAM traffic per launch of the dominant call from an ncu capture, valid only
 # for the kernel source it was taken on (sha256 of k_osci.cu).  Captured on the
 # 2-expert case (66.4 M weights: pass A + pass B read+write 2852.8 MB) and
@@ -141,7 +147,7 @@ class Suite:
     profiling a smaller case of the same kernels)."""
 
     ORDER = ("nvfp4_small", "mxfp4_weight", "nvfp4_act", "ste_backward", "grad_2level",
-             "grad_rht_rowcol", "osci_update_reset")
+             "grad_rht_rowcol", "act_outliers", "osci_update_reset")
 
     def __init__(self, dev, only=None, experts=None):
         import torch
@@ -195,6 +201,21 @@ class Suite:
             self.rq6 = fq.alloc_qtensor(r6, c6, fq.NVFP4_2LEVEL, dev)
             self.cq6 = fq.alloc_qtensor(c6, r6, fq.NVFP4_2LEVEL, dev)
             self.elems["grad_rht_rowcol"] = self.x6.numel()
+        if "act_outliers" in want:
+            c = W.WORKLOADS["channel_act"]
+            self.x7 = W.channel_act(device=dev)
+            r7, c7 = self.x7.shape
+            amax = torch.zeros(c7, dtype=torch.float32, device=dev)
+            for t in (1, 2):       # calibration window: two earlier batches
+                fq.fq_channel_amax(W.channel_act(seed=c["seed"] + t, device=dev), amax)
+            self.sel7 = fq.fq_select_channels(amax, c7 // 10)
+            self.cfg7 = fq.Config(fq.NVFP4)
+            self.q7 = fq.alloc_qtensor(r7, c7, fq.NVFP4, dev)
+            self.fp87 = torch.empty((r7, c7 // 10), dtype=torch.uint8, device=dev)
+            self.xh7 = torch.empty(self.x7.shape, dtype=torch.bfloat16, device=dev)
+            self.m7 = self._mask(self.x7)
+            self.ws7 = torch.empty(256, dtype=torch.uint8, device=dev)
+            self.elems["act_outliers"] = self.x7.numel()
         if "osci_update_reset" in want:
             m = W.WORKLOADS["moe_qat"]
             ws = W.moe_weights(experts or m["experts"], m["up_shape"], m["down_shape"],
@@ -251,6 +272,10 @@ class Suite:
         self.cfg6.offset = self.step_no
         self.fq.fq_quantize(self.x6, self.cfg6, orient=self.fq.ROWCOL, row_out=self.rq6,
                             col_out=self.cq6)
+
+    def act_outliers(self):
+        self.fq.fq_quantize_outliers(self.x7, self.cfg7, self.sel7, out=self.q7, fp8=self.fp87,
+                                     xhat=self.xh7, mask=self.m7, ws=self.ws7)
 
     def osci_update_reset(self):
         # one QAT step that also ends the OsciReset window (reset fused in)
@@ -350,6 +375,9 @@ def e2e_buffers(suite):
         ins.append(suite.x6)
         outs += [suite.rq6.codes, suite.rq6.scales, suite.rq6.tscale, suite.cq6.codes,
                  suite.cq6.scales, suite.cq6.tscale]
+    if "act_outliers" in suite.names:
+        ins.append(suite.x7)
+        outs += [suite.q7.codes, suite.q7.scales, suite.q7.tscale, suite.fp87]
     if "osci_update_reset" in suite.names:
         ins += list(suite.delta)
         outs.append(suite.nreset)
@@ -428,6 +456,14 @@ def oracle_sample(max_seconds=None):
     x6 = f32(W.grad_2level(shape=(2048, 4096), seed=6))
     res["grad_rht_rowcol"] = (x6.size, timed(lambda: oracle.quantize(
         x6, oracle.NVFP4_2LEVEL, oracle.SR, 0x5EED, orient=oracle.ROWCOL, rht_seed=0xB00F)))
+    x7 = W.channel_act(shape=(2048, 8192))
+    am7 = oracle.channel_amax(f32(W.channel_act(shape=(2048, 8192), seed=501)))
+    sel7 = oracle.select_channels(am7, 819)
+
+    def c7():
+        q = oracle.quantize_outliers(f32(x7), sel7["idx"], sel7["fp8_scale"], oracle.NVFP4)
+        oracle.f32_to_bf16_bits(q["xhat"])
+    res["act_outliers"] = (x7.numel(), timed(c7))
     w = W.normal((5760, 5760), 0.02, seed=4).to(__import__("torch").bfloat16)
     st = oracle.OsciState(f32(w), oracle.NVFP4)
     d = W.master_update((5760, 5760), 1).numpy()
@@ -439,7 +475,7 @@ def oracle_sample(max_seconds=None):
     res["osci_update_reset"] = (w.numel(), t_upd + timed(lambda: st.reset(4.0)))
     desc = ("oracle (scalar C, 1 thread) on: nvfp4_small full; mxfp4_weight full; "
             "nvfp4_act 4096 rows row+col; ste_backward 4096x8192; grad_2level 8192 rows SR; "
-            "grad_rht_rowcol 2048 rows; "
+            "grad_rht_rowcol 2048 rows; act_outliers 2048 rows; "
             "osci update+reset on a [5760, 5760] matrix (one expert's weights); per-element "
             "rates scaled to the full step's elements")
     return res, desc
@@ -458,6 +494,7 @@ def oracle_gbs(sample, elems_full):
 FULL_ELEMS = {"nvfp4_small": 256 * 1024, "mxfp4_weight": 4096 * 4096,
               "nvfp4_act": 8192 * 8192, "ste_backward": 8192 * 8192,
               "grad_2level": 16384 * 4096, "grad_rht_rowcol": 16384 * 4096,
+              "act_outliers": 8192 * 8192,
               "osci_update_reset": 32 * 2 * 2880 * 5760}
 
 
@@ -466,12 +503,14 @@ def config_block(names=None, experts=None):
         return {"workload": "subset: " + ",".join(names) + (f"; moe experts={experts}"
                                                            if experts else ""),
                 "l2": "no flush between steps", "bytes": "algorithmic"}
-    return {"workload": "fake-quant suite over the five synthetic workloads (one pass each per "
+    return {"workload": "fake-quant suite over the synthetic workloads (one pass each per "
                         "step): nvfp4_small fp32 256x1024 NVFP4 RNE; mxfp4_weight bf16 "
                         "4096x4096 MXFP4 RNE quant+dequant; nvfp4_act bf16 8192x8192 NVFP4 "
                         "row 1x16 + col 16x1 + xhat + STE mask, then STE backward; grad_2level "
                         "bf16 16384x4096 double-block NVFP4 SR; grad_rht_rowcol the same "
                         "gradient with the 16-point Hadamard transform, both orientations; "
+                        "act_outliers bf16 8192x8192 activation, 819 channels kept in FP8 "
+                        "E4M3 by calibration amax, the rest NVFP4 RNE with xhat + STE mask; "
                         "moe_qat 32 experts x "
                         "(2880x5760 + 5760x2880) FP32 master: one QAT step with OsciReset "
                         "statistics and the window-end reset fused in",
@@ -532,7 +571,7 @@ def main():
             "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
-            "data": "synthetic (seeded torch generators, shapes/distributions of the five "
+            "data": "synthetic (seeded torch generators, shapes/distributions of the "
                     "workloads)",
             "config": config_block(suite.names, args.experts),
             "per_workload": per,

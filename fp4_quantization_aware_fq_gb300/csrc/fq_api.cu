@@ -424,6 +424,98 @@ fq_status fq_osci_reset(const fq_config *cfg, int32_t ntensors, const int64_t *r
     return FQ_OK;
 }
 
+fq_status fq_channel_amax(const void *x, int32_t x_dtype, int64_t rows, int64_t cols,
+                          float *amax_inout, void *stream)
+{
+    if (!valid_dtype(x_dtype) || !x || !amax_inout)
+        return FQ_ERR_INVALID_ARG;
+    if (rows < 0 || cols < 0 || cols % 16 != 0)
+        return FQ_ERR_SHAPE;
+    if (!aligned16(x) || !aligned16(amax_inout))
+        return FQ_ERR_ALIGN;
+    return cuda_status(launch_channel_amax(x, x_dtype == FQ_BF16, rows, cols, amax_inout,
+                                           static_cast<cudaStream_t>(stream)));
+}
+
+fq_status fq_select_channels(const float *channel_amax, int64_t cols, int64_t k, int32_t *idx,
+                             uint32_t *bitmap, float *fp8_scale, void *stream)
+{
+    if (!channel_amax || !bitmap || (k > 0 && (!idx || !fp8_scale)))
+        return FQ_ERR_INVALID_ARG;
+    if (cols < 0 || cols > FQ_MAX_CHANNELS)
+        return FQ_ERR_SHAPE;
+    if (k < 0 || k > cols)
+        return FQ_ERR_INVALID_ARG;
+    if (!aligned16(channel_amax) || !aligned16(bitmap) || (idx && !aligned16(idx)) ||
+        (fp8_scale && !aligned16(fp8_scale)))
+        return FQ_ERR_ALIGN;
+    if (cols == 0)
+        return FQ_OK;
+    return cuda_status(launch_select(channel_amax, (int)cols, (int)k, idx, bitmap, fp8_scale,
+                                     static_cast<cudaStream_t>(stream)));
+}
+
+fq_status fq_quantize_outliers(const fq_config *cfg, const void *x, int32_t x_dtype, int64_t rows,
+                               int64_t cols, const uint32_t *bitmap, int64_t k,
+                               const float *fp8_scale, const fq_qtensor *out, uint8_t *fp8,
+                               void *xhat, int32_t xhat_dtype, uint8_t *mask, void *workspace,
+                               size_t workspace_bytes, void *stream)
+{
+    if (!valid_cfg(cfg) || !valid_dtype(x_dtype) || !x || !bitmap || (k > 0 && !fp8_scale))
+        return FQ_ERR_INVALID_ARG;
+    if (xhat && !valid_dtype(xhat_dtype))
+        return FQ_ERR_INVALID_ARG;
+    const int fmt = cfg->format;
+    if (cfg->rht_seed)
+        return FQ_ERR_UNSUPPORTED;
+    if (rows < 0 || cols < 0 || cols % row_multiple(fmt) != 0 || cols > FQ_MAX_CHANNELS)
+        return FQ_ERR_SHAPE;
+    if (k < 0 || k > cols)
+        return FQ_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(bitmap) || (fp8_scale && !aligned16(fp8_scale)) ||
+        (fp8 && !aligned16(fp8)) || (xhat && !aligned16(xhat)) || (mask && !aligned16(mask)))
+        return FQ_ERR_ALIGN;
+    fq_status st;
+    if (out && (st = check_q(out, fmt)) != FQ_OK)
+        return st;
+    if (fmt == FQ_NVFP4) {
+        if (!workspace || workspace_bytes < sizeof(float))
+            return FQ_ERR_WORKSPACE;
+        if (!aligned16(workspace))
+            return FQ_ERR_ALIGN;
+    }
+    if (rows * cols == 0)
+        return FQ_OK;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const int bf16 = x_dtype == FQ_BF16;
+    OutlierArgs a{};
+    if (fmt == FQ_NVFP4) {
+        float *am = static_cast<float *>(workspace);
+        cudaError_t e = launch_masked_amax(x, bf16, rows, cols, bitmap, am, s);
+        if (e != cudaSuccess)
+            return FQ_ERR_CUDA;
+        a.amax = am;
+    }
+    a.x = x;
+    a.rows = rows;
+    a.cols = cols;
+    a.bitmap = bitmap;
+    a.k = k;
+    a.fp8_scale = fp8_scale;
+    if (out) {
+        a.codes = out->codes;
+        a.scales = out->scales;
+        a.tscale = out->tscale;
+    }
+    a.fp8 = fp8;
+    a.xhat = xhat;
+    a.xhat_bf16 = xhat_dtype == FQ_BF16;
+    a.mask = mask;
+    a.seed = cfg->seed;
+    a.offset = cfg->offset;
+    return cuda_status(launch_outlier_quant(a, bf16, fmt, cfg->rounding, s));
+}
+
 const char *fq_status_string(fq_status status)
 {
     switch (status) {

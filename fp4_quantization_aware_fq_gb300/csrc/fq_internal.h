@@ -90,6 +90,25 @@ struct OsciArgs {
     OsciTensor t[kOsciMaxTensors];
 };
 
+// Split FP4 / FP8 quantization of an activation with retained channels.
+struct OutlierArgs {
+    const void *x;
+    int64_t rows, cols;
+    const uint32_t *bitmap;   // retained channels, bit c % 32 of word c / 32
+    int64_t k;                // number of retained channels
+    const float *fp8_scale;   // [k] static scale of the j-th retained channel
+    const float *amax;        // NVFP4: amax of x without the retained channels
+    uint8_t *codes;
+    uint8_t *scales;
+    float *tscale;
+    uint8_t *fp8;             // [rows, k] E4M3 codes of the retained elements
+    void *xhat;
+    int xhat_bf16;
+    uint8_t *mask;
+    uint64_t seed;
+    uint32_t offset;
+};
+
 int sm_count();
 
 cudaError_t launch_amax(const void *x, int bf16, int64_t n, float *out, cudaStream_t s);
@@ -100,5 +119,13 @@ cudaError_t launch_ste(const void *dy, int bf16, const uint8_t *mask, int64_t n,
                        cudaStream_t s);
 cudaError_t launch_osci_update(const OsciArgs &a, int fmt, int rnd, cudaStream_t s);
 cudaError_t launch_osci_reset(const OsciArgs &a, int fmt, cudaStream_t s);
+cudaError_t launch_channel_amax(const void *x, int bf16, int64_t rows, int64_t cols, float *amax,
+                                cudaStream_t s);
+cudaError_t launch_select(const float *amax, int cols, int k, int32_t *idx, uint32_t *bitmap,
+                          float *fp8_scale, cudaStream_t s);
+cudaError_t launch_masked_amax(const void *x, int bf16, int64_t rows, int64_t cols,
+                               const uint32_t *bitmap, float *out, cudaStream_t s);
+cudaError_t launch_outlier_quant(const OutlierArgs &a, int bf16, int fmt, int rnd,
+                                 cudaStream_t s);
 
 }  // namespace fqk

@@ -1,0 +1,429 @@
+// k_outlier.cu -- static outlier retention ("Resumo Técnico: TetraJet-v2",
+// §2C, OutControl): the channels with the largest norm over a short
+// calibration window stay in FP8 (E4M3, static per-channel scale) while the
+// rest of the activation is quantized to FP4 with those channels removed, so
+// that they no longer inflate the block scales of their rows.
+//
+// channel_amax_kernel  running per-channel max |x| (the calibration norm)
+// select_kernel        top-k channels (ties: lower index), bitmap, FP8 scales
+// masked_amax_kernel   tensor amax without the retained channels (NVFP4)
+// outlier_row_kernel   one thread per row block: FP4 of the block with the
+//                      retained elements zeroed; FP8 codes of those elements
+#include "fq_device.cuh"
+#include "fq_internal.h"
+
+namespace fqk {
+
+constexpr int kOutThreads = 256;
+
+// Exclusive prefix sums of the popcounts of nwords bitmap words (shared or
+// global) into pre[] (shared), by all NT threads of the CTA: each thread sums
+// a contiguous run of words, the runs are scanned across the CTA, and the
+// run is rewritten with its prefixes.  Ends with a __syncthreads.
+template <int NT>
+__device__ __forceinline__ void popc_prefix(const uint32_t *words, int nwords, int *pre)
+{
+    __shared__ int wsum[NT / 32];
+    const int per = (nwords + NT - 1) / NT;
+    const int w0 = threadIdx.x * per;
+    const int w1 = w0 + per < nwords ? w0 + per : nwords;
+    int run = 0;
+    for (int w = w0; w < w1; ++w)
+        run += __popc(words[w]);
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    int inc = run;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int t = __shfl_up_sync(0xFFFFFFFFu, inc, o);
+        if (lane >= o)
+            inc += t;
+    }
+    if (lane == 31)
+        wsum[warp] = inc;
+    __syncthreads();
+    int base = 0;
+    for (int i = 0; i < warp; ++i)
+        base += wsum[i];
+    int acc = base + inc - run;
+    for (int w = w0; w < w1; ++w) {
+        const int p = __popc(words[w]);
+        pre[w] = acc;
+        acc += p;
+    }
+    __syncthreads();
+}
+
+// ------------------------------------------------------------------ calibration
+// A CTA covers 256 column vectors (16 bytes each) of a stripe of rows_per
+// rows; four rows are loaded per iteration.
+template <typename T>
+__global__ void __launch_bounds__(kOutThreads) channel_amax_kernel(const void *__restrict__ x,
+                                                                   int64_t rows, int64_t cols,
+                                                                   int64_t rows_per,
+                                                                   unsigned *__restrict__ amax)
+{
+    constexpr int E = VecInfo<T>::E;
+    const int64_t cv = (int64_t)blockIdx.x * kOutThreads + threadIdx.x;  // column vector
+    if (cv * E >= cols)
+        return;
+    const int64_t r0 = (int64_t)blockIdx.y * rows_per;
+    const int64_t r1 = r0 + rows_per < rows ? r0 + rows_per : rows;
+    const char *p = (const char *)x + (r0 * cols + cv * E) * (int64_t)sizeof(T);
+    const int64_t pitch = cols * (int64_t)sizeof(T);
+    float m[E];
+#pragma unroll
+    for (int i = 0; i < E; ++i)
+        m[i] = 0.0f;
+    int64_t r = r0;
+    for (; r + 4 <= r1; r += 4, p += 4 * pitch) {
+        uint4 u[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+            u[k] = ld16(p + k * pitch);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            float v[E];
+            unpack16<T>(u[k], v);
+#pragma unroll
+            for (int i = 0; i < E; ++i)
+                m[i] = fmaxf(m[i], fabsf(v[i]));
+        }
+    }
+    for (; r < r1; ++r, p += pitch) {
+        float v[E];
+        unpack16<T>(ld16(p), v);
+#pragma unroll
+        for (int i = 0; i < E; ++i)
+            m[i] = fmaxf(m[i], fabsf(v[i]));
+    }
+#pragma unroll
+    for (int i = 0; i < E; ++i)
+        atomicMax(amax + cv * E + i, __float_as_uint(m[i]));
+}
+
+// ------------------------------------------------------------------ selection
+// One CTA.  Channel c gets the unique 64-bit key (|amax_c| bits << 32) | ~c:
+// a larger amax gives a larger key, and among equal amax the lower index.
+// A most-significant-byte-first radix select (eight histogram passes over the
+// keys) finds the k-th largest key K; the selected channels are exactly those
+// with key >= K.  A popcount scan of the resulting bitmap then writes their
+// indices in ascending order.
+constexpr int kSelThreads = 1024;
+constexpr int kMaxOutWords = 4096;  // channels up to 131072
+
+__device__ __forceinline__ uint64_t channel_key(const float *amax, int c)
+{
+    return ((uint64_t)(__float_as_uint(__ldg(amax + c)) & 0x7FFFFFFFu) << 32) |
+           (uint32_t)~(uint32_t)c;
+}
+
+__global__ void __launch_bounds__(kSelThreads) select_kernel(const float *__restrict__ amax,
+                                                             int cols, int k,
+                                                             int32_t *__restrict__ idx,
+                                                             uint32_t *__restrict__ bitmap,
+                                                             float *__restrict__ fp8_scale)
+{
+    __shared__ unsigned hist[256];
+    __shared__ uint64_t s_prefix;
+    __shared__ unsigned s_remaining;
+    __shared__ uint32_t bm[kMaxOutWords];
+    __shared__ int pre[kMaxOutWords];
+    const int nwords = (cols + 31) / 32;
+    uint64_t prefix = 0, pmask = 0;
+    unsigned remaining = (unsigned)k;  // rank of K among the keys still matching
+    for (int byte = 7; byte >= 0 && k > 0; --byte) {
+        for (int i = threadIdx.x; i < 256; i += kSelThreads)
+            hist[i] = 0u;
+        __syncthreads();
+        const int sh = 8 * byte;
+        for (int c = threadIdx.x; c < cols; c += kSelThreads) {
+            const uint64_t key = channel_key(amax, c);
+            if ((key & pmask) == prefix)
+                atomicAdd(&hist[(key >> sh) & 0xFFu], 1u);
+        }
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            unsigned above = 0;
+            int d = 255;
+            for (; d > 0; --d) {
+                if (above + hist[d] >= remaining)
+                    break;
+                above += hist[d];
+            }
+            s_prefix = prefix | ((uint64_t)d << sh);
+            s_remaining = remaining - above;
+        }
+        __syncthreads();
+        prefix = s_prefix;
+        remaining = s_remaining;
+        pmask |= (uint64_t)0xFF << sh;
+        __syncthreads();
+    }
+    for (int w = threadIdx.x; w < nwords; w += kSelThreads) {
+        uint32_t bits = 0u;
+        if (k > 0) {
+            const int c1 = (w + 1) * 32 < cols ? (w + 1) * 32 : cols;
+            for (int c = w * 32; c < c1; ++c)
+                bits |= (uint32_t)(channel_key(amax, c) >= prefix) << (c & 31);
+        }
+        bm[w] = bits;
+    }
+    __syncthreads();
+    popc_prefix<kSelThreads>(bm, nwords, pre);
+    for (int w = threadIdx.x; w < nwords; w += kSelThreads) {
+        uint32_t bits = bm[w];
+        int j = pre[w];
+        while (bits) {
+            const int b = __ffs(bits) - 1;
+            bits &= bits - 1;
+            const int c = w * 32 + b;
+            idx[j] = c;
+            fp8_scale[j] = __fdiv_rn(__ldg(amax + c), 448.0f);
+            ++j;
+        }
+        bitmap[w] = bm[w];
+    }
+}
+
+// ------------------------------------------------------------------ masked amax
+template <typename T>
+__global__ void __launch_bounds__(kOutThreads) masked_amax_kernel(const void *__restrict__ x,
+                                                                  int64_t rows, int64_t cols,
+                                                                  const uint32_t *__restrict__ bm,
+                                                                  unsigned *__restrict__ out)
+{
+    constexpr int E = VecInfo<T>::E;
+    const int64_t nvec = rows * (cols / E);
+    float m = 0.0f;
+    for (int64_t q = (int64_t)blockIdx.x * kOutThreads + threadIdx.x; q < nvec;
+         q += (int64_t)gridDim.x * kOutThreads) {
+        const int64_t c0 = (q % (cols / E)) * E;
+        float v[E];
+        unpack16<T>(ld16((const char *)x + q * 16), v);
+        const uint32_t bits = __ldg(bm + (c0 >> 5)) >> (c0 & 31);
+#pragma unroll
+        for (int i = 0; i < E; ++i)
+            if (!((bits >> i) & 1u))
+                m = fmaxf(m, fabsf(v[i]));
+    }
+    m = group_max<32>(m);
+    __shared__ float wm[kOutThreads / 32];
+    if ((threadIdx.x & 31) == 0)
+        wm[threadIdx.x >> 5] = m;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        float b = wm[0];
+        for (int w = 1; w < kOutThreads / 32; ++w)
+            b = fmaxf(b, wm[w]);
+        atomicMax(out, __float_as_uint(b));
+    }
+}
+
+// ------------------------------------------------------------------ split quantization
+
+template <typename T, int FMT, int RND>
+__global__ void __launch_bounds__(kOutThreads) outlier_row_kernel(OutlierArgs a)
+{
+    constexpr int B = FmtInfo<FMT>::B;
+    __shared__ NvTables tab;
+    __shared__ int pre[kMaxOutWords];
+    const int64_t cols = a.cols, rows = a.rows;
+    const int nwords = (int)((cols + 31) / 32);
+    popc_prefix<kOutThreads>(a.bitmap, nwords, pre);
+    float s_g = 0.0f, inv6 = 0.0f;
+    if (FMT == NVFP4) {
+        s_g = outer_scale(*a.amax);
+        inv6 = nv_inv6(s_g);
+        nv_tables_fill(tab, s_g);
+        if (blockIdx.x == 0 && threadIdx.x == 0 && a.codes)
+            a.tscale[0] = s_g;
+    }
+    __syncthreads();
+    const PhiloxKey key = philox_key(a.seed);
+    const int64_t bpr = cols / B;
+    const int64_t nblk = rows * bpr;
+    const int lane = threadIdx.x & 31;
+    for (int64_t base = (int64_t)blockIdx.x * kOutThreads; base < nblk;
+         base += (int64_t)gridDim.x * kOutThreads) {
+        const int64_t blk = base + threadIdx.x;
+        const bool valid = blk < nblk;
+        const int64_t r = valid ? blk / bpr : 0;
+        const int64_t c0 = valid ? (blk - r * bpr) * B : 0;
+        float v[B], x[B];
+        if (valid)
+            load_block<T, B>((const char *)a.x + blk * B * (int64_t)sizeof(T), x);
+        else
+#pragma unroll
+            for (int i = 0; i < B; ++i)
+                x[i] = 0.0f;
+        const uint32_t word = valid ? __ldg(a.bitmap + (c0 >> 5)) : 0u;
+        const uint32_t ret = (B == 32) ? word : ((word >> (c0 & 31)) & 0xFFFFu);
+#pragma unroll
+        for (int i = 0; i < B; ++i)
+            v[i] = ((ret >> i) & 1u) ? 0.0f : x[i];
+        float am = 0.0f;
+#pragma unroll
+        for (int i = 0; i < B; ++i)
+            am = fmaxf(am, fabsf(v[i]));
+        float s_o = s_g, inv6b = inv6;
+        if (FMT == NV2L) {
+            s_o = outer_scale(group_max<8>(am));
+            inv6b = nv_inv6(s_o);
+        }
+        const Scale sc = block_scale<FMT>(am, s_o, inv6b, &tab);
+        uint32_t q[B / 8];
+        encode_block<B, RND>(v, sc, key, (uint64_t)blk * B, 0u, a.offset, q);
+        if (!valid)
+            continue;
+        if (a.codes) {
+            if (B == 16)
+                *reinterpret_cast<uint2 *>(a.codes + blk * 8) = make_uint2(q[0], q[1]);
+            else
+                *reinterpret_cast<uint4 *>(a.codes + blk * 16) =
+                    make_uint4(q[0], q[1], q[2], q[3]);
+            a.scales[blk] = (uint8_t)sc.code;
+            if (FMT == NV2L && (lane & 7) == 0)
+                a.tscale[blk >> 3] = s_o;
+        }
+        float xh[B];
+#pragma unroll
+        for (int w = 0; w < B / 8; ++w) {
+            e2m1_decode8(q[w], xh + 8 * w);
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+                xh[8 * w + i] = __fmul_rn(xh[8 * w + i], sc.s_eff);
+        }
+        uint32_t mask = block_mask<B>(v, sc.lim);
+        // retained elements: FP8 E4M3 with the channel's static scale (an
+        // unrolled predicated loop keeps x and xh in registers)
+        if (ret) {
+            const int jb = pre[c0 >> 5] + __popc(word & ((1u << (c0 & 31)) - 1u));
+#pragma unroll
+            for (int i = 0; i < B; ++i) {
+                if (!((ret >> i) & 1u))
+                    continue;
+                const int j = jb + __popc(ret & ((1u << i) - 1u));
+                if (j >= a.k)  // more bits set than k: outside the contract, stay in bounds
+                    continue;
+                const float s = __ldg(a.fp8_scale + j);
+                const float rcp = (s == 0.0f) ? 0.0f : __frcp_rn(s);
+                const float y = __fmul_rn(x[i], rcp);
+                const uint32_t code = e4m3_rn_sat(fabsf(y)) | ((__float_as_uint(y) >> 24) & 0x80u);
+                if (a.fp8)
+                    a.fp8[r * a.k + j] = (uint8_t)code;
+                const float m = __fmul_rn(e4m3_value(code & 0x7Fu), s);
+                xh[i] = (code & 0x80u) ? -m : m;
+                const bool in = fabsf(x[i]) <= __fmul_rn(448.0f, s);
+                mask = in ? (mask | (1u << i)) : (mask & ~(1u << i));
+            }
+        }
+        if (a.xhat) {
+#pragma unroll
+            for (int w = 0; w < B / 8; ++w) {
+                const float *h = xh + 8 * w;
+                if (a.xhat_bf16)
+                    *reinterpret_cast<uint4 *>((char *)a.xhat + (blk * B + w * 8) * 2) =
+                        make_uint4(bf16x2_rn(h[0], h[1]), bf16x2_rn(h[2], h[3]),
+                                   bf16x2_rn(h[4], h[5]), bf16x2_rn(h[6], h[7]));
+                else {
+                    float4 *dst = reinterpret_cast<float4 *>((char *)a.xhat + (blk * B + w * 8) * 4);
+                    dst[0] = make_float4(h[0], h[1], h[2], h[3]);
+                    dst[1] = make_float4(h[4], h[5], h[6], h[7]);
+                }
+            }
+        }
+        if (a.mask) {
+            if (B == 16)
+                reinterpret_cast<uint16_t *>(a.mask)[blk] = (uint16_t)mask;
+            else
+                reinterpret_cast<uint32_t *>(a.mask)[blk] = mask;
+        }
+    }
+}
+
+// ------------------------------------------------------------------ launchers
+static int grid_cap(int64_t need, int per_sm)
+{
+    const int64_t cap = (int64_t)sm_count() * per_sm;
+    return (int)(need < cap ? (need > 0 ? need : 1) : cap);
+}
+
+cudaError_t launch_channel_amax(const void *x, int bf16, int64_t rows, int64_t cols,
+                                float *amax, cudaStream_t s)
+{
+    if (rows == 0 || cols == 0)
+        return cudaSuccess;
+    const int E = bf16 ? 8 : 4;
+    const int64_t gx = (cols / E + kOutThreads - 1) / kOutThreads;
+    // enough row stripes for about eight CTAs per SM, at least 16 rows each
+    int64_t gy = ((int64_t)sm_count() * 8 + gx - 1) / gx;
+    const int64_t max_gy = (rows + 15) / 16;
+    gy = gy < max_gy ? gy : max_gy;
+    gy = gy < 65535 ? gy : 65535;
+    const int64_t rows_per = (rows + gy - 1) / gy;
+    gy = (rows + rows_per - 1) / rows_per;
+    dim3 grid((unsigned)gx, (unsigned)gy);
+    if (bf16)
+        channel_amax_kernel<__nv_bfloat16><<<grid, kOutThreads, 0, s>>>(x, rows, cols, rows_per,
+                                                                        (unsigned *)amax);
+    else
+        channel_amax_kernel<float><<<grid, kOutThreads, 0, s>>>(x, rows, cols, rows_per,
+                                                                (unsigned *)amax);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_select(const float *amax, int cols, int k, int32_t *idx, uint32_t *bitmap,
+                          float *fp8_scale, cudaStream_t s)
+{
+    select_kernel<<<1, kSelThreads, 0, s>>>(amax, cols, k, idx, bitmap, fp8_scale);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_masked_amax(const void *x, int bf16, int64_t rows, int64_t cols,
+                               const uint32_t *bitmap, float *out, cudaStream_t s)
+{
+    cudaError_t e = cudaMemsetAsync(out, 0, sizeof(float), s);
+    if (e != cudaSuccess || rows == 0 || cols == 0)
+        return e;
+    const int E = bf16 ? 8 : 4;
+    const int grid = grid_cap(rows * (cols / E) / kOutThreads + 1, 4);
+    if (bf16)
+        masked_amax_kernel<__nv_bfloat16><<<grid, kOutThreads, 0, s>>>(x, rows, cols, bitmap,
+                                                                       (unsigned *)out);
+    else
+        masked_amax_kernel<float><<<grid, kOutThreads, 0, s>>>(x, rows, cols, bitmap,
+                                                               (unsigned *)out);
+    return cudaGetLastError();
+}
+
+template <typename T, int FMT, int RND>
+static cudaError_t outlier_go(const OutlierArgs &a, cudaStream_t s)
+{
+    constexpr int B = FmtInfo<FMT>::B;
+    const int64_t nblk = a.rows * (a.cols / B);
+    if (nblk == 0)
+        return cudaSuccess;
+    outlier_row_kernel<T, FMT, RND><<<grid_cap((nblk + kOutThreads - 1) / kOutThreads, 8),
+                                      kOutThreads, 0, s>>>(a);
+    return cudaGetLastError();
+}
+
+template <typename T>
+static cudaError_t outlier_fmt(const OutlierArgs &a, int fmt, int rnd, cudaStream_t s)
+{
+    switch (fmt * 2 + rnd) {
+    case NVFP4 * 2 + RNE: return outlier_go<T, NVFP4, RNE>(a, s);
+    case NVFP4 * 2 + SR: return outlier_go<T, NVFP4, SR>(a, s);
+    case MXFP4 * 2 + RNE: return outlier_go<T, MXFP4, RNE>(a, s);
+    case MXFP4 * 2 + SR: return outlier_go<T, MXFP4, SR>(a, s);
+    case NV2L * 2 + RNE: return outlier_go<T, NV2L, RNE>(a, s);
+    default: return outlier_go<T, NV2L, SR>(a, s);
+    }
+}
+
+cudaError_t launch_outlier_quant(const OutlierArgs &a, int bf16, int fmt, int rnd, cudaStream_t s)
+{
+    return bf16 ? outlier_fmt<__nv_bfloat16>(a, fmt, rnd, s) : outlier_fmt<float>(a, fmt, rnd, s);
+}
+
+}  // namespace fqk

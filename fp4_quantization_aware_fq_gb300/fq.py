@@ -125,9 +125,14 @@ def lib():
         L.fq_osci_update_reset.argtypes = [P(Config), i32, P(i64), P(i64), P(vp), P(vp), P(vp),
                                            P(vp), P(_QT), P(_QT), P(vp), i32, P(vp),
                                            ctypes.c_float, vp, vp, sz, vp]
+        L.fq_channel_amax.argtypes = [vp, i32, i64, i64, vp, vp]
+        L.fq_select_channels.argtypes = [vp, i64, i64, vp, vp, vp, vp]
+        L.fq_quantize_outliers.argtypes = [P(Config), vp, i32, i64, i64, vp, i64, vp, P(_QT), vp,
+                                           vp, i32, vp, vp, sz, vp]
         for name in ("fq_amax", "fq_quantize", "fq_fakequant_ste", "fq_dequantize",
                      "fq_ste_backward", "fq_osci_update", "fq_osci_reset",
-                     "fq_osci_update_noalloc", "fq_osci_update_reset"):
+                     "fq_osci_update_noalloc", "fq_osci_update_reset", "fq_channel_amax",
+                     "fq_select_channels", "fq_quantize_outliers"):
             getattr(L, name).restype = ctypes.c_int
         L.fq_status_string.argtypes = [ctypes.c_int]
         L.fq_status_string.restype = ctypes.c_char_p
@@ -363,3 +368,76 @@ def fq_osci_reset(cfg: Config, master: Sequence[torch.Tensor], dist_q: Sequence[
         float(threshold), _ptr(n_reset), _stream(stream))
     _check(st, "fq_osci_reset")
     return n_reset
+
+
+# --------------------------------------------------------------------------
+# static outlier retention
+# --------------------------------------------------------------------------
+MAX_CHANNELS = 131072
+
+
+def fq_channel_amax(x: torch.Tensor, amax: Optional[torch.Tensor] = None,
+                    stream=None) -> torch.Tensor:
+    """Running per-channel (column) max |x|; amax accumulates across calls."""
+    rows, cols = _dims(x)
+    if amax is None:
+        amax = torch.zeros(cols, dtype=torch.float32, device=x.device)
+    st = lib().fq_channel_amax(x.data_ptr(), _dtype_code(x), rows, cols, amax.data_ptr(),
+                               _stream(stream))
+    _check(st, "fq_channel_amax")
+    return amax
+
+
+@dataclass
+class Outliers:
+    """Kept channels: ascending indices, bitmap (int32 words), FP8 scales."""
+    idx: torch.Tensor
+    bitmap: torch.Tensor
+    fp8_scale: torch.Tensor
+
+    @property
+    def k(self) -> int:
+        return self.idx.numel()
+
+
+def fq_select_channels(channel_amax: torch.Tensor, k: int, stream=None) -> Outliers:
+    cols = channel_amax.numel()
+    dev = channel_amax.device
+    idx = torch.empty(max(k, 4), dtype=torch.int32, device=dev)
+    bitmap = torch.empty(max((cols + 31) // 32, 4), dtype=torch.int32, device=dev)
+    fp8_scale = torch.empty(max(k, 4), dtype=torch.float32, device=dev)
+    st = lib().fq_select_channels(channel_amax.data_ptr(), cols, k, idx.data_ptr(),
+                                  bitmap.data_ptr(), fp8_scale.data_ptr(), _stream(stream))
+    _check(st, "fq_select_channels")
+    return Outliers(idx[:k], bitmap[:(cols + 31) // 32], fp8_scale[:k])
+
+
+def fq_quantize_outliers(x: torch.Tensor, cfg: Config, sel: Outliers,
+                         out: Optional[QTensor] = None, fp8: Optional[torch.Tensor] = None,
+                         xhat: Optional[torch.Tensor] = None, xhat_dtype=None,
+                         want_q: bool = True, want_fp8: bool = True, want_xhat: bool = True,
+                         want_mask: bool = True, mask: Optional[torch.Tensor] = None,
+                         ws: Optional[torch.Tensor] = None, stream=None):
+    """Split FP4 / FP8 quantization; returns (out, fp8, xhat, mask)."""
+    rows, cols = _dims(x)
+    k = sel.k
+    dev = x.device
+    if out is None and want_q:
+        out = alloc_qtensor(rows, cols, cfg.format, dev)
+    if fp8 is None and want_fp8:
+        fp8 = torch.empty((rows, max(k, 1)), dtype=torch.uint8, device=dev)[:, :k]
+    if xhat is None and want_xhat:
+        xhat = torch.empty((rows, cols), dtype=xhat_dtype or x.dtype, device=dev)
+    if mask is None and want_mask:
+        mask = torch.empty(((rows * cols + 7) // 8 + 15) // 16 * 16, dtype=torch.uint8,
+                           device=dev)
+    if ws is None:
+        ws = workspace(cfg, rows, cols, dev)
+    oq = ctypes.byref(out._c()) if out is not None else None
+    st = lib().fq_quantize_outliers(ctypes.byref(cfg), x.data_ptr(), _dtype_code(x), rows, cols,
+                                    sel.bitmap.data_ptr(), k, sel.fp8_scale.data_ptr(), oq,
+                                    _ptr(fp8), _ptr(xhat),
+                                    _dtype_code(xhat) if xhat is not None else F32, _ptr(mask),
+                                    _ptr(ws), 0 if ws is None else ws.numel(), _stream(stream))
+    _check(st, "fq_quantize_outliers")
+    return out, fp8, xhat, mask

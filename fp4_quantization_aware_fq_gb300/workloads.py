@@ -1,4 +1,4 @@
-"""Seeded synthetic inputs for the five fake-quantization workloads.
+"""Seeded synthetic inputs for the fake-quantization workloads.
 
 This module only draws random tensors; it holds none of the quantization
 arithmetic.  The same tensors feed the CUDA library and the CPU oracle, so
@@ -13,6 +13,8 @@ Workloads (shapes and distributions of the pages' QAT / TetraJet-v2 use):
   grad_2level   bf16 [16384, 4096] ~ Laplace(0, 1e-3)                       seed 3
   moe_qat       32 experts x (bf16 [2880, 5760] + [5760, 2880]) ~ N(0, .02) seed 4,
                 master updates delta_t ~ N(0, 1e-4)                        seed 1000 + t
+  channel_act   bf16 [8192, 8192] ~ N(0, 1), 64 outlier channels x50 shared by every
+                batch of a calibration window (channel seed 5; batch seed 500 + t)
 Each generator takes the shape as an argument so that tests can draw smaller
 tensors with the same recipe.
 """
@@ -26,6 +28,7 @@ WORKLOADS = {
     "nvfp4_act": dict(shape=(8192, 8192), seed=2),
     "grad_2level": dict(shape=(16384, 4096), seed=3),
     "moe_qat": dict(experts=32, up_shape=(2880, 5760), down_shape=(5760, 2880), seed=4),
+    "channel_act": dict(shape=(8192, 8192), seed=500, channel_seed=5, n_outlier_cols=64),
 }
 
 
@@ -64,6 +67,22 @@ def nvfp4_act(shape=(8192, 8192), seed=2, n_outlier_cols=8, device="cpu") -> tor
     x = torch.randn(shape, generator=g, dtype=torch.float32, device=device)
     cols = torch.randperm(shape[1], generator=g, device=device)[:n_outlier_cols]
     x[:, cols] *= 50.0
+    return x.to(torch.bfloat16)
+
+
+def outlier_channels(cols: int, n: int, channel_seed: int) -> torch.Tensor:
+    """The n outlier channels of an activation recipe (uniform random)."""
+    return torch.randperm(cols, generator=_gen(channel_seed))[:n]
+
+
+def channel_act(shape=(8192, 8192), seed=500, channel_seed=5, n_outlier_cols=64, factor=50.0,
+                device="cpu") -> torch.Tensor:
+    """BF16 activations ~ N(0, 1) whose outlier channels -- fixed by
+    channel_seed, so that every batch of a calibration window shares them --
+    are multiplied by factor; seed draws the batch."""
+    g = _gen(seed, device)
+    x = torch.randn(shape, generator=g, dtype=torch.float32, device=device)
+    x[:, outlier_channels(shape[1], n_outlier_cols, channel_seed).to(device)] *= factor
     return x.to(torch.bfloat16)
 
 

@@ -17,7 +17,9 @@
  *  [TJV2]   "Resumo Técnico: TetraJet-v2" -- §2A double-block NVFP4 (FP32 scale
  *           per 128-element outer block, 8-bit scale per 16-element inner
  *           block), stochastic rounding with E[round(x)] = x, 1x16 groups and
- *           the transposed weight; §2B OsciReset (dist_Q / dist_M).
+ *           the transposed weight; §2B OsciReset (dist_Q / dist_M); §2C
+ *           OutControl (random Hadamard transform of backward operands,
+ *           static retention of outlier channels in FP8).
  *
  * Numeric definitions (the pages leave these open; this library's readings):
  *  E2M1 code: bit 3 sign, bits 2..1 exponent (bias 1), bit 0 mantissa;
@@ -253,6 +255,63 @@ FQ_API fq_status fq_osci_reset(const fq_config *cfg, int32_t ntensors, const int
                         const int64_t *cols, float *const *master, float *const *dist_q,
                         float *const *dist_m, const fq_qtensor *cur, float threshold,
                         unsigned long long *n_reset, void *stream);
+
+/* ---- Static outlier retention ([TJV2] §2C, OutControl) -------------------
+ * A few activation channels (columns of a [rows, cols] activation, the
+ * reduction dimension of the GEMM that consumes it) carry values far larger
+ * than the rest; inside a 1x16 block they set the block scale and crush the
+ * other fifteen elements to zero.  OutControl keeps the channels with the
+ * largest norm over a short calibration window in FP8 and quantizes the rest
+ * of the activation to FP4 with those channels removed.  This library's
+ * readings: the norm is max |x| per channel; the k channels with the largest
+ * amax are kept (equal amax: lower index first); each kept channel c has the
+ * static FP8 scale s_c = amax_c / 448 (FP32 division) and is stored as E4M3
+ * (OCP "FN", nearest-even, saturating at 448) of y = x * (1 / s_c); the FP4
+ * part is the row-wise quantization of x with the kept columns set to +0.
+ * Channel counts are limited to FQ_MAX_CHANNELS (FQ_ERR_SHAPE beyond). */
+#define FQ_MAX_CHANNELS 131072
+
+/* Calibration: amax_inout[c] = max(amax_inout[c], max_r |x[r, c]|) for a
+ * [rows, cols] activation, so that consecutive calls over the calibration
+ * batches accumulate the window's per-channel amax (zero-fill amax_inout,
+ * cols floats, before the first).  cols % 16 == 0.  amax_inout must hold
+ * non-negative values (atomic max on the FP32 bit patterns). */
+FQ_API fq_status fq_channel_amax(const void *x, int32_t x_dtype, int64_t rows, int64_t cols,
+                                 float *amax_inout, void *stream);
+
+/* Selection: the k channels with the largest channel_amax (non-negative;
+ * ties go to the lower index), 0 <= k <= cols (FQ_ERR_INVALID_ARG outside).
+ * Writes idx[k] (int32, ascending channel indices), bitmap[ceil(cols/32)]
+ * (bit c % 32 of word c / 32 set iff channel c is kept; unused high bits of
+ * the last word are zero) and fp8_scale[k] = channel_amax[idx[j]] / 448.
+ * idx and fp8_scale may be NULL when k == 0.  One CTA on the GPU. */
+FQ_API fq_status fq_select_channels(const float *channel_amax, int64_t cols, int64_t k,
+                                    int32_t *idx, uint32_t *bitmap, float *fp8_scale,
+                                    void *stream);
+
+/* Split quantization of a [rows, cols] activation under the kept channels
+ * (bitmap and fp8_scale as fq_select_channels writes them; the bitmap must
+ * have exactly k bits set -- a kept channel's rank among the set bits indexes
+ * fp8_scale and the FP8 columns).  Writes, each optional (NULL: skipped):
+ *   out   row-wise FP4 codes / scales / tscale of x with the kept columns
+ *         zeroed (layouts as fq_quantize; NVFP4 takes s_g from the amax of
+ *         that zeroed tensor);
+ *   fp8   [rows, k] bytes: sign | E4M3(|x * (1 / s_j)|) of the kept elements,
+ *         column j holding the j-th kept channel;
+ *   xhat  the fake-quantized activation in xhat_dtype: the FP4 value for
+ *         ordinary elements, E4M3value * s_j (sign applied) for kept ones;
+ *   mask  STE mask: the FP4 rule for ordinary elements, |x| <= 448 * s_j for
+ *         kept ones.
+ * cols % B == 0 (cols % 128 for the double block).  rht_seed must be 0
+ * (FQ_ERR_UNSUPPORTED: OutControl retains outliers on the forward operands
+ * and transforms the backward ones).  The workspace is that of
+ * fq_workspace_size (NVFP4: the masked tensor amax). */
+FQ_API fq_status fq_quantize_outliers(const fq_config *cfg, const void *x, int32_t x_dtype,
+                                      int64_t rows, int64_t cols, const uint32_t *bitmap,
+                                      int64_t k, const float *fp8_scale, const fq_qtensor *out,
+                                      uint8_t *fp8, void *xhat, int32_t xhat_dtype,
+                                      uint8_t *mask, void *workspace, size_t workspace_bytes,
+                                      void *stream);
 
 /* Static description of a status code. */
 FQ_API const char *fq_status_string(fq_status status);

@@ -19,7 +19,8 @@ def test_header_declares_the_boundary():
     names = set(fq.declared_symbols())
     for n in ("fq_quantize", "fq_dequantize", "fq_fakequant_ste", "fq_osci_update",
               "fq_osci_reset", "fq_ste_backward", "fq_amax", "fq_workspace_size",
-              "fq_osci_workspace_size", "fq_status_string"):
+              "fq_osci_workspace_size", "fq_status_string", "fq_channel_amax",
+              "fq_select_channels", "fq_quantize_outliers"):
         assert n in names
 
 
@@ -135,3 +136,40 @@ def test_osci_argument_errors(L):
     r = L.fq_osci_reset
     assert r(ctypes.byref(cfg), 2, rows, cols, ptrs, ptrs, ptrs, None, 4.0, None, None) == 1
     assert r(ctypes.byref(cfg), 2, rows, cols, ptrs, ptrs, ptrs, qs, 4.0, FAKE + 4, None) == 3
+
+
+def test_outlier_argument_errors(L):
+    # channel amax
+    assert L.fq_channel_amax(FAKE, 9, 64, 64, FAKE, None) == 1             # unknown dtype
+    assert L.fq_channel_amax(FAKE, fq.F32, 64, 64, 0, None) == 1           # NULL amax
+    assert L.fq_channel_amax(FAKE, fq.F32, 64, 40, FAKE, None) == 2        # cols % 16
+    assert L.fq_channel_amax(FAKE + 4, fq.F32, 64, 64, FAKE, None) == 3    # misaligned
+    # selection
+    sel = L.fq_select_channels
+    assert sel(0, 64, 4, FAKE, FAKE, FAKE, None) == 1                      # NULL amax
+    assert sel(FAKE, 64, 4, 0, FAKE, FAKE, None) == 1                      # NULL idx, k > 0
+    assert sel(FAKE, 64, 65, FAKE, FAKE, FAKE, None) == 1                  # k > cols
+    assert sel(FAKE, 64, -1, FAKE, FAKE, FAKE, None) == 1                  # k < 0
+    assert sel(FAKE, fq.MAX_CHANNELS + 32, 4, FAKE, FAKE, FAKE, None) == 2  # too many channels
+    assert sel(FAKE, 64, 4, FAKE + 4, FAKE, FAKE, None) == 3               # misaligned idx
+    assert sel(FAKE, 0, 0, 0, FAKE, 0, None) == 0                          # nothing to select
+
+    # split quantization
+    def q(cfg=fq.Config(fq.NVFP4), x=FAKE, rows=64, cols=64, bm=FAKE, k=4, sc=FAKE, out=None,
+          fp8=FAKE, ws=FAKE, wsb=256):
+        o = ctypes.byref(out) if out is not None else None
+        return L.fq_quantize_outliers(ctypes.byref(cfg), x, fq.F32, rows, cols, bm, k, sc, o,
+                                      fp8, None, fq.F32, None, ws, wsb, None)
+    assert q(cfg=fq.Config(7)) == 1                                        # unknown format
+    assert q(bm=0) == 1                                                    # NULL bitmap
+    assert q(sc=0) == 1                                                    # NULL scales, k > 0
+    assert q(k=65) == 1                                                    # k > cols
+    assert q(cols=40) == 2                                                 # cols % 16
+    assert q(cfg=fq.Config(fq.NVFP4_2LEVEL), cols=64) == 2                 # cols % 128
+    assert q(cols=fq.MAX_CHANNELS + 16) == 2                               # too many channels
+    assert q(cfg=fq.Config(fq.MXFP4, fq.SR, 1, 0, rht_seed=3)) == 5        # no transform here
+    assert q(x=FAKE + 8) == 3                                              # misaligned input
+    assert q(out=_qt(scales=FAKE + 1)) == 3                                # misaligned scales
+    assert q(out=_qt(tscale=0)) == 1                                       # NVFP4 needs tscale
+    assert q(ws=0) == 4                                                    # no workspace
+    assert q(cfg=fq.Config(fq.MXFP4), ws=0, wsb=0, rows=0) == 0            # empty: nothing runs

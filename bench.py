@@ -14,12 +14,15 @@ One step = one pass of the whole hot path over the synthetic workloads:
                 channels x50; the 10% of channels (819) with the largest calibration amax
                 (two earlier batches, selected once before timing) go to FP8 E4M3, the rest
                 to NVFP4: codes, scales, s_g, FP8 columns, BF16 xhat, STE mask
+  qad_kl        QAD distillation loss: BF16 teacher and student logits [4096, 201088]
+                (gpt-oss's vocabulary size), per-row KL(teacher || student) at T = 1, its
+                mean, and the BF16 gradient with respect to the student logits
   moe_qat       one QAT step over 32 MoE experts (64 FP32 master matrices [2880, 5760] and
                 [5760, 2880], 1.06 G weights): update + NVFP4 fake-quant + OsciReset
                 statistics, then the OsciReset reset pass over the same weights
 The metric is algorithmic HBM bytes / device time (GB/s); elements/s are
 reported per workload.  Inputs live in HBM before the timed region; the step's
-working set (about 20 GB) is far larger than L2, so every workload starts cold.
+working set (about 26 GB) is far larger than L2, so every workload starts cold.
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 """
@@ -53,12 +56,13 @@ BYTES_PER_ELEM = {
     "grad_2level": 2 + 0.5 + 1 / 16 + 4 / 128,
     "grad_rht_rowcol": 2 + 2 * (0.5 + 1 / 16 + 4 / 128),
     "act_outliers": 2 + 2 + 0.5 + 1 / 16 + 819 / 8192 + 2 + 1 / 8,
+    "qad_kl": 2 + 2 + 2,
     "osci_update_reset": 20 + (4 + 0.5 + 1 / 16 + 8 + 8 + 0.5 + 1 / 16 + 2 + 1 / 8),
 }
 # Our kernels launched per step (memsets not counted).
 LAUNCHES_PER_STEP = {"nvfp4_small": 2, "mxfp4_weight": 1, "nvfp4_act": 2, "ste_backward": 1,
                      "grad_2level": 1, "grad_rht_rowcol": 1, "act_outliers": 2,
-                     "osci_update_reset": 2}
+                     "qad_kl": 2, "osci_update_reset": 2}
 # DRAM traffic per launch of the dominant call from an ncu capture, valid only
 # for the kernel source it was taken on (sha256 of k_osci.cu).  Captured on the
 # 2-expert case (66.4 M weights: pass A + pass B read+write 2852.8 MB) and
@@ -143,13 +147,13 @@ class ClockSampler:
 # --------------------------------------------------------------------------- workloads
 class Suite:
     """The workloads' inputs and outputs, resident on one GPU.  `only` limits
-    the suite to some workloads; `experts` scales the MoE workload down (for
-    profiling a smaller case of the same kernels)."""
+    the suite to some workloads; `experts` scales the MoE workload down and
+    `qad_rows` the logits (for profiling a smaller case of the same kernels)."""
 
     ORDER = ("nvfp4_small", "mxfp4_weight", "nvfp4_act", "ste_backward", "grad_2level",
-             "grad_rht_rowcol", "act_outliers", "osci_update_reset")
+             "grad_rht_rowcol", "act_outliers", "qad_kl", "osci_update_reset")
 
-    def __init__(self, dev, only=None, experts=None):
+    def __init__(self, dev, only=None, experts=None, qad_rows=None):
         import torch
         from fp4_quantization_aware_fq_gb300 import fq
         from fp4_quantization_aware_fq_gb300 import workloads as W
@@ -216,6 +220,15 @@ class Suite:
             self.m7 = self._mask(self.x7)
             self.ws7 = torch.empty(256, dtype=torch.uint8, device=dev)
             self.elems["act_outliers"] = self.x7.numel()
+        if "qad_kl" in want:
+            c = W.WORKLOADS["qad_logits"]
+            r8 = qad_rows or c["shape"][0]
+            self.zt8, self.zs8 = W.qad_logits((r8, c["shape"][1]), seed=c["seed"], device=dev)
+            self.loss8 = torch.empty(r8, dtype=torch.float32, device=dev)
+            self.mean8 = torch.empty(1, dtype=torch.float32, device=dev)
+            self.dz8 = torch.empty_like(self.zs8)
+            self.err8 = torch.zeros(1, dtype=torch.int32, device=dev)
+            self.elems["qad_kl"] = self.zt8.numel()
         if "osci_update_reset" in want:
             m = W.WORKLOADS["moe_qat"]
             ws = W.moe_weights(experts or m["experts"], m["up_shape"], m["down_shape"],
@@ -241,6 +254,11 @@ class Suite:
     def _mask(self, x):
         return self.torch.empty(((x.numel() + 7) // 8 + 15) // 16 * 16, dtype=self.torch.uint8,
                                 device=self.dev)
+
+    def check(self):
+        """Device-side error words of the calls that have them."""
+        if "qad_kl" in self.names and int(self.err8.item()) != 0:
+            raise RuntimeError("fq_qad_kl reported a shared-memory copy timeout")
 
     def step(self):
         for name in self.names:
@@ -277,6 +295,10 @@ class Suite:
         self.fq.fq_quantize_outliers(self.x7, self.cfg7, self.sel7, out=self.q7, fp8=self.fp87,
                                      xhat=self.xh7, mask=self.m7, ws=self.ws7)
 
+    def qad_kl(self):
+        self.fq.fq_qad_kl(self.zt8, self.zs8, loss_rows=self.loss8, loss_mean=self.mean8,
+                          dz=self.dz8, err=self.err8)
+
     def osci_update_reset(self):
         # one QAT step that also ends the OsciReset window (reset fused in)
         self.fq.fq_osci_update_reset(self.cfg5, self.master, self.delta, self.dq, self.dm,
@@ -309,7 +331,7 @@ def job_throughput(world: int, bytes_per_step: float, steps: int, ms: float) -> 
 def run_ours(args, rank, world, dist):
     import torch
     dev = torch.device("cuda", torch.cuda.current_device())
-    suite = Suite(dev, only=args.only, experts=args.experts)
+    suite = Suite(dev, only=args.only, experts=args.experts, qad_rows=args.qad_rows)
     stream = torch.cuda.current_stream()
     bps = bytes_per_step(suite.elems)
     total_bytes = sum(bps.values())
@@ -341,6 +363,7 @@ def run_ours(args, rank, world, dist):
     if dist:
         dist.barrier()
     clk = clocks.stop() if clocks else None
+    suite.check()
     ms = t0.elapsed_time(t1)
     per_ms = {n: sum(a.elapsed_time(b) for a, b in ev[n]) / args.steps for n in suite.names}
     ms = max_over_ranks(ms, dist, dev)
@@ -378,6 +401,9 @@ def e2e_buffers(suite):
     if "act_outliers" in suite.names:
         ins.append(suite.x7)
         outs += [suite.q7.codes, suite.q7.scales, suite.q7.tscale, suite.fp87]
+    if "qad_kl" in suite.names:
+        ins += [suite.zt8, suite.zs8]
+        outs += [suite.loss8, suite.mean8]
     if "osci_update_reset" in suite.names:
         ins += list(suite.delta)
         outs.append(suite.nreset)
@@ -464,6 +490,8 @@ def oracle_sample(max_seconds=None):
         q = oracle.quantize_outliers(f32(x7), sel7["idx"], sel7["fp8_scale"], oracle.NVFP4)
         oracle.f32_to_bf16_bits(q["xhat"])
     res["act_outliers"] = (x7.numel(), timed(c7))
+    zt8, zs8 = W.qad_logits((16, 201088), seed=6)
+    res["qad_kl"] = (zt8.numel(), timed(lambda: oracle.qad_kl(f32(zt8), f32(zs8))))
     w = W.normal((5760, 5760), 0.02, seed=4).to(__import__("torch").bfloat16)
     st = oracle.OsciState(f32(w), oracle.NVFP4)
     d = W.master_update((5760, 5760), 1).numpy()
@@ -475,7 +503,7 @@ def oracle_sample(max_seconds=None):
     res["osci_update_reset"] = (w.numel(), t_upd + timed(lambda: st.reset(4.0)))
     desc = ("oracle (scalar C, 1 thread) on: nvfp4_small full; mxfp4_weight full; "
             "nvfp4_act 4096 rows row+col; ste_backward 4096x8192; grad_2level 8192 rows SR; "
-            "grad_rht_rowcol 2048 rows; act_outliers 2048 rows; "
+            "grad_rht_rowcol 2048 rows; act_outliers 2048 rows; qad_kl 16 rows; "
             "osci update+reset on a [5760, 5760] matrix (one expert's weights); per-element "
             "rates scaled to the full step's elements")
     return res, desc
@@ -494,14 +522,15 @@ def oracle_gbs(sample, elems_full):
 FULL_ELEMS = {"nvfp4_small": 256 * 1024, "mxfp4_weight": 4096 * 4096,
               "nvfp4_act": 8192 * 8192, "ste_backward": 8192 * 8192,
               "grad_2level": 16384 * 4096, "grad_rht_rowcol": 16384 * 4096,
-              "act_outliers": 8192 * 8192,
+              "act_outliers": 8192 * 8192, "qad_kl": 4096 * 201088,
               "osci_update_reset": 32 * 2 * 2880 * 5760}
 
 
-def config_block(names=None, experts=None):
-    if names is not None and (list(names) != list(Suite.ORDER) or experts):
+def config_block(names=None, experts=None, qad_rows=None):
+    if names is not None and (list(names) != list(Suite.ORDER) or experts or qad_rows):
         return {"workload": "subset: " + ",".join(names) + (f"; moe experts={experts}"
-                                                           if experts else ""),
+                                                           if experts else "")
+                + (f"; qad rows={qad_rows}" if qad_rows else ""),
                 "l2": "no flush between steps", "bytes": "algorithmic"}
     return {"workload": "fake-quant suite over the synthetic workloads (one pass each per "
                         "step): nvfp4_small fp32 256x1024 NVFP4 RNE; mxfp4_weight bf16 "
@@ -511,11 +540,13 @@ def config_block(names=None, experts=None):
                         "gradient with the 16-point Hadamard transform, both orientations; "
                         "act_outliers bf16 8192x8192 activation, 819 channels kept in FP8 "
                         "E4M3 by calibration amax, the rest NVFP4 RNE with xhat + STE mask; "
+                        "qad_kl bf16 teacher/student logits 4096x201088: per-row KL at T=1, "
+                        "mean, bf16 student gradient; "
                         "moe_qat 32 experts x "
                         "(2880x5760 + 5760x2880) FP32 master: one QAT step with OsciReset "
                         "statistics and the window-end reset fused in",
             "elements_per_step": sum(FULL_ELEMS.values()),
-            "l2": "no flush: the step's working set (~20 GB) exceeds L2, inputs are cold",
+            "l2": "no flush: the step's working set (~26 GB) exceeds L2, inputs are cold",
             "bytes": "algorithmic (definition reads + writes; NVFP4 amax is a second read)"}
 
 
@@ -531,6 +562,8 @@ def main():
                     help="run only these workloads (profiling a single kernel)")
     ap.add_argument("--experts", type=int, default=None,
                     help="MoE experts in moe_qat (default: the full 32)")
+    ap.add_argument("--qad-rows", type=int, default=None,
+                    help="rows of the qad_kl logits (default: the full 4096)")
     args = ap.parse_args()
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -573,7 +606,7 @@ def main():
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
             "data": "synthetic (seeded torch generators, shapes/distributions of the "
                     "workloads)",
-            "config": config_block(suite.names, args.experts),
+            "config": config_block(suite.names, args.experts, args.qad_rows),
             "per_workload": per,
             "roofline": {"bound": "hbm", "kernel": dom + (" (osci_pass_a + osci_pass_b<reset>)"
                                                            if dom == "osci_update_reset" else ""),
@@ -591,7 +624,8 @@ def main():
                            "unit": UNIT, "h2d_bytes_per_step": e2e["h2d"],
                            "d2h_bytes_per_step": e2e["d2h"], "steps": e2e["steps"],
                            "ms_per_step": round(e2e["ms_total"] / e2e["steps"], 3)}
-        if not args.no_cpu_baseline and world == 1 and not args.only and not args.experts:
+        if (not args.no_cpu_baseline and world == 1 and not args.only and not args.experts
+                and not args.qad_rows):
             sample, desc = oracle_sample()
             gbs, secs = oracle_gbs(sample, suite.elems)
             line["cpu_baseline"] = {"value": round(gbs, 4), "unit": UNIT, "cores": 1,

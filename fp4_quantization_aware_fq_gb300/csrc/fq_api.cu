@@ -1,5 +1,6 @@
 // fq_api.cu -- the C ABI declared in include/fq.h: host-side argument
 // checks, workspace handling, and launches on the caller's stream.
+#include <cmath>
 #include <cstring>
 
 #include "fq.h"
@@ -514,6 +515,41 @@ fq_status fq_quantize_outliers(const fq_config *cfg, const void *x, int32_t x_dt
     a.seed = cfg->seed;
     a.offset = cfg->offset;
     return cuda_status(launch_outlier_quant(a, bf16, fmt, cfg->rounding, s));
+}
+
+fq_status fq_qad_kl(const void *teacher, const void *student, int32_t dtype, int64_t rows,
+                    int64_t vocab, float temperature, float grad_scale, float *loss_rows,
+                    float *loss_mean, void *dstudent, int32_t dstudent_dtype, int32_t *err,
+                    void *stream)
+{
+    if (!valid_dtype(dtype) || (rows > 0 && (!teacher || !student || !loss_rows)))
+        return FQ_ERR_INVALID_ARG;
+    if (dstudent && !valid_dtype(dstudent_dtype))
+        return FQ_ERR_INVALID_ARG;
+    if (!(temperature > 0.0f) || !(temperature < INFINITY) || !(fabsf(grad_scale) < INFINITY))
+        return FQ_ERR_INVALID_ARG;
+    if (rows < 0 || vocab <= 0 || vocab % 8 != 0)
+        return FQ_ERR_SHAPE;
+    if (!aligned16(teacher) || !aligned16(student) || !aligned16(loss_rows) ||
+        (loss_mean && (reinterpret_cast<uintptr_t>(loss_mean) & 3u)) ||
+        (dstudent && !aligned16(dstudent)) || (err && (reinterpret_cast<uintptr_t>(err) & 3u)))
+        return FQ_ERR_ALIGN;
+    KlArgs a{};
+    size_t smem = 0;
+    if (!qad_plan(vocab, dtype == FQ_BF16 ? 2 : 4, &a.csize, &a.chunk, &smem))
+        return FQ_ERR_UNSUPPORTED;
+    a.zt = teacher;
+    a.zs = student;
+    a.rows = rows;
+    a.vocab = vocab;
+    a.k2 = (float)(1.4426950408889634 / (double)temperature);
+    a.gk = (float)((double)grad_scale / (double)temperature);
+    a.loss_rows = loss_rows;
+    a.dz = dstudent;
+    a.dz_bf16 = dstudent_dtype == FQ_BF16;
+    a.err = err;
+    return cuda_status(launch_qad_kl(a, dtype == FQ_BF16, smem, loss_mean,
+                                     static_cast<cudaStream_t>(stream)));
 }
 
 const char *fq_status_string(fq_status status)

@@ -109,6 +109,22 @@ struct OutlierArgs {
     uint32_t offset;
 };
 
+// QAD distillation loss over [rows, vocab] teacher / student logits; each row
+// is split over a cluster of csize CTAs holding `chunk` logits of each.
+struct KlArgs {
+    const void *zt;
+    const void *zs;
+    int64_t rows, vocab;
+    int64_t chunk;
+    int csize;
+    float k2;          // log2(e) / T
+    float gk;          // grad_scale / T
+    float *loss_rows;
+    void *dz;          // optional gradient with respect to zs
+    int dz_bf16;
+    int *err;          // optional device error word
+};
+
 int sm_count();
 
 cudaError_t launch_amax(const void *x, int bf16, int64_t n, float *out, cudaStream_t s);
@@ -127,5 +143,8 @@ cudaError_t launch_masked_amax(const void *x, int bf16, int64_t rows, int64_t co
                                const uint32_t *bitmap, float *out, cudaStream_t s);
 cudaError_t launch_outlier_quant(const OutlierArgs &a, int bf16, int fmt, int rnd,
                                  cudaStream_t s);
+bool qad_plan(int64_t vocab, int esz, int *csize, int64_t *chunk, size_t *smem);
+cudaError_t launch_qad_kl(const KlArgs &a, int bf16, size_t smem, float *loss_mean,
+                          cudaStream_t s);
 
 }  // namespace fqk

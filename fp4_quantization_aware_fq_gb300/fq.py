@@ -129,10 +129,12 @@ def lib():
         L.fq_select_channels.argtypes = [vp, i64, i64, vp, vp, vp, vp]
         L.fq_quantize_outliers.argtypes = [P(Config), vp, i32, i64, i64, vp, i64, vp, P(_QT), vp,
                                            vp, i32, vp, vp, sz, vp]
+        L.fq_qad_kl.argtypes = [vp, vp, i32, i64, i64, ctypes.c_float, ctypes.c_float, vp, vp,
+                                vp, i32, vp, vp]
         for name in ("fq_amax", "fq_quantize", "fq_fakequant_ste", "fq_dequantize",
                      "fq_ste_backward", "fq_osci_update", "fq_osci_reset",
                      "fq_osci_update_noalloc", "fq_osci_update_reset", "fq_channel_amax",
-                     "fq_select_channels", "fq_quantize_outliers"):
+                     "fq_select_channels", "fq_quantize_outliers", "fq_qad_kl"):
             getattr(L, name).restype = ctypes.c_int
         L.fq_status_string.argtypes = [ctypes.c_int]
         L.fq_status_string.restype = ctypes.c_char_p
@@ -441,3 +443,39 @@ def fq_quantize_outliers(x: torch.Tensor, cfg: Config, sel: Outliers,
                                     _ptr(ws), 0 if ws is None else ws.numel(), _stream(stream))
     _check(st, "fq_quantize_outliers")
     return out, fp8, xhat, mask
+
+
+# --------------------------------------------------------------------------
+# QAD distillation loss
+# --------------------------------------------------------------------------
+def fq_qad_kl(teacher: torch.Tensor, student: torch.Tensor, temperature: float = 1.0,
+              grad_scale: Optional[float] = None, want_grad: bool = True, dz_dtype=None,
+              loss_rows: Optional[torch.Tensor] = None,
+              loss_mean: Optional[torch.Tensor] = None, dz: Optional[torch.Tensor] = None,
+              err: Optional[torch.Tensor] = None, stream=None):
+    """Per-row KL(softmax(teacher / T) || softmax(student / T)), its mean, and
+    the student-logit gradient grad_scale * (q - p) / T (grad_scale defaults
+    to 1 / rows, the gradient of the mean).  Returns (loss_rows, loss_mean,
+    dz, err); err is a device int32 that is non-zero if a shared-memory copy
+    timed out (read it after synchronising)."""
+    rows, vocab = _dims(teacher)
+    if student.shape != teacher.shape or student.dtype != teacher.dtype:
+        raise ValueError("teacher and student logits must share shape and dtype")
+    dev = teacher.device
+    if grad_scale is None:
+        grad_scale = 1.0 / rows if rows else 0.0
+    if loss_rows is None:
+        loss_rows = torch.empty(max(rows, 4), dtype=torch.float32, device=dev)[:rows]
+    if loss_mean is None:
+        loss_mean = torch.empty(1, dtype=torch.float32, device=dev)
+    if dz is None and want_grad:
+        dz = torch.empty((rows, vocab), dtype=dz_dtype or student.dtype, device=dev)
+    if err is None:
+        err = torch.zeros(1, dtype=torch.int32, device=dev)
+    st = lib().fq_qad_kl(teacher.data_ptr(), student.data_ptr(), _dtype_code(teacher), rows,
+                         vocab, float(temperature), float(grad_scale), loss_rows.data_ptr(),
+                         loss_mean.data_ptr(), _ptr(dz),
+                         _dtype_code(dz) if dz is not None else F32, err.data_ptr(),
+                         _stream(stream))
+    _check(st, "fq_qad_kl")
+    return loss_rows, loss_mean, dz, err

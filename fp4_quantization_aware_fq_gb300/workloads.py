@@ -15,6 +15,8 @@ Workloads (shapes and distributions of the pages' QAT / TetraJet-v2 use):
                 master updates delta_t ~ N(0, 1e-4)                        seed 1000 + t
   channel_act   bf16 [8192, 8192] ~ N(0, 1), 64 outlier channels x50 shared by every
                 batch of a calibration window (channel seed 5; batch seed 500 + t)
+  qad_logits    bf16 teacher / student logits [4096, 201088] (gpt-oss's vocabulary
+                size): teacher ~ N(0, 3^2), student = teacher + N(0, 0.3^2)      seed 6
 Each generator takes the shape as an argument so that tests can draw smaller
 tensors with the same recipe.
 """
@@ -29,6 +31,7 @@ WORKLOADS = {
     "grad_2level": dict(shape=(16384, 4096), seed=3),
     "moe_qat": dict(experts=32, up_shape=(2880, 5760), down_shape=(5760, 2880), seed=4),
     "channel_act": dict(shape=(8192, 8192), seed=500, channel_seed=5, n_outlier_cols=64),
+    "qad_logits": dict(shape=(4096, 201088), seed=6),
 }
 
 
@@ -84,6 +87,17 @@ def channel_act(shape=(8192, 8192), seed=500, channel_seed=5, n_outlier_cols=64,
     x = torch.randn(shape, generator=g, dtype=torch.float32, device=device)
     x[:, outlier_channels(shape[1], n_outlier_cols, channel_seed).to(device)] *= factor
     return x.to(torch.bfloat16)
+
+
+def qad_logits(shape=(4096, 201088), seed=6, teacher_std=3.0, student_noise=0.3,
+               dtype=torch.bfloat16, device="cpu"):
+    """Teacher and student logits of a distillation step: the teacher ~ N(0,
+    teacher_std^2); the student (a quantized copy of the teacher) adds
+    N(0, student_noise^2).  Both rounded to dtype."""
+    g = _gen(seed, device)
+    zt = torch.randn(shape, generator=g, dtype=torch.float32, device=device) * teacher_std
+    zs = zt + torch.randn(shape, generator=g, dtype=torch.float32, device=device) * student_noise
+    return zt.to(dtype), zs.to(dtype)
 
 
 def grad_2level(shape=(16384, 4096), seed=3, scale=1e-3, device="cpu") -> torch.Tensor:

@@ -20,6 +20,10 @@
  *           the transposed weight; §2B OsciReset (dist_Q / dist_M); §2C
  *           OutControl (random Hadamard transform of backward operands,
  *           static retention of outlier channels in FP8).
+ *  [QADP]   "Quantization-Aware Distillation for NVFP4 Inference Accuracy
+ *           Recovery" -- §2 Metodologia: the NVFP4 student learns the BF16
+ *           teacher's output distribution through a KL-divergence loss at
+ *           softmax temperature T = 1.
  *
  * Numeric definitions (the pages leave these open; this library's readings):
  *  E2M1 code: bit 3 sign, bits 2..1 exponent (bias 1), bit 0 mantissa;
@@ -312,6 +316,32 @@ FQ_API fq_status fq_quantize_outliers(const fq_config *cfg, const void *x, int32
                                       uint8_t *fp8, void *xhat, int32_t xhat_dtype,
                                       uint8_t *mask, void *workspace, size_t workspace_bytes,
                                       void *stream);
+
+/* ---- QAD distillation loss ([QADP] §2; [QATREC] "Detalhes técnicos") ------
+ * For each row r of [rows, vocab] teacher logits zt and student logits zs
+ * (both FP32 or both BF16, dtype):
+ *   p = softmax(zt[r] / T), q = softmax(zs[r] / T),
+ *   loss_rows[r] = KL(p || q) = sum_v p_v log(p_v / q_v)      (FP32, nats)
+ *   loss_mean[0] = mean over rows of loss_rows                (optional)
+ *   dstudent[r, v] = grad_scale * (q_v - p_v) / T             (optional, in
+ *                    dstudent_dtype; the gradient of grad_scale * loss_rows[r]
+ *                    with respect to zs[r, v] -- grad_scale = 1 / rows gives
+ *                    the gradient of loss_mean).
+ * The pages fix T = 1; other T > 0 divide the logits.  Computed in FP32 from
+ * one read of each tensor (row maxima, sums of exponentials, then the terms):
+ * results differ from exact arithmetic by rounding only (a few units of 1e-6
+ * relative in p and q; KL to about 1e-6 absolute for vocabularies of 1e5).
+ * vocab % 8 == 0 (FQ_ERR_SHAPE), vocab <= about 450000 BF16 or 225000 FP32
+ * logits (FQ_ERR_UNSUPPORTED beyond: a row must fit the shared memory of one
+ * 8-CTA cluster).  Logits must be finite; temperature finite and > 0.
+ * err (device int32, may be NULL) is OR-ed with 1 if a copy into shared
+ * memory did not complete within 2 s (results then undefined); the caller
+ * zeroes it and reads it after synchronising.  rows == 0 writes only
+ * loss_mean (0); the tensor pointers may then be NULL. */
+FQ_API fq_status fq_qad_kl(const void *teacher, const void *student, int32_t dtype, int64_t rows,
+                           int64_t vocab, float temperature, float grad_scale, float *loss_rows,
+                           float *loss_mean, void *dstudent, int32_t dstudent_dtype,
+                           int32_t *err, void *stream);
 
 /* Static description of a status code. */
 FQ_API const char *fq_status_string(fq_status status);

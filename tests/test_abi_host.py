@@ -173,3 +173,23 @@ def test_outlier_argument_errors(L):
     assert q(out=_qt(tscale=0)) == 1                                       # NVFP4 needs tscale
     assert q(ws=0) == 4                                                    # no workspace
     assert q(cfg=fq.Config(fq.MXFP4), ws=0, wsb=0, rows=0) == 0            # empty: nothing runs
+
+
+def test_qad_kl_argument_errors(L):
+    def k(zt=FAKE, zs=FAKE, dtype=fq.BF16, rows=4, vocab=64, T=1.0, g=1.0, lr=FAKE, lm=FAKE,
+          dz=FAKE, dzt=fq.BF16, err=FAKE):
+        return L.fq_qad_kl(zt, zs, dtype, rows, vocab, T, g, lr, lm, dz, dzt, err, None)
+    assert k(dtype=7) == 1                       # unknown dtype
+    assert k(zs=0) == 1                          # NULL student
+    assert k(lr=0) == 1                          # NULL per-row losses
+    assert k(dzt=9) == 1                         # unknown gradient dtype
+    assert k(T=0.0) == 1                         # temperature must be > 0
+    assert k(T=float("inf")) == 1
+    assert k(g=float("nan")) == 1
+    assert k(vocab=60) == 2                      # vocab % 8
+    assert k(vocab=0) == 2
+    assert k(rows=-1) == 2
+    assert k(zt=FAKE + 8) == 3                   # misaligned logits
+    assert k(dz=FAKE + 4) == 3                   # misaligned gradient
+    assert k(vocab=460000) == 5                  # a BF16 row no longer fits one cluster
+    assert k(dtype=fq.F32, vocab=230000) == 5    # nor an FP32 one

@@ -188,3 +188,28 @@ def test_full_activation_outliers_nvfp4():
     sel, _ = _select_parity(amax, shape[1] // 10)
     x = W.channel_act(shape).to(DEV)
     _outlier_parity(x, sel, fq.NVFP4, xhat_dtype=torch.bfloat16)
+
+
+def test_column_half_composes_from_quantize_col():
+    """The backward (column-wise, X^T) half of retention: X^T's 16x1 blocks
+    lie inside single channels, so for every channel that is not kept they
+    are fq_quantize(COL) of x under the masked tensor amax -- the amax that
+    fq_quantize_outliers leaves in its workspace."""
+    rows, cols = 256, 512
+    x = _act((rows, cols), 21).to(DEV)
+    sel = fq.fq_select_channels(fq.fq_channel_amax(x), cols // 10)
+    cfg = fq.Config(fq.NVFP4)
+    ws = fq.workspace(cfg, rows, cols, DEV)
+    fq.fq_quantize_outliers(x, cfg, sel, ws=ws)
+    amax_masked = ws[:4].view(torch.float32)
+    _, cq = fq.fq_quantize(x, cfg, orient=fq.COL, amax_in=amax_masked)
+    torch.cuda.synchronize()
+    xz = as_oracle_input(x).copy()
+    kept = npy(sel.idx)
+    xz[:, kept] = 0.0
+    ref = oracle.quantize(xz, oracle.NVFP4, orient=oracle.ROWCOL)["col"]
+    other = np.setdiff1d(np.arange(cols), kept)
+    assert_eq("col.codes", npy(cq.codes)[other], ref["codes"][other])
+    assert_eq("col.scales", npy(cq.scales)[other], ref["scales"][other])
+    assert_eq("col.tscale", npy(cq.tscale)[:1].view(np.uint32),
+              ref["tscale"].reshape(-1)[:1].view(np.uint32))

@@ -2,7 +2,8 @@
 
 The oracle is a plain, slow, scalar C implementation (``fq_oracle.c``) of
 what the CUDA library computes, plus this ctypes wrapper that moves numpy
-arrays in and out.  Only the tests, ``__graft_entry__.smoke()`` and the
+arrays in and out (and, for the block-scaled GEMM, numpy's float64 matmul of
+the dequantized operands).  Only the tests, ``__graft_entry__.smoke()`` and the
 benchmark's CPU-baseline leg may import it; the library never does, and the
 two share no code.  Nothing here performs any of the method's arithmetic
 except through ``fq_oracle.c``; the wrapper only allocates arrays, widens
@@ -395,3 +396,14 @@ def qad_kl(zt: np.ndarray, zs: np.ndarray, temperature: float = 1.0, grad_scale=
                               _ptr(loss), _ptr(mean), _ptr(dz) if want_grad else None,
                               _ptr(scratch)), "qad_kl")
     return {"loss_rows": loss, "loss_mean": float(mean[0]), "dz": dz}
+
+
+def gemm(qa: dict, qb: dict, m: int, n: int, k: int, fmt=NVFP4) -> np.ndarray:
+    """Block-scaled FP4 GEMM by its plain definition: C = deq(A) deq(B)^T for
+    row-wise quantized A [m, k] and B [n, k] (both quantized along the shared
+    reduction dimension k, as the forward GEMM of a QAT linear layer takes
+    them), deq being `dequantize`.  The product is numpy's float64 matmul of
+    the exactly widened dequantized operands."""
+    a = dequantize(qa, m, k, fmt).astype(np.float64)
+    b = dequantize(qb, n, k, fmt).astype(np.float64)
+    return a @ b.T

@@ -410,6 +410,68 @@ def e2e_buffers(suite):
     return ins, outs
 
 
+GEMM_SHAPE = (8192, 8192, 8192)   # M (tokens), N (output features), K (input features)
+FP4_PER_BF16 = 6.0                 # nominal dense FP4 / BF16 tensor throughput (13.5 / 2.25 PF)
+FALLBACK_BF16_TFLOPS = 1900.0
+
+
+def bf16_peak():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        try:
+            with open(p) as f:
+                d = json.load(f)
+            for k in ("bf16_tflops", "bf16_TFLOPs"):
+                if k in d:
+                    return float(d[k]), "measured"
+        except Exception:
+            pass
+    return FALLBACK_BF16_TFLOPS, "fallback"
+
+
+def run_gemm(steps=20, warmup=3):
+    """The forward GEMM of a QAT linear layer on NVFP4 operands: a BF16
+    activation [M, K] ~ N(0, 1) and a weight [N, K] ~ N(0, 0.02), both
+    quantized with fq_quantize, then fq_gemm to a BF16 C, timed with CUDA
+    events on the launching stream (the operands, 64 MB of codes and scales,
+    stay in L2 between launches: this measures the tensor-core path)."""
+    import torch
+    from fp4_quantization_aware_fq_gb300 import fq
+    from fp4_quantization_aware_fq_gb300 import workloads as W
+    dev = torch.device("cuda", torch.cuda.current_device())
+    m, n, k = GEMM_SHAPE
+    cfg = fq.Config(fq.NVFP4)
+    a = W.normal((m, k), 1.0, seed=20, dtype=torch.bfloat16, device=dev)
+    b = W.normal((n, k), 0.02, seed=21, dtype=torch.bfloat16, device=dev)
+    qa, _ = fq.fq_quantize(a, cfg)
+    qb, _ = fq.fq_quantize(b, cfg)
+    del a, b
+    c = torch.empty((m, n), dtype=torch.bfloat16, device=dev)
+    ws = torch.empty(fq.fq_gemm_workspace_size(m, n, k), dtype=torch.uint8, device=dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream()
+    for _ in range(warmup):
+        fq.fq_gemm(qa, qb, m, n, k, cfg, c=c, ws=ws, err=err)
+    torch.cuda.synchronize()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for _ in range(steps):
+        fq.fq_gemm(qa, qb, m, n, k, cfg, c=c, ws=ws, err=err)
+    t1.record(stream)
+    torch.cuda.synchronize()
+    if int(err.item()) != 0:
+        raise RuntimeError("fq_gemm reported a pipeline wait timeout")
+    ms = t0.elapsed_time(t1) / steps
+    tflops = 2.0 * m * n * k / (ms * 1e-3) / 1e12
+    peak, kind = bf16_peak()
+    peak *= FP4_PER_BF16
+    return {"shape_mnk": list(GEMM_SHAPE), "dtype": "nvfp4 x nvfp4 -> bf16", "ms": round(ms, 4),
+            "tflops": round(tflops, 1), "bound": "tensor", "peak_tflops": round(peak, 1),
+            "peak_kind": kind + " bf16 x nominal FP4/BF16 ratio 6", "frac": round(tflops / peak, 3),
+            "launches_per_call": 3, "note": "not part of the suite step; operands L2-resident"}
+
+
 def run_e2e(args, suite, total_bytes):
     import torch
     stream = torch.cuda.current_stream()
@@ -564,6 +626,8 @@ def main():
                     help="MoE experts in moe_qat (default: the full 32)")
     ap.add_argument("--qad-rows", type=int, default=None,
                     help="rows of the qad_kl logits (default: the full 4096)")
+    ap.add_argument("--gemm-only", action="store_true",
+                    help="time only the NVFP4 tensor-core GEMM (one JSON object)")
     args = ap.parse_args()
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -577,6 +641,9 @@ def main():
     if not torch.cuda.is_available():
         raise SystemExit("bench.py needs a CUDA GPU")
     torch.cuda.set_device(local)
+    if args.gemm_only:
+        print(json.dumps(run_gemm(args.steps, args.warmup)), flush=True)
+        return
     dist = None
     if world > 1:
         import torch.distributed as dist
@@ -624,6 +691,8 @@ def main():
                            "unit": UNIT, "h2d_bytes_per_step": e2e["h2d"],
                            "d2h_bytes_per_step": e2e["d2h"], "steps": e2e["steps"],
                            "ms_per_step": round(e2e["ms_total"] / e2e["steps"], 3)}
+        if world == 1 and not args.only and not args.experts and not args.qad_rows:
+            line["gemm_nvfp4"] = run_gemm()
         if (not args.no_cpu_baseline and world == 1 and not args.only and not args.experts
                 and not args.qad_rows):
             sample, desc = oracle_sample()

@@ -535,8 +535,8 @@ fq_status fq_qad_kl(const void *teacher, const void *student, int32_t dtype, int
         (dstudent && !aligned16(dstudent)) || (err && (reinterpret_cast<uintptr_t>(err) & 3u)))
         return FQ_ERR_ALIGN;
     KlArgs a{};
-    size_t smem = 0;
-    if (!qad_plan(vocab, dtype == FQ_BF16 ? 2 : 4, &a.csize, &a.chunk, &smem))
+    QadPlan plan{};
+    if (!qad_plan(vocab, dtype == FQ_BF16 ? 2 : 4, &plan))
         return FQ_ERR_UNSUPPORTED;
     a.zt = teacher;
     a.zs = student;
@@ -548,8 +548,55 @@ fq_status fq_qad_kl(const void *teacher, const void *student, int32_t dtype, int
     a.dz = dstudent;
     a.dz_bf16 = dstudent_dtype == FQ_BF16;
     a.err = err;
-    return cuda_status(launch_qad_kl(a, dtype == FQ_BF16, smem, loss_mean,
+    return cuda_status(launch_qad_kl(a, dtype == FQ_BF16, plan, loss_mean,
                                      static_cast<cudaStream_t>(stream)));
+}
+
+size_t fq_gemm_workspace_size(int64_t m, int64_t n, int64_t k)
+{
+    if (m < 0 || n < 0 || k < 0)
+        return 0;
+    return gemm_workspace_bytes(m, n, k);
+}
+
+fq_status fq_gemm(const fq_config *cfg, const fq_qtensor *a, const fq_qtensor *b, int64_t m,
+                  int64_t n, int64_t k, void *c, int32_t c_dtype, void *workspace,
+                  size_t workspace_bytes, int32_t *err, void *stream)
+{
+    if (!valid_cfg(cfg) || !c || !valid_dtype(c_dtype))
+        return FQ_ERR_INVALID_ARG;
+    if (cfg->format != FQ_NVFP4 || cfg->rht_seed)
+        return FQ_ERR_UNSUPPORTED;
+    fq_status st;
+    if ((st = check_q(a, cfg->format)) != FQ_OK || (st = check_q(b, cfg->format)) != FQ_OK)
+        return st;
+    if (m < 0 || n < 0 || k < 0 || m % 128 || n % 128 || k % 256 || m / 128 > 65535)
+        return FQ_ERR_SHAPE;
+    if (!aligned16(c) || (err && (reinterpret_cast<uintptr_t>(err) & 3u)))
+        return FQ_ERR_ALIGN;
+    if (m == 0 || n == 0)
+        return FQ_OK;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (k == 0)
+        return cuda_status(cudaMemsetAsync(c, 0, (size_t)(m * n) * (c_dtype == FQ_BF16 ? 2 : 4), s));
+    if (!workspace || workspace_bytes < gemm_workspace_bytes(m, n, k))
+        return FQ_ERR_WORKSPACE;
+    if (!aligned16(workspace))
+        return FQ_ERR_ALIGN;
+    GemmArgs g{};
+    g.a_codes = a->codes;
+    g.a_scales = a->scales;
+    g.b_codes = b->codes;
+    g.b_scales = b->scales;
+    g.tscale_a = a->tscale;
+    g.tscale_b = b->tscale;
+    g.m = m;
+    g.n = n;
+    g.k = k;
+    g.c = c;
+    g.c_bf16 = c_dtype == FQ_BF16;
+    g.err = err;
+    return cuda_status(launch_gemm_nvfp4(g, workspace, s));
 }
 
 const char *fq_status_string(fq_status status)

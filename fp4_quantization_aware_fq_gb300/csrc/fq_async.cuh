@@ -138,4 +138,22 @@ __device__ __forceinline__ float4 dsmem_ld_f4(const float4 *local, uint32_t rank
     return v;
 }
 
+// Stores into the shared memory of CTA `rank` of this cluster, at the offset
+// that `local` has in this CTA's shared memory.
+__device__ __forceinline__ void dsmem_st_f4(float4 *local, uint32_t rank, float4 v)
+{
+    uint32_t remote;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_u32(local)), "r"(rank));
+    asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(remote), "f"(v.x),
+                 "f"(v.y), "f"(v.z), "f"(v.w)
+                 : "memory");
+}
+
+__device__ __forceinline__ void dsmem_st_f32(float *local, uint32_t rank, float v)
+{
+    uint32_t remote;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_u32(local)), "r"(rank));
+    asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(remote), "f"(v) : "memory");
+}
+
 }  // namespace fqk

@@ -117,12 +117,25 @@ struct KlArgs {
     int64_t rows, vocab;
     int64_t chunk;
     int csize;
+    int nbuf;          // row buffers per CTA (2: the next row loads during this one)
     float k2;          // log2(e) / T
     float gk;          // grad_scale / T
     float *loss_rows;
     void *dz;          // optional gradient with respect to zs
     int dz_bf16;
     int *err;          // optional device error word
+};
+
+// Block-scaled FP4 GEMM C[m, n] = alpha A[m, k] B[n, k]^T (NVFP4 operands).
+struct GemmArgs {
+    const uint8_t *a_codes, *a_scales;
+    const uint8_t *b_codes, *b_scales;
+    const float *tscale_a, *tscale_b;
+    int64_t m, n, k;
+    const uint8_t *sfa_mma, *sfb_mma;  // scales rearranged for the tensor cores (workspace)
+    void *c;
+    int c_bf16;
+    int *err;
 };
 
 int sm_count();
@@ -143,8 +156,18 @@ cudaError_t launch_masked_amax(const void *x, int bf16, int64_t rows, int64_t co
                                const uint32_t *bitmap, float *out, cudaStream_t s);
 cudaError_t launch_outlier_quant(const OutlierArgs &a, int bf16, int fmt, int rnd,
                                  cudaStream_t s);
-bool qad_plan(int64_t vocab, int esz, int *csize, int64_t *chunk, size_t *smem);
-cudaError_t launch_qad_kl(const KlArgs &a, int bf16, size_t smem, float *loss_mean,
+size_t gemm_smem_bytes();
+size_t gemm_workspace_bytes(int64_t m, int64_t n, int64_t k);
+cudaError_t launch_gemm_nvfp4(const GemmArgs &g, void *ws, cudaStream_t s);
+struct QadPlan {
+    int csize;        // CTAs per cluster (one row per cluster)
+    int64_t chunk;    // logits of each tensor per CTA
+    size_t smem;      // dynamic shared memory per CTA
+    int nbuf;         // row buffers per CTA
+    int threads;      // threads per CTA
+};
+bool qad_plan(int64_t vocab, int esz, QadPlan *p);
+cudaError_t launch_qad_kl(const KlArgs &a, int bf16, const QadPlan &p, float *loss_mean,
                           cudaStream_t s);
 
 }  // namespace fqk

@@ -221,12 +221,37 @@ __global__ void __launch_bounds__(kOutThreads) masked_amax_kernel(const void *__
 
 // ------------------------------------------------------------------ split quantization
 
+// One scalar of x as FP32.
+template <typename T>
+__device__ __forceinline__ float ld_scalar(const void *x, int64_t e);
+template <>
+__device__ __forceinline__ float ld_scalar<float>(const void *x, int64_t e)
+{
+    return __ldg(reinterpret_cast<const float *>(x) + e);
+}
+template <>
+__device__ __forceinline__ float ld_scalar<__nv_bfloat16>(const void *x, int64_t e)
+{
+    const unsigned short u = __ldg(reinterpret_cast<const unsigned short *>(x) + e);
+    return __uint_as_float((uint32_t)u << 16);
+}
+
+// Each thread quantizes one row block to FP4 with its kept elements zeroed
+// (the kept columns are the same in every row, so 10% of the channels touch
+// most blocks).  The kept elements themselves are then encoded by the warp
+// together: the warp's kept elements are numbered by a scan of the per-thread
+// counts and dealt out one per lane, so the FP8 work runs without divergence
+// however the kept columns fall across the warp's blocks.  A lane finds the
+// owner of its element by a binary search over the scan, re-reads the value
+// (an L1 hit: the owner has just loaded it), writes the FP8 code and the
+// kept value of xhat, and patches the owner's mask bits in shared memory.
 template <typename T, int FMT, int RND>
 __global__ void __launch_bounds__(kOutThreads) outlier_row_kernel(OutlierArgs a)
 {
     constexpr int B = FmtInfo<FMT>::B;
     __shared__ NvTables tab;
     __shared__ int pre[kMaxOutWords];
+    __shared__ uint32_t mstage[kOutThreads];
     const int64_t cols = a.cols, rows = a.rows;
     const int nwords = (int)((cols + 31) / 32);
     popc_prefix<kOutThreads>(a.bitmap, nwords, pre);
@@ -242,25 +267,40 @@ __global__ void __launch_bounds__(kOutThreads) outlier_row_kernel(OutlierArgs a)
     const PhiloxKey key = philox_key(a.seed);
     const int64_t bpr = cols / B;
     const int64_t nblk = rows * bpr;
+    const bool narrow = nblk <= 0xFFFFFFFFll;  // 32-bit block -> (row, column) division
     const int lane = threadIdx.x & 31;
+    const int wbase = threadIdx.x & ~31;
     for (int64_t base = (int64_t)blockIdx.x * kOutThreads; base < nblk;
          base += (int64_t)gridDim.x * kOutThreads) {
         const int64_t blk = base + threadIdx.x;
         const bool valid = blk < nblk;
-        const int64_t r = valid ? blk / bpr : 0;
-        const int64_t c0 = valid ? (blk - r * bpr) * B : 0;
-        float v[B], x[B];
-        if (valid)
-            load_block<T, B>((const char *)a.x + blk * B * (int64_t)sizeof(T), x);
-        else
+        int64_t r = 0, c0 = 0;
+        if (valid) {
+            if (narrow) {
+                const uint32_t b32 = (uint32_t)blk, q = b32 / (uint32_t)bpr;
+                r = q;
+                c0 = (int64_t)(b32 - q * (uint32_t)bpr) * B;
+            } else {
+                r = blk / bpr;
+                c0 = (blk - r * bpr) * B;
+            }
+        }
+        float v[B];
+        uint32_t ret = 0u;
+        {
+            float x[B];
+            if (valid)
+                load_block<T, B>((const char *)a.x + blk * B * (int64_t)sizeof(T), x);
+            else
+#pragma unroll
+                for (int i = 0; i < B; ++i)
+                    x[i] = 0.0f;
+            const uint32_t word = valid ? __ldg(a.bitmap + (c0 >> 5)) : 0u;
+            ret = (B == 32) ? word : ((word >> (c0 & 31)) & 0xFFFFu);
 #pragma unroll
             for (int i = 0; i < B; ++i)
-                x[i] = 0.0f;
-        const uint32_t word = valid ? __ldg(a.bitmap + (c0 >> 5)) : 0u;
-        const uint32_t ret = (B == 32) ? word : ((word >> (c0 & 31)) & 0xFFFFu);
-#pragma unroll
-        for (int i = 0; i < B; ++i)
-            v[i] = ((ret >> i) & 1u) ? 0.0f : x[i];
+                v[i] = ((ret >> i) & 1u) ? 0.0f : x[i];
+        }
         float am = 0.0f;
 #pragma unroll
         for (int i = 0; i < B; ++i)
@@ -273,66 +313,103 @@ __global__ void __launch_bounds__(kOutThreads) outlier_row_kernel(OutlierArgs a)
         const Scale sc = block_scale<FMT>(am, s_o, inv6b, &tab);
         uint32_t q[B / 8];
         encode_block<B, RND>(v, sc, key, (uint64_t)blk * B, 0u, a.offset, q);
-        if (!valid)
-            continue;
-        if (a.codes) {
-            if (B == 16)
-                *reinterpret_cast<uint2 *>(a.codes + blk * 8) = make_uint2(q[0], q[1]);
-            else
-                *reinterpret_cast<uint4 *>(a.codes + blk * 16) =
-                    make_uint4(q[0], q[1], q[2], q[3]);
-            a.scales[blk] = (uint8_t)sc.code;
-            if (FMT == NV2L && (lane & 7) == 0)
-                a.tscale[blk >> 3] = s_o;
-        }
-        float xh[B];
-#pragma unroll
-        for (int w = 0; w < B / 8; ++w) {
-            e2m1_decode8(q[w], xh + 8 * w);
-#pragma unroll
-            for (int i = 0; i < 8; ++i)
-                xh[8 * w + i] = __fmul_rn(xh[8 * w + i], sc.s_eff);
-        }
         uint32_t mask = block_mask<B>(v, sc.lim);
-        // retained elements: FP8 E4M3 with the channel's static scale (an
-        // unrolled predicated loop keeps x and xh in registers)
-        if (ret) {
-            const int jb = pre[c0 >> 5] + __popc(word & ((1u << (c0 & 31)) - 1u));
-#pragma unroll
-            for (int i = 0; i < B; ++i) {
-                if (!((ret >> i) & 1u))
-                    continue;
-                const int j = jb + __popc(ret & ((1u << i) - 1u));
-                if (j >= a.k)  // more bits set than k: outside the contract, stay in bounds
-                    continue;
-                const float s = __ldg(a.fp8_scale + j);
-                const float rcp = (s == 0.0f) ? 0.0f : __frcp_rn(s);
-                const float y = __fmul_rn(x[i], rcp);
-                const uint32_t code = e4m3_rn_sat(fabsf(y)) | ((__float_as_uint(y) >> 24) & 0x80u);
-                if (a.fp8)
-                    a.fp8[r * a.k + j] = (uint8_t)code;
-                const float m = __fmul_rn(e4m3_value(code & 0x7Fu), s);
-                xh[i] = (code & 0x80u) ? -m : m;
-                const bool in = fabsf(x[i]) <= __fmul_rn(448.0f, s);
-                mask = in ? (mask | (1u << i)) : (mask & ~(1u << i));
+        if (valid) {
+            if (a.codes) {
+                if (B == 16)
+                    *reinterpret_cast<uint2 *>(a.codes + blk * 8) = make_uint2(q[0], q[1]);
+                else
+                    *reinterpret_cast<uint4 *>(a.codes + blk * 16) =
+                        make_uint4(q[0], q[1], q[2], q[3]);
+                a.scales[blk] = (uint8_t)sc.code;
+                if (FMT == NV2L && (lane & 7) == 0)
+                    a.tscale[blk >> 3] = s_o;
             }
-        }
-        if (a.xhat) {
+            if (a.xhat) {
 #pragma unroll
-            for (int w = 0; w < B / 8; ++w) {
-                const float *h = xh + 8 * w;
-                if (a.xhat_bf16)
-                    *reinterpret_cast<uint4 *>((char *)a.xhat + (blk * B + w * 8) * 2) =
-                        make_uint4(bf16x2_rn(h[0], h[1]), bf16x2_rn(h[2], h[3]),
-                                   bf16x2_rn(h[4], h[5]), bf16x2_rn(h[6], h[7]));
-                else {
-                    float4 *dst = reinterpret_cast<float4 *>((char *)a.xhat + (blk * B + w * 8) * 4);
-                    dst[0] = make_float4(h[0], h[1], h[2], h[3]);
-                    dst[1] = make_float4(h[4], h[5], h[6], h[7]);
+                for (int w = 0; w < B / 8; ++w) {
+                    float h[8];
+                    e2m1_decode8(q[w], h);
+#pragma unroll
+                    for (int i = 0; i < 8; ++i)
+                        h[i] = __fmul_rn(h[i], sc.s_eff);
+                    if (a.xhat_bf16)
+                        *reinterpret_cast<uint4 *>((char *)a.xhat + (blk * B + w * 8) * 2) =
+                            make_uint4(bf16x2_rn(h[0], h[1]), bf16x2_rn(h[2], h[3]),
+                                       bf16x2_rn(h[4], h[5]), bf16x2_rn(h[6], h[7]));
+                    else {
+                        float4 *dst =
+                            reinterpret_cast<float4 *>((char *)a.xhat + (blk * B + w * 8) * 4);
+                        dst[0] = make_float4(h[0], h[1], h[2], h[3]);
+                        dst[1] = make_float4(h[4], h[5], h[6], h[7]);
+                    }
                 }
             }
         }
-        if (a.mask) {
+        // ---- the warp's kept elements, one per lane
+        const uint32_t cnt = valid ? (uint32_t)__popc(ret) : 0u;
+        uint32_t incl = cnt;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const uint32_t t = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+            if (lane >= o)
+                incl += t;
+        }
+        const uint32_t total = __shfl_sync(0xFFFFFFFFu, incl, 31);
+        if (total) {  // warp-uniform
+            mstage[threadIdx.x] = mask;
+            __syncwarp();  // also orders the owners' xhat stores before the patches
+            for (uint32_t t0 = 0; t0 < total; t0 += 32) {
+                const uint32_t t = t0 + (uint32_t)lane;
+                int pos = 0;  // the first lane whose inclusive count exceeds t
+#pragma unroll
+                for (int step = 16; step >= 1; step >>= 1) {
+                    const uint32_t cv = __shfl_sync(0xFFFFFFFFu, incl, pos + step - 1);
+                    if (cv <= t)
+                        pos += step;
+                }
+                const uint32_t ret_o = __shfl_sync(0xFFFFFFFFu, ret, pos);
+                const uint32_t ex_o = __shfl_sync(0xFFFFFFFFu, incl - cnt, pos);
+                const int64_t r_o = __shfl_sync(0xFFFFFFFFu, r, pos);
+                const int64_t c0_o = __shfl_sync(0xFFFFFFFFu, c0, pos);
+                if (t >= total)
+                    continue;
+                uint32_t rest = ret_o;  // drop the owner's first t - ex_o kept positions
+                for (uint32_t n = t - ex_o; n > 0; --n)
+                    rest &= rest - 1u;
+                const int i = __ffs(rest) - 1;
+                const int64_t c = c0_o + i;
+                const uint32_t wd = __ldg(a.bitmap + (c >> 5));
+                const int j = pre[c >> 5] + __popc(wd & ((1u << (c & 31)) - 1u));
+                if (j >= a.k)  // more bits set than k: outside the contract, stay in bounds
+                    continue;
+                const int64_t e = r_o * cols + c;
+                const float xv = ld_scalar<T>(a.x, e);
+                const float sj = __ldg(a.fp8_scale + j);
+                const float rcp = (sj == 0.0f) ? 0.0f : __frcp_rn(sj);
+                const float y = __fmul_rn(xv, rcp);
+                const uint32_t code = e4m3_rn_sat(fabsf(y)) | ((__float_as_uint(y) >> 24) & 0x80u);
+                if (a.fp8)
+                    a.fp8[r_o * a.k + j] = (uint8_t)code;
+                if (a.xhat) {
+                    const float m = __fmul_rn(e4m3_value(code & 0x7Fu), sj);
+                    const float h = (code & 0x80u) ? -m : m;
+                    if (a.xhat_bf16)
+                        reinterpret_cast<unsigned short *>(a.xhat)[e] =
+                            (unsigned short)(bf16x2_rn(h, 0.0f) & 0xFFFFu);
+                    else
+                        reinterpret_cast<float *>(a.xhat)[e] = h;
+                }
+                const uint32_t bit = 1u << i;
+                if (fabsf(xv) <= __fmul_rn(448.0f, sj))
+                    atomicOr(&mstage[wbase + (int)pos], bit);
+                else
+                    atomicAnd(&mstage[wbase + (int)pos], ~bit);
+            }
+            __syncwarp();
+            mask = mstage[threadIdx.x];
+        }
+        if (valid && a.mask) {
             if (B == 16)
                 reinterpret_cast<uint16_t *>(a.mask)[blk] = (uint16_t)mask;
             else

@@ -25,22 +25,33 @@
 
 namespace fqk {
 
-constexpr int kKlThreads = 512;
-constexpr int kKlWarps = kKlThreads / 32;
 constexpr int kKlMaxCluster = 8;
 constexpr size_t kKlSmemTwoPerSm = 110 * 1024;  // two CTAs per SM
 constexpr size_t kKlSmemOnePerSm = 220 * 1024;  // one CTA per SM
 
-bool qad_plan(int64_t vocab, int esz, int *csize, int64_t *chunk, size_t *smem)
+// Preference (measured on the 201088-logit rows): one row buffer and two
+// 512-thread CTAs per SM, so that one CTA's sweeps overlap the other's copies;
+// else two row buffers per 1024-thread CTA, one CTA per SM (the next row
+// loads during the current one); else one buffer, one CTA per SM.  Within
+// each, the smallest cluster whose chunks fit.
+bool qad_plan(int64_t vocab, int esz, QadPlan *p)
 {
-    for (size_t cap : {kKlSmemTwoPerSm, kKlSmemOnePerSm}) {
+    struct Opt {
+        int nbuf, threads;
+        size_t cap;
+    };
+    const Opt opts[3] = {{1, 512, kKlSmemTwoPerSm}, {2, 1024, kKlSmemOnePerSm},
+                         {1, 1024, kKlSmemOnePerSm}};
+    for (const Opt &o : opts) {
         for (int c = 1; c <= kKlMaxCluster; c *= 2) {
             const int64_t L = ((vocab + c - 1) / c + 7) / 8 * 8;
-            const size_t b = 2 * (size_t)L * (size_t)esz;
-            if (b <= cap) {
-                *csize = c;
-                *chunk = L;
-                *smem = b;
+            const size_t b = (size_t)o.nbuf * 2 * (size_t)L * (size_t)esz;
+            if (b <= o.cap) {
+                p->csize = c;
+                p->chunk = L;
+                p->smem = b;
+                p->nbuf = o.nbuf;
+                p->threads = o.threads;
                 return true;
             }
         }
@@ -58,6 +69,59 @@ __device__ __forceinline__ void lds8(const T *base, int g, float *v)
     for (int k = 0; k < 8 / E; ++k)
         unpack16<T>(p[k], v + k * E);
 }
+
+// 2^x on the special-function unit (flushes results below 2^-126 to zero).
+__device__ __forceinline__ float ex2(float x)
+{
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// Running maxima of a chunk of teacher and student logits.  BF16 pairs are
+// compared packed (the maximum of BF16 values is one of them, exactly).
+template <typename T, int NT>
+struct ChunkMax {
+    static __device__ __forceinline__ float2 run(const T *bt, const T *bs, int ng)
+    {
+        float mt = -INFINITY, ms = -INFINITY;
+        for (int g = threadIdx.x; g < ng; g += NT) {
+            float v[8], w[8];
+            lds8<T>(bt, g, v);
+            lds8<T>(bs, g, w);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                mt = fmaxf(mt, v[i]);
+                ms = fmaxf(ms, w[i]);
+            }
+        }
+        return make_float2(mt, ms);
+    }
+};
+
+template <int NT>
+struct ChunkMax<__nv_bfloat16, NT> {
+    static __device__ __forceinline__ float2 run(const __nv_bfloat16 *bt,
+                                                 const __nv_bfloat16 *bs, int ng)
+    {
+        const __nv_bfloat162 ninf = __halves2bfloat162(__ushort_as_bfloat16(0xFF80u),
+                                                       __ushort_as_bfloat16(0xFF80u));
+        __nv_bfloat162 mt = ninf, ms = ninf;
+        for (int g = threadIdx.x; g < ng; g += NT) {
+            const uint4 u = reinterpret_cast<const uint4 *>(bt)[g];
+            const uint4 w = reinterpret_cast<const uint4 *>(bs)[g];
+            const __nv_bfloat162 *pu = reinterpret_cast<const __nv_bfloat162 *>(&u);
+            const __nv_bfloat162 *pw = reinterpret_cast<const __nv_bfloat162 *>(&w);
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                mt = __hmax2(mt, pu[k]);
+                ms = __hmax2(ms, pw[k]);
+            }
+        }
+        return make_float2(fmaxf(__low2float(mt), __high2float(mt)),
+                           fmaxf(__low2float(ms), __high2float(ms)));
+    }
+};
 
 __device__ __forceinline__ float warp_sum(float v)
 {
@@ -78,6 +142,7 @@ __device__ __forceinline__ float warp_max(float v)
 // CTA-wide reductions of two values; every thread gets the results.  The
 // order of the additions is fixed (a butterfly in each warp, then the warps
 // in index order), so the sums are reproducible.
+template <int NW>
 __device__ __forceinline__ float2 cta_max2(float x, float y, float2 *red)
 {
     x = warp_max(x);
@@ -87,12 +152,13 @@ __device__ __forceinline__ float2 cta_max2(float x, float y, float2 *red)
     __syncthreads();
     float2 r = red[0];
 #pragma unroll
-    for (int w = 1; w < kKlWarps; ++w)
+    for (int w = 1; w < NW; ++w)
         r = make_float2(fmaxf(r.x, red[w].x), fmaxf(r.y, red[w].y));
     __syncthreads();
     return r;
 }
 
+template <int NW>
 __device__ __forceinline__ float2 cta_sum2(float x, float y, float2 *red)
 {
     x = warp_sum(x);
@@ -102,26 +168,40 @@ __device__ __forceinline__ float2 cta_sum2(float x, float y, float2 *red)
     __syncthreads();
     float2 r = red[0];
 #pragma unroll
-    for (int w = 1; w < kKlWarps; ++w)
+    for (int w = 1; w < NW; ++w)
         r = make_float2(r.x + red[w].x, r.y + red[w].y);
     __syncthreads();
     return r;
 }
 
-template <typename T>
-__global__ void __launch_bounds__(kKlThreads) qad_kl_kernel(const KlArgs a)
+// Cluster barrier after this CTA's threads 0..C-1 pushed their payload into
+// other CTAs' shared memory: those threads fence (release); every thread
+// arrives relaxed and waits with acquire semantics.
+__device__ __forceinline__ void cluster_sync_pushed()
 {
+    if (threadIdx.x < kKlMaxCluster)
+        asm volatile("fence.acq_rel.cluster;" ::: "memory");
+    asm volatile("barrier.cluster.arrive.relaxed.aligned;\n\t"
+                 "barrier.cluster.wait.acquire.aligned;" ::
+                     : "memory");
+}
+
+template <typename T, int NT>
+__global__ void __launch_bounds__(NT, 1024 / NT) qad_kl_kernel(const KlArgs a)
+{
+    constexpr int NW = NT / 32;
     extern __shared__ __align__(128) unsigned char smem[];
-    T *bt = reinterpret_cast<T *>(smem);
-    T *bs = bt + a.chunk;
-    __shared__ uint64_t bar;
-    __shared__ float4 slot1;   // this CTA's (M_t, S_t, M_s, S_s), base 2
-    __shared__ float4 slot2;   // this CTA's KL partial (x)
+    __shared__ uint64_t bar[2];
+    // per row parity, filled by every CTA of the cluster (remote stores before
+    // the row's cluster barrier): each rank's (M_t, S_t, M_s, S_s) in base 2,
+    // and (rank 0 only) each rank's KL partial
+    __shared__ float4 part1[2][kKlMaxCluster];
+    __shared__ float part2[2][kKlMaxCluster];
     __shared__ float4 comb;    // the row's maxima and log2 sums (G_t, G_s, log2 S_t, log2 S_s)
-    __shared__ float2 red[kKlWarps];
+    __shared__ float2 red[NW];
 
     const uint32_t rank = cluster_rank();
-    const int C = a.csize;
+    const int C = a.csize, nbuf = a.nbuf;
     const int64_t c0 = (int64_t)rank * a.chunk;
     int64_t len = a.vocab - c0;
     len = len < 0 ? 0 : (len > a.chunk ? a.chunk : len);
@@ -129,29 +209,38 @@ __global__ void __launch_bounds__(kKlThreads) qad_kl_kernel(const KlArgs a)
     const uint32_t bytes = (uint32_t)(len * (int64_t)sizeof(T));
     const int64_t row0 = cluster_id_x(), rstep = num_clusters_x();
     const float k2 = a.k2, gk = a.gk;
+    // buffer b: the teacher chunk, then the student chunk
+    auto buf_t = [&](int b) { return reinterpret_cast<T *>(smem) + (size_t)b * 2 * a.chunk; };
 
     if (threadIdx.x == 0) {
-        mbar_init(&bar, 1);
+        mbar_init(&bar[0], 1);
+        mbar_init(&bar[1], 1);
         mbar_init_fence();
     }
     __syncthreads();
-    auto issue = [&](int64_t row) {
-        mbar_arrive_expect_tx(&bar, 2 * bytes);
+    auto issue = [&](int64_t row, int b) {
+        mbar_arrive_expect_tx(&bar[b], 2 * bytes);
         if (bytes) {
             const int64_t off = (row * a.vocab + c0) * (int64_t)sizeof(T);
-            bulk_g2s(bt, (const char *)a.zt + off, bytes, &bar);
-            bulk_g2s(bs, (const char *)a.zs + off, bytes, &bar);
+            bulk_g2s(buf_t(b), (const char *)a.zt + off, bytes, &bar[b]);
+            bulk_g2s(buf_t(b) + a.chunk, (const char *)a.zs + off, bytes, &bar[b]);
         }
     };
-    if (threadIdx.x == 0 && row0 < a.rows)
-        issue(row0);
+    if (threadIdx.x == 0) {
+        for (int b = 0; b < nbuf; ++b)
+            if (row0 + b * rstep < a.rows)
+                issue(row0 + b * rstep, b);
+    }
 
     bool dead = false;  // a copy did not arrive in time: stop loading, keep the barriers
-    uint32_t parity = 0;
-    for (int64_t row = row0; row < a.rows; row += rstep) {
+    int it = 0;
+    for (int64_t row = row0; row < a.rows; row += rstep, ++it) {
+        const int b = it % nbuf;
+        const T *bt = buf_t(b);
+        const T *bs = bt + a.chunk;
         if (!dead) {
-            const bool late = !mbar_wait(&bar, parity);
-            parity ^= 1u;
+            // one thread waits for the copies; the others sleep in the barrier
+            const bool late = threadIdx.x == 0 && !mbar_wait(&bar[b], (uint32_t)(it / nbuf) & 1u);
             if (__syncthreads_or(late)) {
                 dead = true;
                 if (threadIdx.x == 0 && a.err)
@@ -159,57 +248,52 @@ __global__ void __launch_bounds__(kKlThreads) qad_kl_kernel(const KlArgs a)
             }
         }
         // sweep 1: maxima of the raw logits (scaling by k2 > 0 keeps the order)
-        float mt = -INFINITY, ms = -INFINITY;
-        for (int g = threadIdx.x; g < ng; g += kKlThreads) {
-            float v[8], w[8];
-            lds8<T>(bt, g, v);
-            lds8<T>(bs, g, w);
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                mt = fmaxf(mt, v[i]);
-                ms = fmaxf(ms, w[i]);
-            }
-        }
-        const float2 m = cta_max2(mt, ms, red);
+        const float2 lm = ChunkMax<T, NT>::run(bt, bs, ng);
+        const float2 m = cta_max2<NW>(lm.x, lm.y, red);
         const float m2t = m.x * k2, m2s = m.y * k2;
         // sweep 2: sums of 2^(a - M) under this CTA's maxima
         float st = 0.0f, ss = 0.0f;
-        for (int g = threadIdx.x; g < ng; g += kKlThreads) {
+        for (int g = threadIdx.x; g < ng; g += NT) {
             float v[8], w[8];
             lds8<T>(bt, g, v);
             lds8<T>(bs, g, w);
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
-                st += exp2f(fmaf(v[i], k2, -m2t));
-                ss += exp2f(fmaf(w[i], k2, -m2s));
+                st += ex2(fmaf(v[i], k2, -m2t));
+                ss += ex2(fmaf(w[i], k2, -m2s));
             }
         }
-        const float2 s = cta_sum2(st, ss, red);
-        if (threadIdx.x == 0)
-            slot1 = make_float4(m2t, s.x, m2s, s.y);
-        cluster_sync();
-        if (threadIdx.x == 0) {
-            // combine the cluster's partials in rank order (identical in every CTA)
-            float4 part[kKlMaxCluster];
-            float gt = -INFINITY, gs = -INFINITY;
-            for (int r = 0; r < C; ++r) {
-                part[r] = dsmem_ld_f4(&slot1, (uint32_t)r);
-                gt = fmaxf(gt, part[r].x);
-                gs = fmaxf(gs, part[r].z);
+        const float2 s = cta_sum2<NW>(st, ss, red);
+        // push this CTA's partials into every CTA of the cluster (lane r -> rank r)
+        if (threadIdx.x < C)
+            dsmem_st_f4(&part1[it & 1][rank], (uint32_t)threadIdx.x,
+                        make_float4(m2t, s.x, m2s, s.y));
+        // one cluster barrier per row: it publishes this row's partials and
+        // the previous row's KL partials (stored at the end of that row)
+        cluster_sync_pushed();
+        if (threadIdx.x < 32) {
+            const int lane = threadIdx.x;
+            if (rank == 0 && it > 0) {
+                const float tot = warp_sum(lane < C ? part2[(it - 1) & 1][lane] : 0.0f);
+                if (lane == 0)
+                    a.loss_rows[row - rstep] = tot * 0.693147180559945309f;
             }
-            float sum_t = 0.0f, sum_s = 0.0f;
-            for (int r = 0; r < C; ++r) {
-                sum_t += part[r].y * exp2f(part[r].x - gt);
-                sum_s += part[r].w * exp2f(part[r].z - gs);
-            }
-            comb = make_float4(gt, gs, log2f(sum_t), log2f(sum_s));
+            // combine the cluster's partials (the same butterfly in every CTA)
+            float4 pr = make_float4(-INFINITY, 0.0f, -INFINITY, 0.0f);
+            if (lane < C)
+                pr = part1[it & 1][lane];
+            const float gt = warp_max(pr.x), gs = warp_max(pr.z);
+            const float sum_t = warp_sum(lane < C ? pr.y * ex2(pr.x - gt) : 0.0f);
+            const float sum_s = warp_sum(lane < C ? pr.w * ex2(pr.z - gs) : 0.0f);
+            if (lane == 0)
+                comb = make_float4(gt, gs, log2f(sum_t), log2f(sum_s));
         }
         __syncthreads();
         const float gt = comb.x, gs = comb.y, l2t = comb.z, l2s = comb.w;
         // sweep 3: p, q, the KL terms and the gradient
         float kl = 0.0f;
         char *dzrow = a.dz ? (char *)a.dz + (row * a.vocab + c0) * (a.dz_bf16 ? 2 : 4) : nullptr;
-        for (int g = threadIdx.x; g < ng; g += kKlThreads) {
+        for (int g = threadIdx.x; g < ng; g += NT) {
             float v[8], w[8], o[8];
             lds8<T>(bt, g, v);
             lds8<T>(bs, g, w);
@@ -219,10 +303,10 @@ __global__ void __launch_bounds__(kKlThreads) qad_kl_kernel(const KlArgs a)
                 // for every token that matters, whatever the logits' offset
                 const float lp = fmaf(v[i], k2, -gt) - l2t;
                 const float lq = fmaf(w[i], k2, -gs) - l2s;
-                const float p = exp2f(lp);
+                const float p = ex2(lp);
                 kl = fmaf(p, lp - lq, kl);
                 if (dzrow)
-                    o[i] = gk * (exp2f(lq) - p);
+                    o[i] = gk * (ex2(lq) - p);
             }
             if (dzrow) {
                 if (a.dz_bf16) {
@@ -236,24 +320,24 @@ __global__ void __launch_bounds__(kKlThreads) qad_kl_kernel(const KlArgs a)
                 }
             }
         }
-        const float2 k = cta_sum2(kl, 0.0f, red);  // also: every thread is done with the chunk
+        const float2 k = cta_sum2<NW>(kl, 0.0f, red);  // also: every thread is done with the chunk
         if (threadIdx.x == 0) {
-            slot2 = make_float4(k.x, 0.0f, 0.0f, 0.0f);
-            const int64_t next = row + rstep;
+            dsmem_st_f32(&part2[it & 1][rank], 0u, k.x);  // to rank 0
+            const int64_t next = row + (int64_t)nbuf * rstep;  // the row this buffer takes next
             if (!dead && next < a.rows) {
                 fence_proxy_async_smem();
-                issue(next);
+                issue(next, b);
             }
         }
-        cluster_sync();
-        if (rank == 0 && threadIdx.x == 0) {
-            float tot = 0.0f;
-            for (int r = 0; r < C; ++r)
-                tot += dsmem_ld_f4(&slot2, (uint32_t)r).x;
-            a.loss_rows[row] = tot * 0.693147180559945309f;
-        }
     }
-    cluster_sync();  // keep this CTA's slots alive until rank 0 has read them
+    // the last row's KL partials
+    cluster_sync_pushed();
+    if (rank == 0 && it > 0 && threadIdx.x < 32) {
+        const int lane = threadIdx.x;
+        const float tot = warp_sum(lane < C ? part2[(it - 1) & 1][lane] : 0.0f);
+        if (lane == 0)
+            a.loss_rows[row0 + (int64_t)(it - 1) * rstep] = tot * 0.693147180559945309f;
+    }
 }
 
 // Mean of the per-row losses in double precision, in a fixed order.
@@ -281,11 +365,15 @@ __global__ void __launch_bounds__(kMeanThreads) qad_mean_kernel(const float *__r
     }
 }
 
-template <typename T>
-static cudaError_t qad_go(KlArgs a, size_t smem, cudaStream_t s)
+template <typename T, int NT>
+static cudaError_t qad_go(const KlArgs &a, size_t smem, cudaStream_t s)
 {
-    cudaError_t e = cudaFuncSetAttribute(qad_kl_kernel<T>,
+    cudaError_t e = cudaFuncSetAttribute(qad_kl_kernel<T, NT>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(qad_kl_kernel<T, NT>,
+                                 cudaFuncAttributePreferredSharedMemoryCarveout,
+                                 (int)cudaSharedmemCarveoutMaxShared);
     if (e != cudaSuccess)
         return e;
     cudaLaunchConfig_t cfg = {};
@@ -294,7 +382,7 @@ static cudaError_t qad_go(KlArgs a, size_t smem, cudaStream_t s)
     attr[0].val.clusterDim.x = (unsigned)a.csize;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
-    cfg.blockDim = dim3(kKlThreads);
+    cfg.blockDim = dim3(NT);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
     cfg.attrs = attr;
@@ -302,19 +390,27 @@ static cudaError_t qad_go(KlArgs a, size_t smem, cudaStream_t s)
     // as many clusters as fit on the GPU at once (persistent over rows)
     cfg.gridDim = dim3((unsigned)(a.csize * 1024));
     int fit = 0;
-    if (cudaOccupancyMaxActiveClusters(&fit, qad_kl_kernel<T>, &cfg) != cudaSuccess || fit < 1)
+    if (cudaOccupancyMaxActiveClusters(&fit, qad_kl_kernel<T, NT>, &cfg) != cudaSuccess || fit < 1)
         fit = sm_count() / a.csize > 0 ? sm_count() / a.csize : 1;
     (void)cudaGetLastError();
     const int64_t ncl = a.rows < fit ? a.rows : fit;
     cfg.gridDim = dim3((unsigned)(a.csize * ncl));
-    return cudaLaunchKernelEx(&cfg, qad_kl_kernel<T>, a);
+    return cudaLaunchKernelEx(&cfg, qad_kl_kernel<T, NT>, a);
 }
 
-cudaError_t launch_qad_kl(const KlArgs &a, int bf16, size_t smem, float *loss_mean,
+cudaError_t launch_qad_kl(const KlArgs &a0, int bf16, const QadPlan &p, float *loss_mean,
                           cudaStream_t s)
 {
+    KlArgs a = a0;
+    a.csize = p.csize;
+    a.chunk = p.chunk;
+    a.nbuf = p.nbuf;
     if (a.rows > 0) {
-        cudaError_t e = bf16 ? qad_go<__nv_bfloat16>(a, smem, s) : qad_go<float>(a, smem, s);
+        cudaError_t e;
+        if (p.threads == 1024)
+            e = bf16 ? qad_go<__nv_bfloat16, 1024>(a, p.smem, s) : qad_go<float, 1024>(a, p.smem, s);
+        else
+            e = bf16 ? qad_go<__nv_bfloat16, 512>(a, p.smem, s) : qad_go<float, 512>(a, p.smem, s);
         if (e != cudaSuccess)
             return e;
     }

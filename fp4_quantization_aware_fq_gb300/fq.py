@@ -131,10 +131,13 @@ def lib():
                                            vp, i32, vp, vp, sz, vp]
         L.fq_qad_kl.argtypes = [vp, vp, i32, i64, i64, ctypes.c_float, ctypes.c_float, vp, vp,
                                 vp, i32, vp, vp]
+        L.fq_gemm.argtypes = [P(Config), P(_QT), P(_QT), i64, i64, i64, vp, i32, vp, sz, vp, vp]
+        L.fq_gemm_workspace_size.argtypes = [i64, i64, i64]
+        L.fq_gemm_workspace_size.restype = sz
         for name in ("fq_amax", "fq_quantize", "fq_fakequant_ste", "fq_dequantize",
                      "fq_ste_backward", "fq_osci_update", "fq_osci_reset",
                      "fq_osci_update_noalloc", "fq_osci_update_reset", "fq_channel_amax",
-                     "fq_select_channels", "fq_quantize_outliers", "fq_qad_kl"):
+                     "fq_select_channels", "fq_quantize_outliers", "fq_qad_kl", "fq_gemm"):
             getattr(L, name).restype = ctypes.c_int
         L.fq_status_string.argtypes = [ctypes.c_int]
         L.fq_status_string.restype = ctypes.c_char_p
@@ -479,3 +482,31 @@ def fq_qad_kl(teacher: torch.Tensor, student: torch.Tensor, temperature: float =
                          _stream(stream))
     _check(st, "fq_qad_kl")
     return loss_rows, loss_mean, dz, err
+
+
+# --------------------------------------------------------------------------
+# block-scaled FP4 GEMM
+# --------------------------------------------------------------------------
+def fq_gemm_workspace_size(m: int, n: int, k: int) -> int:
+    return lib().fq_gemm_workspace_size(m, n, k)
+
+
+def fq_gemm(a: QTensor, b: QTensor, m: int, n: int, k: int, cfg: Optional[Config] = None,
+            c: Optional[torch.Tensor] = None, c_dtype=torch.float32,
+            ws: Optional[torch.Tensor] = None, err: Optional[torch.Tensor] = None, stream=None):
+    """C[m, n] = deq(A) deq(B)^T for row-wise NVFP4 A [m, k] and B [n, k] on
+    the tensor cores.  Returns (C, err); err is a device int32 that is
+    non-zero if a pipeline wait timed out (read it after synchronising)."""
+    cfg = cfg or Config(NVFP4)
+    dev = a.codes.device
+    if c is None:
+        c = torch.empty((m, n), dtype=c_dtype, device=dev)
+    if ws is None:
+        ws = torch.empty(max(fq_gemm_workspace_size(m, n, k), 16), dtype=torch.uint8, device=dev)
+    if err is None:
+        err = torch.zeros(1, dtype=torch.int32, device=dev)
+    st = lib().fq_gemm(ctypes.byref(cfg), ctypes.byref(a._c()), ctypes.byref(b._c()), m, n, k,
+                       c.data_ptr(), _dtype_code(c), ws.data_ptr(), ws.numel(), err.data_ptr(),
+                       _stream(stream))
+    _check(st, "fq_gemm")
+    return c, err

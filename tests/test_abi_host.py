@@ -193,3 +193,28 @@ def test_qad_kl_argument_errors(L):
     assert k(dz=FAKE + 4) == 3                   # misaligned gradient
     assert k(vocab=460000) == 5                  # a BF16 row no longer fits one cluster
     assert k(dtype=fq.F32, vocab=230000) == 5    # nor an FP32 one
+
+
+def test_gemm_argument_errors(L):
+    def g(cfg=fq.Config(fq.NVFP4), a=None, b=None, m=128, n=128, k=256, c=FAKE, ct=fq.F32,
+          ws=FAKE, wsb=1 << 20, err=FAKE):
+        qa = a if a is not None else _qt()
+        qb = b if b is not None else _qt()
+        return L.fq_gemm(ctypes.byref(cfg), ctypes.byref(qa), ctypes.byref(qb), m, n, k, c, ct,
+                         ws, wsb, err, None)
+    assert fq.fq_gemm_workspace_size(256, 128, 512) == (256 + 128) * 512 // 16
+    assert g(cfg=fq.Config(9)) == 1                       # unknown format
+    assert g(c=0) == 1                                    # NULL output
+    assert g(ct=5) == 1                                   # unknown output dtype
+    assert g(cfg=fq.Config(fq.MXFP4)) == 5                # NVFP4 only
+    assert g(cfg=fq.Config(fq.NVFP4_2LEVEL)) == 5
+    assert g(a=_qt(tscale=0)) == 1                        # NVFP4 needs the tensor scale
+    assert g(b=_qt(codes=FAKE + 4)) == 3                  # misaligned codes
+    assert g(m=100) == 2                                  # m % 128
+    assert g(n=64) == 2                                   # n % 128
+    assert g(k=128) == 2                                  # k % 256
+    assert g(c=FAKE + 8) == 3                             # misaligned output
+    assert g(ws=0) == 4                                   # no workspace
+    assert g(wsb=100) == 4                                # workspace too small
+    assert g(ws=FAKE + 8) == 3                            # misaligned workspace
+    assert g(m=0) == 0                                    # empty: nothing runs

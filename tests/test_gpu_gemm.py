@@ -86,3 +86,33 @@ def test_gemm_bf16_output_and_scale():
 
 def test_gemm_long_k():
     _check(128, 256, 8192, seed=4)
+
+
+def test_gemm_persistent_many_tiles():
+    """More tiles than twice the SM count: every CTA walks several tiles and
+    reuses both TMEM accumulators."""
+    _check(2560, 2048, 512, seed=5)
+
+
+@pytest.mark.slow
+def test_full_gemm_8192_sampled_rows():
+    """The benchmarked 8192^3 product: 48 rows of C spread over all row
+    blocks against the oracle (all columns)."""
+    m = n = k = 8192
+    a = W.normal((m, k), 1.0, seed=20, dtype=torch.bfloat16, device=DEV)
+    b = W.normal((n, k), 0.02, seed=21, dtype=torch.bfloat16, device=DEV)
+    cfg = fq.Config(fq.NVFP4)
+    qa, _ = fq.fq_quantize(a, cfg)
+    qb, _ = fq.fq_quantize(b, cfg)
+    c, err = fq.fq_gemm(qa, qb, m, n, k, c_dtype=torch.bfloat16)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    rows = np.linspace(0, m - 1, 48).astype(np.int64)
+    rt = torch.as_tensor(rows, device=DEV)
+    qsub = {"codes": npy(qa.codes[rt]), "scales": npy(qa.scales[rt]), "tscale": npy(qa.tscale)[:1]}
+    ref = oracle.gemm(qsub, _qdict(qb), len(rows), n, k)
+    da = oracle.dequantize(qsub, len(rows), k).astype(np.float64)
+    db = oracle.dequantize(_qdict(qb), n, k).astype(np.float64)
+    bound = 2.0 ** -16 * (np.abs(da) @ np.abs(db).T) + 2.0 ** -8 * np.abs(ref)
+    got = npy(c[rt].float()).astype(np.float64)
+    assert np.all(np.abs(got - ref) <= bound)

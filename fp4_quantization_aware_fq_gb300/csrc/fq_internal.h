@@ -117,7 +117,6 @@ struct KlArgs {
     int64_t rows, vocab;
     int64_t chunk;
     int csize;
-    int nbuf;          // row buffers per CTA (2: the next row loads during this one)
     float k2;          // log2(e) / T
     float gk;          // grad_scale / T
     float *loss_rows;
@@ -163,7 +162,6 @@ struct QadPlan {
     int csize;        // CTAs per cluster (one row per cluster)
     int64_t chunk;    // logits of each tensor per CTA
     size_t smem;      // dynamic shared memory per CTA
-    int nbuf;         // row buffers per CTA
     int threads;      // threads per CTA
 };
 bool qad_plan(int64_t vocab, int esz, QadPlan *p);

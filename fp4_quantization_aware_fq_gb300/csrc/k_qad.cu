@@ -29,28 +29,24 @@ constexpr int kKlMaxCluster = 8;
 constexpr size_t kKlSmemTwoPerSm = 110 * 1024;  // two CTAs per SM
 constexpr size_t kKlSmemOnePerSm = 220 * 1024;  // one CTA per SM
 
-// Preference (measured on the 201088-logit rows): one row buffer and two
-// 512-thread CTAs per SM, so that one CTA's sweeps overlap the other's copies;
-// else two row buffers per 1024-thread CTA, one CTA per SM (the next row
-// loads during the current one); else one buffer, one CTA per SM.  Within
-// each, the smallest cluster whose chunks fit.
+// Preference: two 512-thread CTAs per SM (one CTA's sweeps overlap the
+// other's copies), else one 1024-thread CTA per SM; within each, the smallest
+// cluster whose chunks fit.
 bool qad_plan(int64_t vocab, int esz, QadPlan *p)
 {
     struct Opt {
-        int nbuf, threads;
+        int threads;
         size_t cap;
     };
-    const Opt opts[3] = {{1, 512, kKlSmemTwoPerSm}, {2, 1024, kKlSmemOnePerSm},
-                         {1, 1024, kKlSmemOnePerSm}};
+    const Opt opts[2] = {{512, kKlSmemTwoPerSm}, {1024, kKlSmemOnePerSm}};
     for (const Opt &o : opts) {
         for (int c = 1; c <= kKlMaxCluster; c *= 2) {
             const int64_t L = ((vocab + c - 1) / c + 7) / 8 * 8;
-            const size_t b = (size_t)o.nbuf * 2 * (size_t)L * (size_t)esz;
+            const size_t b = 2 * (size_t)L * (size_t)esz;
             if (b <= o.cap) {
                 p->csize = c;
                 p->chunk = L;
                 p->smem = b;
-                p->nbuf = o.nbuf;
                 p->threads = o.threads;
                 return true;
             }
@@ -82,10 +78,12 @@ __device__ __forceinline__ float ex2(float x)
 // compared packed (the maximum of BF16 values is one of them, exactly).
 template <typename T, int NT>
 struct ChunkMax {
-    static __device__ __forceinline__ float2 run(const T *bt, const T *bs, int ng)
+    // running maxima (mt, ms) continued over groups g0 .. g1 - 1
+    static __device__ __forceinline__ float2 run(const T *bt, const T *bs, int g0, int g1,
+                                                 float2 m)
     {
-        float mt = -INFINITY, ms = -INFINITY;
-        for (int g = threadIdx.x; g < ng; g += NT) {
+        float mt = m.x, ms = m.y;
+        for (int g = g0 + threadIdx.x; g < g1; g += NT) {
             float v[8], w[8];
             lds8<T>(bt, g, v);
             lds8<T>(bs, g, w);
@@ -102,12 +100,13 @@ struct ChunkMax {
 template <int NT>
 struct ChunkMax<__nv_bfloat16, NT> {
     static __device__ __forceinline__ float2 run(const __nv_bfloat16 *bt,
-                                                 const __nv_bfloat16 *bs, int ng)
+                                                 const __nv_bfloat16 *bs, int g0, int g1,
+                                                 float2 m)
     {
         const __nv_bfloat162 ninf = __halves2bfloat162(__ushort_as_bfloat16(0xFF80u),
                                                        __ushort_as_bfloat16(0xFF80u));
         __nv_bfloat162 mt = ninf, ms = ninf;
-        for (int g = threadIdx.x; g < ng; g += NT) {
+        for (int g = g0 + threadIdx.x; g < g1; g += NT) {
             const uint4 u = reinterpret_cast<const uint4 *>(bt)[g];
             const uint4 w = reinterpret_cast<const uint4 *>(bs)[g];
             const __nv_bfloat162 *pu = reinterpret_cast<const __nv_bfloat162 *>(&u);
@@ -118,8 +117,8 @@ struct ChunkMax<__nv_bfloat16, NT> {
                 ms = __hmax2(ms, pw[k]);
             }
         }
-        return make_float2(fmaxf(__low2float(mt), __high2float(mt)),
-                           fmaxf(__low2float(ms), __high2float(ms)));
+        return make_float2(fmaxf(m.x, fmaxf(__low2float(mt), __high2float(mt))),
+                           fmaxf(m.y, fmaxf(__low2float(ms), __high2float(ms))));
     }
 };
 
@@ -186,12 +185,17 @@ __device__ __forceinline__ void cluster_sync_pushed()
                      : "memory");
 }
 
+// The chunk arrives in kKlParts parts, each with its own mbarrier: the first
+// sweep starts on part 0 while the later parts are still in flight, and the
+// next row's part p is requested as soon as the last sweep has finished with
+// it, while that sweep works on the later parts.
+constexpr int kKlParts = 2;
 template <typename T, int NT>
 __global__ void __launch_bounds__(NT, 1024 / NT) qad_kl_kernel(const KlArgs a)
 {
     constexpr int NW = NT / 32;
     extern __shared__ __align__(128) unsigned char smem[];
-    __shared__ uint64_t bar[2];
+    __shared__ uint64_t bar[kKlParts];  // one per part of the chunk
     // per row parity, filled by every CTA of the cluster (remote stores before
     // the row's cluster barrier): each rank's (M_t, S_t, M_s, S_s) in base 2,
     // and (rank 0 only) each rank's KL partial
@@ -201,54 +205,59 @@ __global__ void __launch_bounds__(NT, 1024 / NT) qad_kl_kernel(const KlArgs a)
     __shared__ float2 red[NW];
 
     const uint32_t rank = cluster_rank();
-    const int C = a.csize, nbuf = a.nbuf;
+    const int C = a.csize;
     const int64_t c0 = (int64_t)rank * a.chunk;
     int64_t len = a.vocab - c0;
     len = len < 0 ? 0 : (len > a.chunk ? a.chunk : len);
-    const int ng = (int)(len / 8);
-    const uint32_t bytes = (uint32_t)(len * (int64_t)sizeof(T));
+    const int ng = (int)(len / 8);    // groups of 8 logits in this CTA's chunk
+    // part p covers groups gpart(p) .. gpart(p + 1) - 1
+    auto gpart = [&](int p) { return (int)(((int64_t)ng * p) / kKlParts); };
     const int64_t row0 = cluster_id_x(), rstep = num_clusters_x();
     const float k2 = a.k2, gk = a.gk;
-    // buffer b: the teacher chunk, then the student chunk
-    auto buf_t = [&](int b) { return reinterpret_cast<T *>(smem) + (size_t)b * 2 * a.chunk; };
+    T *bt = reinterpret_cast<T *>(smem);
+    T *bs = bt + a.chunk;
 
     if (threadIdx.x == 0) {
-        mbar_init(&bar[0], 1);
-        mbar_init(&bar[1], 1);
+        for (int p = 0; p < kKlParts; ++p)
+            mbar_init(&bar[p], 1);
         mbar_init_fence();
     }
     __syncthreads();
-    auto issue = [&](int64_t row, int b) {
-        mbar_arrive_expect_tx(&bar[b], 2 * bytes);
+    auto issue_part = [&](int64_t row, int p) {
+        const int g0 = gpart(p), g1 = gpart(p + 1);
+        const uint32_t bytes = (uint32_t)((g1 - g0) * 8 * (int)sizeof(T));
+        mbar_arrive_expect_tx(&bar[p], 2 * bytes);
         if (bytes) {
-            const int64_t off = (row * a.vocab + c0) * (int64_t)sizeof(T);
-            bulk_g2s(buf_t(b), (const char *)a.zt + off, bytes, &bar[b]);
-            bulk_g2s(buf_t(b) + a.chunk, (const char *)a.zs + off, bytes, &bar[b]);
+            const int64_t off = (row * a.vocab + c0 + 8 * (int64_t)g0) * (int64_t)sizeof(T);
+            bulk_g2s(bt + 8 * g0, (const char *)a.zt + off, bytes, &bar[p]);
+            bulk_g2s(bs + 8 * g0, (const char *)a.zs + off, bytes, &bar[p]);
         }
     };
-    if (threadIdx.x == 0) {
-        for (int b = 0; b < nbuf; ++b)
-            if (row0 + b * rstep < a.rows)
-                issue(row0 + b * rstep, b);
-    }
+    if (threadIdx.x == 0 && row0 < a.rows)
+        for (int p = 0; p < kKlParts; ++p)
+            issue_part(row0, p);
 
     bool dead = false;  // a copy did not arrive in time: stop loading, keep the barriers
+    // one thread waits for a part; the others sleep in the barrier
+    auto wait_part = [&](int p, int it) {
+        if (dead)
+            return;
+        const bool late = threadIdx.x == 0 && !mbar_wait(&bar[p], (uint32_t)it & 1u);
+        if (__syncthreads_or(late)) {
+            dead = true;
+            if (threadIdx.x == 0 && a.err)
+                atomicOr(a.err, (int)kDevErrWaitTimeout);
+        }
+    };
     int it = 0;
     for (int64_t row = row0; row < a.rows; row += rstep, ++it) {
-        const int b = it % nbuf;
-        const T *bt = buf_t(b);
-        const T *bs = bt + a.chunk;
-        if (!dead) {
-            // one thread waits for the copies; the others sleep in the barrier
-            const bool late = threadIdx.x == 0 && !mbar_wait(&bar[b], (uint32_t)(it / nbuf) & 1u);
-            if (__syncthreads_or(late)) {
-                dead = true;
-                if (threadIdx.x == 0 && a.err)
-                    atomicOr(a.err, (int)kDevErrWaitTimeout);
-            }
-        }
+        const int64_t next = row + rstep;
         // sweep 1: maxima of the raw logits (scaling by k2 > 0 keeps the order)
-        const float2 lm = ChunkMax<T, NT>::run(bt, bs, ng);
+        float2 lm = make_float2(-INFINITY, -INFINITY);
+        for (int p = 0; p < kKlParts; ++p) {
+            wait_part(p, it);
+            lm = ChunkMax<T, NT>::run(bt, bs, gpart(p), gpart(p + 1), lm);
+        }
         const float2 m = cta_max2<NW>(lm.x, lm.y, red);
         const float m2t = m.x * k2, m2s = m.y * k2;
         // sweep 2: sums of 2^(a - M) under this CTA's maxima
@@ -290,43 +299,53 @@ __global__ void __launch_bounds__(NT, 1024 / NT) qad_kl_kernel(const KlArgs a)
         }
         __syncthreads();
         const float gt = comb.x, gs = comb.y, l2t = comb.z, l2s = comb.w;
-        // sweep 3: p, q, the KL terms and the gradient
+        // sweep 3: p, q, the KL terms and the gradient, part by part
         float kl = 0.0f;
         char *dzrow = a.dz ? (char *)a.dz + (row * a.vocab + c0) * (a.dz_bf16 ? 2 : 4) : nullptr;
-        for (int g = threadIdx.x; g < ng; g += NT) {
-            float v[8], w[8], o[8];
-            lds8<T>(bt, g, v);
-            lds8<T>(bs, g, w);
+        for (int part = 0; part < kKlParts; ++part) {
+            const int g1 = gpart(part + 1);
+            for (int g = gpart(part) + threadIdx.x; g < g1; g += NT) {
+                float v[8], w[8], o[8];
+                lds8<T>(bt, g, v);
+                lds8<T>(bs, g, w);
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                // log2 p and log2 q relative to each row's own maximum: small
-                // for every token that matters, whatever the logits' offset
-                const float lp = fmaf(v[i], k2, -gt) - l2t;
-                const float lq = fmaf(w[i], k2, -gs) - l2s;
-                const float p = ex2(lp);
-                kl = fmaf(p, lp - lq, kl);
-                if (dzrow)
-                    o[i] = gk * (ex2(lq) - p);
+                for (int i = 0; i < 8; ++i) {
+                    // log2 p and log2 q relative to each row's own maximum: small
+                    // for every token that matters, whatever the logits' offset
+                    const float lp = fmaf(v[i], k2, -gt) - l2t;
+                    const float lq = fmaf(w[i], k2, -gs) - l2s;
+                    const float p = ex2(lp);
+                    kl = fmaf(p, lp - lq, kl);
+                    if (dzrow)
+                        o[i] = gk * (ex2(lq) - p);
+                }
+                if (dzrow) {
+                    if (a.dz_bf16) {
+                        *reinterpret_cast<uint4 *>(dzrow + (size_t)g * 16) =
+                            make_uint4(bf16x2_rn(o[0], o[1]), bf16x2_rn(o[2], o[3]),
+                                       bf16x2_rn(o[4], o[5]), bf16x2_rn(o[6], o[7]));
+                    } else {
+                        float4 *d = reinterpret_cast<float4 *>(dzrow + (size_t)g * 32);
+                        d[0] = make_float4(o[0], o[1], o[2], o[3]);
+                        d[1] = make_float4(o[4], o[5], o[6], o[7]);
+                    }
+                }
             }
-            if (dzrow) {
-                if (a.dz_bf16) {
-                    *reinterpret_cast<uint4 *>(dzrow + (size_t)g * 16) =
-                        make_uint4(bf16x2_rn(o[0], o[1]), bf16x2_rn(o[2], o[3]),
-                                   bf16x2_rn(o[4], o[5]), bf16x2_rn(o[6], o[7]));
-                } else {
-                    float4 *d = reinterpret_cast<float4 *>(dzrow + (size_t)g * 32);
-                    d[0] = make_float4(o[0], o[1], o[2], o[3]);
-                    d[1] = make_float4(o[4], o[5], o[6], o[7]);
+            if (part + 1 < kKlParts) {
+                // every thread is done with this part: request the next row's
+                __syncthreads();
+                if (threadIdx.x == 0 && !dead && next < a.rows) {
+                    fence_proxy_async_smem();
+                    issue_part(next, part);
                 }
             }
         }
-        const float2 k = cta_sum2<NW>(kl, 0.0f, red);  // also: every thread is done with the chunk
+        const float2 k = cta_sum2<NW>(kl, 0.0f, red);  // also: every thread is done with the last part
         if (threadIdx.x == 0) {
             dsmem_st_f32(&part2[it & 1][rank], 0u, k.x);  // to rank 0
-            const int64_t next = row + (int64_t)nbuf * rstep;  // the row this buffer takes next
             if (!dead && next < a.rows) {
                 fence_proxy_async_smem();
-                issue(next, b);
+                issue_part(next, kKlParts - 1);
             }
         }
     }
@@ -404,7 +423,6 @@ cudaError_t launch_qad_kl(const KlArgs &a0, int bf16, const QadPlan &p, float *l
     KlArgs a = a0;
     a.csize = p.csize;
     a.chunk = p.chunk;
-    a.nbuf = p.nbuf;
     if (a.rows > 0) {
         cudaError_t e;
         if (p.threads == 1024)

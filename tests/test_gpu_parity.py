@@ -200,3 +200,13 @@ def test_full_grad_2level_sr_bias():
     xd = as_oracle_input(x).astype(np.float64)
     bias = abs((npy(xhat).astype(np.float64) - xd).mean()) / np.abs(xd).mean()
     assert bias < 1e-3
+
+
+@pytest.mark.parametrize("rows", [1, 16, 256, 257])
+def test_nvfp4_row_sizes_around_the_small_workload(rows):
+    """NVFP4 row-wise fake quantization of 1 to 257 rows of 1024 (the small
+    workload is 256 x 1024), FP32 nearest-even and BF16 stochastic."""
+    x = W.nvfp4_small(shape=(rows, 1024), seed=40 + rows)
+    x[0, 3] = 37.0
+    fakequant_parity(_dev(x), fq.NVFP4, xhat_dtype=torch.float32)
+    fakequant_parity(_dev(x.to(torch.bfloat16)), fq.NVFP4, rnd=fq.SR, seed=5, offset=2)

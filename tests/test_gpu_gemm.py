@@ -116,3 +116,31 @@ def test_full_gemm_8192_sampled_rows():
     bound = 2.0 ** -16 * (np.abs(da) @ np.abs(db).T) + 2.0 ** -8 * np.abs(ref)
     got = npy(c[rt].float()).astype(np.float64)
     assert np.all(np.abs(got - ref) <= bound)
+
+
+def test_qat_linear_layer_three_gemms():
+    """The three GEMMs of a QAT linear layer Y = X W^T from the quantizers'
+    own outputs: forward Y = deq(X) deq(W)^T from the row-wise codes; the input
+    gradient dX = deq(dY) deq(W^T)^T with W^T from the column-wise pass of W;
+    the weight gradient dW = deq(dY^T) deq(X^T)^T from the column-wise passes
+    of dY and X ("Resumo Técnico: TetraJet-v2", §2A: 1x16 groups and the
+    transposed operands of the backward pass)."""
+    m, n, k = 256, 512, 768           # tokens, output features, input features
+    cfg = fq.Config(fq.NVFP4)
+    x = W.nvfp4_act(shape=(m, k), seed=30, n_outlier_cols=2).to(DEV)
+    w = W.normal((n, k), 0.02, seed=31, dtype=torch.bfloat16, device=DEV)
+    dy = W.grad_2level(shape=(m, n), seed=32).to(DEV)
+    xr, xc = fq.fq_quantize(x, cfg, orient=fq.ROWCOL)      # X [m,k] and X^T [k,m]
+    wr, wc = fq.fq_quantize(w, cfg, orient=fq.ROWCOL)      # W [n,k] and W^T [k,n]
+    dr, dc = fq.fq_quantize(dy, cfg, orient=fq.ROWCOL)     # dY [m,n] and dY^T [n,m]
+    cases = [("Y", xr, wr, m, n, k), ("dX", dr, wc, m, k, n), ("dW", dc, xc, n, k, m)]
+    for name, qa, qb, mm, nn, kk in cases:
+        c, err = fq.fq_gemm(qa, qb, mm, nn, kk)
+        torch.cuda.synchronize()
+        assert int(err.item()) == 0, name
+        ref = oracle.gemm(_qdict(qa), _qdict(qb), mm, nn, kk)
+        da = oracle.dequantize(_qdict(qa), mm, kk).astype(np.float64)
+        db = oracle.dequantize(_qdict(qb), nn, kk).astype(np.float64)
+        bound = 2.0 ** -16 * (np.abs(da) @ np.abs(db).T)
+        got = npy(c).astype(np.float64)
+        assert np.all(np.abs(got - ref) <= bound), name

@@ -429,18 +429,18 @@ def bf16_peak():
     return FALLBACK_BF16_TFLOPS, "fallback"
 
 
-def run_gemm(steps=20, warmup=3):
-    """The forward GEMM of a QAT linear layer on NVFP4 operands: a BF16
-    activation [M, K] ~ N(0, 1) and a weight [N, K] ~ N(0, 0.02), both
+def run_gemm(steps=20, warmup=3, fmt_name="nvfp4"):
+    """The forward GEMM of a QAT linear layer on NVFP4 (or MXFP4) operands: a
+    BF16 activation [M, K] ~ N(0, 1) and a weight [N, K] ~ N(0, 0.02), both
     quantized with fq_quantize, then fq_gemm to a BF16 C, timed with CUDA
-    events on the launching stream (the operands, 64 MB of codes and scales,
-    stay in L2 between launches: this measures the tensor-core path)."""
+    events on the launching stream (the operands, about 70 MB of codes and
+    scales, stay in L2 between launches: this measures the tensor-core path)."""
     import torch
     from fp4_quantization_aware_fq_gb300 import fq
     from fp4_quantization_aware_fq_gb300 import workloads as W
     dev = torch.device("cuda", torch.cuda.current_device())
     m, n, k = GEMM_SHAPE
-    cfg = fq.Config(fq.NVFP4)
+    cfg = fq.Config(fq.MXFP4 if fmt_name == "mxfp4" else fq.NVFP4)
     a = W.normal((m, k), 1.0, seed=20, dtype=torch.bfloat16, device=dev)
     b = W.normal((n, k), 0.02, seed=21, dtype=torch.bfloat16, device=dev)
     qa, _ = fq.fq_quantize(a, cfg)
@@ -466,7 +466,8 @@ def run_gemm(steps=20, warmup=3):
     tflops = 2.0 * m * n * k / (ms * 1e-3) / 1e12
     peak, kind = bf16_peak()
     peak *= FP4_PER_BF16
-    return {"shape_mnk": list(GEMM_SHAPE), "dtype": "nvfp4 x nvfp4 -> bf16", "ms": round(ms, 4),
+    return {"shape_mnk": list(GEMM_SHAPE), "dtype": f"{fmt_name} x {fmt_name} -> bf16",
+            "ms": round(ms, 4),
             "tflops": round(tflops, 1), "bound": "tensor", "peak_tflops": round(peak, 1),
             "peak_kind": kind + " bf16 x nominal FP4/BF16 ratio 6", "frac": round(tflops / peak, 3),
             "launches_per_call": 3, "note": "not part of the suite step; operands L2-resident"}
@@ -626,8 +627,8 @@ def main():
                     help="MoE experts in moe_qat (default: the full 32)")
     ap.add_argument("--qad-rows", type=int, default=None,
                     help="rows of the qad_kl logits (default: the full 4096)")
-    ap.add_argument("--gemm-only", action="store_true",
-                    help="time only the NVFP4 tensor-core GEMM (one JSON object)")
+    ap.add_argument("--gemm-only", choices=["nvfp4", "mxfp4"], default=None,
+                    help="time only the tensor-core GEMM of this format (one JSON object)")
     args = ap.parse_args()
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -642,7 +643,7 @@ def main():
         raise SystemExit("bench.py needs a CUDA GPU")
     torch.cuda.set_device(local)
     if args.gemm_only:
-        print(json.dumps(run_gemm(args.steps, args.warmup)), flush=True)
+        print(json.dumps(run_gemm(args.steps, args.warmup, args.gemm_only)), flush=True)
         return
     dist = None
     if world > 1:
@@ -692,7 +693,8 @@ def main():
                            "d2h_bytes_per_step": e2e["d2h"], "steps": e2e["steps"],
                            "ms_per_step": round(e2e["ms_total"] / e2e["steps"], 3)}
         if world == 1 and not args.only and not args.experts and not args.qad_rows:
-            line["gemm_nvfp4"] = run_gemm()
+            line["gemm_nvfp4"] = run_gemm(fmt_name="nvfp4")
+            line["gemm_mxfp4"] = run_gemm(fmt_name="mxfp4")
         if (not args.no_cpu_baseline and world == 1 and not args.only and not args.experts
                 and not args.qad_rows):
             sample, desc = oracle_sample()

@@ -565,7 +565,7 @@ fq_status fq_gemm(const fq_config *cfg, const fq_qtensor *a, const fq_qtensor *b
 {
     if (!valid_cfg(cfg) || !c || !valid_dtype(c_dtype))
         return FQ_ERR_INVALID_ARG;
-    if (cfg->format != FQ_NVFP4 || cfg->rht_seed)
+    if ((cfg->format != FQ_NVFP4 && cfg->format != FQ_MXFP4) || cfg->rht_seed)
         return FQ_ERR_UNSUPPORTED;
     fq_status st;
     if ((st = check_q(a, cfg->format)) != FQ_OK || (st = check_q(b, cfg->format)) != FQ_OK)
@@ -588,15 +588,15 @@ fq_status fq_gemm(const fq_config *cfg, const fq_qtensor *a, const fq_qtensor *b
     g.a_scales = a->scales;
     g.b_codes = b->codes;
     g.b_scales = b->scales;
-    g.tscale_a = a->tscale;
-    g.tscale_b = b->tscale;
+    g.tscale_a = cfg->format == FQ_NVFP4 ? a->tscale : nullptr;
+    g.tscale_b = cfg->format == FQ_NVFP4 ? b->tscale : nullptr;
     g.m = m;
     g.n = n;
     g.k = k;
     g.c = c;
     g.c_bf16 = c_dtype == FQ_BF16;
     g.err = err;
-    return cuda_status(launch_gemm_nvfp4(g, workspace, s));
+    return cuda_status(launch_gemm(g, cfg->format, workspace, s));
 }
 
 const char *fq_status_string(fq_status status)

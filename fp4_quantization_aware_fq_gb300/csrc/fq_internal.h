@@ -125,7 +125,8 @@ struct KlArgs {
     int *err;          // optional device error word
 };
 
-// Block-scaled FP4 GEMM C[m, n] = alpha A[m, k] B[n, k]^T (NVFP4 operands).
+// Block-scaled FP4 GEMM C[m, n] = alpha A[m, k] B[n, k]^T (NVFP4 or MXFP4
+// operands; alpha = the two NVFP4 tensor scales, 1 for MXFP4).
 struct GemmArgs {
     const uint8_t *a_codes, *a_scales;
     const uint8_t *b_codes, *b_scales;
@@ -157,7 +158,7 @@ cudaError_t launch_outlier_quant(const OutlierArgs &a, int bf16, int fmt, int rn
                                  cudaStream_t s);
 size_t gemm_smem_bytes();
 size_t gemm_workspace_bytes(int64_t m, int64_t n, int64_t k);
-cudaError_t launch_gemm_nvfp4(const GemmArgs &g, void *ws, cudaStream_t s);
+cudaError_t launch_gemm(const GemmArgs &g, int fmt, void *ws, cudaStream_t s);
 struct QadPlan {
     int csize;        // CTAs per cluster (one row per cluster)
     int64_t chunk;    // logits of each tensor per CTA

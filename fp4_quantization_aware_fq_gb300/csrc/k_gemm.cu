@@ -1,18 +1,23 @@
 // k_gemm.cu -- block-scaled FP4 GEMM on the 5th-generation tensor cores:
-// C[M, N] = alpha * A[M, K] B[N, K]^T for NVFP4 operands exactly as the
-// quantizers store them (packed E2M1 codes, one E4M3 scale per 1x16 block
-// along K, an FP32 tensor scale each) -- the forward GEMM of a QAT linear layer
+// C[M, N] = alpha * A[M, K] B[N, K]^T for NVFP4 or MXFP4 operands exactly as
+// the quantizers store them (packed E2M1 codes; one E4M3 scale per 1x16 block
+// along K and an FP32 tensor scale each for NVFP4, one E8M0 scale per 1x32
+// block for MXFP4) -- the forward GEMM of a QAT linear layer
 // ("Aprimorando gpt-oss para Precisão e Desempenho com Treinamento Consciente
 // à Quantização", "O que há de novo": NVFP4 with FP8 E4M3 block scales;
 // "Resumo Técnico: TetraJet-v2", §2A: 1x16 groups along the reduction).
 //
-// The tensor cores take the block scales from tensor memory, 4 columns per
-// MMA of K = 64: TMEM lane 32q + i, column c + q holds the four scales of row
-// 32q + i.  That is what tcgen05.cp.32x128b.warpx4 produces from a 512-byte
-// atom in which byte (m % 32) * 16 + (m / 32) * 4 + j is the scale of row m,
-// block j, so sf_to_mma_kernel first rearranges each operand's row-major
-// scales into such atoms ([row block][K-group of 64], 512 bytes each) in the
-// caller's workspace.
+// The tensor cores take the block scales from tensor memory in 4-column
+// groups, one per 4 scales of every row: TMEM lane 32q + i, column c + q
+// holds the four scales of row 32q + i.  That is what
+// tcgen05.cp.32x128b.warpx4 produces from a 512-byte atom in which byte
+// (m % 32) * 16 + (m / 32) * 4 + j is the scale of row m, block j, so
+// sf_to_mma_kernel first rearranges each operand's row-major scales into such
+// atoms ([row block][group of 4 blocks], 512 bytes each) in the caller's
+// workspace.  An NVFP4 atom covers K = 64, one MMA (scale_vec::4X); an MXFP4
+// atom covers K = 128, two MMAs of K = 64 that take two scales each
+// (scale_vec::2X), the second selecting bytes 2-3 of each cell through the
+// instruction's scale-factor ids.
 //
 // One CTA computes a 128 x 128 tile of C with warp-specialised roles:
 //   warp 0   producer: per K-tile of 256 elements, the A and B code tiles by
@@ -44,16 +49,23 @@ constexpr int kGemmStages = 3;
 constexpr int kGemmThreads = 192;
 constexpr uint32_t kTileBytesA = kGemmBM * kGemmBK / 2;   // 16 KB
 constexpr uint32_t kTileBytesB = kGemmBN * kGemmBK / 2;   // 16 KB
-constexpr uint32_t kSfBytesA = kGemmBM * (kGemmBK / 16);  // 2 KB
-constexpr uint32_t kSfBytesB = kGemmBN * (kGemmBK / 16);  // 2 KB
-constexpr uint32_t kStageBytes = kTileBytesA + kTileBytesB + kSfBytesA + kSfBytesB;
 constexpr uint32_t kTmemCols = 256;  // accumulator (128) + per-stage scale columns (32 each)
 constexpr uint32_t kSfColBase = 128;
-constexpr uint32_t kSfAtomBytes = 512;  // the scales of 128 rows x one K-group of 64
+constexpr uint32_t kSfAtomBytes = 512;  // the scales of 128 rows x one group of 4 blocks
 
+// Per-format layout of one pipeline stage (codes, then the scale atoms).
+template <int FMT>
+struct GemmFmt {
+    static constexpr int SB = (FMT == MXFP4) ? 32 : 16;         // elements per scale
+    static constexpr uint32_t kSfBytesA = kGemmBM * (kGemmBK / SB);  // NVFP4 2 KB, MXFP4 1 KB
+    static constexpr uint32_t kSfBytesB = kGemmBN * (kGemmBK / SB);
+    static constexpr uint32_t kStageBytes = kTileBytesA + kTileBytesB + kSfBytesA + kSfBytesB;
+    static constexpr int kAtoms = kGemmBK / (4 * SB);              // scale atoms per K-tile
+};
 size_t gemm_smem_bytes()
 {
-    return (size_t)kGemmStages * kStageBytes + 1024;  // + alignment slack for the 1 KB swizzle atoms
+    // the larger (NVFP4) stage, + alignment slack for the 1 KB swizzle atoms
+    return (size_t)kGemmStages * GemmFmt<NVFP4>::kStageBytes + 1024;
 }
 
 // ---------------------------------------------------------------- descriptors
@@ -68,11 +80,15 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint
 constexpr uint32_t kSwizzleNone = 0;
 constexpr uint32_t kSwizzle128B = 2;
 
-// Instruction descriptor of kind::mxf4nvf4 with block scaling: A and B E2M1,
-// both K-major, N >> 3 at bit 17, scale type (0 = UE4M3) at bit 23, M >> 4 at
-// bit 24; scale-factor data ids 0.
-constexpr uint32_t kGemmIdesc = (1u << 7) | (1u << 10) | ((uint32_t)(kGemmBN >> 3) << 17) |
-                                 (0u << 23) | ((uint32_t)(kGemmBM >> 4) << 24);
+// Instruction descriptor of the block-scaled FP4 kinds: A and B E2M1, both
+// K-major, N >> 3 at bit 17, scale type at bit 23 (0 UE4M3, 1 UE8M0), M >> 4
+// at bit 24, the B and A scale-factor ids (byte offsets inside each 32-bit
+// scale cell) at bits 4 and 29.
+__host__ __device__ constexpr uint32_t gemm_idesc(uint32_t ue8m0, uint32_t sf_id)
+{
+    return (1u << 7) | (1u << 10) | ((uint32_t)(kGemmBN >> 3) << 17) | (ue8m0 << 23) |
+           ((uint32_t)(kGemmBM >> 4) << 24) | (sf_id << 4) | (sf_id << 29);
+}
 
 // ---------------------------------------------------------------- tcgen05 / TMA wrappers
 __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, int x, int y,
@@ -111,16 +127,25 @@ __device__ __forceinline__ void tc_cp_32x128b_x4(uint32_t taddr, uint64_t sdesc)
                  : "memory");
 }
 
-__device__ __forceinline__ void tc_mma_nvf4(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
-                                            uint32_t idesc, uint32_t sfa, uint32_t sfb,
-                                            uint32_t accumulate)
+template <int FMT>
+__device__ __forceinline__ void tc_mma_fp4(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                           uint32_t idesc, uint32_t sfa, uint32_t sfb,
+                                           uint32_t accumulate)
 {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %6, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X"
-        " [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(d_tmem),
-        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa), "r"(sfb), "r"(accumulate)
-        : "memory");
+    if (FMT == MXFP4)
+        asm volatile(
+            "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %6, 0;\n\t"
+            "tcgen05.mma.cta_group::1.kind::mxf4.block_scale.scale_vec::2X"
+            " [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(d_tmem),
+            "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa), "r"(sfb), "r"(accumulate)
+            : "memory");
+    else
+        asm volatile(
+            "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %6, 0;\n\t"
+            "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X"
+            " [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(d_tmem),
+            "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa), "r"(sfb), "r"(accumulate)
+            : "memory");
 }
 
 // Arrives on `bar` once every tcgen05 operation this thread issued so far is done.
@@ -154,10 +179,14 @@ __device__ __forceinline__ void tc_ld_32cols(uint32_t taddr, float *v)
 }
 
 // ---------------------------------------------------------------- kernel
+template <int FMT>
 __global__ void __launch_bounds__(kGemmThreads, 1)
-    gemm_nvfp4_kernel(const __grid_constant__ CUtensorMap map_a,
-                      const __grid_constant__ CUtensorMap map_b, const GemmArgs g)
+    gemm_fp4_kernel(const __grid_constant__ CUtensorMap map_a,
+                    const __grid_constant__ CUtensorMap map_b, const GemmArgs g)
 {
+    using F = GemmFmt<FMT>;
+    constexpr uint32_t kStageBytes = F::kStageBytes, kSfBytesA = F::kSfBytesA,
+                       kSfBytesB = F::kSfBytesB;
     extern __shared__ __align__(1024) unsigned char gsm_raw[];
     // 1 KB alignment for the 128-byte-swizzle atoms
     unsigned char *gsm = gsm_raw + ((1024u - (smem_u32(gsm_raw) & 1023u)) & 1023u);
@@ -201,16 +230,18 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             mbar_arrive_expect_tx(&full[s], kStageBytes);
             tma_load_2d(st, &map_a, kt * (kGemmBK / 2), m0, &full[s]);
             tma_load_2d(st + kTileBytesA, &map_b, kt * (kGemmBK / 2), n0, &full[s]);
-            // the K-tile's four scale atoms of each operand are contiguous
-            const int64_t kgroups = g.k / 64;
-            const uint8_t *sfa = g.sfa_mma + ((int64_t)blockIdx.y * kgroups + 4 * kt) * kSfAtomBytes;
-            const uint8_t *sfb = g.sfb_mma + ((int64_t)blockIdx.x * kgroups + 4 * kt) * kSfAtomBytes;
+            // the K-tile's scale atoms of each operand are contiguous
+            const int64_t kgroups = g.k / (4 * F::SB);
+            const uint8_t *sfa =
+                g.sfa_mma + ((int64_t)blockIdx.y * kgroups + F::kAtoms * kt) * kSfAtomBytes;
+            const uint8_t *sfb =
+                g.sfb_mma + ((int64_t)blockIdx.x * kgroups + F::kAtoms * kt) * kSfAtomBytes;
             bulk_g2s(st + kTileBytesA + kTileBytesB, sfa, kSfBytesA, &full[s]);
             bulk_g2s(st + kTileBytesA + kTileBytesB + kSfBytesA, sfb, kSfBytesB, &full[s]);
         }
     } else if (warp == 1 && lane == 0) {
         // ---- MMA issuer
-        constexpr uint32_t idesc = kGemmIdesc;
+        constexpr uint32_t ue8m0 = FMT == MXFP4 ? 1u : 0u;
         for (int kt = 0; kt < kt_n; ++kt) {
             const int s = kt % kGemmStages;
             if (!mbar_wait(&full[s], (kt / kGemmStages) & 1)) {
@@ -224,24 +255,27 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             const uint32_t a_addr = smem_u32(st), b_addr = smem_u32(st + kTileBytesA);
             const uint32_t sfa_addr = smem_u32(st + kTileBytesA + kTileBytesB);
             const uint32_t sfb_addr = sfa_addr + kSfBytesA;
-            // per stage 16 TMEM columns of A scales then 16 of B scales (4 per MMA)
+            // per stage 16 TMEM columns of A scales then 16 of B scales (4 per atom)
             const uint32_t sfa_t = tmem + kSfColBase + (uint32_t)s * 32;
             const uint32_t sfb_t = sfa_t + 16;
 #pragma unroll
-            for (int kk = 0; kk < kGemmBK / 64; ++kk) {
+            for (int at = 0; at < F::kAtoms; ++at) {
                 // a scale atom: 32 rows of 16 bytes, 8-row core matrices 128 B apart
-                tc_cp_32x128b_x4(sfa_t + 4u * kk,
-                                 smem_desc(sfa_addr + kSfAtomBytes * kk, 16, 128, kSwizzleNone));
-                tc_cp_32x128b_x4(sfb_t + 4u * kk,
-                                 smem_desc(sfb_addr + kSfAtomBytes * kk, 16, 128, kSwizzleNone));
+                tc_cp_32x128b_x4(sfa_t + 4u * at,
+                                 smem_desc(sfa_addr + kSfAtomBytes * at, 16, 128, kSwizzleNone));
+                tc_cp_32x128b_x4(sfb_t + 4u * at,
+                                 smem_desc(sfb_addr + kSfAtomBytes * at, 16, 128, kSwizzleNone));
             }
 #pragma unroll
             for (int kk = 0; kk < kGemmBK / 64; ++kk) {
-                // each MMA takes K = 64 FP4 elements = 32 bytes of every row
+                // each MMA takes K = 64 FP4 elements = 32 bytes of every row; an
+                // NVFP4 MMA reads a whole atom, an MXFP4 MMA half of one
+                const int at = (FMT == MXFP4) ? kk / 2 : kk;
+                const uint32_t idesc = gemm_idesc(ue8m0, (FMT == MXFP4) ? 2u * (kk & 1) : 0u);
                 const uint64_t ad = smem_desc(a_addr + 32u * kk, 16, 1024, kSwizzle128B);
                 const uint64_t bd = smem_desc(b_addr + 32u * kk, 16, 1024, kSwizzle128B);
-                tc_mma_nvf4(tmem, ad, bd, idesc, sfa_t + 4u * kk, sfb_t + 4u * kk,
-                            (kt | kk) ? 1u : 0u);
+                tc_mma_fp4<FMT>(tmem, ad, bd, idesc, sfa_t + 4u * at, sfb_t + 4u * at,
+                                (kt | kk) ? 1u : 0u);
             }
             tc_commit(&empty[s]);
         }
@@ -348,14 +382,16 @@ __global__ void __launch_bounds__(256) sf_to_mma_kernel(const uint8_t *__restric
 
 size_t gemm_workspace_bytes(int64_t m, int64_t n, int64_t k)
 {
-    return (size_t)(m + n) * (size_t)(k / 16);
+    return (size_t)(m + n) * (size_t)(k / 16);  // NVFP4's; MXFP4 needs half
 }
 
-cudaError_t launch_gemm_nvfp4(const GemmArgs &g0, void *ws, cudaStream_t s)
+template <int FMT>
+static cudaError_t gemm_go(const GemmArgs &g0, void *ws, cudaStream_t s)
 {
+    using F = GemmFmt<FMT>;
     GemmArgs g = g0;
     uint8_t *sfa = static_cast<uint8_t *>(ws);
-    uint8_t *sfb = sfa + (size_t)g.m * (size_t)(g.k / 16);
+    uint8_t *sfb = sfa + (size_t)g.m * (size_t)(g.k / F::SB);
     g.sfa_mma = sfa;
     g.sfb_mma = sfb;
     CUtensorMap ma, mb;
@@ -367,20 +403,25 @@ cudaError_t launch_gemm_nvfp4(const GemmArgs &g0, void *ws, cudaStream_t s)
     const int cap = sm_count() * 8;
     for (int op = 0; op < 2; ++op) {
         const int64_t rows = op ? g.n : g.m;
-        const int64_t words = rows * (g.k / 64);
+        const int64_t words = rows * (g.k / (4 * F::SB));
         const int64_t need = (words + 255) / 256;
         sf_to_mma_kernel<<<(unsigned)(need < cap ? need : cap), 256, 0, s>>>(
-            op ? g.b_scales : g.a_scales, rows, g.k / 16,
+            op ? g.b_scales : g.a_scales, rows, g.k / F::SB,
             reinterpret_cast<uint32_t *>(op ? sfb : sfa));
     }
     const size_t smem = gemm_smem_bytes();
-    cudaError_t e = cudaFuncSetAttribute(gemm_nvfp4_kernel,
+    cudaError_t e = cudaFuncSetAttribute(gemm_fp4_kernel<FMT>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess)
         return e;
     dim3 grid((unsigned)(g.n / kGemmBN), (unsigned)(g.m / kGemmBM));
-    gemm_nvfp4_kernel<<<grid, kGemmThreads, smem, s>>>(ma, mb, g);
+    gemm_fp4_kernel<FMT><<<grid, kGemmThreads, smem, s>>>(ma, mb, g);
     return cudaGetLastError();
+}
+
+cudaError_t launch_gemm(const GemmArgs &g, int fmt, void *ws, cudaStream_t s)
+{
+    return fmt == MXFP4 ? gemm_go<MXFP4>(g, ws, s) : gemm_go<NVFP4>(g, ws, s);
 }
 
 }  // namespace fqk

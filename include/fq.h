@@ -344,20 +344,21 @@ FQ_API fq_status fq_qad_kl(const void *teacher, const void *student, int32_t dty
                            int32_t *err, void *stream);
 
 /* ---- Block-scaled FP4 GEMM ([GPTOSS] "O que há de novo"; [TJV2] §2A) ------
- * C[m, n] = s_A s_B sum_k (v(a_mk) e(sa_m,k/16)) (v(b_nk) e(sb_n,k/16)) for
+ * C[m, n] = alpha sum_k (v(a_mk) e(sa_m,k/B)) (v(b_nk) e(sb_n,k/B)) for
  * operands quantized row-wise along the shared reduction dimension k (A is
  * [m, k], e.g. an activation; B is [n, k], e.g. a weight; both exactly as
  * fq_quantize / fq_fakequant_ste write them): the GEMM of the dequantized
- * operands, computed on the tensor cores (FP4 products with E4M3 block
- * scales, FP32 accumulation) and scaled by the two tensor scales in FP32.
- * C is dense row-major [m, n] in c_dtype.  cfg->format must be FQ_NVFP4
- * (FQ_ERR_UNSUPPORTED otherwise); m % 128 == 0, n % 128 == 0, k % 256 == 0
- * (FQ_ERR_SHAPE).  Results equal the exact product up to FP32 accumulation
- * (and the BF16 rounding of C).  The workspace (fq_gemm_workspace_size
- * bytes, 16-byte aligned) receives both operands' block scales rearranged
- * into the tensor cores' layout; it is scratch, owned by the caller.
- * err (device int32, may be NULL) is OR-ed with 1 if an internal pipeline
- * wait timed out (C is then undefined). */
+ * operands, computed on the tensor cores (FP4 products with their block
+ * scales, FP32 accumulation).  cfg->format selects FQ_NVFP4 (E4M3 scales per
+ * 1x16, alpha = s_A s_B, the two tensor scales, applied in FP32) or FQ_MXFP4
+ * (E8M0 scales per 1x32, alpha = 1); the double block returns
+ * FQ_ERR_UNSUPPORTED.  C is dense row-major [m, n] in c_dtype.
+ * m % 128 == 0, n % 128 == 0, k % 256 == 0 (FQ_ERR_SHAPE).  Results equal
+ * the exact product up to FP32 accumulation (and the BF16 rounding of C).
+ * The workspace (fq_gemm_workspace_size bytes, 16-byte aligned) receives
+ * both operands' block scales rearranged into the tensor cores' layout; it
+ * is scratch, owned by the caller.  err (device int32, may be NULL) is OR-ed
+ * with 1 if an internal pipeline wait timed out (C is then undefined). */
 FQ_API size_t fq_gemm_workspace_size(int64_t m, int64_t n, int64_t k);
 FQ_API fq_status fq_gemm(const fq_config *cfg, const fq_qtensor *a, const fq_qtensor *b,
                          int64_t m, int64_t n, int64_t k, void *c, int32_t c_dtype,

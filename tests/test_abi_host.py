@@ -206,8 +206,8 @@ def test_gemm_argument_errors(L):
     assert g(cfg=fq.Config(9)) == 1                       # unknown format
     assert g(c=0) == 1                                    # NULL output
     assert g(ct=5) == 1                                   # unknown output dtype
-    assert g(cfg=fq.Config(fq.MXFP4)) == 5                # NVFP4 only
-    assert g(cfg=fq.Config(fq.NVFP4_2LEVEL)) == 5
+    assert g(cfg=fq.Config(fq.NVFP4_2LEVEL)) == 5          # NVFP4 and MXFP4 only
+    assert g(cfg=fq.Config(fq.MXFP4, rht_seed=3)) == 5
     assert g(a=_qt(tscale=0)) == 1                        # NVFP4 needs the tensor scale
     assert g(b=_qt(codes=FAKE + 4)) == 3                  # misaligned codes
     assert g(m=100) == 2                                  # m % 128

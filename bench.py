@@ -473,6 +473,41 @@ def run_gemm(steps=20, warmup=3, fmt_name="nvfp4"):
             "launches_per_call": 3, "note": "not part of the suite step; operands L2-resident"}
 
 
+def run_small_at_scale(steps=20, warmup=3):
+    """The nvfp4_small call (FP32 NVFP4 fake-quant with codes, scales, FP32 xhat
+    and mask) on a [65536, 1024] tensor of the same recipe: at 256 x 1024 the
+    workload is launch-bound, so the kernels' bandwidth shows only at size.
+    Not part of the step; the input (256 MB) exceeds L2."""
+    import torch
+    from fp4_quantization_aware_fq_gb300 import fq
+    from fp4_quantization_aware_fq_gb300 import workloads as W
+    dev = torch.device("cuda", torch.cuda.current_device())
+    x = W.normal((65536, 1024), 1.0, seed=0, device=dev)
+    cfg = fq.Config(fq.NVFP4)
+    q = fq.alloc_qtensor(*x.shape, fq.NVFP4, dev)
+    xh = torch.empty_like(x)
+    m = torch.empty(((x.numel() + 7) // 8 + 15) // 16 * 16, dtype=torch.uint8, device=dev)
+    ws = torch.empty(256, dtype=torch.uint8, device=dev)
+    call = lambda: fq.fq_fakequant_ste(x, cfg, xhat=xh, mask=m, row_out=q, ws=ws)  # noqa: E731
+    for _ in range(warmup):
+        call()
+    stream = torch.cuda.current_stream()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    t0.record(stream)
+    for _ in range(steps):
+        call()
+    t1.record(stream)
+    torch.cuda.synchronize()
+    ms = t0.elapsed_time(t1) / steps
+    gbs = BYTES_PER_ELEM["nvfp4_small"] * x.numel() / (ms * 1e-3) / 1e9
+    peak, kind = measured_peaks()
+    return {"shape": [65536, 1024], "ms": round(ms, 4), "gbs": round(gbs, 1),
+            "frac_hbm": round(gbs / peak, 3), "peak_kind": kind,
+            "note": "nvfp4_small's two launches on a 64x larger tensor; not part of the step"}
+
+
 def run_e2e(args, suite, total_bytes):
     import torch
     stream = torch.cuda.current_stream()
@@ -505,70 +540,89 @@ def run_e2e(args, suite, total_bytes):
 
 
 # --------------------------------------------------------------------------- oracle timing
-def oracle_sample(max_seconds=None):
-    """Time the oracle on a bounded sample of every workload.  Returns
-    {workload: (elements, seconds)} and a text description."""
-    import numpy as np
+_ORACLE_INPUTS = {}
+
+
+def _oracle_inputs(div):
+    """The oracle's sample inputs, with every sample's rows divided by div
+    (built once per div: the generators are not what is timed)."""
+    if div in _ORACLE_INPUTS:
+        return _ORACLE_INPUTS[div]
+    import torch
     import oracle
     from fp4_quantization_aware_fq_gb300 import workloads as W
     oracle.build()
-    res = {}
     f32 = lambda t: oracle.bf16_bits_to_f32(W.bf16_bits(t)).reshape(t.shape)  # noqa: E731
+    d = {}
+    d["x1"] = W.nvfp4_small(shape=(256 // div, 1024)).numpy()
+    d["x2"] = f32(W.mxfp4_weight(shape=(4096 // div, 4096), seed=1))
+    d["x3"] = f32(W.nvfp4_act(shape=(4096 // div, 8192), seed=2))
+    d["dy"] = W.bf16_bits(W.normal(d["x3"].shape, 1.0, seed=12, dtype=torch.bfloat16))
+    d["x4"] = f32(W.grad_2level(shape=(8192 // div, 4096), seed=3))
+    d["x6"] = f32(W.grad_2level(shape=(2048 // div, 4096), seed=6))
+    d["x7"] = f32(W.channel_act(shape=(2048 // div, 8192)))
+    d["sel7"] = oracle.select_channels(
+        oracle.channel_amax(f32(W.channel_act(shape=(2048 // div, 8192), seed=501))), 819)
+    zt8, zs8 = W.qad_logits((max(16 // div, 1), 201088), seed=6)
+    d["zt8"], d["zs8"] = f32(zt8), f32(zs8)
+    d["w5"] = f32(W.normal((5760 // div, 5760), 0.02, seed=4).to(torch.bfloat16))
+    d["d5"] = W.master_update((5760 // div, 5760), 1).numpy()
+    _ORACLE_INPUTS[div] = d
+    return d
+
+
+def oracle_sample(div=1):
+    """Time the oracle on a bounded sample of every workload (row counts of the
+    samples divided by div).  Returns {workload: (elements, seconds)} and a
+    text description."""
+    import oracle
+    d = _oracle_inputs(div)
+    res = {}
 
     def timed(fn):
         t = time.perf_counter()
         fn()
         return time.perf_counter() - t
 
-    x1 = W.nvfp4_small().numpy()
-    res["nvfp4_small"] = (x1.size, timed(lambda: oracle.quantize(
-        x1, oracle.NVFP4, want_xhat=True, want_mask=True)))
-    x2 = f32(W.mxfp4_weight(shape=(4096, 4096), seed=1))
-    res["mxfp4_weight"] = (x2.size, timed(lambda: oracle.quantize(
-        x2, oracle.MXFP4, want_xhat=True, want_mask=True)))
-    x3 = f32(W.nvfp4_act(shape=(4096, 8192), seed=2))
+    res["nvfp4_small"] = (d["x1"].size, timed(lambda: oracle.quantize(
+        d["x1"], oracle.NVFP4, want_xhat=True, want_mask=True)))
+    res["mxfp4_weight"] = (d["x2"].size, timed(lambda: oracle.quantize(
+        d["x2"], oracle.MXFP4, want_xhat=True, want_mask=True)))
 
     def c3():
-        q = oracle.quantize(x3, oracle.NVFP4, orient=oracle.ROWCOL, want_xhat=True,
+        q = oracle.quantize(d["x3"], oracle.NVFP4, orient=oracle.ROWCOL, want_xhat=True,
                             want_mask=True)
         oracle.f32_to_bf16_bits(q["row"]["xhat"])
         return q
-    q3 = None
     t = time.perf_counter()
     q3 = c3()
-    res["nvfp4_act"] = (x3.size, time.perf_counter() - t)
-    dy = W.bf16_bits(W.normal(x3.shape, 1.0, seed=12, dtype=__import__("torch").bfloat16))
-    res["ste_backward"] = (dy.size, timed(lambda: oracle.ste_backward(dy, q3["row"]["mask"])))
-    x4 = f32(W.grad_2level(shape=(8192, 4096), seed=3))
-    res["grad_2level"] = (x4.size, timed(lambda: oracle.quantize(
-        x4, oracle.NVFP4_2LEVEL, oracle.SR, 0x5EED)))
-    x6 = f32(W.grad_2level(shape=(2048, 4096), seed=6))
-    res["grad_rht_rowcol"] = (x6.size, timed(lambda: oracle.quantize(
-        x6, oracle.NVFP4_2LEVEL, oracle.SR, 0x5EED, orient=oracle.ROWCOL, rht_seed=0xB00F)))
-    x7 = W.channel_act(shape=(2048, 8192))
-    am7 = oracle.channel_amax(f32(W.channel_act(shape=(2048, 8192), seed=501)))
-    sel7 = oracle.select_channels(am7, 819)
+    res["nvfp4_act"] = (d["x3"].size, time.perf_counter() - t)
+    res["ste_backward"] = (d["dy"].size, timed(lambda: oracle.ste_backward(
+        d["dy"], q3["row"]["mask"])))
+    res["grad_2level"] = (d["x4"].size, timed(lambda: oracle.quantize(
+        d["x4"], oracle.NVFP4_2LEVEL, oracle.SR, 0x5EED)))
+    res["grad_rht_rowcol"] = (d["x6"].size, timed(lambda: oracle.quantize(
+        d["x6"], oracle.NVFP4_2LEVEL, oracle.SR, 0x5EED, orient=oracle.ROWCOL, rht_seed=0xB00F)))
 
     def c7():
-        q = oracle.quantize_outliers(f32(x7), sel7["idx"], sel7["fp8_scale"], oracle.NVFP4)
+        q = oracle.quantize_outliers(d["x7"], d["sel7"]["idx"], d["sel7"]["fp8_scale"],
+                                     oracle.NVFP4)
         oracle.f32_to_bf16_bits(q["xhat"])
-    res["act_outliers"] = (x7.numel(), timed(c7))
-    zt8, zs8 = W.qad_logits((16, 201088), seed=6)
-    res["qad_kl"] = (zt8.numel(), timed(lambda: oracle.qad_kl(f32(zt8), f32(zs8))))
-    w = W.normal((5760, 5760), 0.02, seed=4).to(__import__("torch").bfloat16)
-    st = oracle.OsciState(f32(w), oracle.NVFP4)
-    d = W.master_update((5760, 5760), 1).numpy()
+    res["act_outliers"] = (d["x7"].size, timed(c7))
+    res["qad_kl"] = (d["zt8"].size, timed(lambda: oracle.qad_kl(d["zt8"], d["zs8"])))
+    st = oracle.OsciState(d["w5"], oracle.NVFP4)
 
     def upd():
-        out = st.step(d, offset=1)
+        out = st.step(d["d5"], offset=1)
         oracle.f32_to_bf16_bits(out["xhat"])
     t_upd = timed(upd)
-    res["osci_update_reset"] = (w.numel(), t_upd + timed(lambda: st.reset(4.0)))
-    desc = ("oracle (scalar C, 1 thread) on: nvfp4_small full; mxfp4_weight full; "
-            "nvfp4_act 4096 rows row+col; ste_backward 4096x8192; grad_2level 8192 rows SR; "
-            "grad_rht_rowcol 2048 rows; act_outliers 2048 rows; qad_kl 16 rows; "
-            "osci update+reset on a [5760, 5760] matrix (one expert's weights); per-element "
-            "rates scaled to the full step's elements")
+    res["osci_update_reset"] = (d["w5"].size, t_upd + timed(lambda: st.reset(4.0)))
+    r = lambda n: n // div  # noqa: E731
+    desc = (f"oracle (scalar C, 1 thread) on: nvfp4_small {r(256)} rows; mxfp4_weight "
+            f"{r(4096)} rows; nvfp4_act {r(4096)} rows row+col; ste_backward {r(4096)}x8192; "
+            f"grad_2level {r(8192)} rows SR; grad_rht_rowcol {r(2048)} rows; act_outliers "
+            f"{r(2048)} rows; qad_kl {max(16 // div, 1)} rows; osci update+reset on a "
+            f"[{r(5760)}, 5760] matrix; per-element rates scaled to the full step's elements")
     return res, desc
 
 
@@ -693,6 +747,7 @@ def main():
                            "d2h_bytes_per_step": e2e["d2h"], "steps": e2e["steps"],
                            "ms_per_step": round(e2e["ms_total"] / e2e["steps"], 3)}
         if world == 1 and not args.only and not args.experts and not args.qad_rows:
+            line["nvfp4_small_at_scale"] = run_small_at_scale()
             line["gemm_nvfp4"] = run_gemm(fmt_name="nvfp4")
             line["gemm_mxfp4"] = run_gemm(fmt_name="mxfp4")
         if (not args.no_cpu_baseline and world == 1 and not args.only and not args.experts
@@ -714,12 +769,14 @@ def main_reference(args, rank, world):
     sample of every workload; value = the suite's bytes at the sampled rates."""
     if rank != 0:
         return
+    # each step times a sample an eighth the size of the cpu_baseline's (about
+    # a second of oracle work), so that the whole run stays within minutes
     for _ in range(args.warmup):
-        oracle_sample()
+        oracle_sample(div=8)
     vals, secs = [], []
     desc = ""
     for _ in range(args.steps):
-        sample, desc = oracle_sample()
+        sample, desc = oracle_sample(div=8)
         v, s = oracle_gbs(sample, FULL_ELEMS)
         vals.append(v)
         secs.append(sum(t for _, t in sample.values()))

@@ -184,7 +184,7 @@ __global__ void __launch_bounds__(kThreads) row_kernel(RowArgs a)
 // ------------------------------------------------------------------ tiled row + column
 template <int FMT>
 struct TileShape {
-    static constexpr int TR = (FMT == NV2L) ? 128 : 64;  // tile rows
+    static constexpr int TR = 128;                       // tile rows
     static constexpr int TC = (FMT == NV2L) ? 128 : 64;  // tile cols
     static constexpr int BC = FmtInfo<FMT>::B;           // column block (rows)
     static constexpr int CP = TR / 2 + 8;                // staged code bytes per column (padded)

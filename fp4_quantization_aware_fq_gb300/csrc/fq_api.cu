@@ -570,7 +570,9 @@ fq_status fq_gemm(const fq_config *cfg, const fq_qtensor *a, const fq_qtensor *b
     fq_status st;
     if ((st = check_q(a, cfg->format)) != FQ_OK || (st = check_q(b, cfg->format)) != FQ_OK)
         return st;
-    if (m < 0 || n < 0 || k < 0 || m % 128 || n % 128 || k % 256 || m / 128 > 65535)
+    // k: the codes' row pitch (k / 2 bytes) must be a multiple of 16 for the tensor maps;
+    // n: the epilogue stores 32-column chunks
+    if (m < 0 || n < 0 || k < 0 || n % 32 || k % 32 || (m + 127) / 128 > 65535)
         return FQ_ERR_SHAPE;
     if (!aligned16(c) || (err && (reinterpret_cast<uintptr_t>(err) & 3u)))
         return FQ_ERR_ALIGN;

@@ -196,7 +196,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int m0 = blockIdx.y * kGemmBM, n0 = blockIdx.x * kGemmBN;
-    const int kt_n = (int)(g.k / kGemmBK);
+    const int kt_n = (int)((g.k + kGemmBK - 1) / kGemmBK);  // the last K-tile zero-filled past k
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kGemmStages; ++s) {
@@ -231,7 +231,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             tma_load_2d(st, &map_a, kt * (kGemmBK / 2), m0, &full[s]);
             tma_load_2d(st + kTileBytesA, &map_b, kt * (kGemmBK / 2), n0, &full[s]);
             // the K-tile's scale atoms of each operand are contiguous
-            const int64_t kgroups = g.k / (4 * F::SB);
+            const int64_t kgroups = (int64_t)kt_n * F::kAtoms;  // padded to whole K-tiles
             const uint8_t *sfa =
                 g.sfa_mma + ((int64_t)blockIdx.y * kgroups + F::kAtoms * kt) * kSfAtomBytes;
             const uint8_t *sfb =
@@ -292,6 +292,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         if (__all_sync(0xFFFFFFFFu, ok && !*(volatile int *)&abort_flag)) {
             const int q = warp & 3;
             const int row = m0 + 32 * q + lane;
+            const bool row_ok = row < g.m;  // rows past m hold the tile's zero padding
             float alpha = 1.0f;
             if (g.tscale_a && g.tscale_b)
                 alpha = __fmul_rn(__ldg(g.tscale_a), __ldg(g.tscale_b));
@@ -303,6 +304,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 for (int i = 0; i < 32; ++i)
                     v[i] = __fmul_rn(v[i], alpha);
                 const int64_t off = (int64_t)row * g.n + n0 + 32 * c;
+                if (!row_ok || n0 + 32 * c >= g.n)  // n % 32 == 0: a 32-column chunk is all in or out
+                    continue;
                 if (g.c_bf16) {
                     uint4 *dst = reinterpret_cast<uint4 *>((char *)g.c + off * 2);
 #pragma unroll
@@ -361,28 +364,46 @@ static bool make_map(CUtensorMap *map, const void *base, uint64_t rows, uint64_t
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// Row-major scales [rows, k/16] -> MMA atoms [rows/128][k/64][512 B]: one
+// Row-major scales [rows, kb] (kb = k / B) -> MMA atoms [ceil(rows / 128)]
+// [kgroups][512 B], kgroups = 4-scale groups padded to whole K-tiles: one
 // thread per 4-byte word of the output (the four scales of one row and one
-// K-group of 64).
+// group).  Rows past `rows` and scales past kb are written as 0 (a finite
+// scale: the codes the tensor map reads there are zero-filled).
 __global__ void __launch_bounds__(256) sf_to_mma_kernel(const uint8_t *__restrict__ scales,
                                                         int64_t rows, int64_t kb,
+                                                        int64_t kgroups,
                                                         uint32_t *__restrict__ out)
 {
-    const int64_t kgroups = kb / 4;
-    const int64_t words = rows / 128 * kgroups * 128;
+    const int64_t words = (rows + 127) / 128 * kgroups * 128;
     for (int64_t w = (int64_t)blockIdx.x * 256 + threadIdx.x; w < words;
          w += (int64_t)gridDim.x * 256) {
         const int pos = (int)(w & 127);
         const int64_t atom = w >> 7;
         const int64_t kg = atom % kgroups, rb = atom / kgroups;
-        const int m = 32 * (pos & 3) + (pos >> 2);
-        out[w] = __ldg(reinterpret_cast<const uint32_t *>(scales + (rb * 128 + m) * kb) + kg);
+        const int64_t m = rb * 128 + 32 * (pos & 3) + (pos >> 2);
+        uint32_t word = 0;
+        if (m < rows) {
+            const uint8_t *src = scales + m * kb + 4 * kg;
+            if ((kb & 3) == 0 && 4 * kg + 3 < kb) {
+                word = __ldg(reinterpret_cast<const uint32_t *>(src));  // aligned, in range
+            } else {
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                    if (4 * kg + j < kb)
+                        word |= (uint32_t)__ldg(src + j) << (8 * j);
+            }
+        }
+        out[w] = word;
     }
 }
 
+// Both operands' scale atoms, rows padded to 128 and k to whole K-tiles
+// (NVFP4's size; MXFP4 needs half).
+static int64_t pad_to(int64_t v, int64_t q) { return (v + q - 1) / q * q; }
+
 size_t gemm_workspace_bytes(int64_t m, int64_t n, int64_t k)
 {
-    return (size_t)(m + n) * (size_t)(k / 16);  // NVFP4's; MXFP4 needs half
+    return (size_t)(pad_to(m, 128) + pad_to(n, 128)) * (size_t)(pad_to(k, kGemmBK) / 16);
 }
 
 template <int FMT>
@@ -390,8 +411,9 @@ static cudaError_t gemm_go(const GemmArgs &g0, void *ws, cudaStream_t s)
 {
     using F = GemmFmt<FMT>;
     GemmArgs g = g0;
+    const int64_t kgroups = pad_to(g.k, kGemmBK) / (4 * F::SB);
     uint8_t *sfa = static_cast<uint8_t *>(ws);
-    uint8_t *sfb = sfa + (size_t)g.m * (size_t)(g.k / F::SB);
+    uint8_t *sfb = sfa + (size_t)pad_to(g.m, 128) * (size_t)kgroups * 4;
     g.sfa_mma = sfa;
     g.sfb_mma = sfb;
     CUtensorMap ma, mb;
@@ -403,10 +425,10 @@ static cudaError_t gemm_go(const GemmArgs &g0, void *ws, cudaStream_t s)
     const int cap = sm_count() * 8;
     for (int op = 0; op < 2; ++op) {
         const int64_t rows = op ? g.n : g.m;
-        const int64_t words = rows * (g.k / (4 * F::SB));
+        const int64_t words = pad_to(rows, 128) * kgroups;
         const int64_t need = (words + 255) / 256;
         sf_to_mma_kernel<<<(unsigned)(need < cap ? need : cap), 256, 0, s>>>(
-            op ? g.b_scales : g.a_scales, rows, g.k / F::SB,
+            op ? g.b_scales : g.a_scales, rows, g.k / F::SB, kgroups,
             reinterpret_cast<uint32_t *>(op ? sfb : sfa));
     }
     const size_t smem = gemm_smem_bytes();
@@ -414,7 +436,7 @@ static cudaError_t gemm_go(const GemmArgs &g0, void *ws, cudaStream_t s)
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess)
         return e;
-    dim3 grid((unsigned)(g.n / kGemmBN), (unsigned)(g.m / kGemmBM));
+    dim3 grid((unsigned)((g.n + kGemmBN - 1) / kGemmBN), (unsigned)((g.m + kGemmBM - 1) / kGemmBM));
     gemm_fp4_kernel<FMT><<<grid, kGemmThreads, smem, s>>>(ma, mb, g);
     return cudaGetLastError();
 }

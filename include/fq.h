@@ -353,7 +353,9 @@ FQ_API fq_status fq_qad_kl(const void *teacher, const void *student, int32_t dty
  * 1x16, alpha = s_A s_B, the two tensor scales, applied in FP32) or FQ_MXFP4
  * (E8M0 scales per 1x32, alpha = 1); the double block returns
  * FQ_ERR_UNSUPPORTED.  C is dense row-major [m, n] in c_dtype.
- * m % 128 == 0, n % 128 == 0, k % 256 == 0 (FQ_ERR_SHAPE).  Results equal
+ * n % 32 == 0 and k % 32 == 0 (FQ_ERR_SHAPE); m is free.  Tiles are 128 x
+ * 128 x 256: the parts of a tile past m, n or k are zero-filled, so any such
+ * shape runs (for example gpt-oss's 2880 and 5760).  Results equal
  * the exact product up to FP32 accumulation (and the BF16 rounding of C).
  * The workspace (fq_gemm_workspace_size bytes, 16-byte aligned) receives
  * both operands' block scales rearranged into the tensor cores' layout; it

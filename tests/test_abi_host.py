@@ -203,6 +203,7 @@ def test_gemm_argument_errors(L):
         return L.fq_gemm(ctypes.byref(cfg), ctypes.byref(qa), ctypes.byref(qb), m, n, k, c, ct,
                          ws, wsb, err, None)
     assert fq.fq_gemm_workspace_size(256, 128, 512) == (256 + 128) * 512 // 16
+    assert fq.fq_gemm_workspace_size(200, 96, 2880) == (256 + 128) * 3072 // 16  # padded
     assert g(cfg=fq.Config(9)) == 1                       # unknown format
     assert g(c=0) == 1                                    # NULL output
     assert g(ct=5) == 1                                   # unknown output dtype
@@ -210,9 +211,8 @@ def test_gemm_argument_errors(L):
     assert g(cfg=fq.Config(fq.MXFP4, rht_seed=3)) == 5
     assert g(a=_qt(tscale=0)) == 1                        # NVFP4 needs the tensor scale
     assert g(b=_qt(codes=FAKE + 4)) == 3                  # misaligned codes
-    assert g(m=100) == 2                                  # m % 128
-    assert g(n=64) == 2                                   # n % 128
-    assert g(k=128) == 2                                  # k % 256
+    assert g(n=48) == 2                                   # n % 32
+    assert g(k=48) == 2                                   # k % 32
     assert g(c=FAKE + 8) == 3                             # misaligned output
     assert g(ws=0) == 4                                   # no workspace
     assert g(wsb=100) == 4                                # workspace too small

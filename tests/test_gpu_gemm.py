@@ -144,3 +144,11 @@ def test_qat_linear_layer_three_gemms():
         bound = 2.0 ** -16 * (np.abs(da) @ np.abs(db).T)
         got = npy(c).astype(np.float64)
         assert np.all(np.abs(got - ref) <= bound), name
+
+
+@pytest.mark.parametrize("m,n,k", [(200, 160, 2880), (1, 32, 32), (130, 96, 544),
+                                   (256, 5760, 2880)])
+def test_gemm_shapes_off_the_tile_grid(m, n, k):
+    """m free, n and k multiples of 32: the parts of the 128 x 128 x 256 tiles
+    past the operands are zero-filled (gpt-oss's 2880 and 5760 included)."""
+    _check(m, n, k, seed=m + n + k)

@@ -70,3 +70,8 @@ def test_mxfp4_gemm_varied_scales():
 def test_mxfp4_gemm_bf16_output_long_k():
     _run(W.normal((128, 4096), 0.5, seed=25), W.normal((256, 4096), 0.02, seed=26),
          c_dtype=torch.bfloat16)
+
+
+@pytest.mark.parametrize("m,n,k", [(200, 160, 2880), (3, 64, 96)])
+def test_mxfp4_gemm_shapes_off_the_tile_grid(m, n, k):
+    _run(W.normal((m, k), 1.0, seed=m), W.normal((n, k), 0.02, seed=n))

@@ -376,38 +376,32 @@ def run_ours(args, rank, world, dist):
 
 
 def e2e_buffers(suite):
-    """Device tensors that each step takes from the host (its inputs) and the
-    results it hands back (packed codes and scales, the reset count)."""
-    ins, outs = [], []
+    """Per workload (in step order): the device tensors that each step takes
+    from the host (its inputs) and the results it hands back (packed codes and
+    scales, losses, the reset count)."""
+    io = {}
     if "nvfp4_small" in suite.names:
-        ins.append(suite.x1)
-        outs += [suite.q1.codes, suite.q1.scales, suite.q1.tscale]
+        io["nvfp4_small"] = ([suite.x1], [suite.q1.codes, suite.q1.scales, suite.q1.tscale])
     if "mxfp4_weight" in suite.names:
-        ins.append(suite.x2)
-        outs += [suite.q2.codes, suite.q2.scales]
+        io["mxfp4_weight"] = ([suite.x2], [suite.q2.codes, suite.q2.scales])
     if "nvfp4_act" in suite.names:
-        ins.append(suite.x3)
-        outs += [suite.rq3.codes, suite.rq3.scales, suite.cq3.codes, suite.cq3.scales]
+        io["nvfp4_act"] = ([suite.x3], [suite.rq3.codes, suite.rq3.scales, suite.cq3.codes,
+                                        suite.cq3.scales])
     if "ste_backward" in suite.names:
-        ins.append(suite.dy3)
-        outs.append(suite.dx3)
+        io["ste_backward"] = ([suite.dy3], [suite.dx3])
     if "grad_2level" in suite.names:
-        ins.append(suite.x4)
-        outs += [suite.q4.codes, suite.q4.scales, suite.q4.tscale]
+        io["grad_2level"] = ([suite.x4], [suite.q4.codes, suite.q4.scales, suite.q4.tscale])
     if "grad_rht_rowcol" in suite.names:
-        ins.append(suite.x6)
-        outs += [suite.rq6.codes, suite.rq6.scales, suite.rq6.tscale, suite.cq6.codes,
-                 suite.cq6.scales, suite.cq6.tscale]
+        io["grad_rht_rowcol"] = ([suite.x6], [suite.rq6.codes, suite.rq6.scales, suite.rq6.tscale,
+                                              suite.cq6.codes, suite.cq6.scales, suite.cq6.tscale])
     if "act_outliers" in suite.names:
-        ins.append(suite.x7)
-        outs += [suite.q7.codes, suite.q7.scales, suite.q7.tscale, suite.fp87]
+        io["act_outliers"] = ([suite.x7], [suite.q7.codes, suite.q7.scales, suite.q7.tscale,
+                                           suite.fp87])
     if "qad_kl" in suite.names:
-        ins += [suite.zt8, suite.zs8]
-        outs += [suite.loss8, suite.mean8]
+        io["qad_kl"] = ([suite.zt8, suite.zs8], [suite.loss8, suite.mean8])
     if "osci_update_reset" in suite.names:
-        ins += list(suite.delta)
-        outs.append(suite.nreset)
-    return ins, outs
+        io["osci_update_reset"] = (list(suite.delta), [suite.nreset])
+    return io
 
 
 GEMM_SHAPE = (8192, 8192, 8192)   # M (tokens), N (output features), K (input features)
@@ -509,20 +503,50 @@ def run_small_at_scale(steps=20, warmup=3):
 
 
 def run_e2e(args, suite, total_bytes):
+    """The suite end to end: every step copies each workload's inputs from
+    pinned host memory to the device (copy stream), runs the workload's calls
+    (the current stream) and reads its results back to pinned host memory
+    (read-back stream).  Events order each workload's copy-in before its calls
+    and its read-back after them, and keep the next step's copy-in (or calls)
+    from overwriting a buffer that this step still reads: the copies of later
+    workloads overlap the calls of earlier ones, as in a training loop that
+    streams its batches in."""
     import torch
     stream = torch.cuda.current_stream()
-    ins, outs = e2e_buffers(suite)
-    h_in = [(d, d.cpu().pin_memory()) for d in ins]
-    h_out = [torch.empty(o.shape, dtype=o.dtype).pin_memory() for o in outs]
-    h2d = sum(h.numel() * h.element_size() for _, h in h_in)
-    d2h = sum(o.numel() * o.element_size() for o in outs)
+    cs, ds = torch.cuda.Stream(), torch.cuda.Stream()
+    io = e2e_buffers(suite)
+    names = [n for n in suite.names if n in io]
+    h_in = {n: [(d, d.cpu().pin_memory()) for d in io[n][0]] for n in names}
+    h_out = {n: [(o, torch.empty(o.shape, dtype=o.dtype).pin_memory()) for o in io[n][1]]
+             for n in names}
+    h2d = sum(h.numel() * h.element_size() for n in names for _, h in h_in[n])
+    d2h = sum(h.numel() * h.element_size() for n in names for _, h in h_out[n])
+    ev_in = {n: torch.cuda.Event() for n in names}    # inputs are on the device
+    ev_used = {n: torch.cuda.Event() for n in names}  # the calls are done (inputs read, outputs written)
+    ev_out = {n: torch.cuda.Event() for n in names}   # outputs are back on the host
+    recorded = set()
 
     def step():
-        for d, h in h_in:
-            d.copy_(h, non_blocking=True)
-        suite.step()
-        for o, h in zip(outs, h_out):
-            h.copy_(o, non_blocking=True)
+        for n in names:
+            if n in recorded:
+                cs.wait_event(ev_used[n])
+            with torch.cuda.stream(cs):
+                for d, h in h_in[n]:
+                    d.copy_(h, non_blocking=True)
+            ev_in[n].record(cs)
+        for n in names:
+            stream.wait_event(ev_in[n])
+            if n in recorded:
+                stream.wait_event(ev_out[n])
+            getattr(suite, n)()
+            ev_used[n].record(stream)
+            ds.wait_event(ev_used[n])
+            with torch.cuda.stream(ds):
+                for o, h in h_out[n]:
+                    h.copy_(o, non_blocking=True)
+            ev_out[n].record(ds)
+            recorded.add(n)
+        suite.step_no += 1
 
     for _ in range(max(1, min(args.warmup, 2))):
         step()
@@ -531,8 +555,12 @@ def run_e2e(args, suite, total_bytes):
     a = torch.cuda.Event(enable_timing=True)
     b = torch.cuda.Event(enable_timing=True)
     a.record(stream)
+    cs.wait_event(a)
+    ds.wait_event(a)
     for _ in range(k):
         step()
+    stream.wait_stream(cs)
+    stream.wait_stream(ds)
     b.record(stream)
     torch.cuda.synchronize()
     ms = a.elapsed_time(b)

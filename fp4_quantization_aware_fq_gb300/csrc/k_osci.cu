@@ -9,7 +9,8 @@
 // FP32 master weights tile by tile across the whole group:
 //   A: w += delta, dist_M += |w_t - w_{t-1}|, per-tensor amax of w_t (atomic);
 //   B: fake-quantize w_t under the new tensor scale, decode w_{t-1}'s stored
-//      codes, dist_Q += |xhat_t - xhat_{t-1}|, write codes/scales/xhat/mask.
+//      codes, dist_Q += |xhat_t - xhat_{t-1}|, write codes/scales/xhat/mask
+//      (one lane per 16-byte chunk; the lanes of a block share its scale).
 // The tensor amax is the only dependency between the passes, hence the split.
 #include "fq_device.cuh"
 #include "fq_internal.h"
@@ -17,7 +18,15 @@
 namespace fqk {
 
 constexpr int kOsciThreads = 256;
-constexpr int kOsciU = 4;
+constexpr int kOsciU = 4;   // chunks in flight per thread: the reset pass
+// Pass A: eight chunks in flight per thread (one CTA per SM at its register
+// count) measured 1% faster on the 32-expert step than four.
+constexpr int kOsciAU = 8;
+// Pass B: one chunk per thread at a time with four CTAs per SM (at most 64
+// registers) measured fastest on the 32-expert step: 7.17 ms, against 7.35
+// with two chunks and 7.84 with four at the registers those need.
+constexpr int kOsciBU = 1;
+constexpr int kOsciBMinCtas = 4;
 
 __device__ __forceinline__ float4 ldf4(const float *p)
 {
@@ -46,10 +55,10 @@ __global__ void __launch_bounds__(kOsciThreads) osci_pass_a(const __grid_constan
         const int64_t nch = T.n / 4;
         const int64_t cbeg = (tile - a.tile_start[t]) * kOsciTileChunks;
         float m = 0.0f;
-        for (int k0 = 0; k0 < kOsciTileChunks; k0 += kOsciThreads * kOsciU) {
-            float4 w[kOsciU], d[kOsciU], dm[kOsciU];
+        for (int k0 = 0; k0 < kOsciTileChunks; k0 += kOsciThreads * kOsciAU) {
+            float4 w[kOsciAU], d[kOsciAU], dm[kOsciAU];
 #pragma unroll
-            for (int k = 0; k < kOsciU; ++k) {
+            for (int k = 0; k < kOsciAU; ++k) {
                 const int64_t ch = cbeg + k0 + k * kOsciThreads + threadIdx.x;
                 if (ch < nch) {
                     w[k] = ldf4_rw(T.master + ch * 4);
@@ -58,7 +67,7 @@ __global__ void __launch_bounds__(kOsciThreads) osci_pass_a(const __grid_constan
                 }
             }
 #pragma unroll
-            for (int k = 0; k < kOsciU; ++k) {
+            for (int k = 0; k < kOsciAU; ++k) {
                 const int64_t ch = cbeg + k0 + k * kOsciThreads + threadIdx.x;
                 if (ch < nch) {
                     float4 wn;
@@ -93,32 +102,90 @@ __global__ void __launch_bounds__(kOsciThreads) osci_pass_a(const __grid_constan
     }
 }
 
-// Pass B: one thread per block of 16 (32 for MXFP4) master weights, NB blocks
-// per thread per iteration with all their loads issued before any compute.
+// Four E2M1 nibbles of four values (16 bits; element 2j in the low nibble of
+// byte j), nearest-even and saturating.
+__device__ __forceinline__ uint32_t e2m1_rn_pack4(float y0, float y1, float y2, float y3)
+{
+    uint32_t out;
+    asm("{\n\t"
+        ".reg .b8 q0, q1;\n\t"
+        ".reg .b16 h;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 q0, %2, %1;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 q1, %4, %3;\n\t"
+        "mov.b16 h, {q0, q1};\n\t"
+        "cvt.u32.u16 %0, h;\n\t"
+        "}"
+        : "=r"(out)
+        : "f"(y0), "f"(y1), "f"(y2), "f"(y3));
+    return out;
+}
+
+// Grid values of four E2M1 nibbles (the low 16 bits of q).
+__device__ __forceinline__ void e2m1_decode4(uint32_t q, float *out)
+{
+    uint32_t h[2];
+    asm("{\n\t"
+        ".reg .b8 q0, q1, q2, q3;\n\t"
+        "mov.b32 {q0, q1, q2, q3}, %2;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %0, q0;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %1, q1;\n\t"
+        "}"
+        : "=r"(h[0]), "=r"(h[1])
+        : "r"(q));
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+        const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&h[i]));
+        out[2 * i] = f.x;
+        out[2 * i + 1] = f.y;
+    }
+}
+
+// Maximum, and OR, over aligned groups of L lanes.
+template <int L>
+__device__ __forceinline__ float lanes_max(float v)
+{
+#pragma unroll
+    for (int o = 1; o < L; o <<= 1)
+        v = fmaxf(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
+    return v;
+}
+template <int L>
+__device__ __forceinline__ uint32_t lanes_or(uint32_t v)
+{
+#pragma unroll
+    for (int o = 1; o < L; o <<= 1)
+        v |= __shfl_xor_sync(0xFFFFFFFFu, v, o);
+    return v;
+}
+
+// Pass B: one thread per 16-byte chunk of 4 master weights (kOsciBU chunks
+// per thread at a time), so every load and store of the per-weight arrays is
+// a coalesced 16-byte vector per lane, as in pass A.  The B/4 lanes of a block
+// (4; 8 for MXFP4) share its amax, scale and mask bits through shuffles; for
+// the double block the 32 lanes of a warp hold one 128-element outer block.
 // With RESET, this step also ends the OsciReset window: where the new
 // dist_Q exceeds threshold * dist_M, the master weight becomes xhat_t, and
 // both accumulators are written back as zero (the same bits as the separate
 // reset pass after this update).
 template <int FMT, int RND, bool RESET>
-__global__ void __launch_bounds__(kOsciThreads) osci_pass_b(const __grid_constant__ OsciArgs a)
+__global__ void __launch_bounds__(kOsciThreads, kOsciBMinCtas)
+    osci_pass_b(const __grid_constant__ OsciArgs a)
 {
     constexpr int B = FmtInfo<FMT>::B;
-    constexpr int BPTILE = kOsciTileChunks * 4 / B;  // blocks per tile
-    // two blocks in flight per thread, one when dist_M is read as well
-    constexpr int NB = (!RESET && BPTILE >= 2 * kOsciThreads) ? 2 : 1;
-    static_assert(BPTILE % (NB * kOsciThreads) == 0, "tile must split evenly");
+    constexpr int L = B / 4;  // lanes per block
     __shared__ NvTables tab, tabp;  // NVFP4: this step's and the previous step's tensor scale
     const int64_t ntiles = a.tile_start[a.ntensors];
     const PhiloxKey key = philox_key(a.seed);
     int t = 0, t_tab = -1;
     const int lane = threadIdx.x & 31;
+    const int sub = lane & (L - 1);  // this lane's chunk within its block
     unsigned long long cnt = 0;
     for (int64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
         while (a.tile_start[t + 1] <= tile)
             ++t;
         const OsciTensor &T = a.t[t];
-        const int64_t nblk = T.n / B;
-        const int64_t bbeg = (tile - a.tile_start[t]) * BPTILE;
+        const int64_t nch = T.n / 4;
+        const int64_t cbeg = (tile - a.tile_start[t]) * kOsciTileChunks;
         float s_g = 0.0f, inv6 = 0.0f;
         if (FMT == NVFP4) {
             s_g = outer_scale(__ldg(a.amax + t));
@@ -130,140 +197,109 @@ __global__ void __launch_bounds__(kOsciThreads) osci_pass_b(const __grid_constan
                 __syncthreads();
                 t_tab = t;
             }
-            if (bbeg == 0 && threadIdx.x == 0)
+            if (cbeg == 0 && threadIdx.x == 0)
                 T.ntscale[0] = s_g;
         }
-        for (int k = 0; k < BPTILE; k += NB * kOsciThreads) {
-            float v[NB][B], dq[NB][B], dm[NB][B];
-            uint32_t qp[NB][B / 8];
-            uint32_t scp[NB];
-            float so_p[NB];
+        for (int k0 = 0; k0 < kOsciTileChunks; k0 += kOsciThreads * kOsciBU) {
+            float4 w[kOsciBU], dq[kOsciBU], dm[kOsciBU];
+            uint32_t qp[kOsciBU], scp[kOsciBU];
+            float so_p[kOsciBU];
 #pragma unroll
-            for (int j = 0; j < NB; ++j) {
-                const int64_t blk = bbeg + k + j * kOsciThreads + threadIdx.x;
-                if (blk < nblk) {
-#pragma unroll
-                    for (int i = 0; i < B / 4; ++i) {
-                        const float4 w = ldf4_rw(T.master + blk * B + 4 * i);
-                        v[j][4 * i] = w.x;
-                        v[j][4 * i + 1] = w.y;
-                        v[j][4 * i + 2] = w.z;
-                        v[j][4 * i + 3] = w.w;
-                        const float4 d = ldf4_rw(T.dist_q + blk * B + 4 * i);
-                        dq[j][4 * i] = d.x;
-                        dq[j][4 * i + 1] = d.y;
-                        dq[j][4 * i + 2] = d.z;
-                        dq[j][4 * i + 3] = d.w;
-                        if (RESET) {
-                            const float4 e = ldf4_rw(T.dist_m + blk * B + 4 * i);
-                            dm[j][4 * i] = e.x;
-                            dm[j][4 * i + 1] = e.y;
-                            dm[j][4 * i + 2] = e.z;
-                            dm[j][4 * i + 3] = e.w;
-                        }
-                    }
-                    if (B == 16) {
-                        const uint2 p2 = __ldg(reinterpret_cast<const uint2 *>(T.pcodes) + blk);
-                        qp[j][0] = p2.x;
-                        qp[j][1] = p2.y;
-                    } else {
-                        const uint4 p4 = __ldg(reinterpret_cast<const uint4 *>(T.pcodes) + blk);
-                        qp[j][0] = p4.x;
-                        qp[j][1] = p4.y;
-                        qp[j][2] = p4.z;
-                        qp[j][3] = p4.w;
-                    }
-                    scp[j] = __ldg(T.pscales + blk);
-                    so_p[j] = (FMT == NV2L) ? __ldg(T.ptscale + (blk >> 3)) : 0.0f;
+            for (int k = 0; k < kOsciBU; ++k) {
+                const int64_t ch = cbeg + k0 + k * kOsciThreads + threadIdx.x;
+                if (ch < nch) {
+                    w[k] = ldf4_rw(T.master + ch * 4);
+                    dq[k] = ldf4_rw(T.dist_q + ch * 4);
+                    if (RESET)
+                        dm[k] = ldf4_rw(T.dist_m + ch * 4);
+                    qp[k] = __ldg(reinterpret_cast<const uint16_t *>(T.pcodes) + ch);
+                    scp[k] = __ldg(T.pscales + ch / L);
+                    so_p[k] = (FMT == NV2L) ? __ldg(T.ptscale + ch / 32) : 0.0f;
                 } else {
-#pragma unroll
-                    for (int i = 0; i < B; ++i)
-                        v[j][i] = dq[j][i] = dm[j][i] = 0.0f;
-#pragma unroll
-                    for (int w = 0; w < B / 8; ++w)
-                        qp[j][w] = 0;
-                    scp[j] = 0;
-                    so_p[j] = 0.0f;
+                    w[k] = dq[k] = dm[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+                    qp[k] = scp[k] = 0;
+                    so_p[k] = 0.0f;
                 }
             }
 #pragma unroll
-            for (int j = 0; j < NB; ++j) {
-                const int64_t blk = bbeg + k + j * kOsciThreads + threadIdx.x;
-                const bool valid = blk < nblk;
-                float am = 0.0f;
-#pragma unroll
-                for (int i = 0; i < B; ++i)
-                    am = fmaxf(am, fabsf(v[j][i]));
+            for (int k = 0; k < kOsciBU; ++k) {
+                const int64_t ch = cbeg + k0 + k * kOsciThreads + threadIdx.x;
+                const bool valid = ch < nch;  // uniform over a block's lanes (nch % L == 0)
+                const int64_t blk = ch / L;
+                const float v[4] = {w[k].x, w[k].y, w[k].z, w[k].w};
+                float am = fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3])));
+                am = lanes_max<L>(am);
                 float s_o = s_g, inv6b = inv6;
                 if (FMT == NV2L) {
-                    s_o = outer_scale(group_max<8>(am));
+                    s_o = outer_scale(lanes_max<32>(am));
                     inv6b = nv_inv6(s_o);
                 }
                 const Scale sc = block_scale<FMT>(am, s_o, inv6b, &tab);
-                uint32_t q[B / 8];
-                encode_block<B, RND>(v[j], sc, key, (uint64_t)blk * B, 0u, a.offset, q);
+                float y[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                    y[i] = __fmul_rn(v[i], sc.r);
+                if (RND == SR) {
+                    // elements 4ch .. 4ch+3: half ch % 2 of Philox group ch / 2
+                    const uint4 rb = sr_bits8(key, (uint64_t)ch >> 1, 0u, a.offset);
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+                        y[i] = e2m1_sr_value(y[i], u16_of(rb, 4 * (int)(ch & 1) + i));
+                }
+                const uint32_t q = e2m1_rn_pack4(y[0], y[1], y[2], y[3]);
+                uint32_t clip = 0;
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                    clip |= (__float_as_uint(__fsub_rn(sc.lim, fabsf(v[i]))) >> 31) << i;
+                const uint32_t mask = lanes_or<L>((~clip & 15u) << (4 * sub));
                 if (!valid)
                     continue;
-                const float seff_p = (FMT == NVFP4) ? tabp.s_eff[scp[j] & 127u]
-                                                    : stored_s_eff<FMT>(scp[j], so_p[j]);
+                const float seff_p = (FMT == NVFP4) ? tabp.s_eff[scp[k] & 127u]
+                                                    : stored_s_eff<FMT>(scp[k], so_p[k]);
+                float xh[4], xp[4];
+                e2m1_decode4(q, xh);
+                e2m1_decode4(qp[k], xp);
+                const float q4[4] = {dq[k].x, dq[k].y, dq[k].z, dq[k].w};
+                const float m4[4] = {dm[k].x, dm[k].y, dm[k].z, dm[k].w};
+                float dn[4];
                 uint32_t hit = 0;
 #pragma unroll
-                for (int w = 0; w < B / 8; ++w) {
-                    float xh[8], xp[8];
-                    e2m1_decode8(q[w], xh);
-                    e2m1_decode8(qp[j][w], xp);
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) {
-                        xh[i] = __fmul_rn(xh[i], sc.s_eff);
-                        xp[i] = __fmul_rn(xp[i], seff_p);
-                        const float dn =
-                            __fadd_rn(dq[j][w * 8 + i], fabsf(__fsub_rn(xh[i], xp[i])));
-                        if (RESET) {
-                            const int e = w * 8 + i;
-                            if (dn > __fmul_rn(a.threshold, dm[j][e])) {
-                                T.master[blk * B + e] = xh[i];
-                                hit |= 1u << e;
-                            }
-                            dq[j][e] = 0.0f;
-                        } else {
-                            dq[j][w * 8 + i] = dn;
-                        }
-                    }
-                    if (T.xhat) {
-                        if (a.xhat_bf16) {
-                            *reinterpret_cast<uint4 *>((char *)T.xhat + (blk * B + w * 8) * 2) =
-                                make_uint4(bf16x2_rn(xh[0], xh[1]), bf16x2_rn(xh[2], xh[3]),
-                                           bf16x2_rn(xh[4], xh[5]), bf16x2_rn(xh[6], xh[7]));
-                        } else {
-                            float *xo = reinterpret_cast<float *>(T.xhat) + blk * B + w * 8;
-                            stf4(xo, make_float4(xh[0], xh[1], xh[2], xh[3]));
-                            stf4(xo + 4, make_float4(xh[4], xh[5], xh[6], xh[7]));
-                        }
+                for (int i = 0; i < 4; ++i) {
+                    xh[i] = __fmul_rn(xh[i], sc.s_eff);
+                    xp[i] = __fmul_rn(xp[i], seff_p);
+                    dn[i] = __fadd_rn(q4[i], fabsf(__fsub_rn(xh[i], xp[i])));
+                    if (RESET && dn[i] > __fmul_rn(a.threshold, m4[i])) {
+                        T.master[ch * 4 + i] = xh[i];
+                        hit |= 1u << i;
                     }
                 }
-#pragma unroll
-                for (int i = 0; i < B / 4; ++i) {
-                    stf4(T.dist_q + blk * B + 4 * i,
-                         make_float4(dq[j][4 * i], dq[j][4 * i + 1], dq[j][4 * i + 2],
-                                     dq[j][4 * i + 3]));
-                    if (RESET)
-                        stf4(T.dist_m + blk * B + 4 * i, make_float4(0.f, 0.f, 0.f, 0.f));
-                }
-                cnt += __popc(hit);
-                if (B == 16)
-                    reinterpret_cast<uint2 *>(T.ncodes)[blk] = make_uint2(q[0], q[1]);
-                else
-                    reinterpret_cast<uint4 *>(T.ncodes)[blk] = make_uint4(q[0], q[1], q[2], q[3]);
-                T.nscales[blk] = (uint8_t)sc.code;
-                if (FMT == NV2L && (lane & 7) == 0)
-                    T.ntscale[blk >> 3] = s_o;
-                if (T.mask) {
-                    const uint32_t mask = block_mask<B>(v[j], sc.lim);
-                    if (B == 16)
-                        reinterpret_cast<uint16_t *>(T.mask)[blk] = (uint16_t)mask;
+                if (T.xhat) {
+                    if (a.xhat_bf16)
+                        *reinterpret_cast<uint2 *>((char *)T.xhat + ch * 8) =
+                            make_uint2(bf16x2_rn(xh[0], xh[1]), bf16x2_rn(xh[2], xh[3]));
                     else
-                        reinterpret_cast<uint32_t *>(T.mask)[blk] = mask;
+                        stf4(reinterpret_cast<float *>(T.xhat) + ch * 4,
+                             make_float4(xh[0], xh[1], xh[2], xh[3]));
                 }
+                if (RESET) {
+                    stf4(T.dist_q + ch * 4, make_float4(0.f, 0.f, 0.f, 0.f));
+                    stf4(T.dist_m + ch * 4, make_float4(0.f, 0.f, 0.f, 0.f));
+                    cnt += __popc(hit);
+                } else {
+                    stf4(T.dist_q + ch * 4, make_float4(dn[0], dn[1], dn[2], dn[3]));
+                }
+                reinterpret_cast<uint16_t *>(T.ncodes)[ch] = (uint16_t)q;
+                if (sub == 0) {
+                    T.nscales[blk] = (uint8_t)sc.code;
+                    if (T.mask) {
+                        if (B == 16)
+                            reinterpret_cast<uint16_t *>(T.mask)[blk] = (uint16_t)mask;
+                        else
+                            reinterpret_cast<uint32_t *>(T.mask)[blk] = mask;
+                    }
+                }
+                if (FMT == NV2L && lane == 0)
+                    T.ntscale[ch / 32] = s_o;
             }
         }
     }

@@ -18,6 +18,17 @@
 namespace fqk {
 
 constexpr int kThreads = 256;
+// CTAs per SM the register allocation must allow, measured: row kernels 4
+// (at most 64 registers; the double-block SR call 3-4% faster despite a few
+// spills), the MXFP4 and double-block tile kernels 3 (the Hadamard-transformed
+// SR call 2% faster); the NVFP4 tile kernel is left free (at 64 registers its
+// spills cost more than the occupancy gains).
+constexpr int kRowMinCtas = 4;
+template <int FMT>
+constexpr int tile_min_ctas()
+{
+    return FMT == NVFP4 ? 1 : 3;
+}
 
 // ------------------------------------------------------------------ amax
 template <typename T>
@@ -140,7 +151,7 @@ __device__ __forceinline__ void row_block(float *v, int64_t blk, bool valid, flo
 // One thread per block; each iteration a thread holds BPT blocks' loads in
 // flight (about 64 bytes).
 template <typename T, int FMT, int RND>
-__global__ void __launch_bounds__(kThreads) row_kernel(RowArgs a)
+__global__ void __launch_bounds__(kThreads, kRowMinCtas) row_kernel(RowArgs a)
 {
     constexpr int B = FmtInfo<FMT>::B;
     constexpr int BPT = (B * sizeof(T) >= 64) ? 1 : 2;
@@ -201,7 +212,7 @@ constexpr size_t tile_smem_bytes()
 }
 
 template <typename T, int FMT, int RND>
-__global__ void __launch_bounds__(kThreads) tile_kernel(TileArgs a)
+__global__ void __launch_bounds__(kThreads, tile_min_ctas<FMT>()) tile_kernel(TileArgs a)
 {
     using S = TileShape<FMT>;
     constexpr int E = VecInfo<T>::E;

@@ -20,14 +20,14 @@ namespace fqk {
 constexpr int kThreads = 256;
 // CTAs per SM the register allocation must allow, measured: row kernels 4
 // (at most 64 registers; the double-block SR call 3-4% faster despite a few
-// spills), the MXFP4 and double-block tile kernels 3 (the Hadamard-transformed
-// SR call 2% faster); the NVFP4 tile kernel is left free (at 64 registers its
-// spills cost more than the occupancy gains).
+// spills), BF16 tile kernels 3 (80 registers; the Hadamard-transformed SR call
+// 2% faster, the NVFP4 row + column call 1.5%).  The FP32 tile kernels, whose
+// tiles need far more registers, are left free.
 constexpr int kRowMinCtas = 4;
-template <int FMT>
+template <typename T, int FMT>
 constexpr int tile_min_ctas()
 {
-    return FMT == NVFP4 ? 1 : 3;
+    return sizeof(T) == 2 ? 3 : 1;
 }
 
 // ------------------------------------------------------------------ amax
@@ -212,7 +212,7 @@ constexpr size_t tile_smem_bytes()
 }
 
 template <typename T, int FMT, int RND>
-__global__ void __launch_bounds__(kThreads, tile_min_ctas<FMT>()) tile_kernel(TileArgs a)
+__global__ void __launch_bounds__(kThreads, tile_min_ctas<T, FMT>()) tile_kernel(TileArgs a)
 {
     using S = TileShape<FMT>;
     constexpr int E = VecInfo<T>::E;
@@ -306,7 +306,21 @@ __global__ void __launch_bounds__(kThreads, tile_min_ctas<FMT>()) tile_kernel(Ti
     }
     __syncthreads();
 
-    // Phase 2: column blocks (BC rows x 1 column) out of shared memory.
+    // Phase 2: column blocks (BC rows x 1 column) out of shared memory.  BF16
+    // NVFP4 tiles are read two columns at a time (one 32-bit word per row).
+    const uint32_t *tile32 = reinterpret_cast<const uint32_t *>(tile);
+    auto col_amax = [&](float *w) {  // double block: inner amax for the outer scale
+        if (rht) {
+#pragma unroll
+            for (int j = 0; j < BC / 16; ++j)
+                rht16(w + 16 * j, signs);
+        }
+        float m = 0.0f;
+#pragma unroll
+        for (int i = 0; i < BC; ++i)
+            m = fmaxf(m, fabsf(w[i]));
+        return m;
+    };
     if (FMT == NV2L) {
         for (int task = threadIdx.x; task < TC * NRB; task += kThreads) {
             const int c = task % TC, rb = task / TC;
@@ -314,28 +328,13 @@ __global__ void __launch_bounds__(kThreads, tile_min_ctas<FMT>()) tile_kernel(Ti
 #pragma unroll
             for (int i = 0; i < BC; ++i)
                 w[i] = static_cast<float>(tile[(rb * BC + i) * TC + c]);
-            if (rht) {
-#pragma unroll
-                for (int j = 0; j < BC / 16; ++j)
-                    rht16(w + 16 * j, signs);
-            }
-            float m = 0.0f;
-#pragma unroll
-            for (int i = 0; i < BC; ++i)
-                m = fmaxf(m, fabsf(w[i]));
-            am16[rb * TC + c] = m;
+            am16[rb * TC + c] = col_amax(w);
         }
         __syncthreads();
     }
-    for (int task = threadIdx.x; task < TC * NRB; task += kThreads) {
-        const int c = task % TC, rb = task / TC;
+    // quantize column block (c, rb) of the tile, held in v, into the staging buffers
+    auto col_quant = [&](int c, int rb, float *v) {
         const int64_t gc = c0 + c, gr0 = r0 + (int64_t)rb * BC;
-        if (gc >= cols || gr0 >= rows)
-            continue;
-        float v[BC];
-#pragma unroll
-        for (int i = 0; i < BC; ++i)
-            v[i] = static_cast<float>(tile[(rb * BC + i) * TC + c]);
         if (FMT != NVFP4 && rht) {
 #pragma unroll
             for (int j = 0; j < BC / 16; ++j)
@@ -366,6 +365,38 @@ __global__ void __launch_bounds__(kThreads, tile_min_ctas<FMT>()) tile_kernel(Ti
         for (int w = 0; w < BC / 8; ++w)
             dst[w] = q[w];
         css[c * NRB + rb] = (uint8_t)sc.code;
+    };
+    if constexpr (sizeof(T) == 2 && FMT == NVFP4) {
+        // cols is a multiple of the row block, hence even: a pair is all in or out
+        for (int task = threadIdx.x; task < (TC / 2) * NRB; task += kThreads) {
+            const int c = 2 * (task % (TC / 2)), rb = task / (TC / 2);
+            if (c0 + c >= cols || r0 + (int64_t)rb * BC >= rows)
+                continue;
+            uint32_t wd[BC];
+            float v[BC];
+#pragma unroll
+            for (int i = 0; i < BC; ++i)
+                wd[i] = tile32[((rb * BC + i) * TC + c) / 2];
+#pragma unroll
+            for (int i = 0; i < BC; ++i)
+                v[i] = __uint_as_float(wd[i] << 16);
+            col_quant(c, rb, v);
+#pragma unroll
+            for (int i = 0; i < BC; ++i)
+                v[i] = __uint_as_float(wd[i] & 0xFFFF0000u);
+            col_quant(c + 1, rb, v);
+        }
+    } else {
+        for (int task = threadIdx.x; task < TC * NRB; task += kThreads) {
+            const int c = task % TC, rb = task / TC;
+            if (c0 + c >= cols || r0 + (int64_t)rb * BC >= rows)
+                continue;
+            float v[BC];
+#pragma unroll
+            for (int i = 0; i < BC; ++i)
+                v[i] = static_cast<float>(tile[(rb * BC + i) * TC + c]);
+            col_quant(c, rb, v);
+        }
     }
     __syncthreads();
 

@@ -296,10 +296,16 @@ __device__ __forceinline__ void rht16(float *z, uint32_t signs)
         z[i] = __fmul_rn(z[i], 0.25f);
 }
 
-__device__ __forceinline__ uint32_t u16_of(const uint4 &w, int j)
+// The stochastic-rounding operand of element j (0..7) of a Philox draw: its
+// 16-bit uniform u (half j % 2 of word j / 2) as c = (2^22 - 1 - 64 u) / 2^23,
+// exactly (see e2m1_sr_value).  2^23 + u is assembled as an FP32 bit pattern
+// by a byte permute, so no integer-to-float conversion is needed.
+__device__ __forceinline__ float sr_operand(const uint4 &w, int j)
 {
     const uint32_t word = (j >> 1) == 0 ? w.x : (j >> 1) == 1 ? w.y : (j >> 1) == 2 ? w.z : w.w;
-    return (j & 1) ? (word >> 16) : (word & 0xFFFFu);
+    const uint32_t bits = __byte_perm(word, 0x4B000000u, (j & 1) ? 0x7632u : 0x7610u);
+    const float u = __fsub_rn(__uint_as_float(bits), 8388608.0f);  // exact
+    return __fmaf_rn(u, -7.62939453125e-06f, 0.49999988079071044921875f);  // exact
 }
 
 // ---------------------------------------------------------------- misc
@@ -344,25 +350,31 @@ __device__ __forceinline__ void e2m1_decode8(uint32_t q, float *out)
 
 // Stochastic rounding of y to the E2M1 grid given a 16-bit uniform u, as an
 // FP32 value on the grid (values at or above 6 come out >= 6 and saturate in
-// the final conversion).  With lo the grid magnitude at or below |y| and frac
-// its position in the gap, the result rounds up iff u < frac * 65536.
-//  |y| >= 1: the grid keeps one mantissa bit, frac * 65536 is the 22 dropped
-//    mantissa bits / 64, so adding 2^22 - 1 - 64u below the kept bit and
-//    truncating rounds up exactly when those bits exceed 64u.
-//  |y| < 1: the grid steps are 0.5, so with D = ceil(|y| * 2^17) the number of
-//    steps is (D + 65535 - u) >> 16 (D is exact: a power-of-two scaling).
-__device__ __forceinline__ float e2m1_sr_value(float y, uint32_t u)
+// the final conversion).  With lo the grid magnitude at or below a = |y|, g
+// the gap above it and F = 65536 (a - lo) / g, the result rounds up iff u < F.
+// The work is floating-point, with c = (2^22 - 1 - 64 u) / 2^23 from
+// sr_operand, so that 2c = 1 - (u + 2^-6) / 65536:
+//  a >= 1: g = 2^(e-1) for a in [2^e, 2^(e+1)), and F is a multiple of 2^-6
+//    (a has 23 fraction bits), so u < F iff (a - lo) / g + 2c >= 1.  Hence
+//    t = a + 2^e c, rounded toward zero (which never crosses a grid point:
+//    they are representable) and cut to one mantissa bit, is lo or lo + g; a
+//    sum that crosses into the next binade comes out as its first grid point,
+//    2^(e+1) = lo + g.
+//  a < 1: g = 1/2, as on [1, 2), so the same is done for z = 1 + a rounded
+//    up, and the 1 is subtracted again.  Rounding up moves F only up to the
+//    next multiple of 2^-6, which decides u < F the same way for every
+//    integer u; a z of 2 rounds up, as then F > 65536 - 2^-6.
+// The sign of y is copied (a zero result keeps it).
+__device__ __forceinline__ float e2m1_sr_value(float y, float c)
 {
-    const uint32_t b = __float_as_uint(y);
     const float a = fabsf(y);
-    const uint32_t hi = (b + (0x3FFFFFu - (u << 6))) & 0xFFC00000u;
-    // 2^23 + ceil(|y| * 2^17): an exact product, one upward rounding in the add
-    const uint32_t cb = __float_as_uint(__fmaf_ru(a, 131072.0f, 8388608.0f));
-    const uint32_t n = (cb - 0x4B000000u + 65535u - u) >> 16;
-    // n half-steps as a value: 0.5 n, except that n = 0 gives 0.25, which the
-    // final nearest-even conversion sends to (signed) zero
-    const uint32_t lo = ((n << 23) + 0x3E800000u) | (b & 0x80000000u);
-    return __uint_as_float(a < 1.0f ? lo : hi);
+    const float q = (a < 1.0f) ? 1.0f : 0.0f;
+    const float z = __fadd_ru(a, q);                                     // a + 1 or a
+    const float p = __uint_as_float(__float_as_uint(z) & 0x7F800000u);   // 2^e of z
+    const float t = __fmaf_rz(c, p, z);
+    const float m = __uint_as_float(__float_as_uint(t) & 0xFFC00000u);   // on the grid
+    const float r = __fsub_rn(m, q);                                     // exact
+    return __uint_as_float(__float_as_uint(r) | (__float_as_uint(y) & 0x80000000u));
 }
 
 // Encode B values (already loaded as FP32) of one block under scale sc into
@@ -384,7 +396,7 @@ __device__ __forceinline__ void encode_block(const float *v, const Scale &sc, co
             const uint4 rb = sr_bits8(key, (e0 >> 3) + w, stream_id, offset);
 #pragma unroll
             for (int i = 0; i < 8; ++i)
-                y[i] = e2m1_sr_value(y[i], u16_of(rb, i));
+                y[i] = e2m1_sr_value(y[i], sr_operand(rb, i));
         }
         q[w] = e2m1_rn_pack8(y);
     }

@@ -244,7 +244,7 @@ __global__ void __launch_bounds__(kOsciThreads, kOsciBMinCtas)
                     const uint4 rb = sr_bits8(key, (uint64_t)ch >> 1, 0u, a.offset);
 #pragma unroll
                     for (int i = 0; i < 4; ++i)
-                        y[i] = e2m1_sr_value(y[i], u16_of(rb, 4 * (int)(ch & 1) + i));
+                        y[i] = e2m1_sr_value(y[i], sr_operand(rb, 4 * (int)(ch & 1) + i));
                 }
                 const uint32_t q = e2m1_rn_pack4(y[0], y[1], y[2], y[3]);
                 uint32_t clip = 0;

@@ -74,6 +74,37 @@ __device__ __forceinline__ float ex2(float x)
     return y;
 }
 
+// Packed FP32 pairs (the f32x2 forms): one instruction for two lanes, each
+// rounded exactly as the scalar operation would be.
+__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c)
+{
+    float2 d;
+    asm("{\n\t.reg .b64 A, B, C, D;\n\t"
+        "mov.b64 A, {%2, %3};\n\tmov.b64 B, {%4, %5};\n\tmov.b64 C, {%6, %7};\n\t"
+        "fma.rn.f32x2 D, A, B, C;\n\tmov.b64 {%0, %1}, D;\n\t}"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+    return d;
+}
+
+#define FQK_F32X2_BINARY(name, op)                                                          \
+    __device__ __forceinline__ float2 name(float2 a, float2 b)                              \
+    {                                                                                       \
+        float2 d;                                                                           \
+        asm("{\n\t.reg .b64 A, B, D;\n\t"                                                   \
+            "mov.b64 A, {%2, %3};\n\tmov.b64 B, {%4, %5};\n\t" op                           \
+            ".rn.f32x2 D, A, B;\n\tmov.b64 {%0, %1}, D;\n\t}"                               \
+            : "=f"(d.x), "=f"(d.y)                                                          \
+            : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));                                      \
+        return d;                                                                           \
+    }
+FQK_F32X2_BINARY(add2, "add")
+FQK_F32X2_BINARY(sub2, "sub")
+FQK_F32X2_BINARY(mul2, "mul")
+#undef FQK_F32X2_BINARY
+
+__device__ __forceinline__ float2 ex2x2(float2 x) { return make_float2(ex2(x.x), ex2(x.y)); }
+
 // Running maxima of a chunk of teacher and student logits.  BF16 pairs are
 // compared packed (the maximum of BF16 values is one of them, exactly).
 template <typename T, int NT>
@@ -261,18 +292,20 @@ __global__ void __launch_bounds__(NT, 1024 / NT) qad_kl_kernel(const KlArgs a)
         const float2 m = cta_max2<NW>(lm.x, lm.y, red);
         const float m2t = m.x * k2, m2s = m.y * k2;
         // sweep 2: sums of 2^(a - M) under this CTA's maxima
-        float st = 0.0f, ss = 0.0f;
+        const float2 vk2 = make_float2(k2, k2);
+        const float2 nmt = make_float2(-m2t, -m2t), nms = make_float2(-m2s, -m2s);
+        float2 st2 = make_float2(0.0f, 0.0f), ss2 = make_float2(0.0f, 0.0f);
         for (int g = threadIdx.x; g < ng; g += NT) {
             float v[8], w[8];
             lds8<T>(bt, g, v);
             lds8<T>(bs, g, w);
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                st += ex2(fmaf(v[i], k2, -m2t));
-                ss += ex2(fmaf(w[i], k2, -m2s));
+            for (int i = 0; i < 8; i += 2) {
+                st2 = add2(st2, ex2x2(fma2(make_float2(v[i], v[i + 1]), vk2, nmt)));
+                ss2 = add2(ss2, ex2x2(fma2(make_float2(w[i], w[i + 1]), vk2, nms)));
             }
         }
-        const float2 s = cta_sum2<NW>(st, ss, red);
+        const float2 s = cta_sum2<NW>(st2.x + st2.y, ss2.x + ss2.y, red);
         // push this CTA's partials into every CTA of the cluster (lane r -> rank r)
         if (threadIdx.x < C)
             dsmem_st_f4(&part1[it & 1][rank], (uint32_t)threadIdx.x,
@@ -300,7 +333,10 @@ __global__ void __launch_bounds__(NT, 1024 / NT) qad_kl_kernel(const KlArgs a)
         __syncthreads();
         const float gt = comb.x, gs = comb.y, l2t = comb.z, l2s = comb.w;
         // sweep 3: p, q, the KL terms and the gradient, part by part
-        float kl = 0.0f;
+        const float2 ngt = make_float2(-gt, -gt), ngs = make_float2(-gs, -gs);
+        const float2 vl2t = make_float2(l2t, l2t), vl2s = make_float2(l2s, l2s);
+        const float2 vgk = make_float2(gk, gk);
+        float2 kl2 = make_float2(0.0f, 0.0f);
         char *dzrow = a.dz ? (char *)a.dz + (row * a.vocab + c0) * (a.dz_bf16 ? 2 : 4) : nullptr;
         for (int part = 0; part < kKlParts; ++part) {
             const int g1 = gpart(part + 1);
@@ -309,15 +345,18 @@ __global__ void __launch_bounds__(NT, 1024 / NT) qad_kl_kernel(const KlArgs a)
                 lds8<T>(bt, g, v);
                 lds8<T>(bs, g, w);
 #pragma unroll
-                for (int i = 0; i < 8; ++i) {
+                for (int i = 0; i < 8; i += 2) {
                     // log2 p and log2 q relative to each row's own maximum: small
                     // for every token that matters, whatever the logits' offset
-                    const float lp = fmaf(v[i], k2, -gt) - l2t;
-                    const float lq = fmaf(w[i], k2, -gs) - l2s;
-                    const float p = ex2(lp);
-                    kl = fmaf(p, lp - lq, kl);
-                    if (dzrow)
-                        o[i] = gk * (ex2(lq) - p);
+                    const float2 lp = sub2(fma2(make_float2(v[i], v[i + 1]), vk2, ngt), vl2t);
+                    const float2 lq = sub2(fma2(make_float2(w[i], w[i + 1]), vk2, ngs), vl2s);
+                    const float2 p = ex2x2(lp);
+                    kl2 = fma2(p, sub2(lp, lq), kl2);
+                    if (dzrow) {
+                        const float2 d = mul2(vgk, sub2(ex2x2(lq), p));
+                        o[i] = d.x;
+                        o[i + 1] = d.y;
+                    }
                 }
                 if (dzrow) {
                     if (a.dz_bf16) {
@@ -340,7 +379,7 @@ __global__ void __launch_bounds__(NT, 1024 / NT) qad_kl_kernel(const KlArgs a)
                 }
             }
         }
-        const float2 k = cta_sum2<NW>(kl, 0.0f, red);  // also: every thread is done with the last part
+        const float2 k = cta_sum2<NW>(kl2.x + kl2.y, 0.0f, red);  // also: every thread is done with the last part
         if (threadIdx.x == 0) {
             dsmem_st_f32(&part2[it & 1][rank], 0u, k.x);  // to rank 0
             if (!dead && next < a.rows) {

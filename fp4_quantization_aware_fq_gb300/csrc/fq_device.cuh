@@ -39,6 +39,40 @@ struct VecInfo<__nv_bfloat16> {
     static constexpr int E = 8;
 };
 
+// ---------------------------------------------------------------- packed FP32 pairs
+// Blackwell's f32x2 forms: one instruction for two lanes, each rounded exactly
+// as the scalar operation with the same rounding mode would be.
+#define FQK_F32X2_TERNARY(name, op)                                                         \
+    __device__ __forceinline__ float2 name(float2 a, float2 b, float2 c)                    \
+    {                                                                                       \
+        float2 d;                                                                           \
+        asm("{\n\t.reg .b64 A, B, C, D;\n\t"                                                \
+            "mov.b64 A, {%2, %3};\n\tmov.b64 B, {%4, %5};\n\tmov.b64 C, {%6, %7};\n\t" op  \
+            " D, A, B, C;\n\tmov.b64 {%0, %1}, D;\n\t}"                                     \
+            : "=f"(d.x), "=f"(d.y)                                                          \
+            : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));                  \
+        return d;                                                                           \
+    }
+#define FQK_F32X2_BINARY(name, op)                                                          \
+    __device__ __forceinline__ float2 name(float2 a, float2 b)                              \
+    {                                                                                       \
+        float2 d;                                                                           \
+        asm("{\n\t.reg .b64 A, B, D;\n\t"                                                   \
+            "mov.b64 A, {%2, %3};\n\tmov.b64 B, {%4, %5};\n\t" op                           \
+            " D, A, B;\n\tmov.b64 {%0, %1}, D;\n\t}"                                        \
+            : "=f"(d.x), "=f"(d.y)                                                          \
+            : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));                                      \
+        return d;                                                                           \
+    }
+FQK_F32X2_TERNARY(fma2, "fma.rn.f32x2")
+FQK_F32X2_TERNARY(fma2_rz, "fma.rz.f32x2")
+FQK_F32X2_BINARY(add2, "add.rn.f32x2")
+FQK_F32X2_BINARY(add2_ru, "add.rp.f32x2")
+FQK_F32X2_BINARY(sub2, "sub.rn.f32x2")
+FQK_F32X2_BINARY(mul2, "mul.rn.f32x2")
+#undef FQK_F32X2_TERNARY
+#undef FQK_F32X2_BINARY
+
 // ---------------------------------------------------------------- loads
 __device__ __forceinline__ uint4 ld16(const void *p)
 {
@@ -377,6 +411,33 @@ __device__ __forceinline__ float e2m1_sr_value(float y, float c)
     return __uint_as_float(__float_as_uint(r) | (__float_as_uint(y) & 0x80000000u));
 }
 
+// sr_operand for elements 2k and 2k + 1 (both halves of word k).
+__device__ __forceinline__ float2 sr_operand2(uint32_t word)
+{
+    const float2 b = make_float2(__uint_as_float(__byte_perm(word, 0x4B000000u, 0x7610u)),
+                                 __uint_as_float(__byte_perm(word, 0x4B000000u, 0x7632u)));
+    const float2 u = sub2(b, make_float2(8388608.0f, 8388608.0f));  // exact
+    return fma2(u, make_float2(-7.62939453125e-06f, -7.62939453125e-06f),
+                make_float2(0.49999988079071044921875f, 0.49999988079071044921875f));
+}
+
+// e2m1_sr_value on a pair, the floating-point steps in packed form.
+__device__ __forceinline__ float2 e2m1_sr_value2(float2 y, float2 c)
+{
+    const float2 a = make_float2(fabsf(y.x), fabsf(y.y));
+    const float2 q = make_float2(a.x < 1.0f ? 1.0f : 0.0f, a.y < 1.0f ? 1.0f : 0.0f);
+    const float2 z = add2_ru(a, q);
+    const float2 p = make_float2(__uint_as_float(__float_as_uint(z.x) & 0x7F800000u),
+                                 __uint_as_float(__float_as_uint(z.y) & 0x7F800000u));
+    const float2 t = fma2_rz(c, p, z);
+    const float2 m = make_float2(__uint_as_float(__float_as_uint(t.x) & 0xFFC00000u),
+                                 __uint_as_float(__float_as_uint(t.y) & 0xFFC00000u));
+    const float2 r = sub2(m, q);
+    return make_float2(
+        __uint_as_float(__float_as_uint(r.x) | (__float_as_uint(y.x) & 0x80000000u)),
+        __uint_as_float(__float_as_uint(r.y) | (__float_as_uint(y.y) & 0x80000000u)));
+}
+
 // Encode B values (already loaded as FP32) of one block under scale sc into
 // B/8 words of packed codes, and the block's STE mask bits (bit i = element i
 // inside [-6 s_eff, 6 s_eff]).  e0 is the flat index of the block's first
@@ -386,17 +447,26 @@ __device__ __forceinline__ void encode_block(const float *v, const Scale &sc, co
                                              uint64_t e0, uint32_t stream_id, uint32_t offset,
                                              uint32_t *q)
 {
+    const float2 r2 = make_float2(sc.r, sc.r);
 #pragma unroll
     for (int w = 0; w < B / 8; ++w) {
         float y[8];
 #pragma unroll
-        for (int i = 0; i < 8; ++i)
-            y[i] = __fmul_rn(v[w * 8 + i], sc.r);
+        for (int i = 0; i < 8; i += 2) {
+            const float2 p = mul2(make_float2(v[w * 8 + i], v[w * 8 + i + 1]), r2);
+            y[i] = p.x;
+            y[i + 1] = p.y;
+        }
         if (RND == SR) {
             const uint4 rb = sr_bits8(key, (e0 >> 3) + w, stream_id, offset);
+            const uint32_t words[4] = {rb.x, rb.y, rb.z, rb.w};
 #pragma unroll
-            for (int i = 0; i < 8; ++i)
-                y[i] = e2m1_sr_value(y[i], sr_operand(rb, i));
+            for (int k = 0; k < 4; ++k) {
+                const float2 s = e2m1_sr_value2(make_float2(y[2 * k], y[2 * k + 1]),
+                                                sr_operand2(words[k]));
+                y[2 * k] = s.x;
+                y[2 * k + 1] = s.y;
+            }
         }
         q[w] = e2m1_rn_pack8(y);
     }

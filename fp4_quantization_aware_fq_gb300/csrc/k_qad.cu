@@ -74,35 +74,6 @@ __device__ __forceinline__ float ex2(float x)
     return y;
 }
 
-// Packed FP32 pairs (the f32x2 forms): one instruction for two lanes, each
-// rounded exactly as the scalar operation would be.
-__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c)
-{
-    float2 d;
-    asm("{\n\t.reg .b64 A, B, C, D;\n\t"
-        "mov.b64 A, {%2, %3};\n\tmov.b64 B, {%4, %5};\n\tmov.b64 C, {%6, %7};\n\t"
-        "fma.rn.f32x2 D, A, B, C;\n\tmov.b64 {%0, %1}, D;\n\t}"
-        : "=f"(d.x), "=f"(d.y)
-        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
-    return d;
-}
-
-#define FQK_F32X2_BINARY(name, op)                                                          \
-    __device__ __forceinline__ float2 name(float2 a, float2 b)                              \
-    {                                                                                       \
-        float2 d;                                                                           \
-        asm("{\n\t.reg .b64 A, B, D;\n\t"                                                   \
-            "mov.b64 A, {%2, %3};\n\tmov.b64 B, {%4, %5};\n\t" op                           \
-            ".rn.f32x2 D, A, B;\n\tmov.b64 {%0, %1}, D;\n\t}"                               \
-            : "=f"(d.x), "=f"(d.y)                                                          \
-            : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));                                      \
-        return d;                                                                           \
-    }
-FQK_F32X2_BINARY(add2, "add")
-FQK_F32X2_BINARY(sub2, "sub")
-FQK_F32X2_BINARY(mul2, "mul")
-#undef FQK_F32X2_BINARY
-
 __device__ __forceinline__ float2 ex2x2(float2 x) { return make_float2(ex2(x.x), ex2(x.y)); }
 
 // Running maxima of a chunk of teacher and student logits.  BF16 pairs are

@@ -311,23 +311,39 @@ __device__ __forceinline__ uint32_t rht_signs(uint32_t rht_seed, uint32_t offset
 
 __device__ __forceinline__ void rht16(float *z, uint32_t signs)
 {
+    // Strides 1, 2 and 4 on packed pairs (z[i], z[i + 8]), two butterflies per
+    // instruction; stride 8 combines the two halves of each pair; then the
+    // scaling on pairs (z[2k], z[2k + 1]).  Every element sees the same FP32
+    // additions in the same order as the scalar butterflies.
+    float2 p[8];
 #pragma unroll
-    for (int i = 0; i < 16; ++i)
-        z[i] = __uint_as_float(__float_as_uint(z[i]) ^ (((signs >> i) & 1u) << 31));
+    for (int i = 0; i < 8; ++i)
+        p[i] = make_float2(
+            __uint_as_float(__float_as_uint(z[i]) ^ (((signs >> i) & 1u) << 31)),
+            __uint_as_float(__float_as_uint(z[i + 8]) ^ (((signs >> (i + 8)) & 1u) << 31)));
 #pragma unroll
-    for (int h = 1; h < 16; h *= 2) {
+    for (int h = 1; h < 8; h *= 2) {
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
+        for (int i = 0; i < 8; ++i) {
             if (i & h)
                 continue;
-            const float a = z[i], b = z[i + h];
-            z[i] = __fadd_rn(a, b);
-            z[i + h] = __fsub_rn(a, b);
+            const float2 a = p[i], b = p[i + h];
+            p[i] = add2(a, b);
+            p[i + h] = sub2(a, b);
         }
     }
 #pragma unroll
-    for (int i = 0; i < 16; ++i)
-        z[i] = __fmul_rn(z[i], 0.25f);
+    for (int i = 0; i < 8; ++i) {
+        z[i] = __fadd_rn(p[i].x, p[i].y);
+        z[i + 8] = __fsub_rn(p[i].x, p[i].y);
+    }
+    const float2 quarter = make_float2(0.25f, 0.25f);
+#pragma unroll
+    for (int i = 0; i < 16; i += 2) {
+        const float2 q = mul2(make_float2(z[i], z[i + 1]), quarter);
+        z[i] = q.x;
+        z[i + 1] = q.y;
+    }
 }
 
 // The stochastic-rounding operand of element j (0..7) of a Philox draw: its

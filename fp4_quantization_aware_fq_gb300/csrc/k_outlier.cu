@@ -110,6 +110,7 @@ __global__ void __launch_bounds__(kOutThreads) channel_amax_kernel(const void *_
 // indices in ascending order.
 constexpr int kSelThreads = 1024;
 constexpr int kMaxOutWords = 4096;  // channels up to 131072
+constexpr int64_t kFastKept = 8192;  // retained channels listed in shared memory
 
 __device__ __forceinline__ uint64_t channel_key(const float *amax, int c)
 {
@@ -246,15 +247,26 @@ __device__ __forceinline__ float ld_scalar<__nv_bfloat16>(const void *x, int64_t
 // (an L1 hit: the owner has just loaded it), writes the FP8 code and the
 // kept value of xhat, and patches the owner's mask bits in shared memory.
 template <typename T, int FMT, int RND>
-__global__ void __launch_bounds__(kOutThreads) outlier_row_kernel(OutlierArgs a)
+__global__ void __launch_bounds__(kOutThreads) outlier_row_kernel(OutlierArgs a, int fast)
 {
     constexpr int B = FmtInfo<FMT>::B;
     __shared__ NvTables tab;
     __shared__ int pre[kMaxOutWords];
     __shared__ uint32_t mstage[kOutThreads];
+    extern __shared__ int kcols[];  // fast: the retained columns in ascending order
     const int64_t cols = a.cols, rows = a.rows;
     const int nwords = (int)((cols + 31) / 32);
+    const int kk = (int)a.k;
     popc_prefix<kOutThreads>(a.bitmap, nwords, pre);
+    if (fast) {
+        for (int w = threadIdx.x; w < nwords; w += kOutThreads) {
+            uint32_t wd = __ldg(a.bitmap + w);
+            for (int idx = pre[w]; wd; wd &= wd - 1u, ++idx)
+                if (idx < kk)
+                    kcols[idx] = 32 * w + __ffs(wd) - 1;
+        }
+        __syncthreads();
+    }
     float s_g = 0.0f, inv6 = 0.0f;
     if (FMT == NVFP4) {
         s_g = outer_scale(*a.amax);
@@ -347,6 +359,58 @@ __global__ void __launch_bounds__(kOutThreads) outlier_row_kernel(OutlierArgs a)
             }
         }
         // ---- the warp's kept elements, one per lane
+        if (fast) {
+            // The warp's 32 blocks are one span of 32 B columns of one row (a row
+            // holds a whole number of spans): its retained elements are the
+            // slice [s0, s1) of the sorted column list, their ranks s0 .. s1 - 1.
+            mstage[threadIdx.x] = mask;
+            __syncwarp();  // also orders the owners' xhat stores before the patches
+            const int64_t blk0 = base + wbase;
+            if (blk0 < nblk) {  // warp-uniform: the span is all in or all out
+                const int64_t r_w = blk0 / bpr;
+                const int64_t cspan = (blk0 - r_w * bpr) * B;
+                const int64_t cend = cspan + 32 * B;
+                const int s0 = pre[cspan >> 5];
+                int s1 = cend >= cols ? kk : pre[cend >> 5];
+                s1 = s1 < kk ? s1 : kk;
+                for (int t = s0 + lane; t < s1; t += 32) {
+                    const int c = kcols[t];
+                    const int owner = (int)((c - cspan) / B), i = (int)((c - cspan) % B);
+                    const int64_t e = r_w * cols + c;
+                    const float xv = ld_scalar<T>(a.x, e);
+                    const float sj = __ldg(a.fp8_scale + t);
+                    const float rcp = (sj == 0.0f) ? 0.0f : __frcp_rn(sj);
+                    const float y = __fmul_rn(xv, rcp);
+                    const uint32_t code =
+                        e4m3_rn_sat(fabsf(y)) | ((__float_as_uint(y) >> 24) & 0x80u);
+                    if (a.fp8)
+                        a.fp8[r_w * a.k + t] = (uint8_t)code;
+                    if (a.xhat) {
+                        const float m = __fmul_rn(e4m3_value(code & 0x7Fu), sj);
+                        const float h = (code & 0x80u) ? -m : m;
+                        if (a.xhat_bf16)
+                            reinterpret_cast<unsigned short *>(a.xhat)[e] =
+                                (unsigned short)(bf16x2_rn(h, 0.0f) & 0xFFFFu);
+                        else
+                            reinterpret_cast<float *>(a.xhat)[e] = h;
+                    }
+                    const uint32_t bit = 1u << i;
+                    if (fabsf(xv) <= __fmul_rn(448.0f, sj))
+                        atomicOr(&mstage[wbase + owner], bit);
+                    else
+                        atomicAnd(&mstage[wbase + owner], ~bit);
+                }
+            }
+            __syncwarp();
+            mask = mstage[threadIdx.x];
+            if (valid && a.mask) {
+                if (B == 16)
+                    reinterpret_cast<uint16_t *>(a.mask)[blk] = (uint16_t)mask;
+                else
+                    reinterpret_cast<uint32_t *>(a.mask)[blk] = mask;
+            }
+            continue;
+        }
         const uint32_t cnt = valid ? (uint32_t)__popc(ret) : 0u;
         uint32_t incl = cnt;
 #pragma unroll
@@ -480,8 +544,19 @@ static cudaError_t outlier_go(const OutlierArgs &a, cudaStream_t s)
     const int64_t nblk = a.rows * (a.cols / B);
     if (nblk == 0)
         return cudaSuccess;
+    // the sorted-list path: the list fits in shared memory and every row is a
+    // whole number of 32-block warp spans
+    const int fast = a.k > 0 && a.k <= kFastKept && (a.cols / B) % 32 == 0;
+    const size_t smem = fast ? (size_t)a.k * sizeof(int) : 0;
+    if (smem) {
+        const cudaError_t e = cudaFuncSetAttribute(outlier_row_kernel<T, FMT, RND>,
+                                                   cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                   (int)smem);
+        if (e != cudaSuccess)
+            return e;
+    }
     outlier_row_kernel<T, FMT, RND><<<grid_cap((nblk + kOutThreads - 1) / kOutThreads, 8),
-                                      kOutThreads, 0, s>>>(a);
+                                      kOutThreads, smem, s>>>(a, fast);
     return cudaGetLastError();
 }
 

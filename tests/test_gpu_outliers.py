@@ -122,6 +122,44 @@ def test_quantize_outliers_small(dtype, fmt, rnd):
     _outlier_parity(x.to(DEV), sel, fmt, rnd, seed=0xF00D, offset=11)
 
 
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+@pytest.mark.parametrize("fmt", [fq.NVFP4, fq.MXFP4, fq.NVFP4_2LEVEL])
+@pytest.mark.parametrize("rnd", [fq.RNE, fq.SR])
+def test_quantize_outliers_whole_warp_spans(dtype, fmt, rnd):
+    """Rows of a whole number of 32-block spans (1024 columns: 64 blocks of 16
+    or 32 of 32): the retained elements come from the shared sorted column
+    list rather than a per-warp search."""
+    rows, cols = 96, 1024
+    calib = _calib_batches((rows, cols), 2, seed=17, dtype=dtype)
+    amax = torch.zeros(cols, dtype=torch.float32, device=DEV)
+    for xb in calib:
+        fq.fq_channel_amax(xb.to(DEV), amax)
+    sel, _ = _select_parity(amax, cols // 10)
+    x = _act((rows, cols), 18, dtype)
+    x[3] = x[3] * 3.0
+    x[7, :] = 0.0
+    x[10, 5] = -0.0
+    _outlier_parity(x.to(DEV), sel, fmt, rnd, seed=0xBEEF, offset=3)
+
+
+def test_quantize_outliers_whole_spans_every_channel_kept():
+    rows, cols = 8, 512
+    x = W.nvfp4_act(shape=(rows, cols), seed=19, n_outlier_cols=4).to(DEV)
+    sel, _ = _select_parity(fq.fq_channel_amax(x), cols)
+    for fmt in (fq.NVFP4, fq.MXFP4, fq.NVFP4_2LEVEL):
+        _outlier_parity(x, sel, fmt)
+
+
+@pytest.mark.parametrize("k", [8192, 8200])
+def test_quantize_outliers_long_channel_lists(k):
+    """8192 retained channels (the longest list kept in shared memory) and
+    8200 (the per-warp search instead), on 16384 columns."""
+    rows, cols = 4, 16384
+    x = W.channel_act((rows, cols), seed=20, channel_seed=21, n_outlier_cols=64).to(DEV)
+    sel, _ = _select_parity(fq.fq_channel_amax(x), k)
+    _outlier_parity(x, sel, fq.NVFP4)
+
+
 @pytest.mark.parametrize("fmt", [fq.NVFP4, fq.MXFP4, fq.NVFP4_2LEVEL])
 def test_quantize_outliers_k_zero_matches_plain_fakequant(fmt):
     rows, cols = 64, 256

@@ -110,7 +110,7 @@ __global__ void __launch_bounds__(kOutThreads) channel_amax_kernel(const void *_
 // indices in ascending order.
 constexpr int kSelThreads = 1024;
 constexpr int kMaxOutWords = 4096;  // channels up to 131072
-constexpr int64_t kFastKept = 8192;  // retained channels listed in shared memory
+constexpr int64_t kFastKept = 8192;  // retained channels listed in shared memory (8 B each)
 
 __device__ __forceinline__ uint64_t channel_key(const float *amax, int c)
 {
@@ -253,10 +253,13 @@ __global__ void __launch_bounds__(kOutThreads) outlier_row_kernel(OutlierArgs a,
     __shared__ NvTables tab;
     __shared__ int pre[kMaxOutWords];
     __shared__ uint32_t mstage[kOutThreads];
-    extern __shared__ int kcols[];  // fast: the retained columns in ascending order
+    // fast: the retained columns in ascending order, then 1 / s_j for each
+    extern __shared__ int kcols[];
+    __shared__ float e4m3v[128];  // E4M3 magnitudes by code (0x7F unused)
     const int64_t cols = a.cols, rows = a.rows;
     const int nwords = (int)((cols + 31) / 32);
     const int kk = (int)a.k;
+    float *krcp = reinterpret_cast<float *>(kcols + kk);
     popc_prefix<kOutThreads>(a.bitmap, nwords, pre);
     if (fast) {
         for (int w = threadIdx.x; w < nwords; w += kOutThreads) {
@@ -265,6 +268,12 @@ __global__ void __launch_bounds__(kOutThreads) outlier_row_kernel(OutlierArgs a,
                 if (idx < kk)
                     kcols[idx] = 32 * w + __ffs(wd) - 1;
         }
+        for (int t = threadIdx.x; t < kk; t += kOutThreads) {
+            const float sj = __ldg(a.fp8_scale + t);
+            krcp[t] = (sj == 0.0f) ? 0.0f : __frcp_rn(sj);
+        }
+        for (int c = threadIdx.x; c < 128; c += kOutThreads)
+            e4m3v[c] = c < 0x7F ? e4m3_value((uint32_t)c) : 0.0f;
         __syncthreads();
     }
     float s_g = 0.0f, inv6 = 0.0f;
@@ -373,26 +382,30 @@ __global__ void __launch_bounds__(kOutThreads) outlier_row_kernel(OutlierArgs a,
                 const int s0 = pre[cspan >> 5];
                 int s1 = cend >= cols ? kk : pre[cend >> 5];
                 s1 = s1 < kk ? s1 : kk;
+                // the span's row, with 32-bit offsets inside it
+                const T *xrow = reinterpret_cast<const T *>(a.x) + r_w * cols + cspan;
+                uint8_t *fp8row = a.fp8 ? a.fp8 + r_w * a.k : nullptr;
+                char *xhrow = a.xhat ? (char *)a.xhat + (r_w * cols + cspan) * (a.xhat_bf16 ? 2 : 4)
+                                     : nullptr;
+                const int c0s = (int)cspan;
                 for (int t = s0 + lane; t < s1; t += 32) {
-                    const int c = kcols[t];
-                    const int owner = (int)((c - cspan) / B), i = (int)((c - cspan) % B);
-                    const int64_t e = r_w * cols + c;
-                    const float xv = ld_scalar<T>(a.x, e);
-                    const float sj = __ldg(a.fp8_scale + t);
-                    const float rcp = (sj == 0.0f) ? 0.0f : __frcp_rn(sj);
-                    const float y = __fmul_rn(xv, rcp);
+                    const int off = kcols[t] - c0s;  // column inside the span
+                    const int owner = off / B, i = off % B;
+                    const float xv = ld_scalar<T>(xrow, off);
+                    const float y = __fmul_rn(xv, krcp[t]);
                     const uint32_t code =
                         e4m3_rn_sat(fabsf(y)) | ((__float_as_uint(y) >> 24) & 0x80u);
-                    if (a.fp8)
-                        a.fp8[r_w * a.k + t] = (uint8_t)code;
-                    if (a.xhat) {
-                        const float m = __fmul_rn(e4m3_value(code & 0x7Fu), sj);
+                    const float sj = __ldg(a.fp8_scale + t);
+                    if (fp8row)
+                        fp8row[t] = (uint8_t)code;
+                    if (xhrow) {
+                        const float m = __fmul_rn(e4m3v[code & 0x7Fu], sj);
                         const float h = (code & 0x80u) ? -m : m;
                         if (a.xhat_bf16)
-                            reinterpret_cast<unsigned short *>(a.xhat)[e] =
+                            reinterpret_cast<unsigned short *>(xhrow)[off] =
                                 (unsigned short)(bf16x2_rn(h, 0.0f) & 0xFFFFu);
                         else
-                            reinterpret_cast<float *>(a.xhat)[e] = h;
+                            reinterpret_cast<float *>(xhrow)[off] = h;
                     }
                     const uint32_t bit = 1u << i;
                     if (fabsf(xv) <= __fmul_rn(448.0f, sj))
@@ -547,7 +560,7 @@ static cudaError_t outlier_go(const OutlierArgs &a, cudaStream_t s)
     // the sorted-list path: the list fits in shared memory and every row is a
     // whole number of 32-block warp spans
     const int fast = a.k > 0 && a.k <= kFastKept && (a.cols / B) % 32 == 0;
-    const size_t smem = fast ? (size_t)a.k * sizeof(int) : 0;
+    const size_t smem = fast ? (size_t)a.k * (sizeof(int) + sizeof(float)) : 0;
     if (smem) {
         const cudaError_t e = cudaFuncSetAttribute(outlier_row_kernel<T, FMT, RND>,
                                                    cudaFuncAttributeMaxDynamicSharedMemorySize,

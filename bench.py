@@ -65,11 +65,11 @@ LAUNCHES_PER_STEP = {"nvfp4_small": 2, "mxfp4_weight": 1, "nvfp4_act": 2, "ste_b
                      "qad_kl": 2, "osci_update_reset": 2}
 # DRAM traffic per launch of the dominant call from an ncu capture, valid only
 # for the kernel source it was taken on (sha256 of k_osci.cu).  Captured on the
-# 2-expert case (66.4 M weights: pass A + pass B read+write 2848.6 MB) and
+# 2-expert case (66.4 M weights: pass A + pass B read+write 2844.7 MB) and
 # scaled by the weights processed to the 32-expert launch (traffic is linear
 # in the number of weights).
-NCU_TRAFFIC = {"osci_update_reset": {"bytes": int(2848.6e6 / 66355200 * 1061683200),
-                                      "src_sha256": "a469a46e9dd31a071222cd0becdb77d1d0b7e5c8522b69af688ad27f7d98bc49"}}
+NCU_TRAFFIC = {"osci_update_reset": {"bytes": int(2844748032 / 66355200 * 1061683200),
+                                      "src_sha256": "7e866ef343a372161cbe1b7829c856a1ffbda3ab8a1405138b7bf34a63f3ac83"}}
 
 
 def log(*a):

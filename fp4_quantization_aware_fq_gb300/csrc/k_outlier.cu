@@ -187,25 +187,42 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(const float *__rest
 }
 
 // ------------------------------------------------------------------ masked amax
+// A CTA covers 256 column vectors (16 bytes each) of a stripe of rows_per
+// rows, as channel_amax_kernel: each thread's retained-channel bits are read
+// once, and four rows' loads are in flight.
 template <typename T>
 __global__ void __launch_bounds__(kOutThreads) masked_amax_kernel(const void *__restrict__ x,
                                                                   int64_t rows, int64_t cols,
+                                                                  int64_t rows_per,
                                                                   const uint32_t *__restrict__ bm,
                                                                   unsigned *__restrict__ out)
 {
     constexpr int E = VecInfo<T>::E;
-    const int64_t nvec = rows * (cols / E);
+    constexpr int U = 4;
+    const int64_t vpr = cols / E;
+    const int64_t cv = (int64_t)blockIdx.x * kOutThreads + threadIdx.x;
+    const int64_t r0 = (int64_t)blockIdx.y * rows_per;
+    const int64_t r1 = r0 + rows_per < rows ? r0 + rows_per : rows;
     float m = 0.0f;
-    for (int64_t q = (int64_t)blockIdx.x * kOutThreads + threadIdx.x; q < nvec;
-         q += (int64_t)gridDim.x * kOutThreads) {
-        const int64_t c0 = (q % (cols / E)) * E;
-        float v[E];
-        unpack16<T>(ld16((const char *)x + q * 16), v);
+    if (cv < vpr) {
+        const int64_t c0 = cv * E;
         const uint32_t bits = __ldg(bm + (c0 >> 5)) >> (c0 & 31);
+        const char *col = (const char *)x + cv * 16;
+        for (int64_t r = r0; r < r1; r += U) {
+            uint4 raw[U];
 #pragma unroll
-        for (int i = 0; i < E; ++i)
-            if (!((bits >> i) & 1u))
-                m = fmaxf(m, fabsf(v[i]));
+            for (int k = 0; k < U; ++k)
+                raw[k] = r + k < r1 ? ld16(col + (r + k) * vpr * 16) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+            for (int k = 0; k < U; ++k) {
+                float v[E];
+                unpack16<T>(raw[k], v);
+#pragma unroll
+                for (int i = 0; i < E; ++i)
+                    if (!((bits >> i) & 1u))
+                        m = fmaxf(m, fabsf(v[i]));
+            }
+        }
     }
     m = group_max<32>(m);
     __shared__ float wm[kOutThreads / 32];
@@ -540,12 +557,20 @@ cudaError_t launch_masked_amax(const void *x, int bf16, int64_t rows, int64_t co
     if (e != cudaSuccess || rows == 0 || cols == 0)
         return e;
     const int E = bf16 ? 8 : 4;
-    const int grid = grid_cap(rows * (cols / E) / kOutThreads + 1, 4);
+    const int64_t gx = (cols / E + kOutThreads - 1) / kOutThreads;
+    // enough row stripes for about eight CTAs per SM, at least 16 rows each
+    int64_t gy = ((int64_t)sm_count() * 8 + gx - 1) / gx;
+    const int64_t max_gy = (rows + 15) / 16;
+    gy = gy < max_gy ? gy : max_gy;
+    gy = gy < 65535 ? gy : 65535;
+    const int64_t rows_per = (rows + gy - 1) / gy;
+    gy = (rows + rows_per - 1) / rows_per;
+    dim3 grid((unsigned)gx, (unsigned)gy);
     if (bf16)
-        masked_amax_kernel<__nv_bfloat16><<<grid, kOutThreads, 0, s>>>(x, rows, cols, bitmap,
-                                                                       (unsigned *)out);
+        masked_amax_kernel<__nv_bfloat16><<<grid, kOutThreads, 0, s>>>(x, rows, cols, rows_per,
+                                                                       bitmap, (unsigned *)out);
     else
-        masked_amax_kernel<float><<<grid, kOutThreads, 0, s>>>(x, rows, cols, bitmap,
+        masked_amax_kernel<float><<<grid, kOutThreads, 0, s>>>(x, rows, cols, rows_per, bitmap,
                                                                (unsigned *)out);
     return cudaGetLastError();
 }

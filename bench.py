@@ -90,9 +90,18 @@ def measured_peaks():
     return FALLBACK_HBM_GBS, "fallback"
 
 
-def src_sha(name):
-    with open(os.path.join(ROOT, "fp4_quantization_aware_fq_gb300", "csrc", name), "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()
+def src_sha(*names):
+    """SHA-256 over the named csrc files, in order (a kernel's source and the
+    headers it includes)."""
+    h = hashlib.sha256()
+    for name in names:
+        with open(os.path.join(ROOT, "fp4_quantization_aware_fq_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+# the sources the OsciReset kernels are compiled from
+OSCI_SOURCES = ("k_osci.cu", "fq_device.cuh", "fq_internal.h")
 
 
 # --------------------------------------------------------------------------- clocks
@@ -749,7 +758,7 @@ def main():
         dom = max(suite.names, key=lambda n: per_ms[n])
         achieved = bps[dom] / (per_ms[dom] / 1e3) / 1e9
         tr = NCU_TRAFFIC.get(dom, {})
-        traffic = tr.get("bytes") if tr.get("src_sha256") == src_sha("k_osci.cu") else None
+        traffic = tr.get("bytes") if tr.get("src_sha256") == src_sha(*OSCI_SOURCES) else None
         line = {
             "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),

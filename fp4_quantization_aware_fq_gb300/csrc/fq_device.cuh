@@ -102,6 +102,67 @@ __device__ __forceinline__ void unpack16<__nv_bfloat16>(const uint4 &u, float *v
     }
 }
 
+// max(|a|, |b|) lane by lane on two BF16 pairs.  The result's sign bits are
+// the XOR of the operands' and carry no meaning here: callers mask them off.
+__device__ __forceinline__ uint32_t bf16x2_absmax(uint32_t a, uint32_t b)
+{
+    uint32_t d;
+    asm("max.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+
+// Lane-wise largest BF16 magnitude over N packed pairs (N a power of two),
+// reduced as a tree.  Exact: the maximum of BF16 magnitudes is one of them.
+// The low half of the result holds the low lanes' maximum, the high half the
+// high lanes'; read them with bf16_lo / bf16_hi.
+template <int N>
+__device__ __forceinline__ uint32_t bf16x2_absmax_tree(const uint32_t *w)
+{
+    uint32_t m[N];
+#pragma unroll
+    for (int i = 0; i < N; ++i)
+        m[i] = w[i];
+#pragma unroll
+    for (int n = N; n > 1; n >>= 1)
+#pragma unroll
+        for (int i = 0; i < n / 2; ++i)
+            m[i] = bf16x2_absmax(m[i], m[i + n / 2]);
+    return m[0];
+}
+__device__ __forceinline__ float bf16_lo_abs(uint32_t m)
+{
+    return fabsf(__uint_as_float(m << 16));
+}
+__device__ __forceinline__ float bf16_hi_abs(uint32_t m)
+{
+    return fabsf(__uint_as_float(m & 0xFFFF0000u));
+}
+
+// Amax of one block of B elements of type T held as raw 16-byte vectors.
+// BF16 blocks reduce the packed pairs; both forms give max |x| exactly.
+template <typename T, int B>
+__device__ __forceinline__ float block_amax(const uint4 *raw)
+{
+    uint32_t w[B * sizeof(T) / 4];
+#pragma unroll
+    for (int k = 0; k < B * (int)sizeof(T) / 16; ++k) {
+        w[4 * k] = raw[k].x;
+        w[4 * k + 1] = raw[k].y;
+        w[4 * k + 2] = raw[k].z;
+        w[4 * k + 3] = raw[k].w;
+    }
+    if constexpr (sizeof(T) == 2) {
+        const uint32_t m = bf16x2_absmax_tree<B / 2>(w);
+        return fmaxf(bf16_lo_abs(m), bf16_hi_abs(m));
+    } else {
+        float am = 0.0f;
+#pragma unroll
+        for (int i = 0; i < B; ++i)
+            am = fmaxf(am, fabsf(__uint_as_float(w[i])));
+        return am;
+    }
+}
+
 // ---------------------------------------------------------------- E2M1
 // Nearest-even, saturating conversion of 8 floats to 8 packed E2M1 nibbles
 // (element 2j in the low nibble of byte j).  The cvt instruction takes its
@@ -200,19 +261,17 @@ __device__ __forceinline__ Scale nv_scale(float amax_b, float s_outer, float inv
 // Per-code tables of one tensor scale s_g (NVFP4): the effective scale, its
 // reciprocal and 6 s_eff for each of the 127 finite non-negative E4M3 codes.
 // Built once per CTA in shared memory (fill with all threads, then sync).
+// One 16-byte entry per code, {s_eff, r, lim, 0}, so that a block reads its
+// three values with one shared-memory load.
 struct NvTables {
-    float s_eff[128];
-    float r[128];
-    float lim[128];
+    float4 e[128];
 };
 
 __device__ __forceinline__ void nv_tables_fill(NvTables &t, float s_g)
 {
     for (int c = threadIdx.x; c < 128; c += blockDim.x) {
         const float se = (c < 0x7F) ? __fmul_rn(e4m3_value(c), s_g) : 0.0f;
-        t.s_eff[c] = se;
-        t.r[c] = (se == 0.0f) ? 0.0f : __frcp_rn(se);
-        t.lim[c] = __fmul_rn(6.0f, se);
+        t.e[c] = make_float4(se, (se == 0.0f) ? 0.0f : __frcp_rn(se), __fmul_rn(6.0f, se), 0.0f);
     }
 }
 
@@ -221,9 +280,10 @@ __device__ __forceinline__ Scale nv_scale_tab(float amax_b, float s_g, float inv
 {
     Scale s;
     s.code = nv_scale_code(amax_b, s_g, inv6);
-    s.s_eff = t.s_eff[s.code];
-    s.r = t.r[s.code];
-    s.lim = t.lim[s.code];
+    const float4 e = t.e[s.code];
+    s.s_eff = e.x;
+    s.r = e.y;
+    s.lim = e.z;
     return s;
 }
 

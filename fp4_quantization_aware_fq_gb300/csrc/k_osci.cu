@@ -254,7 +254,7 @@ __global__ void __launch_bounds__(kOsciThreads, kOsciBMinCtas)
                 const uint32_t mask = lanes_or<L>((~clip & 15u) << (4 * sub));
                 if (!valid)
                     continue;
-                const float seff_p = (FMT == NVFP4) ? tabp.s_eff[scp[k] & 127u]
+                const float seff_p = (FMT == NVFP4) ? tabp.e[scp[k] & 127u].x
                                                     : stored_s_eff<FMT>(scp[k], so_p[k]);
                 float xh[4], xp[4];
                 e2m1_decode4(q, xh);

@@ -21,8 +21,9 @@ constexpr int kThreads = 256;
 // CTAs per SM the register allocation must allow, measured: row kernels 4
 // (at most 64 registers; the double-block SR call 3-4% faster despite a few
 // spills), BF16 tile kernels 3 (80 registers; the Hadamard-transformed SR call
-// 2% faster, the NVFP4 row + column call 1.5%).  The FP32 tile kernels, whose
-// tiles need far more registers, are left free.
+// 2% faster, the NVFP4 row + column call 1.5%; the NVFP4 tile kernel fits 60
+// registers without spills, but four CTAs per SM ran 2.5% slower than three).
+// The FP32 tile kernels, whose tiles need far more registers, are left free.
 constexpr int kRowMinCtas = 4;
 template <typename T, int FMT>
 constexpr int tile_min_ctas()
@@ -80,12 +81,13 @@ struct RowOut {
     uint8_t *mask;
 };
 
-// Quantize one row-wise block of B values held by this thread.  `blk` is the
-// flat block index in the tensor (flat element index blk * B).  For the double
-// block, the 8 inner blocks of an outer block sit on 8 consecutive lanes, and
-// all 32 lanes of the warp must call this together.
+// Quantize one row-wise block of B values held by this thread (v) whose
+// amax is am (recomputed here after the Hadamard transform, when there is
+// one).  `blk` is the flat block index in the tensor (flat element index
+// blk * B).  For the double block, the 8 inner blocks of an outer block sit on
+// 8 consecutive lanes, and all 32 lanes of the warp must call this together.
 template <int FMT, int RND>
-__device__ __forceinline__ void row_block(float *v, int64_t blk, bool valid, float s_g,
+__device__ __forceinline__ void row_block(float *v, float am, int64_t blk, bool valid, float s_g,
                                           float inv6, const NvTables *tab, const RowOut &o,
                                           const PhiloxKey &key, uint32_t offset,
                                           uint32_t stream_id, bool rht, uint32_t signs)
@@ -95,11 +97,11 @@ __device__ __forceinline__ void row_block(float *v, int64_t blk, bool valid, flo
 #pragma unroll
         for (int j = 0; j < B / 16; ++j)
             rht16(v + 16 * j, signs);
-    }
-    float am = 0.0f;
+        am = 0.0f;
 #pragma unroll
-    for (int i = 0; i < B; ++i)
-        am = fmaxf(am, fabsf(v[i]));
+        for (int i = 0; i < B; ++i)
+            am = fmaxf(am, fabsf(v[i]));
+    }
     float s_o = s_g;
     if (FMT == NV2L) {
         s_o = outer_scale(group_max<8>(am));
@@ -171,22 +173,48 @@ __global__ void __launch_bounds__(kThreads, kRowMinCtas) row_kernel(RowArgs a)
     const bool rht = a.rht_seed != 0;
     const uint32_t signs = rht ? rht_signs(a.rht_seed, a.offset) : 0u;
     const int64_t stride = (int64_t)gridDim.x * kThreads * BPT;
+    constexpr int NV = B / VecInfo<T>::E;  // 16-byte vectors per block
     for (int64_t base = (int64_t)blockIdx.x * kThreads * BPT; base < nblk; base += stride) {
-        float v[BPT][B];
+        if constexpr (B == 16) {
+            // 1x16 blocks: the amax comes from the raw vectors (packed pairs
+            // for BF16), then the values are widened.
+            uint4 raw[BPT][NV];
 #pragma unroll
-        for (int k = 0; k < BPT; ++k) {
-            const int64_t blk = base + k * kThreads + threadIdx.x;
+            for (int k = 0; k < BPT; ++k) {
+                const int64_t blk = base + k * kThreads + threadIdx.x;
+                const char *src = (const char *)a.x + blk * B * (int64_t)sizeof(T);
+#pragma unroll
+                for (int i = 0; i < NV; ++i)
+                    raw[k][i] = (blk < nblk) ? ld16(src + 16 * i) : make_uint4(0, 0, 0, 0);
+            }
+#pragma unroll
+            for (int k = 0; k < BPT; ++k) {
+                const int64_t blk = base + k * kThreads + threadIdx.x;
+                const float am = block_amax<T, B>(raw[k]);
+                float v[B];
+#pragma unroll
+                for (int i = 0; i < NV; ++i)
+                    unpack16<T>(raw[k][i], v + i * VecInfo<T>::E);
+                row_block<FMT, RND>(v, am, blk, blk < nblk, s_g, inv6, &tab, o, key, a.offset,
+                                    a.stream_id, rht, signs);
+            }
+        } else {
+            // 1x32 blocks (one per thread): widened as they load, which keeps
+            // the raw vectors out of the register budget.
+            static_assert(BPT == 1, "one 1x32 block per thread and iteration");
+            const int64_t blk = base + threadIdx.x;
+            float v[B];
             if (blk < nblk)
-                load_block<T, B>((const char *)a.x + blk * B * (int64_t)sizeof(T), v[k]);
+                load_block<T, B>((const char *)a.x + blk * B * (int64_t)sizeof(T), v);
             else
 #pragma unroll
                 for (int i = 0; i < B; ++i)
-                    v[k][i] = 0.0f;
-        }
+                    v[i] = 0.0f;
+            float am = 0.0f;
 #pragma unroll
-        for (int k = 0; k < BPT; ++k) {
-            const int64_t blk = base + k * kThreads + threadIdx.x;
-            row_block<FMT, RND>(v[k], blk, blk < nblk, s_g, inv6, &tab, o, key, a.offset,
+            for (int i = 0; i < B; ++i)
+                am = fmaxf(am, fabsf(v[i]));
+            row_block<FMT, RND>(v, am, blk, blk < nblk, s_g, inv6, &tab, o, key, a.offset,
                                 a.stream_id, rht, signs);
         }
     }
@@ -200,12 +228,20 @@ struct TileShape {
     static constexpr int BC = FmtInfo<FMT>::B;           // column block (rows)
     static constexpr int CP = TR / 2 + 8;                // staged code bytes per column (padded)
 };
+// Row stride of the staged x tile in elements: one 16-byte vector of padding
+// shifts each row by four banks, so the 8 threads of a quarter warp that stage
+// two rows of BF16 1x16 blocks hit distinct banks.
+template <typename T, int FMT>
+__host__ __device__ constexpr int tile_pitch()
+{
+    return TileShape<FMT>::TC + 16 / (int)sizeof(T);
+}
 
 template <typename T, int FMT>
 constexpr size_t tile_smem_bytes()
 {
     using S = TileShape<FMT>;
-    return (size_t)S::TR * S::TC * sizeof(T)          // x tile
+    return (size_t)S::TR * tile_pitch<T, FMT>() * sizeof(T)  // x tile
            + (size_t)S::TC * S::CP                    // staged column codes
            + (size_t)S::TC * (S::TR / S::BC)          // staged column scales
            + (FMT == NV2L ? (size_t)S::TC * (S::TR / S::BC) * 4 : 0);  // inner amax
@@ -222,7 +258,8 @@ __global__ void __launch_bounds__(kThreads, tile_min_ctas<T, FMT>()) tile_kernel
     constexpr int NRB = TR / BC;          // column blocks per tile column
     extern __shared__ __align__(16) unsigned char smem[];
     T *tile = reinterpret_cast<T *>(smem);
-    uint8_t *ccs = smem + (size_t)TR * TC * sizeof(T);   // [TC][CP]
+    constexpr int TCP = tile_pitch<T, FMT>();
+    uint8_t *ccs = smem + (size_t)TR * TCP * sizeof(T);  // [TC][CP]
     uint8_t *css = ccs + (size_t)TC * CP;                // [TC][NRB]
     float *am16 = reinterpret_cast<float *>(css + (size_t)TC * NRB);  // [NRB][TC]
 
@@ -245,64 +282,81 @@ __global__ void __launch_bounds__(kThreads, tile_min_ctas<T, FMT>()) tile_kernel
     const PhiloxKey key = philox_key(a.seed);
     const bool rht = a.rht_seed != 0;
     const uint32_t signs = rht ? rht_signs(a.rht_seed, a.offset) : 0u;
-    const int64_t ntc = (cols + TC - 1) / TC;
-    const int64_t ntiles = ntc * ((rows + TR - 1) / TR);
 
     // Each thread owns RPT row blocks of a tile.  The loads of the next tile
-    // are issued before the current tile is processed, so they overlap its
-    // column pass and write-out.
+    // are issued once the current tile is staged in shared memory, so they
+    // overlap its row pass, column pass and write-out.
     constexpr int RPT = (TR * RBPR + kThreads - 1) / kThreads;
-    uint4 nxt[RPT][BR / E];
-    auto load_tile = [&](int64_t id) {
-        const int64_t lr0 = (id / ntc) * TR, lc0 = (id % ntc) * TC;
+    constexpr int NV = BR / E;  // 16-byte vectors per row block
+    uint4 nxt[RPT][NV];
+    auto load_tile = [&](int ty, int tx) {
+        const int64_t lr0 = (int64_t)ty * TR, lc0 = (int64_t)tx * TC;
 #pragma unroll
         for (int j = 0; j < RPT; ++j) {
             const int t = threadIdx.x + j * kThreads;
             const int tr = t / RBPR, tb = t % RBPR;
             const int64_t gr = lr0 + tr, gc = lc0 + (int64_t)tb * BR;
             const bool valid = t < TR * RBPR && gr < rows && gc < cols;
+            const char *src = (const char *)a.x + (gr * cols + gc) * (int64_t)sizeof(T);
 #pragma unroll
-            for (int k = 0; k < BR / E; ++k)
-                nxt[j][k] = valid ? ld16((const char *)a.x +
-                                         ((gr * cols + gc) + k * E) * (int64_t)sizeof(T))
-                                  : make_uint4(0, 0, 0, 0);
+            for (int k = 0; k < NV; ++k)
+                nxt[j][k] = valid ? ld16(src + 16 * k) : make_uint4(0, 0, 0, 0);
         }
     };
-    if ((int64_t)blockIdx.x < ntiles)
-        load_tile(blockIdx.x);
 
-    // Persistent CTAs walk the tiles in row-major order.
-    for (int64_t tile_id = blockIdx.x; tile_id < ntiles; tile_id += gridDim.x) {
-    const int64_t r0 = (tile_id / ntc) * TR;
-    const int64_t c0 = (tile_id % ntc) * TC;
-    uint4 cur[RPT][BR / E];
-#pragma unroll
-    for (int j = 0; j < RPT; ++j)
-#pragma unroll
-        for (int k = 0; k < BR / E; ++k)
-            cur[j][k] = nxt[j][k];
-    if (tile_id + gridDim.x < ntiles)
-        load_tile(tile_id + gridDim.x);
+    // Persistent CTAs walk the tiles in row-major order, gridDim.x tiles per
+    // step: (ty, tx) advances by (dy, dx) with a carry, without a division.
+    // The launcher keeps both tile counts below 2^31.
+    const int ntr = (int)((rows + TR - 1) / TR), ntc = (int)((cols + TC - 1) / TC);
+    const int dy = (int)gridDim.x / ntc, dx = (int)gridDim.x % ntc;
+    int ty = (int)blockIdx.x / ntc, tx = (int)blockIdx.x % ntc;
+    if (ty < ntr)
+        load_tile(ty, tx);
+    while (ty < ntr) {
+    const int64_t r0 = (int64_t)ty * TR;
+    const int64_t c0 = (int64_t)tx * TC;
+    int ny = ty + dy, nx = tx + dx;
+    if (nx >= ntc) {
+        nx -= ntc;
+        ++ny;
+    }
 
-    // Phase 1: stage the tile's row blocks in shared memory and, when asked,
-    // run the row-wise pass on them.
+    // Phase 1: stage the tile's row blocks in shared memory, start the next
+    // tile's loads, then (when asked) run the row-wise pass on the staged
+    // blocks, each thread reading back its own.
 #pragma unroll
     for (int j = 0; j < RPT; ++j) {
         const int t = threadIdx.x + j * kThreads;
         if (RPT * kThreads > TR * RBPR && t >= TR * RBPR)
             break;
         const int tr = t / RBPR, tb = t % RBPR;
-        const int64_t gr = r0 + tr, gc = c0 + (int64_t)tb * BR;
-        const bool valid = gr < rows && gc < cols;
-        float v[BR];
 #pragma unroll
-        for (int k = 0; k < BR / E; ++k) {
-            *reinterpret_cast<uint4 *>(tile + tr * TC + tb * BR + k * E) = cur[j][k];
-            unpack16<T>(cur[j][k], v + k * E);
-        }
-        if (a.do_row)
-            row_block<FMT, RND>(v, (gr * cols + gc) / BR, valid, s_g, inv6, &tab, o, key,
+        for (int k = 0; k < NV; ++k)
+            *reinterpret_cast<uint4 *>(tile + tr * TCP + tb * BR + k * E) = nxt[j][k];
+    }
+    if (ny < ntr)
+        load_tile(ny, nx);
+    if (a.do_row) {
+#pragma unroll
+        for (int j = 0; j < RPT; ++j) {
+            const int t = threadIdx.x + j * kThreads;
+            if (RPT * kThreads > TR * RBPR && t >= TR * RBPR)
+                break;
+            const int tr = t / RBPR, tb = t % RBPR;
+            const int64_t gr = r0 + tr, gc = c0 + (int64_t)tb * BR;
+            const bool valid = gr < rows && gc < cols;
+            uint4 raw[NV];
+#pragma unroll
+            for (int k = 0; k < NV; ++k)
+                raw[k] = *reinterpret_cast<const uint4 *>(tile + tr * TCP + tb * BR + k * E);
+            const float am = block_amax<T, BR>(raw);
+            float v[BR];
+#pragma unroll
+            for (int k = 0; k < NV; ++k)
+                unpack16<T>(raw[k], v + k * E);
+            row_block<FMT, RND>(v, am, (gr * cols + gc) / BR, valid, s_g, inv6, &tab, o, key,
                                 a.offset, 0u, rht, signs);
+        }
     }
     __syncthreads();
 
@@ -327,23 +381,15 @@ __global__ void __launch_bounds__(kThreads, tile_min_ctas<T, FMT>()) tile_kernel
             float w[BC];
 #pragma unroll
             for (int i = 0; i < BC; ++i)
-                w[i] = static_cast<float>(tile[(rb * BC + i) * TC + c]);
+                w[i] = static_cast<float>(tile[(rb * BC + i) * TCP + c]);
             am16[rb * TC + c] = col_amax(w);
         }
         __syncthreads();
     }
-    // quantize column block (c, rb) of the tile, held in v, into the staging buffers
-    auto col_quant = [&](int c, int rb, float *v) {
+    // quantize column block (c, rb) of the tile into the staging buffers: v
+    // holds the block (after the Hadamard transform, if any), m its amax
+    auto col_quant = [&](int c, int rb, float *v, float m) {
         const int64_t gc = c0 + c, gr0 = r0 + (int64_t)rb * BC;
-        if (FMT != NVFP4 && rht) {
-#pragma unroll
-            for (int j = 0; j < BC / 16; ++j)
-                rht16(v + 16 * j, signs);
-        }
-        float m = 0.0f;
-#pragma unroll
-        for (int i = 0; i < BC; ++i)
-            m = fmaxf(m, fabsf(v[i]));
         float s_o = s_g, inv6c = inv6;
         if (FMT == NV2L) {
             float mo = 0.0f;
@@ -376,15 +422,17 @@ __global__ void __launch_bounds__(kThreads, tile_min_ctas<T, FMT>()) tile_kernel
             float v[BC];
 #pragma unroll
             for (int i = 0; i < BC; ++i)
-                wd[i] = tile32[((rb * BC + i) * TC + c) / 2];
+                wd[i] = tile32[((rb * BC + i) * TCP + c) / 2];
+            // both columns' amax from one tree over the packed pairs
+            const uint32_t mw = bf16x2_absmax_tree<BC>(wd);
 #pragma unroll
             for (int i = 0; i < BC; ++i)
                 v[i] = __uint_as_float(wd[i] << 16);
-            col_quant(c, rb, v);
+            col_quant(c, rb, v, bf16_lo_abs(mw));
 #pragma unroll
             for (int i = 0; i < BC; ++i)
                 v[i] = __uint_as_float(wd[i] & 0xFFFF0000u);
-            col_quant(c + 1, rb, v);
+            col_quant(c + 1, rb, v, bf16_hi_abs(mw));
         }
     } else {
         for (int task = threadIdx.x; task < TC * NRB; task += kThreads) {
@@ -394,8 +442,17 @@ __global__ void __launch_bounds__(kThreads, tile_min_ctas<T, FMT>()) tile_kernel
             float v[BC];
 #pragma unroll
             for (int i = 0; i < BC; ++i)
-                v[i] = static_cast<float>(tile[(rb * BC + i) * TC + c]);
-            col_quant(c, rb, v);
+                v[i] = static_cast<float>(tile[(rb * BC + i) * TCP + c]);
+            if (FMT != NVFP4 && rht) {
+#pragma unroll
+                for (int j = 0; j < BC / 16; ++j)
+                    rht16(v + 16 * j, signs);
+            }
+            float m = 0.0f;
+#pragma unroll
+            for (int i = 0; i < BC; ++i)
+                m = fmaxf(m, fabsf(v[i]));
+            col_quant(c, rb, v, m);
         }
     }
     __syncthreads();
@@ -416,6 +473,8 @@ __global__ void __launch_bounds__(kThreads, tile_min_ctas<T, FMT>()) tile_kernel
             a.cscales[gc * (rows / BC) + gr / BC] = css[c * NRB + j];
     }
     __syncthreads();  // the next tile overwrites the tile and staging buffers
+    ty = ny;
+    tx = nx;
     }
 }
 
@@ -499,7 +558,10 @@ static cudaError_t tile_go(const TileArgs &a, cudaStream_t s)
         if (e != cudaSuccess)
             return e;
     }
-    const int64_t ntiles = ((a.cols + S::TC - 1) / S::TC) * ((a.rows + S::TR - 1) / S::TR);
+    const int64_t ntc = (a.cols + S::TC - 1) / S::TC, ntr = (a.rows + S::TR - 1) / S::TR;
+    if (ntc >= INT32_MAX || ntr >= INT32_MAX)
+        return cudaErrorInvalidValue;
+    const int64_t ntiles = ntc * ntr;
     int per_sm = 0;
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, tile_kernel<T, FMT, RND>, kThreads,
                                                       smem) != cudaSuccess || per_sm < 1)

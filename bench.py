@@ -64,12 +64,13 @@ LAUNCHES_PER_STEP = {"nvfp4_small": 2, "mxfp4_weight": 1, "nvfp4_act": 2, "ste_b
                      "grad_2level": 1, "grad_rht_rowcol": 1, "act_outliers": 2,
                      "qad_kl": 2, "osci_update_reset": 2}
 # DRAM traffic per launch of the dominant call from an ncu capture, valid only
-# for the kernel source it was taken on (sha256 of k_osci.cu).  Captured on the
-# 2-expert case (66.4 M weights: pass A + pass B read+write 2844.7 MB) and
+# for the kernel source it was taken on (sha256 of the OsciReset sources).
+# Captured on the 2-expert case (66.4 M weights: pass A + pass B read+write
+# 2844.8 MB) and
 # scaled by the weights processed to the 32-expert launch (traffic is linear
 # in the number of weights).
-NCU_TRAFFIC = {"osci_update_reset": {"bytes": int(2844748032 / 66355200 * 1061683200),
-                                      "src_sha256": "7e866ef343a372161cbe1b7829c856a1ffbda3ab8a1405138b7bf34a63f3ac83"}}
+NCU_TRAFFIC = {"osci_update_reset": {"bytes": int(2844842752 / 66355200 * 1061683200),
+                                      "src_sha256": "a252e6e457263ecd8e33d830c14ccee3282d2a38dc8a63aea208aa87e49fa883"}}
 
 
 def log(*a):

@@ -222,25 +222,29 @@ struct Scale {
     uint32_t code;
 };
 
-// 1 / (6 s_outer), rounded; 0 when s_outer = 0.  Used to find block scale
-// codes without dividing (nv_scale_code).
+// 1 / (6 s_outer), rounded, used to find block scale codes without dividing
+// (nv_scale_code).  0 when s_outer is 0 or below 2^-120: there 6 s_outer or its
+// reciprocal would leave the normal range, and nv_scale_code divides instead.
 __device__ __forceinline__ float nv_inv6(float s_outer)
 {
-    return (s_outer == 0.0f) ? 0.0f : __frcp_rn(__fmul_rn(6.0f, s_outer));
+    return (s_outer < 0x1p-120f) ? 0.0f : __frcp_rn(__fmul_rn(6.0f, s_outer));
 }
 
 // E4M3 code of the block scale s_b = (amax_b / 6) / s_outer (two IEEE
-// divisions, in that order).  amax_b * inv6 is within 5 ulps of s_b (three
-// roundings on each side), so both round to the same E4M3 code unless the
-// product lies within 64 ulps of an E4M3 rounding boundary -- in the E4M3
-// normal range every boundary has FP32 mantissa bits 19..0 equal to 0x80000
-// -- or below 2^-6, where E4M3 is subnormal.  Those rare blocks take the
-// exact divisions.
+// divisions, in that order).  With every operand and quotient normal,
+// amax_b * inv6 is within 5 ulps of s_b (three roundings on each side), so
+// both round to the same E4M3 code unless the product lies within 64 ulps of
+// an E4M3 rounding boundary -- in the E4M3 normal range every boundary has
+// FP32 mantissa bits 19..0 equal to 0x80000 -- or below 2^-6, where E4M3 is
+// subnormal.  Those rare blocks take the exact divisions, and so do blocks
+// whose amax_b / 6 would be subnormal (amax_b < 2^-123) or whose outer scale
+// has no product form (inv6 = 0).
 __device__ __forceinline__ uint32_t nv_scale_code(float amax_b, float s_outer, float inv6)
 {
     float sb = __fmul_rn(amax_b, inv6);
     const uint32_t low = __float_as_uint(sb) & 0xFFFFFu;
-    const bool near = amax_b != 0.0f && ((low - 0x7FFC0u) < 128u || sb < 0.0157f);
+    const bool near = amax_b != 0.0f && ((low - 0x7FFC0u) < 128u || sb < 0.0157f ||
+                                         amax_b < 0x1p-123f || inv6 == 0.0f);
     if (near)
         sb = (s_outer == 0.0f) ? 0.0f : __fdiv_rn(__fdiv_rn(amax_b, 6.0f), s_outer);
     return e4m3_rn_sat(sb);
@@ -550,14 +554,16 @@ __device__ __forceinline__ void encode_block(const float *v, const Scale &sc, co
 
 // STE mask bits of a block: bit i = element i inside [-6 s_eff, 6 s_eff].
 // The clip bit is the sign of (lim - |x|): exact, since a non-zero difference
-// of two floats never rounds to zero without flush-to-zero.
+// of two floats never rounds to zero without flush-to-zero.  A funnel shift
+// moves each sign bit into the accumulator, last element first, so bit i ends
+// at position i: one instruction per element besides the subtraction.
 template <int B>
 __device__ __forceinline__ uint32_t block_mask(const float *v, float lim)
 {
     uint32_t clip = 0;
 #pragma unroll
-    for (int i = 0; i < B; ++i)
-        clip |= (__float_as_uint(__fsub_rn(lim, fabsf(v[i]))) >> 31) << i;
+    for (int i = B - 1; i >= 0; --i)
+        clip = __funnelshift_l(__float_as_uint(__fsub_rn(lim, fabsf(v[i]))), clip, 1);
     return (B == 32) ? ~clip : (~clip & ((1u << B) - 1u));
 }
 

@@ -128,8 +128,11 @@ __device__ __forceinline__ void row_block(float *v, float am, int64_t blk, bool 
             float xh[8];
             e2m1_decode8(q[w], xh);
 #pragma unroll
-            for (int i = 0; i < 8; ++i)
-                xh[i] = __fmul_rn(xh[i], sc.s_eff);
+            for (int i = 0; i < 8; i += 2) {
+                const float2 p = mul2(make_float2(xh[i], xh[i + 1]), make_float2(sc.s_eff, sc.s_eff));
+                xh[i] = p.x;
+                xh[i + 1] = p.y;
+            }
             if (o.xhat_bf16) {
                 *reinterpret_cast<uint4 *>((char *)o.xhat + (blk * B + w * 8) * 2) =
                     make_uint4(bf16x2_rn(xh[0], xh[1]), bf16x2_rn(xh[2], xh[3]),

@@ -149,6 +149,48 @@ def test_saturation_near_six_and_subnormals():
     fakequant_parity(_dev(y), fq.NVFP4, rnd=fq.SR, seed=1, orient=fq.ROWCOL)
 
 
+@pytest.mark.parametrize("fmt", [fq.NVFP4, fq.MXFP4, fq.NVFP4_2LEVEL])
+@pytest.mark.parametrize("orient", [fq.ROW, fq.ROWCOL])
+def test_bf16_subnormal_blocks(fmt, orient):
+    """BF16 blocks whose values, and so whose amax, are BF16 subnormals, with
+    mixed signs and signed zeros: the BF16 kernels reduce the block amax on
+    packed pairs.  One normal value in every row's and every column's
+    128-element run keeps the tensor and outer scales normal (MXFP4 scales
+    such blocks by 2^127)."""
+    g = torch.Generator().manual_seed(7)
+    rows, cols = 128, 512
+    x = torch.randn((rows, cols), generator=g) * 1e-39
+    x[:, 3::16] = -0.0
+    x[5, :] = 0.0
+    x[1, 0:32] = -2.0 ** -133                    # the smallest BF16 subnormal
+    c = torch.arange(cols)
+    x[c % rows, c] = torch.where(c % 3 == 0, -1.0, 1.0)
+    xb = x.to(torch.bfloat16)
+    assert ((xb.float().abs() < 2.0 ** -126) & (xb != 0)).sum() > 10000
+    fakequant_parity(_dev(xb), fmt, orient=orient)
+    fakequant_parity(_dev(xb), fmt, rnd=fq.SR, seed=3, orient=orient)
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+@pytest.mark.parametrize("fmt", [fq.NVFP4, fq.NVFP4_2LEVEL])
+@pytest.mark.parametrize("orient", [fq.ROW, fq.ROWCOL])
+def test_tiny_tensor_and_outer_scales(dtype, fmt, orient):
+    """Tensors (NVFP4) and 1x128 / 128x1 runs (double block) whose amax is
+    about 1e-37: the tensor or outer scale amax / 2688 is an FP32 subnormal,
+    where the scale codes need the two divisions themselves.  Magnitudes stay
+    within a factor 2 of the amax, so every block's s_eff keeps a finite
+    reciprocal."""
+    g = torch.Generator().manual_seed(11)
+    rows, cols = 256, 384
+    mag = 0.5 + 0.5 * torch.rand((rows, cols), generator=g)
+    sign = torch.where(torch.rand((rows, cols), generator=g) < 0.5, -1.0, 1.0)
+    scale = torch.tensor([1e-37, 5e-37, 2.5e-36, 7e-37])[torch.arange(rows) % 4]
+    x = (sign * mag * scale[:, None]).to(dtype)
+    assert (x != 0).all()
+    fakequant_parity(_dev(x), fmt, orient=orient)
+    fakequant_parity(_dev(x), fmt, rnd=fq.SR, seed=5, offset=2, orient=orient)
+
+
 # ------------------------------------------------------------------ Hadamard transform
 @pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
 @pytest.mark.parametrize("fmt,rnd", [(fq.NVFP4_2LEVEL, fq.SR), (fq.NVFP4_2LEVEL, fq.RNE),

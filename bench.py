@@ -66,9 +66,8 @@ LAUNCHES_PER_STEP = {"nvfp4_small": 2, "mxfp4_weight": 1, "nvfp4_act": 2, "ste_b
 # DRAM traffic per launch of the dominant call from an ncu capture, valid only
 # for the kernel source it was taken on (sha256 of the OsciReset sources).
 # Captured on the 2-expert case (66.4 M weights: pass A + pass B read+write
-# 2844.8 MB) and
-# scaled by the weights processed to the 32-expert launch (traffic is linear
-# in the number of weights).
+# 2844.8 MB) and scaled by the weights processed to the 32-expert launch
+# (traffic is linear in the number of weights).
 NCU_TRAFFIC = {"osci_update_reset": {"bytes": int(2844842752 / 66355200 * 1061683200),
                                       "src_sha256": "a252e6e457263ecd8e33d830c14ccee3282d2a38dc8a63aea208aa87e49fa883"}}
 

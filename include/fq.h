@@ -69,10 +69,11 @@
  *    never allocate device memory, and may return before the GPU finishes.
  *  - Argument errors are detected on the host and returned before any launch;
  *    nothing is written then.  A failed launch returns FQ_ERR_CUDA.
- *  - Inputs must be finite.  For NVFP4 the tensor amax (for the double block:
- *    each 1x128 block amax) must be 0 or at least 2^-100, so that every
- *    effective scale is a normal FP32 number; smaller non-zero ranges are
- *    outside the contract.
+ *  - Inputs must be finite.  A block whose effective scale s_eff is non-zero
+ *    but below 2^-128 has no finite FP32 reciprocal (x * (1 / s_eff) is
+ *    infinite, and NaN for a zero element); such blocks are outside the
+ *    contract.  For NVFP4 none occurs while the tensor amax (for the double
+ *    block: each 1x128 block amax) is 0 or at least 2^-107.
  *  - Calls keep no state between them and may run concurrently on different
  *    streams with different workspaces.
  */

@@ -98,6 +98,28 @@ def test_oracle_matches_vectorised_restatement(fmt):
                               ref["tscale"].reshape(-1).view(np.uint32))
 
 
+@pytest.mark.parametrize("fmt", [oracle.NVFP4, oracle.NVFP4_2LEVEL])
+def test_oracle_matches_vectorised_restatement_tiny_scales(fmt):
+    """Tensor and outer amax near 1e-37: the tensor / outer scale amax / 2688
+    is an FP32 subnormal, where the scale code rests on IEEE division with
+    gradual underflow.  Magnitudes within a factor 2 of each row's scale keep
+    every block's s_eff reciprocal finite."""
+    g = np.random.default_rng(11)
+    rows, cols = 64, 256
+    mag = 0.5 + 0.5 * g.random((rows, cols))
+    sign = np.where(g.random((rows, cols)) < 0.5, -1.0, 1.0)
+    scale = np.array([1e-37, 5e-37, 2.5e-36, 7e-37])[np.arange(rows) % 4]
+    x = (sign * mag * scale[:, None]).astype(np.float32)
+    got = oracle.quantize(x, fmt, want_xhat=True, want_mask=True)["row"]
+    assert np.min(got["tscale"]) < np.finfo(np.float32).tiny        # subnormal scales
+    ref = vectorised(x, fmt)
+    for k in ("codes", "scales", "mask"):
+        assert np.array_equal(got[k], ref[k]), k
+    assert np.array_equal(got["xhat"].view(np.uint32), ref["xhat"].view(np.uint32))
+    assert np.array_equal(got["tscale"].reshape(-1).view(np.uint32),
+                          ref["tscale"].reshape(-1).view(np.uint32))
+
+
 @pytest.mark.parametrize("fmt", [oracle.NVFP4, oracle.MXFP4, oracle.NVFP4_2LEVEL])
 def test_dequantize_reproduces_quantizer_xhat(fmt):
     x = _test_tensor(seed=3)

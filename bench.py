@@ -157,12 +157,14 @@ class ClockSampler:
 class Suite:
     """The workloads' inputs and outputs, resident on one GPU.  `only` limits
     the suite to some workloads; `experts` scales the MoE workload down and
-    `qad_rows` the logits (for profiling a smaller case of the same kernels)."""
+    `qad_rows` the logits (for profiling a smaller case of the same kernels);
+    `mxfp4_rows` sets the rows of the MXFP4 weight (a larger case shows that
+    kernel's DRAM traffic, which at 4096 rows still sits in L2 when it ends)."""
 
     ORDER = ("nvfp4_small", "mxfp4_weight", "nvfp4_act", "ste_backward", "grad_2level",
              "grad_rht_rowcol", "act_outliers", "qad_kl", "osci_update_reset")
 
-    def __init__(self, dev, only=None, experts=None, qad_rows=None):
+    def __init__(self, dev, only=None, experts=None, qad_rows=None, mxfp4_rows=None):
         import torch
         from fp4_quantization_aware_fq_gb300 import fq
         from fp4_quantization_aware_fq_gb300 import workloads as W
@@ -180,7 +182,7 @@ class Suite:
             self.ws1 = torch.empty(256, dtype=torch.uint8, device=dev)
             self.elems["nvfp4_small"] = self.x1.numel()
         if "mxfp4_weight" in want:
-            self.x2 = W.mxfp4_weight(device=dev)
+            self.x2 = W.mxfp4_weight(shape=(mxfp4_rows or 4096, 4096), device=dev)
             self.cfg2 = fq.Config(fq.MXFP4)
             self.q2 = fq.alloc_qtensor(*self.x2.shape, fq.MXFP4, dev)
             self.xh2 = torch.empty(self.x2.shape, dtype=torch.bfloat16, device=dev)
@@ -340,7 +342,8 @@ def job_throughput(world: int, bytes_per_step: float, steps: int, ms: float) -> 
 def run_ours(args, rank, world, dist):
     import torch
     dev = torch.device("cuda", torch.cuda.current_device())
-    suite = Suite(dev, only=args.only, experts=args.experts, qad_rows=args.qad_rows)
+    suite = Suite(dev, only=args.only, experts=args.experts, qad_rows=args.qad_rows,
+                  mxfp4_rows=args.mxfp4_rows)
     stream = torch.cuda.current_stream()
     bps = bytes_per_step(suite.elems)
     total_bytes = sum(bps.values())
@@ -680,11 +683,13 @@ FULL_ELEMS = {"nvfp4_small": 256 * 1024, "mxfp4_weight": 4096 * 4096,
               "osci_update_reset": 32 * 2 * 2880 * 5760}
 
 
-def config_block(names=None, experts=None, qad_rows=None):
-    if names is not None and (list(names) != list(Suite.ORDER) or experts or qad_rows):
+def config_block(names=None, experts=None, qad_rows=None, mxfp4_rows=None):
+    if names is not None and (list(names) != list(Suite.ORDER) or experts or qad_rows
+                              or mxfp4_rows):
         return {"workload": "subset: " + ",".join(names) + (f"; moe experts={experts}"
                                                            if experts else "")
-                + (f"; qad rows={qad_rows}" if qad_rows else ""),
+                + (f"; qad rows={qad_rows}" if qad_rows else "")
+                + (f"; mxfp4 rows={mxfp4_rows}" if mxfp4_rows else ""),
                 "l2": "no flush between steps", "bytes": "algorithmic"}
     return {"workload": "fake-quant suite over the synthetic workloads (one pass each per "
                         "step): nvfp4_small fp32 256x1024 NVFP4 RNE; mxfp4_weight bf16 "
@@ -718,6 +723,8 @@ def main():
                     help="MoE experts in moe_qat (default: the full 32)")
     ap.add_argument("--qad-rows", type=int, default=None,
                     help="rows of the qad_kl logits (default: the full 4096)")
+    ap.add_argument("--mxfp4-rows", type=int, default=None,
+                    help="rows of the mxfp4_weight tensor (default: the full 4096)")
     ap.add_argument("--gemm-only", choices=["nvfp4", "mxfp4"], default=None,
                     help="time only the tensor-core GEMM of this format (one JSON object)")
     args = ap.parse_args()
@@ -765,7 +772,7 @@ def main():
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
             "data": "synthetic (seeded torch generators, shapes/distributions of the "
                     "workloads)",
-            "config": config_block(suite.names, args.experts, args.qad_rows),
+            "config": config_block(suite.names, args.experts, args.qad_rows, args.mxfp4_rows),
             "per_workload": per,
             "roofline": {"bound": "hbm", "kernel": dom + (" (osci_pass_a + osci_pass_b<reset>)"
                                                            if dom == "osci_update_reset" else ""),
@@ -783,12 +790,12 @@ def main():
                            "unit": UNIT, "h2d_bytes_per_step": e2e["h2d"],
                            "d2h_bytes_per_step": e2e["d2h"], "steps": e2e["steps"],
                            "ms_per_step": round(e2e["ms_total"] / e2e["steps"], 3)}
-        if world == 1 and not args.only and not args.experts and not args.qad_rows:
+        reduced = bool(args.only or args.experts or args.qad_rows or args.mxfp4_rows)
+        if world == 1 and not reduced:
             line["nvfp4_small_at_scale"] = run_small_at_scale()
             line["gemm_nvfp4"] = run_gemm(fmt_name="nvfp4")
             line["gemm_mxfp4"] = run_gemm(fmt_name="mxfp4")
-        if (not args.no_cpu_baseline and world == 1 and not args.only and not args.experts
-                and not args.qad_rows):
+        if not args.no_cpu_baseline and world == 1 and not reduced:
             sample, desc = oracle_sample()
             gbs, secs = oracle_gbs(sample, suite.elems)
             line["cpu_baseline"] = {"value": round(gbs, 4), "unit": UNIT, "cores": 1,

@@ -1,6 +1,6 @@
 // fq_async.cuh -- bulk asynchronous copies (TMA, 1-D) into shared memory with
-// mbarrier completion, and thread-block-cluster helpers (rank, barrier,
-// distributed shared memory loads).
+// mbarrier completion, and thread-block-cluster helpers (rank, distributed
+// shared memory stores).
 //
 // Every mbarrier wait is bounded: mbar_wait gives up after kWaitLimitNs of
 // wall-clock time (read from %globaltimer) and reports failure, so that a
@@ -111,31 +111,6 @@ __device__ __forceinline__ uint32_t num_clusters_x()
     uint32_t r;
     asm volatile("mov.u32 %0, %%nclusterid.x;" : "=r"(r));
     return r;
-}
-
-// Every thread of every CTA of the cluster: release this CTA's earlier shared
-// memory writes, then wait until all CTAs of the cluster have arrived.  (A
-// hardware barrier: all CTAs of a cluster are resident together and run the
-// same number of these.)
-__device__ __forceinline__ void cluster_sync()
-{
-    asm volatile("barrier.cluster.arrive.release.aligned;\n\t"
-                 "barrier.cluster.wait.acquire.aligned;" ::
-                     : "memory");
-}
-
-// Loads a float4 from the shared memory of CTA `rank` of this cluster, at the
-// offset that `local` has in this CTA's shared memory.
-__device__ __forceinline__ float4 dsmem_ld_f4(const float4 *local, uint32_t rank)
-{
-    uint32_t remote;
-    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_u32(local)), "r"(rank));
-    float4 v;
-    asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
-                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
-                 : "r"(remote)
-                 : "memory");
-    return v;
 }
 
 // Stores into the shared memory of CTA `rank` of this cluster, at the offset

@@ -121,6 +121,26 @@ def test_oracle_matches_vectorised_restatement_tiny_scales(fmt):
 
 
 @pytest.mark.parametrize("fmt", [oracle.NVFP4, oracle.MXFP4, oracle.NVFP4_2LEVEL])
+def test_oracle_matches_vectorised_restatement_subnormal_blocks(fmt):
+    """Blocks of FP32 subnormals with signed zeros, under normal tensor and
+    outer scales (one value of 1 in every row's 128-run): MXFP4 scales them by
+    2^127, the E4M3 formats give them a zero scale."""
+    g = np.random.default_rng(7)
+    rows, cols = 32, 256
+    x = (g.standard_normal((rows, cols)) * 1e-39).astype(np.float32)
+    x[:, 3::16] = -0.0
+    x[2, 0:32] = -np.float32(2.0 ** -149)
+    c = np.arange(cols)
+    x[c % rows, c] = 1.0
+    assert ((np.abs(x) < np.finfo(np.float32).tiny) & (x != 0)).sum() > 5000
+    got = oracle.quantize(x, fmt, want_xhat=True, want_mask=True)["row"]
+    ref = vectorised(x, fmt)
+    for k in ("codes", "scales", "mask"):
+        assert np.array_equal(got[k], ref[k]), k
+    assert np.array_equal(got["xhat"].view(np.uint32), ref["xhat"].view(np.uint32))
+
+
+@pytest.mark.parametrize("fmt", [oracle.NVFP4, oracle.MXFP4, oracle.NVFP4_2LEVEL])
 def test_dequantize_reproduces_quantizer_xhat(fmt):
     x = _test_tensor(seed=3)
     q = oracle.quantize(x, fmt, want_xhat=True)["row"]

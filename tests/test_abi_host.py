@@ -2,6 +2,8 @@
 exports every entry point include/fq.h declares, and argument errors come back
 as the documented status codes before anything is launched."""
 import ctypes
+import os
+import re
 
 import pytest
 
@@ -136,6 +138,38 @@ def test_osci_argument_errors(L):
     r = L.fq_osci_reset
     assert r(ctypes.byref(cfg), 2, rows, cols, ptrs, ptrs, ptrs, None, 4.0, None, None) == 1
     assert r(ctypes.byref(cfg), 2, rows, cols, ptrs, ptrs, ptrs, qs, 4.0, FAKE + 4, None) == 3
+
+
+def test_osci_update_reset_and_noalloc_argument_errors(L):
+    cfg = fq.Config(fq.NVFP4)
+    vp, i64 = ctypes.c_void_p, ctypes.c_int64
+    rows = (i64 * 2)(64, 64)
+    cols = (i64 * 2)(64, 40)
+    ptrs = (vp * 2)(FAKE, FAKE)
+    qs = (fq._QT * 2)(_qt(), _qt())
+    ur = L.fq_osci_update_reset
+    c = ctypes.byref(cfg)
+    assert ur(c, 2, rows, cols, ptrs, ptrs, ptrs, ptrs, qs, qs, None, fq.BF16, None, 4.0,
+              None, FAKE, 256, None) == 2                                  # 40 % 16 != 0
+    cols[1] = 64
+    assert ur(c, 2, rows, cols, ptrs, ptrs, ptrs, ptrs, qs, qs, None, fq.BF16, None, 4.0,
+              None, None, 0, None) == 4                                    # no workspace
+    assert ur(c, 2, rows, cols, ptrs, ptrs, ptrs, ptrs, qs, qs, None, fq.BF16, None, 4.0,
+              FAKE + 4, FAKE, 256, None) == 3                              # n_reset not 8-aligned
+    assert ur(c, 2, rows, cols, ptrs, None, ptrs, ptrs, qs, qs, None, fq.BF16, None, 4.0,
+              None, FAKE, 256, None) == 1                                  # no delta
+    assert ur(c, -1, rows, cols, ptrs, ptrs, ptrs, ptrs, qs, qs, None, fq.BF16, None, 4.0,
+              None, FAKE, 256, None) == 1
+    na = L.fq_osci_update_noalloc
+    header = open(os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))),
+                               "include", "fq.h")).read()
+    cap = int(re.search(r"#define FQ_NOALLOC_MAX_TENSORS (\d+)", header).group(1))
+    assert na(c, cap + 1, rows, cols, ptrs, ptrs, ptrs, ptrs, qs, qs, None, fq.BF16, None,
+              None) == 4                                                   # beyond its scratch
+    assert na(c, -1, rows, cols, ptrs, ptrs, ptrs, ptrs, qs, qs, None, fq.BF16, None,
+              None) == 1
+    assert na(c, 0, None, None, None, None, None, None, None, None, None, fq.BF16, None,
+              None) == 0                                                   # nothing to do
 
 
 def test_outlier_argument_errors(L):

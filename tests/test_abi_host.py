@@ -83,6 +83,23 @@ def test_quantize_argument_errors(L):
     assert _quant(L, ok, row=_qt(), wsb=2) == 4                            # workspace too small
 
 
+@pytest.mark.parametrize("fmt", [fq.NVFP4, fq.MXFP4, fq.NVFP4_2LEVEL])
+def test_empty_tensors_succeed_without_touching_the_device(L, fmt):
+    """rows * cols == 0 is a valid call that does nothing: FQ_OK, returned before
+    any CUDA call (on a machine without a GPU any call would come back as
+    FQ_ERR_CUDA, so these also show that nothing was launched)."""
+    cfg = fq.Config(fmt)
+    c = ctypes.byref(cfg)
+    q, q2 = _qt(), _qt()
+    assert _quant(L, cfg, rows=0, cols=128, row=q) == 0
+    assert _quant(L, cfg, rows=0, cols=128, orient=fq.ROWCOL, row=q, col=q2) == 0
+    assert _quant(L, cfg, rows=128, cols=0, row=q) == 0
+    assert L.fq_fakequant_ste(c, FAKE, fq.BF16, 0, 128, FAKE, fq.BF16, FAKE, ctypes.byref(q),
+                              None, None, FAKE, 256, None) == 0
+    assert L.fq_dequantize(c, ctypes.byref(q), 0, 128, FAKE, fq.F32, None) == 0
+    assert L.fq_ste_backward(FAKE, fq.BF16, FAKE, 0, FAKE, None) == 0
+
+
 def test_hadamard_transform_needs_block_local_scales(L):
     cfg = fq.Config(fq.NVFP4, fq.SR, 1, 0, rht_seed=7)
     assert _quant(L, cfg, row=_qt()) == 5                                  # unsupported

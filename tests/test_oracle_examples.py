@@ -85,3 +85,24 @@ def test_osci_flip_e4():
     assert abs(float(st.master[0, 2]) - 0.11) < 1e-6  # control weight untouched
     assert float(st.master[0, 0]) == 6.0 and float(st.master[0, 16]) == 2688.0
     assert not st.dist_q.any() and not st.dist_m.any()
+
+
+def test_nvfp4_2level_e5():
+    g = _load("nvfp4_2level_e5.json")
+    x = np.zeros((g["rows"], g["cols"]), dtype=np.float32)
+    for k, v in g["x_nonzero"].items():
+        x[0, int(k)] = v
+    r = oracle.quantize(x, oracle.NVFP4_2LEVEL, want_xhat=True, want_mask=True)["row"]
+    assert list(r["tscale"].reshape(-1)) == g["tscale"]
+    assert list(r["scales"].reshape(-1)) == g["scales"]
+    want = [0] * g["cols"]
+    for k, v in g["codes_nonzero"].items():
+        want[int(k)] = v
+    assert _nibbles(r["codes"], g["cols"]) == want
+    xh = r["xhat"].reshape(-1)
+    want_xh = np.zeros(g["cols"], np.float32)
+    for k, v in g["xhat_nonzero"].items():
+        want_xh[int(k)] = v
+    assert np.array_equal(xh.view(np.uint32), want_xh.view(np.uint32))   # zeros are +0
+    assert list(r["mask"].reshape(-1)) == g["mask_words"]
+

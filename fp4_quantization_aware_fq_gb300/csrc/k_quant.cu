@@ -299,11 +299,16 @@ __global__ void __launch_bounds__(kThreads, tile_min_ctas<T, FMT>()) tile_kernel
             const int t = threadIdx.x + j * kThreads;
             const int tr = t / RBPR, tb = t % RBPR;
             const int64_t gr = lr0 + tr, gc = lc0 + (int64_t)tb * BR;
-            const bool valid = t < TR * RBPR && gr < rows && gc < cols;
+            const bool valid = t < TR * RBPR && gr < rows;
             const char *src = (const char *)a.x + (gr * cols + gc) * (int64_t)sizeof(T);
+            // Each 16-byte vector is fetched only if it lies inside the row:
+            // a column-only MXFP4 call admits cols % 32 == 16, where the last
+            // 1x32 row block of a row holds only 16 elements (cols is a
+            // multiple of 16, hence of E, so a vector is all in or all out).
 #pragma unroll
             for (int k = 0; k < NV; ++k)
-                nxt[j][k] = valid ? ld16(src + 16 * k) : make_uint4(0, 0, 0, 0);
+                nxt[j][k] = (valid && gc + (int64_t)k * E < cols) ? ld16(src + 16 * k)
+                                                                  : make_uint4(0, 0, 0, 0);
         }
     };
 

@@ -237,7 +237,10 @@ FQ_API fq_status fq_osci_update_reset(const fq_config *cfg, int32_t ntensors, co
  *    errors are those of fq_osci_update.
  *  - The first call on each device looks up the array's device address with
  *    that device current (cudaGetSymbolAddress); make that first call before
- *    any stream capture.
+ *    any stream capture.  The address is kept for the life of the process:
+ *    it belongs to the device's primary context, so after cudaDeviceReset
+ *    (which destroys that context and the array with it) this entry point
+ *    must not be called again in that process.
  *  - Every call shares the one array; each call clears the slots it uses on
  *    its stream before using them, but calls that overlap on the GPU (other
  *    streams, other threads) race on it. */

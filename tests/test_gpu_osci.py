@@ -133,38 +133,52 @@ def test_osci_flip_example():
     assert float(g.master[0][0, 16]) == 2688.0
 
 
-@pytest.mark.slow
-def test_osci_full_moe_two_steps():
+def _full_moe_group(checked_idx, seed=1234):
     """The 32-expert MoE workload at full size (64 matrices, 1.06 G weights):
-    two update steps through the grouped launch; the first and last matrices
-    are checked against the oracle bit for bit, every matrix for invariants."""
+    the matrices in checked_idx come from the CPU generator (so the oracle can
+    take them), the rest from a device generator."""
     spec = W.WORKLOADS["moe_qat"]
     E, up, down = spec["experts"], spec["up_shape"], spec["down_shape"]
     shapes = [up, down] * E
-    checked = {0: None, len(shapes) - 1: None}
     gen = torch.Generator(device=DEV)
-    gen.manual_seed(1234)
-    ws = []
+    gen.manual_seed(seed)
+    ws, host = [], {}
     for i, s in enumerate(shapes):
-        if i in checked:
+        if i in checked_idx:
             w = W.normal(s, 0.02, seed=500 + i).to(torch.bfloat16)
-            checked[i] = w
+            host[i] = w
             ws.append(w)
         else:
             ws.append((torch.randn(s, generator=gen, device=DEV) * 0.02).to(torch.bfloat16))
+    return shapes, ws, host, gen
+
+
+def _full_moe_deltas(shapes, checked_idx, t, gen):
+    deltas, host = [], {}
+    for i, s in enumerate(shapes):
+        if i in checked_idx:
+            d = W.master_update(s, t)
+            host[i] = d
+            deltas.append(d.to(DEV))
+        else:
+            deltas.append(torch.randn(s, generator=gen, device=DEV) * 1e-4)
+    return deltas, host
+
+
+@pytest.mark.slow
+def test_osci_full_moe_two_steps():
+    """Two update steps through the grouped launch on the full MoE group;
+    eight matrices spread over the group (both shapes, first and last) are
+    checked against the oracle bit for bit after each step, every matrix for
+    invariants."""
+    checked = (0, 9, 18, 27, 36, 45, 54, 63)
+    shapes, ws, host_w, gen = _full_moe_group(checked)
     cfg = fq.Config(fq.NVFP4, fq.RNE)
     g = GpuOsci(ws, cfg)
     del ws
-    sts = {i: oracle.OsciState(w.float().numpy(), oracle.NVFP4) for i, w in checked.items()}
+    sts = {i: oracle.OsciState(w.float().numpy(), oracle.NVFP4) for i, w in host_w.items()}
     for t in (1, 2):
-        deltas, host = [], {}
-        for i, s in enumerate(shapes):
-            if i in checked:
-                d = W.master_update(s, t)
-                host[i] = d
-                deltas.append(d.to(DEV))
-            else:
-                deltas.append(torch.randn(s, generator=gen, device=DEV) * 1e-4)
+        deltas, host = _full_moe_deltas(shapes, checked, t, gen)
         g.step(deltas, t)
         torch.cuda.synchronize()
         del deltas
@@ -174,3 +188,62 @@ def test_osci_full_moe_two_steps():
     for i in range(len(shapes)):
         assert torch.isfinite(g.dq[i]).all() and (g.dq[i] >= 0).all()
         assert (g.dm[i] > 0).float().mean() > 0.99
+
+
+@pytest.mark.slow
+def test_osci_full_moe_fused_reset():
+    """The benchmark's dominant call, fq_osci_update_reset, on the full MoE
+    group after one ordinary update.  The first, a middle and the last matrix
+    are checked against the oracle's step + reset bit for bit.  Every matrix
+    is checked against the unfused path (fq_osci_update then fq_osci_reset on
+    a copy of the state), and the fused call's reset count equals the number
+    of weights with dist_Q > 4 dist_M after the update, summed over all 64
+    matrices; over the checked matrices that number equals the oracle's."""
+    checked = (0, 31, 63)
+    shapes, ws, host_w, gen = _full_moe_group(checked, seed=4321)
+    cfg = fq.Config(fq.NVFP4, fq.RNE)
+    g = GpuOsci(ws, cfg)
+    del ws
+    sts = {i: oracle.OsciState(w.float().numpy(), oracle.NVFP4) for i, w in host_w.items()}
+    # step 1: ordinary update, large enough to move some weights across bins
+    deltas, host = _full_moe_deltas(shapes, checked, 1, gen)
+    deltas = [d * 30 for d in deltas]
+    host = {i: d * 30 for i, d in host.items()}
+    g.step(deltas, 1)
+    for i, st in sts.items():
+        st.step(host[i].numpy(), offset=1)
+    del deltas
+    # step 2: the window-end step, fused and unfused (on a copy)
+    deltas, host = _full_moe_deltas(shapes, checked, 2, gen)
+    u = GpuOsci.__new__(GpuOsci)
+    u.cfg = cfg
+    u.master = [m.clone() for m in g.master]
+    u.dq = [d.clone() for d in g.dq]
+    u.dm = [d.clone() for d in g.dm]
+    u.prev = [fq.QTensor(q.codes.clone(), q.scales.clone(), q.tscale.clone()) for q in g.prev]
+    u.next = [fq.alloc_qtensor(*m.shape, fq.NVFP4, DEV) for m in g.master]
+    u.xhat = [torch.empty_like(x) for x in g.xhat]
+    u.mask = [torch.empty_like(x) for x in g.mask]
+    cnt = torch.zeros(1, dtype=torch.int64, device=DEV)
+    fq.fq_osci_update_reset(fq.Config(fq.NVFP4, fq.RNE, 0, 2), g.master, deltas, g.dq, g.dm,
+                            g.prev, g.next, 4.0, n_reset=cnt, xhat=g.xhat, mask=g.mask)
+    g.prev, g.next = g.next, g.prev
+    u.step(deltas, 2)
+    torch.cuda.synchronize()
+    del deltas
+    per = [int((dq > 4.0 * dm).sum().item()) for dq, dm in zip(u.dq, u.dm)]
+    ucnt = u.reset(4.0)
+    torch.cuda.synchronize()
+    assert int(cnt.item()) == int(ucnt.item()) == sum(per)
+    assert sum(per) > 0
+    for i in range(len(shapes)):
+        for name, a, b in (("master", g.master[i], u.master[i]), ("dq", g.dq[i], u.dq[i]),
+                           ("dm", g.dm[i], u.dm[i]), ("xhat", g.xhat[i], u.xhat[i]),
+                           ("codes", g.prev[i].codes, u.prev[i].codes),
+                           ("scales", g.prev[i].scales, u.prev[i].scales)):
+            assert torch.equal(a.view(torch.uint8), b.view(torch.uint8)), (i, name)
+    for i, st in sts.items():
+        out = st.step(host[i].numpy(), offset=2)
+        n = st.reset(4.0)
+        assert n == per[i], (i, n, per[i])
+        _compare(f"fused.{i}", g, i, st, out)

@@ -17,11 +17,15 @@ One step = one pass of the whole hot path over the synthetic workloads:
   qad_kl        QAD distillation loss: BF16 teacher and student logits [4096, 201088]
                 (gpt-oss's vocabulary size), per-row KL(teacher || student) at T = 1, its
                 mean, and the BF16 gradient with respect to the student logits
-  moe_qat       one QAT step over 32 MoE experts (64 FP32 master matrices [2880, 5760] and
-                [5760, 2880], 1.06 G weights): update + NVFP4 fake-quant + OsciReset
-                statistics, then the OsciReset reset pass over the same weights
+  osci_update   one ordinary QAT step over 32 MoE experts (64 FP32 master matrices
+                [2880, 5760] and [5760, 2880], 1.06 G weights): update + NVFP4
+                fake-quant + OsciReset statistics (what 99 of every 100 steps of an
+                OsciReset window run)
+  osci_update_reset  the window's last step over the same weights: the same update
+                with the OsciReset reset fused into its second pass
 The metric is algorithmic HBM bytes / device time (GB/s); elements/s are
-reported per workload.  Inputs live in HBM before the timed region; the step's
+reported per workload, with fractions of the measured copy bandwidth and of
+the ~8 TB/s HBM3e spec.  Inputs live in HBM before the timed region; the step's
 working set (about 26 GB) is far larger than L2, so every workload starts cold.
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
@@ -45,6 +49,7 @@ if ROOT not in sys.path:
 METRIC = "fake-quant HBM GB/s and % of GB300 HBM peak; Gelem/s per format"
 UNIT = "GB/s"
 FALLBACK_HBM_GBS = 6800.0
+SPEC_HBM_GBS = 8000.0   # GB300 HBM3e peak as specified (~8 TB/s)
 
 # Bytes per element each workload must move (reads + writes of its definition;
 # the NVFP4 tensor amax is a second read of x).
@@ -57,12 +62,13 @@ BYTES_PER_ELEM = {
     "grad_rht_rowcol": 2 + 2 * (0.5 + 1 / 16 + 4 / 128),
     "act_outliers": 2 + 2 + 0.5 + 1 / 16 + 819 / 8192 + 2 + 1 / 8,
     "qad_kl": 2 + 2 + 2,
+    "osci_update": 20 + (4 + 0.5 + 1 / 16 + 8 + 0.5 + 1 / 16 + 2 + 1 / 8),
     "osci_update_reset": 20 + (4 + 0.5 + 1 / 16 + 8 + 8 + 0.5 + 1 / 16 + 2 + 1 / 8),
 }
 # Our kernels launched per step (memsets not counted).
 LAUNCHES_PER_STEP = {"nvfp4_small": 2, "mxfp4_weight": 1, "nvfp4_act": 2, "ste_backward": 1,
                      "grad_2level": 1, "grad_rht_rowcol": 1, "act_outliers": 2,
-                     "qad_kl": 2, "osci_update_reset": 2}
+                     "qad_kl": 2, "osci_update": 2, "osci_update_reset": 2}
 # DRAM traffic per launch of the dominant call from an ncu capture, valid only
 # for the kernel source it was taken on (sha256 of the OsciReset sources).
 # Captured on the 2-expert case (66.4 M weights: pass A + pass B read+write
@@ -162,7 +168,7 @@ class Suite:
     kernel's DRAM traffic, which at 4096 rows still sits in L2 when it ends)."""
 
     ORDER = ("nvfp4_small", "mxfp4_weight", "nvfp4_act", "ste_backward", "grad_2level",
-             "grad_rht_rowcol", "act_outliers", "qad_kl", "osci_update_reset")
+             "grad_rht_rowcol", "act_outliers", "qad_kl", "osci_update", "osci_update_reset")
 
     def __init__(self, dev, only=None, experts=None, qad_rows=None, mxfp4_rows=None):
         import torch
@@ -240,14 +246,18 @@ class Suite:
             self.dz8 = torch.empty_like(self.zs8)
             self.err8 = torch.zeros(1, dtype=torch.int32, device=dev)
             self.elems["qad_kl"] = self.zt8.numel()
-        if "osci_update_reset" in want:
+        if want & {"osci_update", "osci_update_reset"}:
             m = W.WORKLOADS["moe_qat"]
             ws = W.moe_weights(experts or m["experts"], m["up_shape"], m["down_shape"],
                                seed=4, device=dev)
             self.cfg5 = fq.Config(fq.NVFP4)
             self.master = [w.float() for w in ws]
             del ws
+            # one update per step call; each step reuses its update tensors: the
+            # work (every weight read and written) does not depend on their values
             self.delta = [W.master_update(t.shape, 1, device=dev) for t in self.master]
+            self.delta_u = ([W.master_update(t.shape, 2, device=dev) for t in self.master]
+                            if "osci_update" in want else None)
             self.dq = [torch.zeros_like(t) for t in self.master]
             self.dm = [torch.zeros_like(t) for t in self.master]
             self.prev = [fq.fq_quantize(t, self.cfg5)[0] for t in self.master]
@@ -258,7 +268,8 @@ class Suite:
             self.ws5 = torch.empty(fq.fq_osci_workspace_size(len(self.master)),
                                    dtype=torch.uint8, device=dev)
             self.nreset = torch.zeros(1, dtype=torch.int64, device=dev)
-            self.elems["osci_update_reset"] = sum(t.numel() for t in self.master)
+            nw = sum(t.numel() for t in self.master)
+            self.elems.update({"osci_update": nw, "osci_update_reset": nw})
         self.elems = {k: v for k, v in self.elems.items() if k in want}
         torch.cuda.synchronize()
 
@@ -309,6 +320,12 @@ class Suite:
     def qad_kl(self):
         self.fq.fq_qad_kl(self.zt8, self.zs8, loss_rows=self.loss8, loss_mean=self.mean8,
                           dz=self.dz8, err=self.err8)
+
+    def osci_update(self):
+        # an ordinary QAT step of the OsciReset window
+        self.fq.fq_osci_update(self.cfg5, self.master, self.delta_u, self.dq, self.dm,
+                               self.prev, self.next, xhat=self.xh5, mask=self.m5, ws=self.ws5)
+        self.prev, self.next = self.next, self.prev
 
     def osci_update_reset(self):
         # one QAT step that also ends the OsciReset window (reset fused in)
@@ -411,6 +428,8 @@ def e2e_buffers(suite):
                                            suite.fp87])
     if "qad_kl" in suite.names:
         io["qad_kl"] = ([suite.zt8, suite.zs8], [suite.loss8, suite.mean8])
+    if "osci_update" in suite.names:
+        io["osci_update"] = (list(suite.delta_u), [suite.dq[0][:1]])
     if "osci_update_reset" in suite.names:
         io["osci_update_reset"] = (list(suite.delta), [suite.nreset])
     return io
@@ -607,16 +626,16 @@ def _oracle_inputs(div):
     d["zt8"], d["zs8"] = f32(zt8), f32(zs8)
     d["w5"] = f32(W.normal((5760 // div, 5760), 0.02, seed=4).to(torch.bfloat16))
     d["d5"] = W.master_update((5760 // div, 5760), 1).numpy()
+    d["d5b"] = W.master_update((5760 // div, 5760), 2).numpy()
     _ORACLE_INPUTS[div] = d
     return d
 
 
-def oracle_sample(div=1):
-    """Time the oracle on a bounded sample of every workload (row counts of the
-    samples divided by div).  Returns {workload: (elements, seconds)} and a
-    text description."""
+def _oracle_run(d):
+    """One pass of the oracle over every workload's sample: {workload:
+    (elements, seconds)}.  The OsciReset state is built before the clock
+    starts."""
     import oracle
-    d = _oracle_inputs(div)
     res = {}
 
     def timed(fn):
@@ -624,6 +643,7 @@ def oracle_sample(div=1):
         fn()
         return time.perf_counter() - t
 
+    st = oracle.OsciState(d["w5"], oracle.NVFP4)
     res["nvfp4_small"] = (d["x1"].size, timed(lambda: oracle.quantize(
         d["x1"], oracle.NVFP4, want_xhat=True, want_mask=True)))
     res["mxfp4_weight"] = (d["x2"].size, timed(lambda: oracle.quantize(
@@ -650,20 +670,63 @@ def oracle_sample(div=1):
         oracle.f32_to_bf16_bits(q["xhat"])
     res["act_outliers"] = (d["x7"].size, timed(c7))
     res["qad_kl"] = (d["zt8"].size, timed(lambda: oracle.qad_kl(d["zt8"], d["zs8"])))
-    st = oracle.OsciState(d["w5"], oracle.NVFP4)
 
-    def upd():
-        out = st.step(d["d5"], offset=1)
+    def upd(delta, offset):
+        out = st.step(delta, offset=offset)
         oracle.f32_to_bf16_bits(out["xhat"])
-    t_upd = timed(upd)
-    res["osci_update_reset"] = (d["w5"].size, t_upd + timed(lambda: st.reset(4.0)))
+    res["osci_update"] = (d["w5"].size, timed(lambda: upd(d["d5"], 1)))
+    res["osci_update_reset"] = (d["w5"].size, timed(lambda: upd(d["d5b"], 2))
+                                + timed(lambda: st.reset(4.0)))
+    return res
+
+
+def host_cores():
+    """The host cores this process may run on."""
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def oracle_sample(div=1, threads=1):
+    """Time the oracle on a bounded sample of every workload (row counts of the
+    samples divided by div).  With threads > 1, that many threads each run the
+    whole sample at once (the oracle's C code runs without the interpreter
+    lock), so the per-element times are those of all cores working together:
+    each thread's time divided by the number of threads.  Returns ({workload:
+    (elements, seconds per element-equivalent run)}, description, wall
+    seconds)."""
+    import threading
+    d = _oracle_inputs(div)
+    if threads <= 1:
+        t0 = time.perf_counter()
+        res = _oracle_run(d)
+        wall = time.perf_counter() - t0
+    else:
+        outs = [None] * threads
+        go = threading.Barrier(threads + 1)
+
+        def work(i):
+            go.wait()
+            outs[i] = _oracle_run(d)
+        ths = [threading.Thread(target=work, args=(i,)) for i in range(threads)]
+        for th in ths:
+            th.start()
+        go.wait()
+        t0 = time.perf_counter()
+        for th in ths:
+            th.join()
+        wall = time.perf_counter() - t0
+        res = {k: (outs[0][k][0], sum(o[k][1] for o in outs) / threads / threads)
+               for k in outs[0]}
     r = lambda n: n // div  # noqa: E731
-    desc = (f"oracle (scalar C, 1 thread) on: nvfp4_small {r(256)} rows; mxfp4_weight "
-            f"{r(4096)} rows; nvfp4_act {r(4096)} rows row+col; ste_backward {r(4096)}x8192; "
-            f"grad_2level {r(8192)} rows SR; grad_rht_rowcol {r(2048)} rows; act_outliers "
-            f"{r(2048)} rows; qad_kl {max(16 // div, 1)} rows; osci update+reset on a "
-            f"[{r(5760)}, 5760] matrix; per-element rates scaled to the full step's elements")
-    return res, desc
+    desc = (f"oracle (scalar C) on {threads} host thread(s), each running: nvfp4_small "
+            f"{r(256)} rows; mxfp4_weight {r(4096)} rows; nvfp4_act {r(4096)} rows row+col; "
+            f"ste_backward {r(4096)}x8192; grad_2level {r(8192)} rows SR; grad_rht_rowcol "
+            f"{r(2048)} rows; act_outliers {r(2048)} rows; qad_kl {max(16 // div, 1)} rows; "
+            f"osci update, then update+reset, on a [{r(5760)}, 5760] matrix; per-element rates "
+            f"scaled to the full step's elements")
+    return res, desc, wall
 
 
 def oracle_gbs(sample, elems_full):
@@ -671,7 +734,8 @@ def oracle_gbs(sample, elems_full):
     the sampled per-element rates)."""
     secs = 0.0
     for k, (n, t) in sample.items():
-        secs += elems_full[k] * (t / n)
+        if k in elems_full:
+            secs += elems_full[k] * (t / n)
     total = sum(BYTES_PER_ELEM[k] * elems_full[k] for k in elems_full)
     return total / secs / 1e9, secs
 
@@ -680,6 +744,7 @@ FULL_ELEMS = {"nvfp4_small": 256 * 1024, "mxfp4_weight": 4096 * 4096,
               "nvfp4_act": 8192 * 8192, "ste_backward": 8192 * 8192,
               "grad_2level": 16384 * 4096, "grad_rht_rowcol": 16384 * 4096,
               "act_outliers": 8192 * 8192, "qad_kl": 4096 * 201088,
+              "osci_update": 32 * 2 * 2880 * 5760,
               "osci_update_reset": 32 * 2 * 2880 * 5760}
 
 
@@ -701,11 +766,11 @@ def config_block(names=None, experts=None, qad_rows=None, mxfp4_rows=None):
                         "E4M3 by calibration amax, the rest NVFP4 RNE with xhat + STE mask; "
                         "qad_kl bf16 teacher/student logits 4096x201088: per-row KL at T=1, "
                         "mean, bf16 student gradient; "
-                        "moe_qat 32 experts x "
-                        "(2880x5760 + 5760x2880) FP32 master: one QAT step with OsciReset "
-                        "statistics and the window-end reset fused in",
+                        "osci_update: 32 MoE experts x (2880x5760 + 5760x2880) FP32 master, one "
+                        "ordinary QAT step with OsciReset statistics; osci_update_reset: the "
+                        "window's last step on the same weights, the reset fused in",
             "elements_per_step": sum(FULL_ELEMS.values()),
-            "l2": "no flush: the step's working set (~26 GB) exceeds L2, inputs are cold",
+            "l2": "no flush: the step's working set (~30 GB) exceeds L2, inputs are cold",
             "bytes": "algorithmic (definition reads + writes; NVFP4 amax is a second read)"}
 
 
@@ -761,7 +826,8 @@ def main():
             per[n] = {"gbs": round(bps[n] / t / 1e9, 1),
                       "gelem_s": round(suite.elems[n] / t / 1e9, 3),
                       "ms": round(per_ms[n], 4),
-                      "frac_hbm": round(bps[n] / t / 1e9 / peak, 3)}
+                      "frac_hbm": round(bps[n] / t / 1e9 / peak, 3),
+                      "frac_spec": round(bps[n] / t / 1e9 / SPEC_HBM_GBS, 3)}
         dom = max(suite.names, key=lambda n: per_ms[n])
         achieved = bps[dom] / (per_ms[dom] / 1e3) / 1e9
         tr = NCU_TRAFFIC.get(dom, {})
@@ -779,6 +845,8 @@ def main():
                          "achieved": round(achieved, 1), "peak": peak,
                          "peak_kind": f"{peak_kind} copy bandwidth",
                          "unit": "GB/s", "frac": round(achieved / peak, 3),
+                         "frac_spec": round(achieved / SPEC_HBM_GBS, 3),
+                         "spec_peak": SPEC_HBM_GBS,
                          "traffic": traffic,
                          "algorithmic_bytes_per_launch": int(bps[dom])},
             "gpu_launches": sum(LAUNCHES_PER_STEP[n] for n in suite.names) * args.steps,
@@ -796,12 +864,19 @@ def main():
             line["gemm_nvfp4"] = run_gemm(fmt_name="nvfp4")
             line["gemm_mxfp4"] = run_gemm(fmt_name="mxfp4")
         if not args.no_cpu_baseline and world == 1 and not reduced:
-            sample, desc = oracle_sample()
+            # all host cores (one sample per thread, at once), then one core
+            cores = host_cores()
+            sample, desc, wall = oracle_sample(threads=cores)
             gbs, secs = oracle_gbs(sample, suite.elems)
-            line["cpu_baseline"] = {"value": round(gbs, 4), "unit": UNIT, "cores": 1,
+            sample1, desc1, wall1 = oracle_sample(threads=1)
+            gbs1, secs1 = oracle_gbs(sample1, suite.elems)
+            line["cpu_baseline"] = {"value": round(gbs, 4), "unit": UNIT, "cores": cores,
                                     "kind": "oracle", "sample": desc,
-                                    "sample_seconds": round(sum(t for _, t in sample.values()), 2),
-                                    "est_seconds_per_step": round(secs, 1)}
+                                    "sample_wall_seconds": round(wall, 2),
+                                    "est_seconds_per_step": round(secs, 2),
+                                    "single_thread": {"value": round(gbs1, 4), "cores": 1,
+                                                      "sample_wall_seconds": round(wall1, 2),
+                                                      "est_seconds_per_step": round(secs1, 1)}}
         print(json.dumps(line), flush=True)
     if dist:
         dist.barrier()
@@ -809,31 +884,41 @@ def main():
 
 
 def main_reference(args, rank, world):
-    """The oracle as it stands, on the host cores: each step times a bounded
-    sample of every workload; value = the suite's bytes at the sampled rates."""
+    """The oracle as it stands, on all host cores: each step has every core run
+    a bounded sample of every workload at once; value = the suite's bytes at
+    the sampled per-element rates.  ms_per_step is the measured wall time of
+    one such sampled step; the time the oracle would take for the full-size
+    step is reported beside it as an estimate."""
     if rank != 0:
         return
-    # each step times a sample an eighth the size of the cpu_baseline's (about
+    cores = host_cores()
+    # each thread's sample is an eighth the size of the cpu_baseline's (about
     # a second of oracle work), so that the whole run stays within minutes
     for _ in range(args.warmup):
-        oracle_sample(div=8)
-    vals, secs = [], []
+        oracle_sample(div=8, threads=cores)
+    vals, walls, ests = [], [], []
     desc = ""
     for _ in range(args.steps):
-        sample, desc = oracle_sample(div=8)
+        sample, desc, wall = oracle_sample(div=8, threads=cores)
         v, s = oracle_gbs(sample, FULL_ELEMS)
         vals.append(v)
-        secs.append(sum(t for _, t in sample.values()))
+        walls.append(wall)
+        ests.append(s)
     value = statistics.median(vals)
-    total = sum(BYTES_PER_ELEM[k] * FULL_ELEMS[k] for k in FULL_ELEMS)
+    ms = statistics.median(walls) * 1e3
     line = {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": UNIT,
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
-            "ms_per_step": round(total / (value * 1e9) * 1e3, 1), "higher_is_better": True,
+            "ms_per_step": round(ms, 1),
+            "ms_per_step_basis": "measured wall time of one sampled step (every core runs an "
+                                 "eighth-size sample of each workload); value is the suite's "
+                                 "bytes at the per-element rates measured there",
+            "ms_per_step_full_size_estimate": round(statistics.median(ests) * 1e3, 1),
+            "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f32",
             "data": "synthetic (seeded torch generators)", "config": config_block(),
-            "cpu_baseline": {"kind": "oracle", "cores": 1, "sample": desc,
+            "cpu_baseline": {"kind": "oracle", "cores": cores, "sample": desc,
                              "value": round(value, 4), "unit": UNIT,
-                             "sample_seconds_per_step": round(statistics.median(secs), 2)},
+                             "sample_wall_seconds_per_step": round(ms / 1e3, 2)},
             "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)

@@ -368,6 +368,18 @@ def run_ours(args, rank, world, dist):
     for _ in range(args.warmup):
         suite.step()
     torch.cuda.synchronize()
+    graph = None
+    if not args.eager:
+        try:
+            graph = capture_step(suite)
+        except Exception as e:  # capture is an optimisation of the launches only
+            log(f"CUDA graph capture failed ({e!r}); timing eager launches")
+            graph = None
+            torch.cuda.synchronize()
+    if graph is not None:
+        for _ in range(args.warmup):
+            graph[0].replay()
+        torch.cuda.synchronize()
     if dist:
         dist.barrier()
     torch.cuda.synchronize()
@@ -379,14 +391,17 @@ def run_ours(args, rank, world, dist):
     t1 = torch.cuda.Event(enable_timing=True)
     t0.record(stream)
     for _ in range(args.steps):
-        for name in suite.names:
-            a = torch.cuda.Event(enable_timing=True)
-            b = torch.cuda.Event(enable_timing=True)
-            a.record(stream)
-            getattr(suite, name)()
-            b.record(stream)
-            ev[name].append((a, b))
-        suite.step_no += 1
+        if graph is not None:
+            graph[0].replay()
+        else:
+            for name in suite.names:
+                a = torch.cuda.Event(enable_timing=True)
+                b = torch.cuda.Event(enable_timing=True)
+                a.record(stream)
+                getattr(suite, name)()
+                b.record(stream)
+                ev[name].append((a, b))
+            suite.step_no += 1
     t1.record(stream)
     torch.cuda.synchronize()
     if dist:
@@ -394,14 +409,47 @@ def run_ours(args, rank, world, dist):
     clk = clocks.stop() if clocks else None
     suite.check()
     ms = t0.elapsed_time(t1)
-    per_ms = {n: sum(a.elapsed_time(b) for a, b in ev[n]) / args.steps for n in suite.names}
+    if graph is not None:
+        # per-workload times: the events the graph records between workloads,
+        # read after each of a second series of replays
+        g, evs = graph
+        acc = [0.0] * len(suite.names)
+        for _ in range(args.steps):
+            g.replay()
+            torch.cuda.synchronize()
+            for i in range(len(suite.names)):
+                acc[i] += evs[i].elapsed_time(evs[i + 1])
+        per_ms = {n: acc[i] / args.steps for i, n in enumerate(suite.names)}
+    else:
+        per_ms = {n: sum(a.elapsed_time(b) for a, b in ev[n]) / args.steps for n in suite.names}
     ms = max_over_ranks(ms, dist, dev)
+    suite.launch_mode = "cuda_graph" if graph is not None else "eager"
 
     # end-to-end: pinned host inputs -> device, the same calls, results -> host
     e2e = run_e2e(args, suite, total_bytes) if not args.no_e2e else None
     if e2e is not None:
         e2e["ms_total"] = max_over_ranks(e2e["ms_total"], dist, dev)
     return suite, bps, total_bytes, ms, per_ms, clk, e2e
+
+
+def capture_step(suite):
+    """One step of the suite (every workload once) captured as a CUDA graph,
+    with timing events that the graph itself records between the workloads.
+    The step's two OsciReset calls swap the ping-pong quantized buffers twice,
+    so every replay starts from the buffers the capture started from; the
+    stochastic-rounding offsets are those of the captured step."""
+    import torch
+    names = suite.names
+    evs = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(len(names) + 1)]
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, capture_error_mode="relaxed"):
+        s = torch.cuda.current_stream()
+        evs[0].record(s)
+        for i, name in enumerate(names):
+            getattr(suite, name)()
+            evs[i + 1].record(s)
+    suite.step_no += 1
+    return g, evs
 
 
 def e2e_buffers(suite):
@@ -781,6 +829,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--eager", action="store_true",
+                    help="time eager launches instead of a CUDA graph of the step")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--only", nargs="*", choices=Suite.ORDER, default=None,
                     help="run only these workloads (profiling a single kernel)")
@@ -838,7 +888,8 @@ def main():
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
             "data": "synthetic (seeded torch generators, shapes/distributions of the "
                     "workloads)",
-            "config": config_block(suite.names, args.experts, args.qad_rows, args.mxfp4_rows),
+            "config": {**config_block(suite.names, args.experts, args.qad_rows, args.mxfp4_rows),
+                       "launch": suite.launch_mode},
             "per_workload": per,
             "roofline": {"bound": "hbm", "kernel": dom + (" (osci_pass_a + osci_pass_b<reset>)"
                                                            if dom == "osci_update_reset" else ""),

@@ -126,6 +126,7 @@ fq_status quantize_common(const fq_config *cfg, const void *x, int32_t x_dtype, 
         a.offset = cfg->offset;
         a.stream_id = 0;
         a.rht_seed = cfg->rht_seed;
+        a.key = philox_key(cfg->seed);
         return cuda_status(launch_row(a, bf16, fmt, cfg->rounding, s));
     }
     TileArgs t{};
@@ -148,6 +149,7 @@ fq_status quantize_common(const fq_config *cfg, const void *x, int32_t x_dtype, 
     t.seed = cfg->seed;
     t.offset = cfg->offset;
     t.rht_seed = cfg->rht_seed;
+    t.key = philox_key(cfg->seed);
     return cuda_status(launch_tile(t, bf16, fmt, cfg->rounding, s));
 }
 
@@ -230,6 +232,7 @@ static fq_status osci_update_impl(const fq_config *cfg, int32_t ntensors, const 
         a.n_reset = reset ? n_reset : nullptr;
         a.seed = cfg->seed;
         a.offset = cfg->offset;
+        a.key = philox_key(cfg->seed);
         a.amax = static_cast<float *>(workspace);
         for (int32_t j = 0; j < cnt; ++j) {
             const int32_t i = i0 + j;
@@ -514,6 +517,7 @@ fq_status fq_quantize_outliers(const fq_config *cfg, const void *x, int32_t x_dt
     a.mask = mask;
     a.seed = cfg->seed;
     a.offset = cfg->offset;
+    a.key = philox_key(cfg->seed);
     return cuda_status(launch_outlier_quant(a, bf16, fmt, cfg->rounding, s));
 }
 

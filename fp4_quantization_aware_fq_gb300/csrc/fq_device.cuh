@@ -16,6 +16,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "fq_internal.h"
+
 namespace fqk {
 
 enum Fmt : int { NVFP4 = 0, MXFP4 = 1, NV2L = 2 };
@@ -202,16 +204,22 @@ __device__ __forceinline__ uint32_t e4m3_rn_sat(float s)
     return out & 0xFFu;
 }
 
-// Value of a non-negative E4M3 code (never 0x7F here): subnormal m * 2^-9,
-// normal (8 + m) * 2^(e - 10).
+// Value of a non-negative E4M3 code (never 0x7F here).  Every E4M3 value is
+// exact in FP16 (normals (8 + m) 2^(e - 10), subnormals m 2^-9), so the
+// hardware E4M3 -> FP16 conversion followed by the exact FP16 -> FP32 widening
+// gives it in two conversions.  The code sits in both bytes of the pair, so
+// either half of the result holds it.
 __device__ __forceinline__ float e4m3_value(uint32_t code)
 {
-    const uint32_t e = (code >> 3) & 15u, m = code & 7u;
-    const uint32_t mant = e ? (8u | m) : m;
-    const uint32_t ee = e ? e : 1u;
-    // 2^(ee - 10) as an FP32 bit pattern: ee - 10 ranges over [-9, 5]
-    const float p2 = __uint_as_float((ee - 10u + 127u) << 23);
-    return __fmul_rn(__uint2float_rn(mant), p2);
+    uint32_t h;
+    asm("{\n\t"
+        ".reg .b16 c;\n\t"
+        "cvt.u16.u32 c, %1;\n\t"
+        "cvt.rn.f16x2.e4m3x2 %0, c;\n\t"
+        "}"
+        : "=r"(h)
+        : "r"(code * 0x101u));
+    return __half2float(__ushort_as_half((unsigned short)(h & 0xFFFFu)));
 }
 
 // ---------------------------------------------------------------- block scales
@@ -222,21 +230,25 @@ struct Scale {
     uint32_t code;
 };
 
-// 1 / (6 s_outer), rounded, used to find block scale codes without dividing
-// (nv_scale_code).  0 when s_outer is 0 or below 2^-120: there 6 s_outer or its
-// reciprocal would leave the normal range, and nv_scale_code divides instead.
+// An approximation of 1 / (6 s_outer) (the hardware reciprocal, within 1 ulp),
+// used to find block scale codes without dividing (nv_scale_code).  0 when
+// s_outer is 0 or below 2^-120: there 6 s_outer or its reciprocal would leave
+// the normal range, and nv_scale_code divides instead.
 __device__ __forceinline__ float nv_inv6(float s_outer)
 {
-    return (s_outer < 0x1p-120f) ? 0.0f : __frcp_rn(__fmul_rn(6.0f, s_outer));
+    float r;
+    asm("rcp.approx.f32 %0, %1;" : "=f"(r) : "f"(__fmul_rn(6.0f, s_outer)));
+    return (s_outer < 0x1p-120f) ? 0.0f : r;
 }
 
 // E4M3 code of the block scale s_b = (amax_b / 6) / s_outer (two IEEE
 // divisions, in that order).  With every operand and quotient normal,
-// amax_b * inv6 is within 5 ulps of s_b (three roundings on each side), so
-// both round to the same E4M3 code unless the product lies within 64 ulps of
-// an E4M3 rounding boundary -- in the E4M3 normal range every boundary has
-// FP32 mantissa bits 19..0 equal to 0x80000 -- or below 2^-6, where E4M3 is
-// subnormal.  Those rare blocks take the exact divisions, and so do blocks
+// amax_b * inv6 differs from s_b by at most 3 * 2^-23 relative (two roundings
+// in s_b; the rounding of 6 s_outer, the reciprocal's 1 ulp and the product's
+// rounding in the estimate), i.e. by at most 6 ulps, so both round to the same
+// E4M3 code unless the product lies within 64 ulps of an E4M3 rounding
+// boundary -- in the E4M3 normal range every boundary has FP32 mantissa bits
+// 19..0 equal to 0x80000 -- or below 2^-6, where E4M3 is subnormal.  Those rare blocks take the exact divisions, and so do blocks
 // whose amax_b / 6 would be subnormal (amax_b < 2^-123) or whose outer scale
 // has no product form (inv6 = 0).
 __device__ __forceinline__ uint32_t nv_scale_code(float amax_b, float s_outer, float inv6)
@@ -306,9 +318,18 @@ __device__ __forceinline__ Scale mx_scale(float amax_b)
     return s;
 }
 
+// amax_o / 2688 rounded to nearest (IEEE division).  q0 = amax_o * R with
+// R = RN(1 / 2688), then one FMA step with the exact residual amax_o - 2688 q0.
+// This equals the IEEE quotient for every finite amax_o >= 2^-119 (checked
+// exhaustively against division on the host); smaller amax_o, whose quotient
+// is subnormal or nearly so, take the division.
 __device__ __forceinline__ float outer_scale(float amax_o)
 {
-    return __fdiv_rn(amax_o, 2688.0f);
+    if (amax_o < 0x1p-119f)
+        return __fdiv_rn(amax_o, 2688.0f);
+    const float R = 0x1.861862p-12f;
+    const float q0 = __fmul_rn(amax_o, R);
+    return __fmaf_rn(__fmaf_rn(-q0, 2688.0f, amax_o), R, q0);
 }
 
 // Effective scale of a stored block (for dequantization).
@@ -323,24 +344,8 @@ __device__ __forceinline__ float stored_s_eff(uint32_t code, float s_outer)
 // ---------------------------------------------------------------- Philox4x32-10
 // Salmon, Moraes, Dror, Shaw, "Parallel Random Numbers: As Easy as 1, 2, 3"
 // (SC'11): ten rounds; each round multiplies counter words 0 and 2 by the two
-// round multipliers, mixes the high halves with words 1 / 3 and the key, and
-// the key is bumped by the two Weyl constants between rounds.  The round keys
-// (the key plus r times the Weyl constants) are computed once per thread.
-struct PhiloxKey {
-    uint32_t k0[10], k1[10];
-};
-
-__device__ __forceinline__ PhiloxKey philox_key(uint64_t seed)
-{
-    PhiloxKey k;
-#pragma unroll
-    for (int r = 0; r < 10; ++r) {
-        k.k0[r] = (uint32_t)seed + 0x9E3779B9u * (uint32_t)r;
-        k.k1[r] = (uint32_t)(seed >> 32) + 0xBB67AE85u * (uint32_t)r;
-    }
-    return k;
-}
-
+// round multipliers, mixes the high halves with words 1 / 3 and the round key
+// (PhiloxKey, fq_internal.h).
 __device__ __forceinline__ uint4 philox4x32_10(uint4 c, const PhiloxKey &k)
 {
 #pragma unroll
@@ -481,9 +486,10 @@ __device__ __forceinline__ void e2m1_decode8(uint32_t q, float *out)
 // The sign of y is copied (a zero result keeps it).
 __device__ __forceinline__ float e2m1_sr_value(float y, float c)
 {
-    const float a = fabsf(y);
-    const float q = (a < 1.0f) ? 1.0f : 0.0f;
-    const float z = __fadd_ru(a, q);                                     // a + 1 or a
+    // q = 1 for |y| < 1, else 0 (one set instruction)
+    float q;
+    asm("set.lt.f32.f32 %0, %1, 0f3F800000;" : "=f"(q) : "f"(fabsf(y)));
+    const float z = __fadd_ru(fabsf(y), q);                              // |y| + 1 or |y|
     const float p = __uint_as_float(__float_as_uint(z) & 0x7F800000u);   // 2^e of z
     const float t = __fmaf_rz(c, p, z);
     const float m = __uint_as_float(__float_as_uint(t) & 0xFFC00000u);   // on the grid
@@ -494,8 +500,13 @@ __device__ __forceinline__ float e2m1_sr_value(float y, float c)
 // sr_operand for elements 2k and 2k + 1 (both halves of word k).
 __device__ __forceinline__ float2 sr_operand2(uint32_t word)
 {
+    // 2^23 + u as FP32 bits for both halves: the low half by a byte permute,
+    // the high half as the high word of word * 2^16 plus 2^23's bits (one
+    // integer multiply-add, which runs beside the permutes and logic ops)
+    uint32_t hi;
+    asm("mad.hi.u32 %0, %1, 65536, 0x4B000000;" : "=r"(hi) : "r"(word));
     const float2 b = make_float2(__uint_as_float(__byte_perm(word, 0x4B000000u, 0x7610u)),
-                                 __uint_as_float(__byte_perm(word, 0x4B000000u, 0x7632u)));
+                                 __uint_as_float(hi));
     const float2 u = sub2(b, make_float2(8388608.0f, 8388608.0f));  // exact
     return fma2(u, make_float2(-7.62939453125e-06f, -7.62939453125e-06f),
                 make_float2(0.49999988079071044921875f, 0.49999988079071044921875f));
@@ -542,10 +553,9 @@ __device__ __forceinline__ void encode_block(const float *v, const Scale &sc, co
             const uint32_t words[4] = {rb.x, rb.y, rb.z, rb.w};
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
-                const float2 s = e2m1_sr_value2(make_float2(y[2 * k], y[2 * k + 1]),
-                                                sr_operand2(words[k]));
-                y[2 * k] = s.x;
-                y[2 * k + 1] = s.y;
+                const float2 c = sr_operand2(words[k]);
+                y[2 * k] = e2m1_sr_value(y[2 * k], c.x);
+                y[2 * k + 1] = e2m1_sr_value(y[2 * k + 1], c.y);
             }
         }
         q[w] = e2m1_rn_pack8(y);

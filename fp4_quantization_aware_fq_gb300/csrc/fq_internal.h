@@ -5,7 +5,32 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#if defined(__CUDACC__)
+#define FQK_HD __host__ __device__
+#else
+#define FQK_HD
+#endif
+
 namespace fqk {
+
+// Round keys of Philox4x32-10 (Salmon, Moraes, Dror, Shaw, "Parallel Random
+// Numbers: As Easy as 1, 2, 3", SC'11): the key (seed low, seed high) plus r
+// times the two Weyl constants for rounds r = 0..9.  The host computes them
+// once per call and passes them in the kernel arguments, where the kernels
+// read them as constants.
+struct PhiloxKey {
+    uint32_t k0[10], k1[10];
+};
+
+FQK_HD inline PhiloxKey philox_key(uint64_t seed)
+{
+    PhiloxKey k;
+    for (int r = 0; r < 10; ++r) {
+        k.k0[r] = (uint32_t)seed + 0x9E3779B9u * (uint32_t)r;
+        k.k1[r] = (uint32_t)(seed >> 32) + 0xBB67AE85u * (uint32_t)r;
+    }
+    return k;
+}
 
 // Row-wise quantization of a dense tensor seen as a flat array of n elements
 // (n a multiple of the block length).
@@ -23,6 +48,7 @@ struct RowArgs {
     uint32_t offset;
     uint32_t stream_id;
     uint32_t rht_seed;  // 0: no Hadamard transform
+    PhiloxKey key;      // round keys of seed
 };
 
 // Tiled quantization producing the column-wise (transposed) output and,
@@ -44,6 +70,7 @@ struct TileArgs {
     uint64_t seed;
     uint32_t offset;
     uint32_t rht_seed;  // 0: no Hadamard transform
+    PhiloxKey key;      // round keys of seed
 };
 
 struct DequantArgs {
@@ -83,6 +110,7 @@ struct OsciArgs {
     int reset;                         // update: also end the OsciReset window
     uint64_t seed;
     uint32_t offset;
+    PhiloxKey key;                     // round keys of seed
     float threshold;
     float *amax;                       // one float per tensor (workspace)
     unsigned long long *n_reset;
@@ -107,6 +135,7 @@ struct OutlierArgs {
     uint8_t *mask;
     uint64_t seed;
     uint32_t offset;
+    PhiloxKey key;            // round keys of seed
 };
 
 // QAD distillation loss over [rows, vocab] teacher / student logits; each row

@@ -175,7 +175,7 @@ __global__ void __launch_bounds__(kOsciThreads, kOsciBMinCtas)
     constexpr int L = B / 4;  // lanes per block
     __shared__ NvTables tab, tabp;  // NVFP4: this step's and the previous step's tensor scale
     const int64_t ntiles = a.tile_start[a.ntensors];
-    const PhiloxKey key = philox_key(a.seed);
+    const PhiloxKey &key = a.key;
     int t = 0, t_tab = -1;
     const int lane = threadIdx.x & 31;
     const int sub = lane & (L - 1);  // this lane's chunk within its block

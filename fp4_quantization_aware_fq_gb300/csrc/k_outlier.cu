@@ -264,7 +264,7 @@ __device__ __forceinline__ float ld_scalar<__nv_bfloat16>(const void *x, int64_t
 // (an L1 hit: the owner has just loaded it), writes the FP8 code and the
 // kept value of xhat, and patches the owner's mask bits in shared memory.
 template <typename T, int FMT, int RND>
-__global__ void __launch_bounds__(kOutThreads) outlier_row_kernel(OutlierArgs a, int fast)
+__global__ void __launch_bounds__(kOutThreads) outlier_row_kernel(const __grid_constant__ OutlierArgs a, int fast)
 {
     constexpr int B = FmtInfo<FMT>::B;
     __shared__ NvTables tab;
@@ -302,7 +302,7 @@ __global__ void __launch_bounds__(kOutThreads) outlier_row_kernel(OutlierArgs a,
             a.tscale[0] = s_g;
     }
     __syncthreads();
-    const PhiloxKey key = philox_key(a.seed);
+    const PhiloxKey &key = a.key;
     const int64_t bpr = cols / B;
     const int64_t nblk = rows * bpr;
     const bool narrow = nblk <= 0xFFFFFFFFll;  // 32-bit block -> (row, column) division

@@ -112,6 +112,8 @@ __device__ __forceinline__ void row_block(float *v, float am, int64_t blk, bool 
     encode_block<B, RND>(v, sc, key, (uint64_t)blk * B, stream_id, offset, q);
     if (!valid)
         return;
+    // the mask first: after it the block's values are no longer needed
+    const uint32_t mbits = o.mask ? block_mask<B>(v, sc.lim) : 0u;
     const int lane = threadIdx.x & 31;
     if (o.codes) {
         if (B == 16)
@@ -145,18 +147,17 @@ __device__ __forceinline__ void row_block(float *v, float am, int64_t blk, bool 
         }
     }
     if (o.mask) {
-        const uint32_t mask = block_mask<B>(v, sc.lim);
         if (B == 16)
-            reinterpret_cast<uint16_t *>(o.mask)[blk] = (uint16_t)mask;
+            reinterpret_cast<uint16_t *>(o.mask)[blk] = (uint16_t)mbits;
         else
-            reinterpret_cast<uint32_t *>(o.mask)[blk] = mask;
+            reinterpret_cast<uint32_t *>(o.mask)[blk] = mbits;
     }
 }
 
 // One thread per block; each iteration a thread holds BPT blocks' loads in
 // flight (about 64 bytes).
 template <typename T, int FMT, int RND>
-__global__ void __launch_bounds__(kThreads, kRowMinCtas) row_kernel(RowArgs a)
+__global__ void __launch_bounds__(kThreads, kRowMinCtas) row_kernel(const __grid_constant__ RowArgs a)
 {
     constexpr int B = FmtInfo<FMT>::B;
     constexpr int BPT = (B * sizeof(T) >= 64) ? 1 : 2;
@@ -172,11 +173,15 @@ __global__ void __launch_bounds__(kThreads, kRowMinCtas) row_kernel(RowArgs a)
             a.tscale[0] = s_g;
     }
     const RowOut o{a.codes, a.scales, a.tscale, a.xhat, a.xhat_bf16, a.mask};
-    const PhiloxKey key = philox_key(a.seed);
+    const PhiloxKey &key = a.key;
     const bool rht = a.rht_seed != 0;
     const uint32_t signs = rht ? rht_signs(a.rht_seed, a.offset) : 0u;
     const int64_t stride = (int64_t)gridDim.x * kThreads * BPT;
     constexpr int NV = B / VecInfo<T>::E;  // 16-byte vectors per block
+    // NVFP4 follows a full read of x (the tensor amax) and walks the blocks
+    // from the end of x back to the start, so that it first meets the part of
+    // x that the amax pass left in L2.
+    auto block_at = [&](int64_t b) { return FMT == NVFP4 ? nblk - 1 - b : b; };
     for (int64_t base = (int64_t)blockIdx.x * kThreads * BPT; base < nblk; base += stride) {
         if constexpr (B == 16) {
             // 1x16 blocks: the amax comes from the raw vectors (packed pairs
@@ -184,31 +189,31 @@ __global__ void __launch_bounds__(kThreads, kRowMinCtas) row_kernel(RowArgs a)
             uint4 raw[BPT][NV];
 #pragma unroll
             for (int k = 0; k < BPT; ++k) {
-                const int64_t blk = base + k * kThreads + threadIdx.x;
-                const char *src = (const char *)a.x + blk * B * (int64_t)sizeof(T);
+                const int64_t b = base + k * kThreads + threadIdx.x;
+                const char *src = (const char *)a.x + block_at(b) * B * (int64_t)sizeof(T);
 #pragma unroll
                 for (int i = 0; i < NV; ++i)
-                    raw[k][i] = (blk < nblk) ? ld16(src + 16 * i) : make_uint4(0, 0, 0, 0);
+                    raw[k][i] = (b < nblk) ? ld16(src + 16 * i) : make_uint4(0, 0, 0, 0);
             }
 #pragma unroll
             for (int k = 0; k < BPT; ++k) {
-                const int64_t blk = base + k * kThreads + threadIdx.x;
+                const int64_t b = base + k * kThreads + threadIdx.x;
                 const float am = block_amax<T, B>(raw[k]);
                 float v[B];
 #pragma unroll
                 for (int i = 0; i < NV; ++i)
                     unpack16<T>(raw[k][i], v + i * VecInfo<T>::E);
-                row_block<FMT, RND>(v, am, blk, blk < nblk, s_g, inv6, &tab, o, key, a.offset,
-                                    a.stream_id, rht, signs);
+                row_block<FMT, RND>(v, am, block_at(b), b < nblk, s_g, inv6, &tab, o, key,
+                                    a.offset, a.stream_id, rht, signs);
             }
         } else {
             // 1x32 blocks (one per thread): widened as they load, which keeps
             // the raw vectors out of the register budget.
             static_assert(BPT == 1, "one 1x32 block per thread and iteration");
-            const int64_t blk = base + threadIdx.x;
+            const int64_t b = base + threadIdx.x;
             float v[B];
-            if (blk < nblk)
-                load_block<T, B>((const char *)a.x + blk * B * (int64_t)sizeof(T), v);
+            if (b < nblk)
+                load_block<T, B>((const char *)a.x + block_at(b) * B * (int64_t)sizeof(T), v);
             else
 #pragma unroll
                 for (int i = 0; i < B; ++i)
@@ -217,7 +222,7 @@ __global__ void __launch_bounds__(kThreads, kRowMinCtas) row_kernel(RowArgs a)
 #pragma unroll
             for (int i = 0; i < B; ++i)
                 am = fmaxf(am, fabsf(v[i]));
-            row_block<FMT, RND>(v, am, blk, blk < nblk, s_g, inv6, &tab, o, key, a.offset,
+            row_block<FMT, RND>(v, am, block_at(b), b < nblk, s_g, inv6, &tab, o, key, a.offset,
                                 a.stream_id, rht, signs);
         }
     }
@@ -251,7 +256,8 @@ constexpr size_t tile_smem_bytes()
 }
 
 template <typename T, int FMT, int RND>
-__global__ void __launch_bounds__(kThreads, tile_min_ctas<T, FMT>()) tile_kernel(TileArgs a)
+__global__ void __launch_bounds__(kThreads, tile_min_ctas<T, FMT>())
+    tile_kernel(const __grid_constant__ TileArgs a)
 {
     using S = TileShape<FMT>;
     constexpr int E = VecInfo<T>::E;
@@ -282,7 +288,7 @@ __global__ void __launch_bounds__(kThreads, tile_min_ctas<T, FMT>()) tile_kernel
         }
     }
     const RowOut o{a.rcodes, a.rscales, a.rtscale, a.xhat, a.xhat_bf16, a.mask};
-    const PhiloxKey key = philox_key(a.seed);
+    const PhiloxKey &key = a.key;
     const bool rht = a.rht_seed != 0;
     const uint32_t signs = rht ? rht_signs(a.rht_seed, a.offset) : 0u;
 
@@ -318,11 +324,17 @@ __global__ void __launch_bounds__(kThreads, tile_min_ctas<T, FMT>()) tile_kernel
     const int ntr = (int)((rows + TR - 1) / TR), ntc = (int)((cols + TC - 1) / TC);
     const int dy = (int)gridDim.x / ntc, dx = (int)gridDim.x % ntc;
     int ty = (int)blockIdx.x / ntc, tx = (int)blockIdx.x % ntc;
+    // NVFP4 follows a full read of x (the tensor amax): its walk visits the
+    // tiles in reverse order (tile (ty, tx) of the walk is tile (ntr - 1 - ty,
+    // ntc - 1 - tx) of x), so that it starts on the part of x that the amax
+    // pass left in L2.
+    auto tr_of = [&](int y) { return FMT == NVFP4 ? ntr - 1 - y : y; };
+    auto tc_of = [&](int x) { return FMT == NVFP4 ? ntc - 1 - x : x; };
     if (ty < ntr)
-        load_tile(ty, tx);
+        load_tile(tr_of(ty), tc_of(tx));
     while (ty < ntr) {
-    const int64_t r0 = (int64_t)ty * TR;
-    const int64_t c0 = (int64_t)tx * TC;
+    const int64_t r0 = (int64_t)tr_of(ty) * TR;
+    const int64_t c0 = (int64_t)tc_of(tx) * TC;
     int ny = ty + dy, nx = tx + dx;
     if (nx >= ntc) {
         nx -= ntc;
@@ -343,7 +355,7 @@ __global__ void __launch_bounds__(kThreads, tile_min_ctas<T, FMT>()) tile_kernel
             *reinterpret_cast<uint4 *>(tile + tr * TCP + tb * BR + k * E) = nxt[j][k];
     }
     if (ny < ntr)
-        load_tile(ny, nx);
+        load_tile(tr_of(ny), tc_of(nx));
     if (a.do_row) {
 #pragma unroll
         for (int j = 0; j < RPT; ++j) {

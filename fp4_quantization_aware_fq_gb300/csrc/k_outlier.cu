@@ -224,6 +224,7 @@ __global__ void __launch_bounds__(kOutThreads) masked_amax_kernel(const void *__
             }
         }
     }
+    allow_dependent_launch();  // the split quantizer waits for this grid's atomics itself
     m = group_max<32>(m);
     __shared__ float wm[kOutThreads / 32];
     if ((threadIdx.x & 31) == 0)
@@ -277,6 +278,7 @@ __global__ void __launch_bounds__(kOutThreads) outlier_row_kernel(const __grid_c
     const int nwords = (int)((cols + 31) / 32);
     const int kk = (int)a.k;
     float *krcp = reinterpret_cast<float *>(kcols + kk);
+    wait_prior_grid();
     popc_prefix<kOutThreads>(a.bitmap, nwords, pre);
     if (fast) {
         for (int w = threadIdx.x; w < nwords; w += kOutThreads) {
@@ -593,9 +595,9 @@ static cudaError_t outlier_go(const OutlierArgs &a, cudaStream_t s)
         if (e != cudaSuccess)
             return e;
     }
-    outlier_row_kernel<T, FMT, RND><<<grid_cap((nblk + kOutThreads - 1) / kOutThreads, 8),
-                                      kOutThreads, smem, s>>>(a, fast);
-    return cudaGetLastError();
+    return launch_dependent(outlier_row_kernel<T, FMT, RND>,
+                            dim3(grid_cap((nblk + kOutThreads - 1) / kOutThreads, 8)),
+                            dim3(kOutThreads), smem, s, a, fast);
 }
 
 template <typename T>

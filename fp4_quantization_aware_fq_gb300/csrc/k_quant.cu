@@ -163,6 +163,7 @@ __global__ void __launch_bounds__(kThreads, kRowMinCtas) row_kernel(const __grid
     constexpr int BPT = (B * sizeof(T) >= 64) ? 1 : 2;
     const int64_t nblk = a.n / B;
     __shared__ NvTables tab;
+    wait_prior_grid();
     float s_g = 0.0f, inv6 = 0.0f;
     if (FMT == NVFP4) {
         s_g = outer_scale(*a.amax);
@@ -274,6 +275,7 @@ __global__ void __launch_bounds__(kThreads, tile_min_ctas<T, FMT>())
 
     const int64_t rows = a.rows, cols = a.cols;
     __shared__ NvTables tab;
+    wait_prior_grid();
     float s_g = 0.0f, inv6 = 0.0f;
     if (FMT == NVFP4) {
         s_g = outer_scale(*a.amax);
@@ -541,9 +543,14 @@ static cudaError_t row_go(const RowArgs &a, cudaStream_t s)
     const int64_t nblk = a.n / B;
     if (nblk == 0)
         return cudaSuccess;
-    const int grid = persistent_grid(nblk, kThreads * BPT, 8);
-    row_kernel<T, FMT, RND><<<grid, kThreads, 0, s>>>(a);
-    return cudaGetLastError();
+    // Stochastic rounding is bound by its arithmetic: a grid of eight CTAs per
+    // SM walks the tensor (69.7 us for the double-block SR gradient, 71.7 us
+    // with one CTA per 256 x BPT blocks).  Nearest-even rounding is bound by
+    // memory: one CTA per 256 x BPT blocks, handed out in address order, keeps
+    // the reads sequential (MXFP4 weight [32768, 4096]: 98 us against 118 us
+    // for the grid-stride walk).
+    const int grid = persistent_grid(nblk, kThreads * BPT, RND == SR ? 8 : 1 << 20);
+    return launch_dependent(row_kernel<T, FMT, RND>, dim3(grid), dim3(kThreads), 0, s, a);
 }
 
 template <typename T>
@@ -588,8 +595,7 @@ static cudaError_t tile_go(const TileArgs &a, cudaStream_t s)
         per_sm = 1;
     const int64_t cap = (int64_t)sm_count() * per_sm;
     const unsigned grid = (unsigned)(ntiles < cap ? ntiles : cap);
-    tile_kernel<T, FMT, RND><<<grid, kThreads, smem, s>>>(a);
-    return cudaGetLastError();
+    return launch_dependent(tile_kernel<T, FMT, RND>, dim3(grid), dim3(kThreads), smem, s, a);
 }
 
 template <typename T>

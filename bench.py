@@ -69,13 +69,17 @@ BYTES_PER_ELEM = {
 LAUNCHES_PER_STEP = {"nvfp4_small": 2, "mxfp4_weight": 1, "nvfp4_act": 2, "ste_backward": 1,
                      "grad_2level": 1, "grad_rht_rowcol": 1, "act_outliers": 2,
                      "qad_kl": 2, "osci_update": 2, "osci_update_reset": 2}
-# DRAM traffic per launch of the dominant call from an ncu capture, valid only
-# for the kernel source it was taken on (sha256 of the OsciReset sources).
-# Captured on the 2-expert case (66.4 M weights: pass A + pass B read+write
-# 2844.8 MB) and scaled by the weights processed to the 32-expert launch
-# (traffic is linear in the number of weights).
-NCU_TRAFFIC = {"osci_update_reset": {"bytes": int(2844842752 / 66355200 * 1061683200),
-                                      "src_sha256": "a252e6e457263ecd8e33d830c14ccee3282d2a38dc8a63aea208aa87e49fa883"}}
+# DRAM traffic per call of the OsciReset steps from an ncu capture, valid only
+# for the kernel sources it was taken on (sha256 of the OsciReset sources).
+# Captured on the 2-expert case (66.4 M weights; pass A + pass B read + write:
+# 2229.2 MB for the ordinary step, 2823.9 MB for the window-end step) and
+# scaled by the weights processed to the 32-expert call (traffic is linear in
+# the number of weights).
+_OSCI_SCALE = 1061683200 / 66355200
+NCU_TRAFFIC = {"osci_update": {"bytes": int((1270560512 + 958597376) * _OSCI_SCALE),
+                               "src_sha256": "3c791881fdcc631a31b08074b293df1f231820c753018babf261f32a98e46e73"},
+               "osci_update_reset": {"bytes": int((1267416832 + 1556510976) * _OSCI_SCALE),
+                                     "src_sha256": "3c791881fdcc631a31b08074b293df1f231820c753018babf261f32a98e46e73"}}
 
 
 def log(*a):

@@ -5,9 +5,9 @@
 //
 // A row (a vocabulary of up to a few hundred thousand logits) is spread over
 // a thread-block cluster of C CTAs; each CTA pulls its chunk of both rows
-// into shared memory with two bulk copies and keeps it there for the three
-// sweeps the row needs (maxima, sums of exponentials, then p, q, the KL terms
-// and the gradient).  The per-CTA maxima and sums are combined through
+// into shared memory with two bulk copies and keeps it there for the two
+// sweeps the row needs (maxima with the sums of exponentials under running
+// maxima, then p, q, the KL terms and the gradient).  The per-CTA maxima and sums are combined through
 // distributed shared memory, so HBM sees each logit once and each gradient
 // once.  Clusters are persistent over rows; the next row's copies are issued
 // as soon as the current chunk has been read for the last time.
@@ -76,54 +76,6 @@ __device__ __forceinline__ float ex2(float x)
 
 __device__ __forceinline__ float2 ex2x2(float2 x) { return make_float2(ex2(x.x), ex2(x.y)); }
 
-// Running maxima of a chunk of teacher and student logits.  BF16 pairs are
-// compared packed (the maximum of BF16 values is one of them, exactly).
-template <typename T, int NT>
-struct ChunkMax {
-    // running maxima (mt, ms) continued over groups g0 .. g1 - 1
-    static __device__ __forceinline__ float2 run(const T *bt, const T *bs, int g0, int g1,
-                                                 float2 m)
-    {
-        float mt = m.x, ms = m.y;
-        for (int g = g0 + threadIdx.x; g < g1; g += NT) {
-            float v[8], w[8];
-            lds8<T>(bt, g, v);
-            lds8<T>(bs, g, w);
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                mt = fmaxf(mt, v[i]);
-                ms = fmaxf(ms, w[i]);
-            }
-        }
-        return make_float2(mt, ms);
-    }
-};
-
-template <int NT>
-struct ChunkMax<__nv_bfloat16, NT> {
-    static __device__ __forceinline__ float2 run(const __nv_bfloat16 *bt,
-                                                 const __nv_bfloat16 *bs, int g0, int g1,
-                                                 float2 m)
-    {
-        const __nv_bfloat162 ninf = __halves2bfloat162(__ushort_as_bfloat16(0xFF80u),
-                                                       __ushort_as_bfloat16(0xFF80u));
-        __nv_bfloat162 mt = ninf, ms = ninf;
-        for (int g = g0 + threadIdx.x; g < g1; g += NT) {
-            const uint4 u = reinterpret_cast<const uint4 *>(bt)[g];
-            const uint4 w = reinterpret_cast<const uint4 *>(bs)[g];
-            const __nv_bfloat162 *pu = reinterpret_cast<const __nv_bfloat162 *>(&u);
-            const __nv_bfloat162 *pw = reinterpret_cast<const __nv_bfloat162 *>(&w);
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                mt = __hmax2(mt, pu[k]);
-                ms = __hmax2(ms, pw[k]);
-            }
-        }
-        return make_float2(fmaxf(m.x, fmaxf(__low2float(mt), __high2float(mt))),
-                           fmaxf(m.y, fmaxf(__low2float(ms), __high2float(ms))));
-    }
-};
-
 __device__ __forceinline__ float warp_sum(float v)
 {
 #pragma unroll
@@ -140,25 +92,9 @@ __device__ __forceinline__ float warp_max(float v)
     return v;
 }
 
-// CTA-wide reductions of two values; every thread gets the results.  The
-// order of the additions is fixed (a butterfly in each warp, then the warps
-// in index order), so the sums are reproducible.
-template <int NW>
-__device__ __forceinline__ float2 cta_max2(float x, float y, float2 *red)
-{
-    x = warp_max(x);
-    y = warp_max(y);
-    if ((threadIdx.x & 31) == 0)
-        red[threadIdx.x >> 5] = make_float2(x, y);
-    __syncthreads();
-    float2 r = red[0];
-#pragma unroll
-    for (int w = 1; w < NW; ++w)
-        r = make_float2(fmaxf(r.x, red[w].x), fmaxf(r.y, red[w].y));
-    __syncthreads();
-    return r;
-}
-
+// CTA-wide sum of two values; every thread gets the results.  The order of
+// the additions is fixed (a butterfly in each warp, then the warps in index
+// order), so the sums are reproducible.
 template <int NW>
 __device__ __forceinline__ float2 cta_sum2(float x, float y, float2 *red)
 {
@@ -173,6 +109,40 @@ __device__ __forceinline__ float2 cta_sum2(float x, float y, float2 *red)
         r = make_float2(r.x + red[w].x, r.y + red[w].y);
     __syncthreads();
     return r;
+}
+
+// Combines each thread's (running maximum m, sum s of 2^(x k2 - m k2)) pairs
+// of two tensors into the CTA's: the maximum M and the sum under it,
+// sum s 2^(m k2 - M k2) (a thread or warp with no logits has m = -inf and
+// s = 0 and adds nothing).  Returns (M_t, S_t, M_s, S_s) to every thread; the
+// order of the additions is fixed, so the sums are reproducible.
+template <int NW>
+__device__ __forceinline__ float4 cta_max_sum2(float mt, float st, float ms, float ss, float k2,
+                                               float4 *red)
+{
+    static_assert(NW <= 32, "one warp combines the warps' pairs");
+    const float wmt = warp_max(mt), wms = warp_max(ms);
+    float ct = (wmt == -INFINITY) ? 0.0f : st * ex2(mt * k2 - wmt * k2);
+    float cs = (wms == -INFINITY) ? 0.0f : ss * ex2(ms * k2 - wms * k2);
+    ct = warp_sum(ct);
+    cs = warp_sum(cs);
+    if ((threadIdx.x & 31) == 0)
+        red[threadIdx.x >> 5] = make_float4(wmt, ct, wms, cs);
+    __syncthreads();
+    if (threadIdx.x < 32) {
+        const int lane = threadIdx.x;
+        const float4 r = lane < NW ? red[lane] : make_float4(-INFINITY, 0.0f, -INFINITY, 0.0f);
+        const float Mt = warp_max(r.x), Ms = warp_max(r.z);
+        const float St = warp_sum(r.x == -INFINITY ? 0.0f : r.y * ex2(r.x * k2 - Mt * k2));
+        const float Ss = warp_sum(r.z == -INFINITY ? 0.0f : r.w * ex2(r.z * k2 - Ms * k2));
+        __syncwarp();
+        if (lane == 0)
+            red[NW] = make_float4(Mt, St, Ms, Ss);
+    }
+    __syncthreads();
+    const float4 out = red[NW];
+    __syncthreads();
+    return out;
 }
 
 // Cluster barrier after this CTA's threads 0..C-1 pushed their payload into
@@ -205,6 +175,7 @@ __global__ void __launch_bounds__(NT, 1024 / NT) qad_kl_kernel(const KlArgs a)
     __shared__ float part2[2][kKlMaxCluster];
     __shared__ float4 comb;    // the row's maxima and log2 sums (G_t, G_s, log2 S_t, log2 S_s)
     __shared__ float2 red[NW];
+    __shared__ float4 red4[NW + 1];
 
     const uint32_t rank = cluster_rank();
     const int C = a.csize;
@@ -254,29 +225,49 @@ __global__ void __launch_bounds__(NT, 1024 / NT) qad_kl_kernel(const KlArgs a)
     int it = 0;
     for (int64_t row = row0; row < a.rows; row += rstep, ++it) {
         const int64_t next = row + rstep;
-        // sweep 1: maxima of the raw logits (scaling by k2 > 0 keeps the order)
-        float2 lm = make_float2(-INFINITY, -INFINITY);
+        // sweep 1: maxima and sums of exponentials in one pass.  Each thread
+        // keeps a running maximum of the raw logits (scaling by k2 > 0 keeps
+        // the order) and the sum of 2^(a - M) under it, rescaling the sum when
+        // a group of 8 raises the maximum; the CTA then combines the threads'
+        // (maximum, sum) pairs under the CTA's maximum.
+        const float2 vk2 = make_float2(k2, k2);
+        float mt = -INFINITY, ms = -INFINITY, st = 0.0f, ss = 0.0f;
         for (int p = 0; p < kKlParts; ++p) {
             wait_part(p, it);
-            lm = ChunkMax<T, NT>::run(bt, bs, gpart(p), gpart(p + 1), lm);
-        }
-        const float2 m = cta_max2<NW>(lm.x, lm.y, red);
-        const float m2t = m.x * k2, m2s = m.y * k2;
-        // sweep 2: sums of 2^(a - M) under this CTA's maxima
-        const float2 vk2 = make_float2(k2, k2);
-        const float2 nmt = make_float2(-m2t, -m2t), nms = make_float2(-m2s, -m2s);
-        float2 st2 = make_float2(0.0f, 0.0f), ss2 = make_float2(0.0f, 0.0f);
-        for (int g = threadIdx.x; g < ng; g += NT) {
-            float v[8], w[8];
-            lds8<T>(bt, g, v);
-            lds8<T>(bs, g, w);
+            const int g1 = gpart(p + 1);
+            for (int g = gpart(p) + threadIdx.x; g < g1; g += NT) {
+                float v[8], w[8];
+                lds8<T>(bt, g, v);
+                lds8<T>(bs, g, w);
+                float gmt = v[0], gms = w[0];
 #pragma unroll
-            for (int i = 0; i < 8; i += 2) {
-                st2 = add2(st2, ex2x2(fma2(make_float2(v[i], v[i + 1]), vk2, nmt)));
-                ss2 = add2(ss2, ex2x2(fma2(make_float2(w[i], w[i + 1]), vk2, nms)));
+                for (int i = 1; i < 8; ++i) {
+                    gmt = fmaxf(gmt, v[i]);
+                    gms = fmaxf(gms, w[i]);
+                }
+                if (gmt > mt) {
+                    st *= ex2(mt * k2 - gmt * k2);
+                    mt = gmt;
+                }
+                if (gms > ms) {
+                    ss *= ex2(ms * k2 - gms * k2);
+                    ms = gms;
+                }
+                const float2 nmt = make_float2(-mt * k2, -mt * k2);
+                const float2 nms = make_float2(-ms * k2, -ms * k2);
+                float2 st2 = make_float2(0.0f, 0.0f), ss2 = make_float2(0.0f, 0.0f);
+#pragma unroll
+                for (int i = 0; i < 8; i += 2) {
+                    st2 = add2(st2, ex2x2(fma2(make_float2(v[i], v[i + 1]), vk2, nmt)));
+                    ss2 = add2(ss2, ex2x2(fma2(make_float2(w[i], w[i + 1]), vk2, nms)));
+                }
+                st += st2.x + st2.y;
+                ss += ss2.x + ss2.y;
             }
         }
-        const float2 s = cta_sum2<NW>(st2.x + st2.y, ss2.x + ss2.y, red);
+        const float4 ms4 = cta_max_sum2<NW>(mt, st, ms, ss, k2, red4);
+        const float m2t = ms4.x * k2, m2s = ms4.z * k2;
+        const float2 s = make_float2(ms4.y, ms4.w);
         // push this CTA's partials into every CTA of the cluster (lane r -> rank r)
         if (threadIdx.x < C)
             dsmem_st_f4(&part1[it & 1][rank], (uint32_t)threadIdx.x,

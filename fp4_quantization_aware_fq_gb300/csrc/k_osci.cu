@@ -22,10 +22,16 @@ constexpr int kOsciU = 4;   // chunks in flight per thread: the reset pass
 // Pass A: eight chunks in flight per thread (one CTA per SM at its register
 // count) measured 1% faster on the 32-expert step than four.
 constexpr int kOsciAU = 8;
-// Pass B: one chunk per thread at a time with four CTAs per SM (at most 64
-// registers) measured fastest on the 32-expert step: 7.17 ms, against 7.35
-// with two chunks and 7.84 with four at the registers those need.
-constexpr int kOsciBU = 1;
+// Pass B, four CTAs per SM (at most 64 registers).  With the window-end reset
+// (eleven streams per chunk) one chunk per thread at a time measured fastest
+// on the 32-expert step: 7.10 ms, against 7.22 with two chunks and 7.84 with
+// four.  The ordinary step's pass B (nine streams) holds two chunks per
+// thread: 5.61 ms against 5.88 with one.
+template <bool RESET>
+__host__ __device__ constexpr int osci_bu()
+{
+    return RESET ? 1 : 2;
+}
 constexpr int kOsciBMinCtas = 4;
 
 __device__ __forceinline__ float4 ldf4(const float *p)
@@ -158,7 +164,7 @@ __device__ __forceinline__ uint32_t lanes_or(uint32_t v)
     return v;
 }
 
-// Pass B: one thread per 16-byte chunk of 4 master weights (kOsciBU chunks
+// Pass B: one thread per 16-byte chunk of 4 master weights (osci_bu chunks
 // per thread at a time), so every load and store of the per-weight arrays is
 // a coalesced 16-byte vector per lane, as in pass A.  The B/4 lanes of a block
 // (4; 8 for MXFP4) share its amax, scale and mask bits through shuffles; for
@@ -200,12 +206,13 @@ __global__ void __launch_bounds__(kOsciThreads, kOsciBMinCtas)
             if (cbeg == 0 && threadIdx.x == 0)
                 T.ntscale[0] = s_g;
         }
-        for (int k0 = 0; k0 < kOsciTileChunks; k0 += kOsciThreads * kOsciBU) {
-            float4 w[kOsciBU], dq[kOsciBU], dm[kOsciBU];
-            uint32_t qp[kOsciBU], scp[kOsciBU];
-            float so_p[kOsciBU];
+        constexpr int BU = osci_bu<RESET>();
+        for (int k0 = 0; k0 < kOsciTileChunks; k0 += kOsciThreads * BU) {
+            float4 w[BU], dq[BU], dm[BU];
+            uint32_t qp[BU], scp[BU];
+            float so_p[BU];
 #pragma unroll
-            for (int k = 0; k < kOsciBU; ++k) {
+            for (int k = 0; k < BU; ++k) {
                 const int64_t ch = cbeg + k0 + k * kOsciThreads + threadIdx.x;
                 if (ch < nch) {
                     w[k] = ldf4_rw(T.master + ch * 4);
@@ -222,7 +229,7 @@ __global__ void __launch_bounds__(kOsciThreads, kOsciBMinCtas)
                 }
             }
 #pragma unroll
-            for (int k = 0; k < kOsciBU; ++k) {
+            for (int k = 0; k < BU; ++k) {
                 const int64_t ch = cbeg + k0 + k * kOsciThreads + threadIdx.x;
                 const bool valid = ch < nch;  // uniform over a block's lanes (nch % L == 0)
                 const int64_t blk = ch / L;

@@ -494,7 +494,11 @@ __global__ void __launch_bounds__(kThreads, tile_min_ctas<T, FMT>())
         if (gc < cols && gr < rows)
             a.cscales[gc * (rows / BC) + gr / BC] = css[c * NRB + j];
     }
-    __syncthreads();  // the next tile overwrites the tile and staging buffers
+    // No barrier here: the next tile's phase 1 writes only the x tile, which
+    // every thread finished reading before the barrier that ended phase 2;
+    // the staging buffers read above are written again in the next tile's
+    // phase 2, after the barrier that ends its phase 1, which every thread
+    // reaches only once it is done here.
     ty = ny;
     tx = nx;
     }

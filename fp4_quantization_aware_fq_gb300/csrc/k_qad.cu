@@ -94,7 +94,9 @@ __device__ __forceinline__ float warp_max(float v)
 
 // CTA-wide sum of two values; every thread gets the results.  The order of
 // the additions is fixed (a butterfly in each warp, then the warps in index
-// order), so the sums are reproducible.
+// order), so the sums are reproducible.  One barrier: the caller alternates
+// between two `red` buffers, so a buffer is written again only after further
+// barriers that every reader of it has passed.
 template <int NW>
 __device__ __forceinline__ float2 cta_sum2(float x, float y, float2 *red)
 {
@@ -107,7 +109,6 @@ __device__ __forceinline__ float2 cta_sum2(float x, float y, float2 *red)
 #pragma unroll
     for (int w = 1; w < NW; ++w)
         r = make_float2(r.x + red[w].x, r.y + red[w].y);
-    __syncthreads();
     return r;
 }
 
@@ -115,7 +116,8 @@ __device__ __forceinline__ float2 cta_sum2(float x, float y, float2 *red)
 // of two tensors into the CTA's: the maximum M and the sum under it,
 // sum s 2^(m k2 - M k2) (a thread or warp with no logits has m = -inf and
 // s = 0 and adds nothing).  Returns (M_t, S_t, M_s, S_s) to every thread; the
-// order of the additions is fixed, so the sums are reproducible.
+// order of the additions is fixed, so the sums are reproducible.  Two
+// barriers; as for cta_sum2, the caller alternates between two `red` buffers.
 template <int NW>
 __device__ __forceinline__ float4 cta_max_sum2(float mt, float st, float ms, float ss, float k2,
                                                float4 *red)
@@ -140,9 +142,7 @@ __device__ __forceinline__ float4 cta_max_sum2(float mt, float st, float ms, flo
             red[NW] = make_float4(Mt, St, Ms, Ss);
     }
     __syncthreads();
-    const float4 out = red[NW];
-    __syncthreads();
-    return out;
+    return red[NW];
 }
 
 // Cluster barrier after this CTA's threads 0..C-1 pushed their payload into
@@ -174,8 +174,8 @@ __global__ void __launch_bounds__(NT, 1024 / NT) qad_kl_kernel(const KlArgs a)
     __shared__ float4 part1[2][kKlMaxCluster];
     __shared__ float part2[2][kKlMaxCluster];
     __shared__ float4 comb;    // the row's maxima and log2 sums (G_t, G_s, log2 S_t, log2 S_s)
-    __shared__ float2 red[NW];
-    __shared__ float4 red4[NW + 1];
+    __shared__ float2 red[2][NW];      // by row parity
+    __shared__ float4 red4[2][NW + 1];
 
     const uint32_t rank = cluster_rank();
     const int C = a.csize;
@@ -210,15 +210,17 @@ __global__ void __launch_bounds__(NT, 1024 / NT) qad_kl_kernel(const KlArgs a)
         for (int p = 0; p < kKlParts; ++p)
             issue_part(row0, p);
 
-    bool dead = false;  // a copy did not arrive in time: stop loading, keep the barriers
-    // one thread waits for a part; the others sleep in the barrier
+    // A copy that did not arrive in time: this thread stops waiting (thread 0
+    // also stops loading), records the error and keeps joining the barriers.
+    // Every thread waits on the part's barrier itself, so no CTA barrier is
+    // spent on the wait; after a timeout each thread gives up on its own, once.
+    bool dead = false;
     auto wait_part = [&](int p, int it) {
         if (dead)
             return;
-        const bool late = threadIdx.x == 0 && !mbar_wait(&bar[p], (uint32_t)it & 1u);
-        if (__syncthreads_or(late)) {
+        if (!mbar_wait(&bar[p], (uint32_t)it & 1u)) {
             dead = true;
-            if (threadIdx.x == 0 && a.err)
+            if (a.err)
                 atomicOr(a.err, (int)kDevErrWaitTimeout);
         }
     };
@@ -265,7 +267,7 @@ __global__ void __launch_bounds__(NT, 1024 / NT) qad_kl_kernel(const KlArgs a)
                 ss += ss2.x + ss2.y;
             }
         }
-        const float4 ms4 = cta_max_sum2<NW>(mt, st, ms, ss, k2, red4);
+        const float4 ms4 = cta_max_sum2<NW>(mt, st, ms, ss, k2, red4[it & 1]);
         const float m2t = ms4.x * k2, m2s = ms4.z * k2;
         const float2 s = make_float2(ms4.y, ms4.w);
         // push this CTA's partials into every CTA of the cluster (lane r -> rank r)
@@ -341,7 +343,7 @@ __global__ void __launch_bounds__(NT, 1024 / NT) qad_kl_kernel(const KlArgs a)
                 }
             }
         }
-        const float2 k = cta_sum2<NW>(kl2.x + kl2.y, 0.0f, red);  // also: every thread is done with the last part
+        const float2 k = cta_sum2<NW>(kl2.x + kl2.y, 0.0f, red[it & 1]);  // also: every thread is done with the last part
         if (threadIdx.x == 0) {
             dsmem_st_f32(&part2[it & 1][rank], 0u, k.x);  // to rank 0
             if (!dead && next < a.rows) {

@@ -244,6 +244,22 @@ def test_full_grad_2level_sr_bias():
     assert bias < 1e-3
 
 
+@pytest.mark.slow
+def test_full_grad_rht_rowcol():
+    """The benchmarked backward-operand call at full size: a BF16 [16384, 4096]
+    Laplace gradient, 16-point random Hadamard transform, double-block NVFP4
+    with stochastic rounding, row and column orientations in one call
+    ("Resumo Técnico: TetraJet-v2", §2C and §2A)."""
+    x = _dev(W.grad_2level(seed=6))
+    cfg = fq.Config(fq.NVFP4_2LEVEL, fq.SR, 0x5EED, 3, rht_seed=0xB00F)
+    rq, cq = fq.fq_quantize(x, cfg, orient=fq.ROWCOL)
+    torch.cuda.synchronize()
+    ref = oracle.quantize(as_oracle_input(x), oracle.NVFP4_2LEVEL, oracle.SR, 0x5EED, 3,
+                          orient=oracle.ROWCOL, rht_seed=0xB00F)
+    check_q("row", rq, ref["row"], fq.NVFP4_2LEVEL)
+    check_q("col", cq, ref["col"], fq.NVFP4_2LEVEL)
+
+
 @pytest.mark.parametrize("rows", [1, 16, 256, 257])
 def test_nvfp4_row_sizes_around_the_small_workload(rows):
     """NVFP4 row-wise fake quantization of 1 to 257 rows of 1024 (the small

@@ -58,8 +58,21 @@ fq_status check_q(const fq_qtensor *q, int fmt)
 constexpr size_t kWsAmaxBytes = 256;
 
 // Shared body of fq_quantize and fq_fakequant_ste.
+// A row pitch: at least the row length, rows 16-byte aligned, and the
+// strided extent addressable.
+fq_status check_pitch(int64_t rows, int64_t cols, int64_t ld, int esize)
+{
+    if (ld < cols)
+        return FQ_ERR_SHAPE;
+    if ((ld * esize) % 16 != 0)
+        return FQ_ERR_ALIGN;
+    if (rows > 0 && ld > INT64_MAX / 4 / rows)
+        return FQ_ERR_SHAPE;
+    return FQ_OK;
+}
+
 fq_status quantize_common(const fq_config *cfg, const void *x, int32_t x_dtype, int64_t rows,
-                          int64_t cols, bool want_row_q, const fq_qtensor *row_out,
+                          int64_t cols, int64_t ld, bool want_row_q, const fq_qtensor *row_out,
                           const fq_qtensor *col_out, void *xhat, int32_t xhat_dtype,
                           uint8_t *mask, const float *amax_in, void *ws, size_t ws_bytes,
                           void *stream)
@@ -81,10 +94,12 @@ fq_status quantize_common(const fq_config *cfg, const void *x, int32_t x_dtype, 
             return FQ_ERR_SHAPE;
 
     }
+    fq_status st = check_pitch(rows, cols, ld, x_dtype == FQ_BF16 ? 2 : 4);
+    if (st != FQ_OK)
+        return st;
     if (!aligned16(x) || (xhat && !aligned16(xhat)) || (mask && !aligned16(mask)) ||
         (amax_in && (reinterpret_cast<uintptr_t>(amax_in) & 3u)))
         return FQ_ERR_ALIGN;
-    fq_status st;
     if (want_row_q && (st = check_q(row_out, fmt)) != FQ_OK)
         return st;
     if (do_col && (st = check_q(col_out, fmt)) != FQ_OK)
@@ -104,7 +119,9 @@ fq_status quantize_common(const fq_config *cfg, const void *x, int32_t x_dtype, 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const int bf16 = x_dtype == FQ_BF16;
     if (fmt == FQ_NVFP4 && !amax_in) {
-        cudaError_t e = launch_amax(x, bf16, n, static_cast<float *>(ws), s);
+        cudaError_t e = ld == cols ? launch_amax(x, bf16, n, static_cast<float *>(ws), s)
+                                   : launch_amax_rows(x, bf16, rows, cols, ld,
+                                                      static_cast<float *>(ws), s);
         if (e != cudaSuccess)
             return FQ_ERR_CUDA;
         amax = static_cast<const float *>(ws);
@@ -113,6 +130,8 @@ fq_status quantize_common(const fq_config *cfg, const void *x, int32_t x_dtype, 
         RowArgs a{};
         a.x = x;
         a.n = n;
+        a.cols = cols;
+        a.ld = ld;
         a.amax = amax;
         if (want_row_q) {
             a.codes = row_out->codes;
@@ -133,6 +152,7 @@ fq_status quantize_common(const fq_config *cfg, const void *x, int32_t x_dtype, 
     t.x = x;
     t.rows = rows;
     t.cols = cols;
+    t.ld = ld;
     t.amax = amax;
     t.do_row = do_row ? 1 : 0;
     if (want_row_q) {
@@ -290,7 +310,7 @@ fq_status fq_amax(const void *x, int32_t x_dtype, int64_t n, float *amax_out, vo
 }
 
 fq_status fq_quantize(const fq_config *cfg, const void *x, int32_t x_dtype, int64_t rows,
-                      int64_t cols, int32_t orient, const fq_qtensor *row_out,
+                      int64_t cols, int64_t ld, int32_t orient, const fq_qtensor *row_out,
                       const fq_qtensor *col_out, const float *amax_in, void *workspace,
                       size_t workspace_bytes, void *stream)
 {
@@ -300,31 +320,34 @@ fq_status fq_quantize(const fq_config *cfg, const void *x, int32_t x_dtype, int6
     const bool want_col = (orient & FQ_COL) != 0;
     if ((want_row && !row_out) || (want_col && !col_out))
         return FQ_ERR_INVALID_ARG;
-    return quantize_common(cfg, x, x_dtype, rows, cols, want_row, row_out,
+    return quantize_common(cfg, x, x_dtype, rows, cols, ld, want_row, row_out,
                            want_col ? col_out : nullptr, nullptr, FQ_F32, nullptr, amax_in,
                            workspace, workspace_bytes, stream);
 }
 
 fq_status fq_fakequant_ste(const fq_config *cfg, const void *x, int32_t x_dtype, int64_t rows,
-                           int64_t cols, void *xhat, int32_t xhat_dtype, uint8_t *mask,
+                           int64_t cols, int64_t ld, void *xhat, int32_t xhat_dtype, uint8_t *mask,
                            const fq_qtensor *row_out, const fq_qtensor *col_out,
                            const float *amax_in, void *workspace, size_t workspace_bytes,
                            void *stream)
 {
     if (!xhat)
         return FQ_ERR_INVALID_ARG;
-    return quantize_common(cfg, x, x_dtype, rows, cols, row_out != nullptr, row_out, col_out,
+    return quantize_common(cfg, x, x_dtype, rows, cols, ld, row_out != nullptr, row_out, col_out,
                            xhat, xhat_dtype, mask, amax_in, workspace, workspace_bytes, stream);
 }
 
 fq_status fq_dequantize(const fq_config *cfg, const fq_qtensor *q, int64_t rows, int64_t cols,
-                        void *y, int32_t y_dtype, void *stream)
+                        void *y, int32_t y_dtype, int64_t ldy, void *stream)
 {
     if (!valid_cfg(cfg) || !y || !valid_dtype(y_dtype))
         return FQ_ERR_INVALID_ARG;
     if (rows < 0 || cols < 0 || cols % row_multiple(cfg->format) != 0)
         return FQ_ERR_SHAPE;
-    fq_status st = check_q(q, cfg->format);
+    fq_status st = check_pitch(rows, cols, ldy, y_dtype == FQ_BF16 ? 2 : 4);
+    if (st != FQ_OK)
+        return st;
+    st = check_q(q, cfg->format);
     if (st != FQ_OK)
         return st;
     if (!aligned16(y))
@@ -334,6 +357,8 @@ fq_status fq_dequantize(const fq_config *cfg, const fq_qtensor *q, int64_t rows,
     a.scales = q->scales;
     a.tscale = q->tscale;
     a.n = rows * cols;
+    a.cols = cols;
+    a.ldy = ldy;
     a.y = y;
     a.y_bf16 = y_dtype == FQ_BF16;
     return cuda_status(launch_dequant(a, cfg->format, static_cast<cudaStream_t>(stream)));

@@ -37,6 +37,7 @@ FQK_HD inline PhiloxKey philox_key(uint64_t seed)
 struct RowArgs {
     const void *x;
     int64_t n;
+    int64_t cols, ld;   // row length and row pitch of x in elements (ld == cols: dense)
     const float *amax;  // NVFP4: device pointer to the tensor amax
     uint8_t *codes;
     uint8_t *scales;
@@ -56,6 +57,7 @@ struct RowArgs {
 struct TileArgs {
     const void *x;
     int64_t rows, cols;
+    int64_t ld;         // row pitch of x in elements (>= cols)
     const float *amax;
     int do_row;
     uint8_t *rcodes;
@@ -78,6 +80,7 @@ struct DequantArgs {
     const uint8_t *scales;
     const float *tscale;
     int64_t n;
+    int64_t cols, ldy;  // row length and row pitch of y in elements (ldy == cols: dense)
     void *y;
     int y_bf16;
 };
@@ -170,6 +173,8 @@ struct GemmArgs {
 int sm_count();
 
 cudaError_t launch_amax(const void *x, int bf16, int64_t n, float *out, cudaStream_t s);
+cudaError_t launch_amax_rows(const void *x, int bf16, int64_t rows, int64_t cols, int64_t ld,
+                             float *out, cudaStream_t s);
 cudaError_t launch_row(const RowArgs &a, int bf16, int fmt, int rnd, cudaStream_t s);
 cudaError_t launch_tile(const TileArgs &a, int bf16, int fmt, int rnd, cudaStream_t s);
 cudaError_t launch_dequant(const DequantArgs &a, int fmt, cudaStream_t s);

@@ -12,8 +12,10 @@ namespace fqk {
 
 constexpr int kAuxThreads = 256;
 
-// One thread = 8 consecutive elements (4 code bytes).
-template <int FMT>
+// One thread = 8 consecutive elements (4 code bytes).  STRIDED: the rows of y
+// lie a.ldy elements apart (cols is a multiple of 8, so a group never spans
+// two rows).
+template <int FMT, bool STRIDED>
 __global__ void __launch_bounds__(kAuxThreads) dequant_kernel(DequantArgs a)
 {
     constexpr int B = FmtInfo<FMT>::B;
@@ -34,12 +36,17 @@ __global__ void __launch_bounds__(kAuxThreads) dequant_kernel(DequantArgs a)
 #pragma unroll
         for (int i = 0; i < 8; ++i)
             xh[i] = __fmul_rn(xh[i], s_eff);
+        int64_t oe = e0;  // element offset of the group in y
+        if constexpr (STRIDED) {
+            const int64_t r = e0 / a.cols;
+            oe = r * a.ldy + (e0 - r * a.cols);
+        }
         if (a.y_bf16) {
             uint4 o = make_uint4(bf16x2_rn(xh[0], xh[1]), bf16x2_rn(xh[2], xh[3]),
                                  bf16x2_rn(xh[4], xh[5]), bf16x2_rn(xh[6], xh[7]));
-            reinterpret_cast<uint4 *>(a.y)[g] = o;
+            *reinterpret_cast<uint4 *>((char *)a.y + oe * 2) = o;
         } else {
-            float4 *dst = reinterpret_cast<float4 *>(a.y) + 2 * g;
+            float4 *dst = reinterpret_cast<float4 *>((char *)a.y + oe * 4);
             dst[0] = make_float4(xh[0], xh[1], xh[2], xh[3]);
             dst[1] = make_float4(xh[4], xh[5], xh[6], xh[7]);
         }
@@ -88,12 +95,16 @@ cudaError_t launch_dequant(const DequantArgs &a, int fmt, cudaStream_t s)
     if (a.n == 0)
         return cudaSuccess;
     const int grid = grid_for(a.n / 8, 8);
+    const bool st = a.ldy != a.cols;
     if (fmt == NVFP4)
-        dequant_kernel<NVFP4><<<grid, kAuxThreads, 0, s>>>(a);
+        st ? dequant_kernel<NVFP4, true><<<grid, kAuxThreads, 0, s>>>(a)
+           : dequant_kernel<NVFP4, false><<<grid, kAuxThreads, 0, s>>>(a);
     else if (fmt == MXFP4)
-        dequant_kernel<MXFP4><<<grid, kAuxThreads, 0, s>>>(a);
+        st ? dequant_kernel<MXFP4, true><<<grid, kAuxThreads, 0, s>>>(a)
+           : dequant_kernel<MXFP4, false><<<grid, kAuxThreads, 0, s>>>(a);
     else
-        dequant_kernel<NV2L><<<grid, kAuxThreads, 0, s>>>(a);
+        st ? dequant_kernel<NV2L, true><<<grid, kAuxThreads, 0, s>>>(a)
+           : dequant_kernel<NV2L, false><<<grid, kAuxThreads, 0, s>>>(a);
     return cudaGetLastError();
 }
 

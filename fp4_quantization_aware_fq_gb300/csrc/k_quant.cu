@@ -70,6 +70,40 @@ __global__ void __launch_bounds__(kThreads) amax_kernel(const void *__restrict__
     }
 }
 
+// The same over the rows of a tensor whose rows lie ld elements apart: the
+// CTAs take whole rows, each thread one 16-byte vector of the row at a time.
+template <typename T>
+__global__ void __launch_bounds__(kThreads) amax_rows_kernel(const void *__restrict__ x, int64_t rows,
+                                                             int64_t cols, int64_t ld,
+                                                             unsigned *__restrict__ out)
+{
+    constexpr int E = VecInfo<T>::E;
+    const int64_t vpr = cols / E;
+    float m = 0.0f;
+    for (int64_t r = blockIdx.x; r < rows; r += gridDim.x) {
+        const char *row = (const char *)x + r * ld * (int64_t)sizeof(T);
+        for (int64_t c = threadIdx.x; c < vpr; c += kThreads) {
+            float v[E];
+            unpack16<T>(ld16(row + c * 16), v);
+#pragma unroll
+            for (int i = 0; i < E; ++i)
+                m = fmaxf(m, fabsf(v[i]));
+        }
+    }
+    m = group_max<32>(m);
+    __shared__ float wm[kThreads / 32];
+    if ((threadIdx.x & 31) == 0)
+        wm[threadIdx.x >> 5] = m;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        float b = wm[0];
+#pragma unroll
+        for (int w = 1; w < kThreads / 32; ++w)
+            b = fmaxf(b, wm[w]);
+        atomicMax(out, __float_as_uint(b));
+    }
+}
+
 // ------------------------------------------------------------------ row-wise core
 // Outputs of the row-wise pass (any pointer may be NULL: not written).
 struct RowOut {
@@ -156,12 +190,23 @@ __device__ __forceinline__ void row_block(float *v, float am, int64_t blk, bool 
 
 // One thread per block; each iteration a thread holds BPT blocks' loads in
 // flight (about 64 bytes).
-template <typename T, int FMT, int RND>
+// STRIDED: the rows of x lie a.ld elements apart; block b (in row-major
+// order) starts at element (b / (cols / B)) * ld + (b % (cols / B)) * B.
+template <typename T, int FMT, int RND, bool STRIDED>
 __global__ void __launch_bounds__(kThreads, kRowMinCtas) row_kernel(const __grid_constant__ RowArgs a)
 {
     constexpr int B = FmtInfo<FMT>::B;
     constexpr int BPT = (B * sizeof(T) >= 64) ? 1 : 2;
     const int64_t nblk = a.n / B;
+    auto src_of = [&](int64_t b) {
+        int64_t e = b * B;
+        if constexpr (STRIDED) {
+            const int64_t bpr = a.cols / B;
+            const int64_t r = b / bpr;
+            e = r * a.ld + (b - r * bpr) * B;
+        }
+        return (const char *)a.x + e * (int64_t)sizeof(T);
+    };
     __shared__ NvTables tab;
     wait_prior_grid();
     float s_g = 0.0f, inv6 = 0.0f;
@@ -191,7 +236,7 @@ __global__ void __launch_bounds__(kThreads, kRowMinCtas) row_kernel(const __grid
 #pragma unroll
             for (int k = 0; k < BPT; ++k) {
                 const int64_t b = base + k * kThreads + threadIdx.x;
-                const char *src = (const char *)a.x + block_at(b) * B * (int64_t)sizeof(T);
+                const char *src = src_of(block_at(b));
 #pragma unroll
                 for (int i = 0; i < NV; ++i)
                     raw[k][i] = (b < nblk) ? ld16(src + 16 * i) : make_uint4(0, 0, 0, 0);
@@ -214,7 +259,7 @@ __global__ void __launch_bounds__(kThreads, kRowMinCtas) row_kernel(const __grid
             const int64_t b = base + threadIdx.x;
             float v[B];
             if (b < nblk)
-                load_block<T, B>((const char *)a.x + block_at(b) * B * (int64_t)sizeof(T), v);
+                load_block<T, B>(src_of(block_at(b)), v);
             else
 #pragma unroll
                 for (int i = 0; i < B; ++i)
@@ -308,7 +353,7 @@ __global__ void __launch_bounds__(kThreads, tile_min_ctas<T, FMT>())
             const int tr = t / RBPR, tb = t % RBPR;
             const int64_t gr = lr0 + tr, gc = lc0 + (int64_t)tb * BR;
             const bool valid = t < TR * RBPR && gr < rows;
-            const char *src = (const char *)a.x + (gr * cols + gc) * (int64_t)sizeof(T);
+            const char *src = (const char *)a.x + (gr * a.ld + gc) * (int64_t)sizeof(T);
             // Each 16-byte vector is fetched only if it lies inside the row:
             // a column-only MXFP4 call admits cols % 32 == 16, where the last
             // 1x32 row block of a row holds only 16 elements (cols is a
@@ -561,6 +606,22 @@ cudaError_t launch_amax(const void *x, int bf16, int64_t n, float *out, cudaStre
     return cudaGetLastError();
 }
 
+cudaError_t launch_amax_rows(const void *x, int bf16, int64_t rows, int64_t cols, int64_t ld,
+                             float *out, cudaStream_t s)
+{
+    cudaError_t e = cudaMemsetAsync(out, 0, sizeof(float), s);
+    if (e != cudaSuccess)
+        return e;
+    if (rows == 0 || cols == 0)
+        return cudaSuccess;
+    const int grid = persistent_grid(rows, 1, 8);
+    if (bf16)
+        amax_rows_kernel<__nv_bfloat16><<<grid, kThreads, 0, s>>>(x, rows, cols, ld, (unsigned *)out);
+    else
+        amax_rows_kernel<float><<<grid, kThreads, 0, s>>>(x, rows, cols, ld, (unsigned *)out);
+    return cudaGetLastError();
+}
+
 template <typename T, int FMT, int RND>
 static cudaError_t row_go(const RowArgs &a, cudaStream_t s)
 {
@@ -576,7 +637,9 @@ static cudaError_t row_go(const RowArgs &a, cudaStream_t s)
     // the reads sequential (MXFP4 weight [32768, 4096]: 98 us against 118 us
     // for the grid-stride walk).
     const int grid = persistent_grid(nblk, kThreads * BPT, RND == SR ? 8 : 1 << 20);
-    return launch_dependent(row_kernel<T, FMT, RND>, dim3(grid), dim3(kThreads), 0, s, a);
+    if (a.ld != a.cols)
+        return launch_dependent(row_kernel<T, FMT, RND, true>, dim3(grid), dim3(kThreads), 0, s, a);
+    return launch_dependent(row_kernel<T, FMT, RND, false>, dim3(grid), dim3(kThreads), 0, s, a);
 }
 
 template <typename T>

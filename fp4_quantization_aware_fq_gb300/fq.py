@@ -110,11 +110,11 @@ def lib():
         L.fq_osci_workspace_size.argtypes = [i32]
         L.fq_osci_workspace_size.restype = sz
         L.fq_amax.argtypes = [vp, i32, i64, vp, vp]
-        L.fq_quantize.argtypes = [P(Config), vp, i32, i64, i64, i32, P(_QT), P(_QT), vp, vp, sz,
+        L.fq_quantize.argtypes = [P(Config), vp, i32, i64, i64, i64, i32, P(_QT), P(_QT), vp, vp, sz,
                                   vp]
-        L.fq_fakequant_ste.argtypes = [P(Config), vp, i32, i64, i64, vp, i32, vp, P(_QT), P(_QT),
+        L.fq_fakequant_ste.argtypes = [P(Config), vp, i32, i64, i64, i64, vp, i32, vp, P(_QT), P(_QT),
                                        vp, vp, sz, vp]
-        L.fq_dequantize.argtypes = [P(Config), P(_QT), i64, i64, vp, i32, vp]
+        L.fq_dequantize.argtypes = [P(Config), P(_QT), i64, i64, vp, i32, i64, vp]
         L.fq_ste_backward.argtypes = [vp, i32, vp, i64, vp, vp]
         L.fq_osci_update.argtypes = [P(Config), i32, P(i64), P(i64), P(vp), P(vp), P(vp), P(vp),
                                      P(_QT), P(_QT), P(vp), i32, P(vp), vp, sz, vp]
@@ -176,6 +176,15 @@ def _dims(x: torch.Tensor):
     return x.shape[0], x.shape[1]
 
 
+def _dims_ld(x: torch.Tensor):
+    """rows, cols and the row pitch of a 2-D tensor whose rows are dense
+    (stride 1 along a row), such as a column slice of a wider tensor."""
+    if x.dim() != 2 or (x.shape[1] > 1 and x.stride(1) != 1):
+        raise ValueError("expected a 2-D tensor with unit stride along its rows")
+    rows, cols = x.shape
+    return rows, cols, (x.stride(0) if rows > 1 else cols)
+
+
 # --------------------------------------------------------------------------
 # entry points (same names as the C ABI)
 # --------------------------------------------------------------------------
@@ -208,7 +217,7 @@ def fq_quantize(x: torch.Tensor, cfg: Config, orient: int = ROW,
                 row_out: Optional[QTensor] = None, col_out: Optional[QTensor] = None,
                 amax_in: Optional[torch.Tensor] = None, ws: Optional[torch.Tensor] = None,
                 stream=None):
-    rows, cols = _dims(x)
+    rows, cols, ld = _dims_ld(x)
     if orient & ROW and row_out is None:
         row_out = alloc_qtensor(rows, cols, cfg.format, x.device)
     if orient & COL and col_out is None:
@@ -217,7 +226,7 @@ def fq_quantize(x: torch.Tensor, cfg: Config, orient: int = ROW,
         ws = workspace(cfg, rows, cols, x.device)
     rq = ctypes.byref(row_out._c()) if orient & ROW else None
     cq = ctypes.byref(col_out._c()) if orient & COL else None
-    st = lib().fq_quantize(ctypes.byref(cfg), x.data_ptr(), _dtype_code(x), rows, cols, orient,
+    st = lib().fq_quantize(ctypes.byref(cfg), x.data_ptr(), _dtype_code(x), rows, cols, ld, orient,
                            rq, cq, _ptr(amax_in), _ptr(ws), 0 if ws is None else ws.numel(),
                            _stream(stream))
     _check(st, "fq_quantize")
@@ -231,7 +240,7 @@ def fq_fakequant_ste(x: torch.Tensor, cfg: Config, xhat: Optional[torch.Tensor] 
                      want_row_q: bool = False, want_col_q: bool = False,
                      amax_in: Optional[torch.Tensor] = None, ws: Optional[torch.Tensor] = None,
                      stream=None):
-    rows, cols = _dims(x)
+    rows, cols, ld = _dims_ld(x)
     if xhat is None:
         xhat = torch.empty((rows, cols), dtype=xhat_dtype or x.dtype, device=x.device)
     if mask is None and want_mask:
@@ -245,7 +254,7 @@ def fq_fakequant_ste(x: torch.Tensor, cfg: Config, xhat: Optional[torch.Tensor] 
         ws = workspace(cfg, rows, cols, x.device)
     rq = ctypes.byref(row_out._c()) if row_out is not None else None
     cq = ctypes.byref(col_out._c()) if col_out is not None else None
-    st = lib().fq_fakequant_ste(ctypes.byref(cfg), x.data_ptr(), _dtype_code(x), rows, cols,
+    st = lib().fq_fakequant_ste(ctypes.byref(cfg), x.data_ptr(), _dtype_code(x), rows, cols, ld,
                                 xhat.data_ptr(), _dtype_code(xhat), _ptr(mask), rq, cq,
                                 _ptr(amax_in), _ptr(ws), 0 if ws is None else ws.numel(),
                                 _stream(stream))
@@ -257,8 +266,11 @@ def fq_dequantize(q: QTensor, rows: int, cols: int, cfg: Config,
                   y: Optional[torch.Tensor] = None, y_dtype=torch.float32, stream=None):
     if y is None:
         y = torch.empty((rows, cols), dtype=y_dtype, device=q.codes.device)
+    if tuple(y.shape) != (rows, cols):
+        raise ValueError("y must be [rows, cols]")
+    _, _, ldy = _dims_ld(y)
     st = lib().fq_dequantize(ctypes.byref(cfg), ctypes.byref(q._c()), rows, cols, y.data_ptr(),
-                             _dtype_code(y), _stream(stream))
+                             _dtype_code(y), ldy, _stream(stream))
     _check(st, "fq_dequantize")
     return y
 

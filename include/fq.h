@@ -49,8 +49,9 @@
  *    for the column-wise pass), stream 0 row-wise / 1 column-wise; element
  *    j = index % 8 takes 16-bit half (j % 2) of output word j / 2.
  *
- * Layouts (all dense, row-major, no padding):
- *  x        [rows, cols] FP32 or BF16.
+ * Layouts (row-major, no padding; x of fq_quantize / fq_fakequant_ste and y of
+ * fq_dequantize may have a row pitch ld >= cols, every other tensor is dense):
+ *  x        [rows, cols] FP32 or BF16, row r starting at element r * ld.
  *  codes    [rows, cols/2] bytes; element 2j in the low nibble of byte j.
  *  scales   [rows, cols/B] bytes, B = 16 (NVFP4, double block) or 32 (MXFP4).
  *  tscale   NVFP4: 1 float (s_g); double block: [rows, cols/128] floats;
@@ -157,9 +158,13 @@ FQ_API fq_status fq_amax(const void *x, int32_t x_dtype, int64_t n, float *amax_
  * pass (cols % 128 for the double block); rows % B == 0 for the column pass
  * (rows % 128 for the double block).  amax_in: optional device float holding
  * the tensor amax to use for NVFP4 (NULL: computed here into the workspace).
- * NVFP4 uses the same s_g for both orientations. */
+ * NVFP4 uses the same s_g for both orientations.
+ * ld: elements between the starts of consecutive rows of x (ld == cols for a
+ * dense tensor; larger for a column slice or a padded row).  ld < cols:
+ * FQ_ERR_SHAPE; a row pitch (ld times the element size) that is not a
+ * multiple of 16 bytes: FQ_ERR_ALIGN.  The outputs are always dense. */
 FQ_API fq_status fq_quantize(const fq_config *cfg, const void *x, int32_t x_dtype, int64_t rows,
-                      int64_t cols, int32_t orient, const fq_qtensor *row_out,
+                      int64_t cols, int64_t ld, int32_t orient, const fq_qtensor *row_out,
                       const fq_qtensor *col_out, const float *amax_in, void *workspace,
                       size_t workspace_bytes, void *stream);
 
@@ -167,17 +172,22 @@ FQ_API fq_status fq_quantize(const fq_config *cfg, const void *x, int32_t x_dtyp
  * "Detalhes técnicos"): xhat = dequant(quant(x)) in xhat_dtype, mask as
  * defined above (NULL: not written), both from the row-wise pass.  row_out
  * and col_out (NULL: not written) additionally receive the packed tensors,
- * so one call does the whole forward/backward quantization of an activation. */
+ * so one call does the whole forward/backward quantization of an activation.
+ * ld as for fq_quantize (the row pitch of x); xhat, mask and the packed
+ * outputs are dense. */
 FQ_API fq_status fq_fakequant_ste(const fq_config *cfg, const void *x, int32_t x_dtype, int64_t rows,
-                           int64_t cols, void *xhat, int32_t xhat_dtype, uint8_t *mask,
+                           int64_t cols, int64_t ld, void *xhat, int32_t xhat_dtype, uint8_t *mask,
                            const fq_qtensor *row_out, const fq_qtensor *col_out,
                            const float *amax_in, void *workspace, size_t workspace_bytes,
                            void *stream);
 
 /* Dequantize a row-wise quantized [rows, cols] tensor: y = E2M1value(code) *
- * s_eff, in y_dtype.  Bit-identical to the xhat of fq_fakequant_ste. */
+ * s_eff, in y_dtype.  Bit-identical to the xhat of fq_fakequant_ste.  ldy:
+ * elements between the starts of consecutive rows of y (cols: dense); the
+ * elements between cols and ldy of each row are not written.  ldy < cols:
+ * FQ_ERR_SHAPE; a row pitch that is not a multiple of 16 bytes: FQ_ERR_ALIGN. */
 FQ_API fq_status fq_dequantize(const fq_config *cfg, const fq_qtensor *q, int64_t rows, int64_t cols,
-                        void *y, int32_t y_dtype, void *stream);
+                        void *y, int32_t y_dtype, int64_t ldy, void *stream);
 
 /* Straight-through-estimator backward ([QATREC]): dx = dy where the mask bit
  * is set, +0 elsewhere.  n elements, n % 8 == 0; dy/dx share dtype. */

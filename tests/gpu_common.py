@@ -11,7 +11,9 @@ FMT_O = {fq.NVFP4: oracle.NVFP4, fq.MXFP4: oracle.MXFP4, fq.NVFP4_2LEVEL: oracle
 
 
 def as_oracle_input(x: torch.Tensor) -> np.ndarray:
-    """The exact FP32 values the kernel sees (BF16 widened bit-exactly)."""
+    """The exact FP32 values the kernel sees (BF16 widened bit-exactly); a
+    row-pitched view is taken as its dense copy."""
+    x = x.contiguous()
     if x.dtype == torch.bfloat16:
         return oracle.bf16_bits_to_f32(workloads.bf16_bits(x)).reshape(x.shape)
     return x.detach().cpu().numpy().astype(np.float32)

@@ -54,11 +54,11 @@ def _qt(codes=FAKE, scales=FAKE, tscale=FAKE):
 
 
 def _quant(L, cfg, x=FAKE, dtype=fq.BF16, rows=64, cols=64, orient=fq.ROW, row=None, col=None,
-           ws=FAKE, wsb=256):
+           ws=FAKE, wsb=256, ld=None):
     r = ctypes.byref(row) if row is not None else None
     c = ctypes.byref(col) if col is not None else None
-    return L.fq_quantize(ctypes.byref(cfg), x, dtype, rows, cols, orient, r, c, None, ws, wsb,
-                         None)
+    return L.fq_quantize(ctypes.byref(cfg), x, dtype, rows, cols, cols if ld is None else ld,
+                         orient, r, c, None, ws, wsb, None)
 
 
 def test_quantize_argument_errors(L):
@@ -81,6 +81,12 @@ def test_quantize_argument_errors(L):
     assert _quant(L, ok, row=_qt(tscale=0)) == 1                           # NVFP4 needs tscale
     assert _quant(L, ok, row=_qt(), ws=0) == 4                             # no workspace
     assert _quant(L, ok, row=_qt(), wsb=2) == 4                            # workspace too small
+    # the row pitch: at least cols, a multiple of 16 bytes, addressable
+    assert _quant(L, ok, ld=48, row=_qt()) == 2                            # ld < cols
+    assert _quant(L, ok, ld=68, row=_qt()) == 3                            # 136-byte BF16 rows
+    assert _quant(L, ok, dtype=fq.F32, rows=0, ld=68, row=_qt()) == 0      # 272-byte FP32 rows
+    assert _quant(L, ok, rows=1 << 40, ld=1 << 40, row=_qt()) == 2         # extent overflows
+    assert _quant(L, ok, rows=0, ld=72, row=_qt()) == 0                    # padded, empty
 
 
 @pytest.mark.parametrize("fmt", [fq.NVFP4, fq.MXFP4, fq.NVFP4_2LEVEL])
@@ -94,9 +100,9 @@ def test_empty_tensors_succeed_without_touching_the_device(L, fmt):
     assert _quant(L, cfg, rows=0, cols=128, row=q) == 0
     assert _quant(L, cfg, rows=0, cols=128, orient=fq.ROWCOL, row=q, col=q2) == 0
     assert _quant(L, cfg, rows=128, cols=0, row=q) == 0
-    assert L.fq_fakequant_ste(c, FAKE, fq.BF16, 0, 128, FAKE, fq.BF16, FAKE, ctypes.byref(q),
-                              None, None, FAKE, 256, None) == 0
-    assert L.fq_dequantize(c, ctypes.byref(q), 0, 128, FAKE, fq.F32, None) == 0
+    assert L.fq_fakequant_ste(c, FAKE, fq.BF16, 0, 128, 128, FAKE, fq.BF16, FAKE,
+                              ctypes.byref(q), None, None, FAKE, 256, None) == 0
+    assert L.fq_dequantize(c, ctypes.byref(q), 0, 128, FAKE, fq.F32, 128, None) == 0
     assert L.fq_ste_backward(FAKE, fq.BF16, FAKE, 0, FAKE, None) == 0
 
 
@@ -114,17 +120,24 @@ def test_hadamard_transform_needs_block_local_scales(L):
 def test_fakequant_dequant_ste_amax_errors(L):
     cfg = fq.Config(fq.NVFP4)
     f = L.fq_fakequant_ste
-    assert f(ctypes.byref(cfg), FAKE, fq.BF16, 64, 64, None, fq.BF16, None, None, None, None,
+    assert f(ctypes.byref(cfg), FAKE, fq.BF16, 64, 64, 64, None, fq.BF16, None, None, None, None,
              FAKE, 256, None) == 1                                         # xhat required
-    assert f(ctypes.byref(cfg), FAKE, fq.BF16, 64, 64, FAKE + 2, fq.BF16, None, None, None, None,
-             FAKE, 256, None) == 3
-    assert f(ctypes.byref(cfg), FAKE, fq.BF16, 64, 64, FAKE, 5, None, None, None, None,
+    assert f(ctypes.byref(cfg), FAKE, fq.BF16, 64, 64, 64, FAKE + 2, fq.BF16, None, None, None,
+             None, FAKE, 256, None) == 3
+    assert f(ctypes.byref(cfg), FAKE, fq.BF16, 64, 64, 64, FAKE, 5, None, None, None, None,
              FAKE, 256, None) == 1
+    assert f(ctypes.byref(cfg), FAKE, fq.BF16, 64, 64, 32, FAKE, fq.BF16, None, None, None, None,
+             FAKE, 256, None) == 2                                         # ld < cols
+    assert f(ctypes.byref(cfg), FAKE, fq.BF16, 64, 64, 100, FAKE, fq.BF16, None, None, None,
+             None, FAKE, 256, None) == 3                                   # 200-byte rows
     q = _qt()
-    assert L.fq_dequantize(ctypes.byref(cfg), ctypes.byref(q), 64, 24, FAKE, fq.F32, None) == 2
-    assert L.fq_dequantize(ctypes.byref(cfg), None, 64, 64, FAKE, fq.F32, None) == 1
-    assert L.fq_dequantize(ctypes.byref(cfg), ctypes.byref(q), 64, 64, FAKE + 1, fq.F32,
-                           None) == 3
+    d = L.fq_dequantize
+    assert d(ctypes.byref(cfg), ctypes.byref(q), 64, 24, FAKE, fq.F32, 24, None) == 2
+    assert d(ctypes.byref(cfg), None, 64, 64, FAKE, fq.F32, 64, None) == 1
+    assert d(ctypes.byref(cfg), ctypes.byref(q), 64, 64, FAKE + 1, fq.F32, 64, None) == 3
+    assert d(ctypes.byref(cfg), ctypes.byref(q), 64, 64, FAKE, fq.F32, 60, None) == 2  # ldy < cols
+    assert d(ctypes.byref(cfg), ctypes.byref(q), 64, 64, FAKE, fq.F32, 66, None) == 3  # 264 B rows
+    assert d(ctypes.byref(cfg), ctypes.byref(q), 64, 64, FAKE, fq.BF16, 68, None) == 3  # 136 B rows
     assert L.fq_ste_backward(FAKE, fq.BF16, FAKE, 12, FAKE, None) == 2
     assert L.fq_ste_backward(FAKE, fq.BF16, None, 16, FAKE, None) == 1
     assert L.fq_ste_backward(FAKE + 2, fq.BF16, FAKE, 16, FAKE, None) == 3

@@ -57,7 +57,6 @@ struct RowArgs {
 struct TileArgs {
     const void *x;
     int64_t rows, cols;
-    int64_t ld;         // row pitch of x in elements (>= cols)
     const float *amax;
     int do_row;
     uint8_t *rcodes;
@@ -73,6 +72,7 @@ struct TileArgs {
     uint32_t offset;
     uint32_t rht_seed;  // 0: no Hadamard transform
     PhiloxKey key;      // round keys of seed
+    int64_t ld;         // row pitch of x in elements (>= cols)
 };
 
 struct DequantArgs {

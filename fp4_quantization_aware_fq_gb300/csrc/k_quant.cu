@@ -301,7 +301,8 @@ constexpr size_t tile_smem_bytes()
            + (FMT == NV2L ? (size_t)S::TC * (S::TR / S::BC) * 4 : 0);  // inner amax
 }
 
-template <typename T, int FMT, int RND>
+// STRIDED: the rows of x lie a.ld elements apart (else a.cols).
+template <typename T, int FMT, int RND, bool STRIDED>
 __global__ void __launch_bounds__(kThreads, tile_min_ctas<T, FMT>())
     tile_kernel(const __grid_constant__ TileArgs a)
 {
@@ -353,7 +354,8 @@ __global__ void __launch_bounds__(kThreads, tile_min_ctas<T, FMT>())
             const int tr = t / RBPR, tb = t % RBPR;
             const int64_t gr = lr0 + tr, gc = lc0 + (int64_t)tb * BR;
             const bool valid = t < TR * RBPR && gr < rows;
-            const char *src = (const char *)a.x + (gr * a.ld + gc) * (int64_t)sizeof(T);
+            const char *src =
+                (const char *)a.x + (gr * (STRIDED ? a.ld : cols) + gc) * (int64_t)sizeof(T);
             // Each 16-byte vector is fetched only if it lies inside the row:
             // a column-only MXFP4 call admits cols % 32 == 16, where the last
             // 1x32 row block of a row holds only 16 elements (cols is a
@@ -667,8 +669,10 @@ static cudaError_t tile_go(const TileArgs &a, cudaStream_t s)
     if (a.rows == 0 || a.cols == 0)
         return cudaSuccess;
     constexpr size_t smem = tile_smem_bytes<T, FMT>();
+    const auto kern =
+        a.ld != a.cols ? tile_kernel<T, FMT, RND, true> : tile_kernel<T, FMT, RND, false>;
     if (smem > 48 * 1024) {
-        cudaError_t e = cudaFuncSetAttribute(tile_kernel<T, FMT, RND>,
+        cudaError_t e = cudaFuncSetAttribute(kern,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              (int)smem);
         if (e != cudaSuccess)
@@ -679,12 +683,12 @@ static cudaError_t tile_go(const TileArgs &a, cudaStream_t s)
         return cudaErrorInvalidValue;
     const int64_t ntiles = ntc * ntr;
     int per_sm = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, tile_kernel<T, FMT, RND>, kThreads,
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads,
                                                       smem) != cudaSuccess || per_sm < 1)
         per_sm = 1;
     const int64_t cap = (int64_t)sm_count() * per_sm;
     const unsigned grid = (unsigned)(ntiles < cap ? ntiles : cap);
-    return launch_dependent(tile_kernel<T, FMT, RND>, dim3(grid), dim3(kThreads), smem, s, a);
+    return launch_dependent(kern, dim3(grid), dim3(kThreads), smem, s, a);
 }
 
 template <typename T>

@@ -585,6 +585,82 @@ def run_small_at_scale(steps=20, warmup=3):
             "note": "nvfp4_small's two launches on a 64x larger tensor; not part of the step"}
 
 
+def run_osci_window(suite, windows=2):
+    """A whole OsciReset observation window on the MoE group: 99 ordinary QAT
+    steps (fq_osci_update) and the window-end step with the reset fused in
+    (fq_osci_update_reset), eager launches on the current stream, timed with
+    CUDA events; each window's 100 steps move about 3.7 TB, far beyond L2.
+    Not part of the suite step."""
+    import torch
+    stream = torch.cuda.current_stream()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    t0.record(stream)
+    for _ in range(windows):
+        for _ in range(99):
+            suite.osci_update()
+        suite.osci_update_reset()
+    t1.record(stream)
+    torch.cuda.synchronize()
+    ms = t0.elapsed_time(t1) / windows
+    nbytes = (99 * BYTES_PER_ELEM["osci_update"] * suite.elems["osci_update"]
+              + BYTES_PER_ELEM["osci_update_reset"] * suite.elems["osci_update_reset"])
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    peak, kind = measured_peaks()
+    return {"steps_per_window": 100, "weights": suite.elems["osci_update"],
+            "ms_per_window": round(ms, 2), "ms_per_step": round(ms / 100, 4),
+            "bytes_per_window": int(nbytes), "gbs": round(gbs, 1),
+            "frac_hbm": round(gbs / peak, 3), "frac_spec": round(gbs / SPEC_HBM_GBS, 3),
+            "peak_kind": kind, "windows_timed": windows,
+            "note": "99 ordinary steps + the window-end step with the reset; not part of the "
+                    "suite step"}
+
+
+def run_quant_dequant(reps=20, warmup=3):
+    """The MXFP4 weight workload as two separate calls, fq_quantize (codes and
+    E8M0 scales) then fq_dequantize (BF16), on the same [4096, 4096] BF16
+    weight.  The input fits in L2, so each rep first writes a 512 MB buffer
+    (outside the timed events) to flush it.  Not part of the suite step."""
+    import torch
+    from fp4_quantization_aware_fq_gb300 import fq
+    from fp4_quantization_aware_fq_gb300 import workloads as W
+    dev = torch.device("cuda", torch.cuda.current_device())
+    x = W.mxfp4_weight(device=dev)
+    rows, cols = x.shape
+    cfg = fq.Config(fq.MXFP4)
+    q = fq.alloc_qtensor(rows, cols, fq.MXFP4, dev)
+    y = torch.empty((rows, cols), dtype=torch.bfloat16, device=dev)
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def call():
+        fq.fq_quantize(x, cfg, row_out=q)
+        fq.fq_dequantize(q, rows, cols, cfg, y=y)
+
+    for _ in range(warmup):
+        call()
+    times = []
+    for i in range(reps):
+        flush.fill_(i & 0xFF)
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        t0.record(stream)
+        call()
+        t1.record(stream)
+        torch.cuda.synchronize()
+        times.append(t0.elapsed_time(t1))
+    times.sort()
+    ms = times[len(times) // 2]
+    nbytes = (2 + 0.5 + 1 / 32 + 0.5 + 1 / 32 + 2) * x.numel()
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    peak, kind = measured_peaks()
+    return {"shape": [rows, cols], "ms_median": round(ms, 4), "ms_min": round(times[0], 4),
+            "gbs": round(gbs, 1), "frac_hbm": round(gbs / peak, 3), "peak_kind": kind,
+            "launches_per_call": 2, "l2": "flushed before each rep (512 MB write)",
+            "note": "mxfp4_weight as quantize then dequantize; not part of the step"}
+
+
 def run_e2e(args, suite, total_bytes):
     """The suite end to end: every step copies each workload's inputs from
     pinned host memory to the device (copy stream), runs the workload's calls
@@ -918,6 +994,8 @@ def main():
             line["nvfp4_small_at_scale"] = run_small_at_scale()
             line["gemm_nvfp4"] = run_gemm(fmt_name="nvfp4")
             line["gemm_mxfp4"] = run_gemm(fmt_name="mxfp4")
+            line["osci_window"] = run_osci_window(suite)
+            line["mxfp4_quant_dequant"] = run_quant_dequant()
         if not args.no_cpu_baseline and world == 1 and not reduced:
             # all host cores (one sample per thread, at once), then one core
             cores = host_cores()

@@ -661,6 +661,52 @@ def run_quant_dequant(reps=20, warmup=3):
             "note": "mxfp4_weight as quantize then dequantize; not part of the step"}
 
 
+def quant_diagnostics(suite):
+    """Quantization error of the workloads' last outputs, for monitoring (not
+    timed): the relative squared error sum (x - xhat)^2 / sum x^2 and the
+    signal-to-quantization-noise ratio in dB, the share of elements the STE
+    mask marks as clipped, and for the stochastically rounded gradient the
+    mean error relative to the mean magnitude (unbiasedness).  xhat is the
+    fake-quantized output of the call, or fq_dequantize of its codes."""
+    import math
+    import torch
+    fq = suite.fq
+    pop = torch.tensor([bin(i).count("1") for i in range(256)], dtype=torch.int64,
+                       device=suite.dev)
+
+    def stats(x, xhat, mask=None):
+        xf, hf = x.double(), xhat.double()
+        err = (hf - xf).pow(2).sum().item()
+        sig = xf.pow(2).sum().item()
+        rel = err / sig if sig > 0 else 0.0
+        d = {"rel_sq_error": float(f"{rel:.4e}"),
+             "sqnr_db": round(-10.0 * math.log10(rel), 2) if rel > 0 else None}
+        if mask is not None:
+            n = x.numel()
+            kept = int(pop[mask[:n // 8].long()].sum().item())
+            d["clipped_share"] = float(f"{1.0 - kept / n:.4e}")
+        return d
+
+    out = {}
+    if "nvfp4_small" in suite.names:
+        out["nvfp4_small"] = stats(suite.x1, suite.xh1, suite.m1)
+    if "mxfp4_weight" in suite.names:
+        out["mxfp4_weight"] = stats(suite.x2, suite.xh2, suite.m2)
+    if "nvfp4_act" in suite.names:
+        out["nvfp4_act"] = stats(suite.x3, suite.xh3, suite.m3)
+    if "act_outliers" in suite.names:
+        out["act_outliers"] = stats(suite.x7, suite.xh7, suite.m7)
+    if "grad_2level" in suite.names:
+        r, c = suite.x4.shape
+        y = fq.fq_dequantize(suite.q4, r, c, suite.cfg4, y_dtype=torch.float32)
+        d = stats(suite.x4, y)
+        x = suite.x4.double()
+        d["rel_bias"] = float(f"{((y.double() - x).mean() / x.abs().mean()).item():.3e}")
+        out["grad_2level"] = d
+    torch.cuda.synchronize()
+    return out
+
+
 def run_e2e(args, suite, total_bytes):
     """The suite end to end: every step copies each workload's inputs from
     pinned host memory to the device (copy stream), runs the workload's calls
@@ -996,6 +1042,7 @@ def main():
             line["gemm_mxfp4"] = run_gemm(fmt_name="mxfp4")
             line["osci_window"] = run_osci_window(suite)
             line["mxfp4_quant_dequant"] = run_quant_dequant()
+            line["quant_diagnostics"] = quant_diagnostics(suite)
         if not args.no_cpu_baseline and world == 1 and not reduced:
             # all host cores (one sample per thread, at once), then one core
             cores = host_cores()

@@ -307,23 +307,23 @@ __global__ void __launch_bounds__(kOutThreads) outlier_row_kernel(const __grid_c
     const PhiloxKey &key = a.key;
     const int64_t bpr = cols / B;
     const int64_t nblk = rows * bpr;
-    const bool narrow = nblk <= 0xFFFFFFFFll;  // 32-bit block -> (row, column) division
     const int lane = threadIdx.x & 31;
     const int wbase = threadIdx.x & ~31;
-    for (int64_t base = (int64_t)blockIdx.x * kOutThreads; base < nblk;
-         base += (int64_t)gridDim.x * kOutThreads) {
+    // (row, block column) of this thread's block: one division for the first,
+    // then each grid step advances them with a carry
+    const int64_t gstep = (int64_t)gridDim.x * kOutThreads;
+    const int64_t dr = gstep / bpr, dcb = gstep - dr * bpr;
+    int64_t rn = ((int64_t)blockIdx.x * kOutThreads + threadIdx.x) / bpr;
+    int64_t cbn = (int64_t)blockIdx.x * kOutThreads + threadIdx.x - rn * bpr;
+    for (int64_t base = (int64_t)blockIdx.x * kOutThreads; base < nblk; base += gstep) {
         const int64_t blk = base + threadIdx.x;
         const bool valid = blk < nblk;
-        int64_t r = 0, c0 = 0;
-        if (valid) {
-            if (narrow) {
-                const uint32_t b32 = (uint32_t)blk, q = b32 / (uint32_t)bpr;
-                r = q;
-                c0 = (int64_t)(b32 - q * (uint32_t)bpr) * B;
-            } else {
-                r = blk / bpr;
-                c0 = (blk - r * bpr) * B;
-            }
+        const int64_t r = rn, c0 = cbn * B;
+        cbn += dcb;
+        rn += dr;
+        if (cbn >= bpr) {
+            cbn -= bpr;
+            ++rn;
         }
         float v[B];
         uint32_t ret = 0u;
@@ -371,8 +371,12 @@ __global__ void __launch_bounds__(kOutThreads) outlier_row_kernel(const __grid_c
                     float h[8];
                     e2m1_decode8(q[w], h);
 #pragma unroll
-                    for (int i = 0; i < 8; ++i)
-                        h[i] = __fmul_rn(h[i], sc.s_eff);
+                    for (int i = 0; i < 8; i += 2) {
+                        const float2 p = mul2(make_float2(h[i], h[i + 1]),
+                                              make_float2(sc.s_eff, sc.s_eff));
+                        h[i] = p.x;
+                        h[i + 1] = p.y;
+                    }
                     if (a.xhat_bf16)
                         *reinterpret_cast<uint4 *>((char *)a.xhat + (blk * B + w * 8) * 2) =
                             make_uint4(bf16x2_rn(h[0], h[1]), bf16x2_rn(h[2], h[3]),
@@ -395,8 +399,9 @@ __global__ void __launch_bounds__(kOutThreads) outlier_row_kernel(const __grid_c
             __syncwarp();  // also orders the owners' xhat stores before the patches
             const int64_t blk0 = base + wbase;
             if (blk0 < nblk) {  // warp-uniform: the span is all in or all out
-                const int64_t r_w = blk0 / bpr;
-                const int64_t cspan = (blk0 - r_w * bpr) * B;
+                // the span lies in this thread's row, and lane 0's block starts it
+                const int64_t r_w = r;
+                const int64_t cspan = c0 - (int64_t)lane * B;
                 const int64_t cend = cspan + 32 * B;
                 const int s0 = pre[cspan >> 5];
                 int s1 = cend >= cols ? kk : pre[cend >> 5];

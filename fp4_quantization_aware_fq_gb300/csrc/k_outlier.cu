@@ -110,7 +110,7 @@ __global__ void __launch_bounds__(kOutThreads) channel_amax_kernel(const void *_
 // indices in ascending order.
 constexpr int kSelThreads = 1024;
 constexpr int kMaxOutWords = 4096;  // channels up to 131072
-constexpr int64_t kFastKept = 8192;  // retained channels listed in shared memory (8 B each)
+constexpr int64_t kFastKept = 8192;  // retained channels listed in shared memory (12 B each)
 
 __device__ __forceinline__ uint64_t channel_key(const float *amax, int c)
 {
@@ -271,13 +271,14 @@ __global__ void __launch_bounds__(kOutThreads) outlier_row_kernel(const __grid_c
     __shared__ NvTables tab;
     __shared__ int pre[kMaxOutWords];
     __shared__ uint32_t mstage[kOutThreads];
-    // fast: the retained columns in ascending order, then 1 / s_j for each
+    // fast: the retained columns in ascending order, then 1 / s_j and s_j for each
     extern __shared__ int kcols[];
     __shared__ float e4m3v[128];  // E4M3 magnitudes by code (0x7F unused)
     const int64_t cols = a.cols, rows = a.rows;
     const int nwords = (int)((cols + 31) / 32);
     const int kk = (int)a.k;
     float *krcp = reinterpret_cast<float *>(kcols + kk);
+    float *ksj = krcp + kk;
     wait_prior_grid();
     popc_prefix<kOutThreads>(a.bitmap, nwords, pre);
     if (fast) {
@@ -290,6 +291,7 @@ __global__ void __launch_bounds__(kOutThreads) outlier_row_kernel(const __grid_c
         for (int t = threadIdx.x; t < kk; t += kOutThreads) {
             const float sj = __ldg(a.fp8_scale + t);
             krcp[t] = (sj == 0.0f) ? 0.0f : __frcp_rn(sj);
+            ksj[t] = sj;
         }
         for (int c = threadIdx.x; c < 128; c += kOutThreads)
             e4m3v[c] = c < 0x7F ? e4m3_value((uint32_t)c) : 0.0f;
@@ -419,7 +421,7 @@ __global__ void __launch_bounds__(kOutThreads) outlier_row_kernel(const __grid_c
                     const float y = __fmul_rn(xv, krcp[t]);
                     const uint32_t code =
                         e4m3_rn_sat(fabsf(y)) | ((__float_as_uint(y) >> 24) & 0x80u);
-                    const float sj = __ldg(a.fp8_scale + t);
+                    const float sj = ksj[t];
                     if (fp8row)
                         fp8row[t] = (uint8_t)code;
                     if (xhrow) {
@@ -431,11 +433,10 @@ __global__ void __launch_bounds__(kOutThreads) outlier_row_kernel(const __grid_c
                         else
                             reinterpret_cast<float *>(xhrow)[off] = h;
                     }
-                    const uint32_t bit = 1u << i;
-                    if (fabsf(xv) <= __fmul_rn(448.0f, sj))
-                        atomicOr(&mstage[wbase + owner], bit);
-                    else
-                        atomicAnd(&mstage[wbase + owner], ~bit);
+                    // the owner's FP4 pass set this bit (a zeroed element is never
+                    // clipped); clear it where the FP8 value clips
+                    if (!(fabsf(xv) <= __fmul_rn(448.0f, sj)))
+                        atomicAnd(&mstage[wbase + owner], ~(1u << i));
                 }
             }
             __syncwarp();
@@ -592,7 +593,7 @@ static cudaError_t outlier_go(const OutlierArgs &a, cudaStream_t s)
     // the sorted-list path: the list fits in shared memory and every row is a
     // whole number of 32-block warp spans
     const int fast = a.k > 0 && a.k <= kFastKept && (a.cols / B) % 32 == 0;
-    const size_t smem = fast ? (size_t)a.k * (sizeof(int) + sizeof(float)) : 0;
+    const size_t smem = fast ? (size_t)a.k * (sizeof(int) + 2 * sizeof(float)) : 0;
     if (smem) {
         const cudaError_t e = cudaFuncSetAttribute(outlier_row_kernel<T, FMT, RND>,
                                                    cudaFuncAttributeMaxDynamicSharedMemorySize,

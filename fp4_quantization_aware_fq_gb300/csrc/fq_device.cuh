@@ -568,6 +568,33 @@ __device__ __forceinline__ float2 e2m1_sr_value2(float2 y, float2 c)
         __uint_as_float(__float_as_uint(r.y) | (__float_as_uint(y.y) & 0x80000000u)));
 }
 
+// One 32-byte store (st.global.v8.b32): a whole sector per lane, where two
+// 16-byte stores from the same lane would each fill half of it in separate
+// instructions.  p must be 32-byte aligned.
+__device__ __forceinline__ void st32(void *p, const uint4 &a, const uint4 &b)
+{
+    asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(a.x),
+                 "r"(a.y), "r"(a.z), "r"(a.w), "r"(b.x), "r"(b.y), "r"(b.z), "r"(b.w)
+                 : "memory");
+}
+
+// BF16 fake-quantized values of eight codes (q: one packed word) under the
+// effective scale s, as one 16-byte vector: v(code) * s in FP32, then RNE.
+__device__ __forceinline__ uint4 xhat8_bf16(uint32_t q, float s)
+{
+    float h[8];
+    e2m1_decode8(q, h);
+    const float2 s2 = make_float2(s, s);
+#pragma unroll
+    for (int i = 0; i < 8; i += 2) {
+        const float2 p = mul2(make_float2(h[i], h[i + 1]), s2);
+        h[i] = p.x;
+        h[i + 1] = p.y;
+    }
+    return make_uint4(bf16x2_rn(h[0], h[1]), bf16x2_rn(h[2], h[3]), bf16x2_rn(h[4], h[5]),
+                      bf16x2_rn(h[6], h[7]));
+}
+
 // Encode B values (already loaded as FP32) of one block under scale sc into
 // B/8 words of packed codes, and the block's STE mask bits (bit i = element i
 // inside [-6 s_eff, 6 s_eff]).  e0 is the flat index of the block's first

@@ -307,6 +307,7 @@ __global__ void __launch_bounds__(kOutThreads) outlier_row_kernel(const __grid_c
     }
     __syncthreads();
     const PhiloxKey &key = a.key;
+    const bool xhat32 = (reinterpret_cast<uintptr_t>(a.xhat) & 31u) == 0;
     const int64_t bpr = cols / B;
     const int64_t nblk = rows * bpr;
     const int lane = threadIdx.x & 31;
@@ -367,7 +368,13 @@ __global__ void __launch_bounds__(kOutThreads) outlier_row_kernel(const __grid_c
                 if (FMT == NV2L && (lane & 7) == 0)
                     a.tscale[blk >> 3] = s_o;
             }
-            if (a.xhat) {
+            if (a.xhat && a.xhat_bf16 && xhat32) {
+                // whole 32-byte sectors: one store per 16 values
+#pragma unroll
+                for (int w = 0; w < B / 8; w += 2)
+                    st32((char *)a.xhat + (blk * B + w * 8) * 2, xhat8_bf16(q[w], sc.s_eff),
+                         xhat8_bf16(q[w + 1], sc.s_eff));
+            } else if (a.xhat) {
 #pragma unroll
                 for (int w = 0; w < B / 8; ++w) {
                     float h[8];

@@ -113,6 +113,7 @@ struct RowOut {
     void *xhat;
     int xhat_bf16;
     uint8_t *mask;
+    bool xhat32;  // xhat is 32-byte aligned (whole-sector stores)
 };
 
 // Quantize one row-wise block of B values held by this thread (v) whose
@@ -158,7 +159,13 @@ __device__ __forceinline__ void row_block(float *v, float am, int64_t blk, bool 
         if (FMT == NV2L && (lane & 7) == 0)
             o.tscale[blk >> 3] = s_o;
     }
-    if (o.xhat) {
+    if (o.xhat && o.xhat_bf16 && o.xhat32) {
+        // whole 32-byte sectors: one store per 16 values
+#pragma unroll
+        for (int w = 0; w < B / 8; w += 2)
+            st32((char *)o.xhat + (blk * B + w * 8) * 2, xhat8_bf16(q[w], sc.s_eff),
+                 xhat8_bf16(q[w + 1], sc.s_eff));
+    } else if (o.xhat) {
 #pragma unroll
         for (int w = 0; w < B / 8; ++w) {
             float xh[8];
@@ -218,7 +225,8 @@ __global__ void __launch_bounds__(kThreads, kRowMinCtas) row_kernel(const __grid
         if (blockIdx.x == 0 && threadIdx.x == 0 && a.tscale)
             a.tscale[0] = s_g;
     }
-    const RowOut o{a.codes, a.scales, a.tscale, a.xhat, a.xhat_bf16, a.mask};
+    const RowOut o{a.codes, a.scales, a.tscale, a.xhat, a.xhat_bf16, a.mask,
+                   (reinterpret_cast<uintptr_t>(a.xhat) & 31u) == 0};
     const PhiloxKey &key = a.key;
     const bool rht = a.rht_seed != 0;
     const uint32_t signs = rht ? rht_signs(a.rht_seed, a.offset) : 0u;
@@ -335,7 +343,8 @@ __global__ void __launch_bounds__(kThreads, tile_min_ctas<T, FMT>())
                 a.rtscale[0] = s_g;
         }
     }
-    const RowOut o{a.rcodes, a.rscales, a.rtscale, a.xhat, a.xhat_bf16, a.mask};
+    const RowOut o{a.rcodes, a.rscales, a.rtscale, a.xhat, a.xhat_bf16, a.mask,
+                   (reinterpret_cast<uintptr_t>(a.xhat) & 31u) == 0};
     const PhiloxKey &key = a.key;
     const bool rht = a.rht_seed != 0;
     const uint32_t signs = rht ? rht_signs(a.rht_seed, a.offset) : 0u;

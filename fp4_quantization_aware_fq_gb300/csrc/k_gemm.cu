@@ -293,6 +293,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             const int q = warp & 3;
             const int row = m0 + 32 * q + lane;
             const bool row_ok = row < g.m;  // rows past m hold the tile's zero padding
+            const bool c32 = (reinterpret_cast<uintptr_t>(g.c) & 31u) == 0;
             float alpha = 1.0f;
             if (g.tscale_a && g.tscale_b)
                 alpha = __fmul_rn(__ldg(g.tscale_a), __ldg(g.tscale_b));
@@ -306,7 +307,21 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 const int64_t off = (int64_t)row * g.n + n0 + 32 * c;
                 if (!row_ok || n0 + 32 * c >= g.n)  // n % 32 == 0: a 32-column chunk is all in or out
                     continue;
-                if (g.c_bf16) {
+                if (g.c_bf16 && c32) {
+                    // whole 32-byte sectors, one store per 16 values
+                    char *dst = (char *)g.c + off * 2;
+#pragma unroll
+                    for (int i = 0; i < 4; i += 2)
+                        st32(dst + 16 * i,
+                             make_uint4(bf16x2_rn(v[8 * i], v[8 * i + 1]),
+                                        bf16x2_rn(v[8 * i + 2], v[8 * i + 3]),
+                                        bf16x2_rn(v[8 * i + 4], v[8 * i + 5]),
+                                        bf16x2_rn(v[8 * i + 6], v[8 * i + 7])),
+                             make_uint4(bf16x2_rn(v[8 * i + 8], v[8 * i + 9]),
+                                        bf16x2_rn(v[8 * i + 10], v[8 * i + 11]),
+                                        bf16x2_rn(v[8 * i + 12], v[8 * i + 13]),
+                                        bf16x2_rn(v[8 * i + 14], v[8 * i + 15])));
+                } else if (g.c_bf16) {
                     uint4 *dst = reinterpret_cast<uint4 *>((char *)g.c + off * 2);
 #pragma unroll
                     for (int i = 0; i < 4; ++i)
@@ -314,6 +329,15 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                                             bf16x2_rn(v[8 * i + 2], v[8 * i + 3]),
                                             bf16x2_rn(v[8 * i + 4], v[8 * i + 5]),
                                             bf16x2_rn(v[8 * i + 6], v[8 * i + 7]));
+                } else if (c32) {
+                    char *dst = (char *)g.c + off * 4;
+#pragma unroll
+                    for (int i = 0; i < 8; i += 2)
+                        st32(dst + 16 * i,
+                             make_uint4(__float_as_uint(v[4 * i]), __float_as_uint(v[4 * i + 1]),
+                                        __float_as_uint(v[4 * i + 2]), __float_as_uint(v[4 * i + 3])),
+                             make_uint4(__float_as_uint(v[4 * i + 4]), __float_as_uint(v[4 * i + 5]),
+                                        __float_as_uint(v[4 * i + 6]), __float_as_uint(v[4 * i + 7])));
                 } else {
                     float4 *dst = reinterpret_cast<float4 *>((char *)g.c + off * 4);
 #pragma unroll

@@ -390,7 +390,13 @@ __global__ void __launch_bounds__(kOutThreads) outlier_row_kernel(const __grid_c
                         *reinterpret_cast<uint4 *>((char *)a.xhat + (blk * B + w * 8) * 2) =
                             make_uint4(bf16x2_rn(h[0], h[1]), bf16x2_rn(h[2], h[3]),
                                        bf16x2_rn(h[4], h[5]), bf16x2_rn(h[6], h[7]));
-                    else {
+                    else if (xhat32) {
+                        st32((char *)a.xhat + (blk * B + w * 8) * 4,
+                             make_uint4(__float_as_uint(h[0]), __float_as_uint(h[1]),
+                                        __float_as_uint(h[2]), __float_as_uint(h[3])),
+                             make_uint4(__float_as_uint(h[4]), __float_as_uint(h[5]),
+                                        __float_as_uint(h[6]), __float_as_uint(h[7])));
+                    } else {
                         float4 *dst =
                             reinterpret_cast<float4 *>((char *)a.xhat + (blk * B + w * 8) * 4);
                         dst[0] = make_float4(h[0], h[1], h[2], h[3]);

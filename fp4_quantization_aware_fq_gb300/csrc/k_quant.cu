@@ -180,6 +180,12 @@ __device__ __forceinline__ void row_block(float *v, float am, int64_t blk, bool 
                 *reinterpret_cast<uint4 *>((char *)o.xhat + (blk * B + w * 8) * 2) =
                     make_uint4(bf16x2_rn(xh[0], xh[1]), bf16x2_rn(xh[2], xh[3]),
                                bf16x2_rn(xh[4], xh[5]), bf16x2_rn(xh[6], xh[7]));
+            } else if (o.xhat32) {
+                st32((char *)o.xhat + (blk * B + w * 8) * 4,
+                     make_uint4(__float_as_uint(xh[0]), __float_as_uint(xh[1]),
+                                __float_as_uint(xh[2]), __float_as_uint(xh[3])),
+                     make_uint4(__float_as_uint(xh[4]), __float_as_uint(xh[5]),
+                                __float_as_uint(xh[6]), __float_as_uint(xh[7])));
             } else {
                 float4 *dst = reinterpret_cast<float4 *>((char *)o.xhat + (blk * B + w * 8) * 4);
                 dst[0] = make_float4(xh[0], xh[1], xh[2], xh[3]);

@@ -665,5 +665,31 @@ __device__ __forceinline__ void load_block(const void *src, float *v)
         unpack16<T>(ld16((const char *)src + 16 * k), v + k * E);
 }
 
+// One 32-byte load (ld.global.nc.v8.b32): a whole sector per lane, where two
+// 16-byte loads from the same lane each take half of it.  p must be 32-byte
+// aligned.
+__device__ __forceinline__ void ld32(const void *p, uint4 &a, uint4 &b)
+{
+    asm("ld.global.nc.v8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+        : "=r"(a.x), "=r"(a.y), "=r"(a.z), "=r"(a.w), "=r"(b.x), "=r"(b.y), "=r"(b.z), "=r"(b.w)
+        : "l"(p));
+}
+
+// NV consecutive 16-byte vectors from src, 32 bytes per load when al32 (src
+// 32-byte aligned; NV even).
+template <int NV>
+__device__ __forceinline__ void load_vecs(const char *src, uint4 *raw, bool al32)
+{
+    if (NV % 2 == 0 && al32) {
+#pragma unroll
+        for (int k = 0; k < NV; k += 2)
+            ld32(src + 16 * k, raw[k], raw[k + 1]);
+    } else {
+#pragma unroll
+        for (int k = 0; k < NV; ++k)
+            raw[k] = ld16(src + 16 * k);
+    }
+}
+
 }  // namespace fqk
 

@@ -361,6 +361,10 @@ __global__ void __launch_bounds__(kThreads, tile_min_ctas<T, FMT>())
     constexpr int RPT = (TR * RBPR + kThreads - 1) / kThreads;
     constexpr int NV = BR / E;  // 16-byte vectors per row block
     uint4 nxt[RPT][NV];
+    // whole-sector loads: x and its row pitch on 32-byte boundaries (row blocks
+    // start at multiples of 16 elements)
+    const bool tal32 = ((reinterpret_cast<uintptr_t>(a.x) |
+                         (uintptr_t)((STRIDED ? a.ld : cols) * (int64_t)sizeof(T))) & 31u) == 0;
     auto load_tile = [&](int ty, int tx) {
         const int64_t lr0 = (int64_t)ty * TR, lc0 = (int64_t)tx * TC;
 #pragma unroll
@@ -375,10 +379,14 @@ __global__ void __launch_bounds__(kThreads, tile_min_ctas<T, FMT>())
             // a column-only MXFP4 call admits cols % 32 == 16, where the last
             // 1x32 row block of a row holds only 16 elements (cols is a
             // multiple of 16, hence of E, so a vector is all in or all out).
+            if (valid && tal32 && gc + (int64_t)NV * E <= cols) {
+                load_vecs<NV>(src, nxt[j], true);
+            } else {
 #pragma unroll
-            for (int k = 0; k < NV; ++k)
-                nxt[j][k] = (valid && gc + (int64_t)k * E < cols) ? ld16(src + 16 * k)
-                                                                  : make_uint4(0, 0, 0, 0);
+                for (int k = 0; k < NV; ++k)
+                    nxt[j][k] = (valid && gc + (int64_t)k * E < cols) ? ld16(src + 16 * k)
+                                                                      : make_uint4(0, 0, 0, 0);
+            }
         }
     };
 

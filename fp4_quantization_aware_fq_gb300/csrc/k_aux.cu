@@ -21,6 +21,9 @@ __global__ void __launch_bounds__(kAuxThreads) dequant_kernel(DequantArgs a)
     constexpr int B = FmtInfo<FMT>::B;
     const int64_t ng = a.n / 8;
     const int64_t stride = (int64_t)gridDim.x * kAuxThreads;
+    // FP32 output in 32-byte stores when every group of 8 starts on a 32-byte
+    // boundary (y aligned, and so is its row pitch)
+    const bool y32 = ((reinterpret_cast<uintptr_t>(a.y) | (uintptr_t)(a.ldy * 4)) & 31u) == 0;
     for (int64_t g = (int64_t)blockIdx.x * kAuxThreads + threadIdx.x; g < ng; g += stride) {
         const uint32_t q = __ldg(reinterpret_cast<const uint32_t *>(a.codes) + g);
         const int64_t e0 = g * 8;
@@ -45,6 +48,12 @@ __global__ void __launch_bounds__(kAuxThreads) dequant_kernel(DequantArgs a)
             uint4 o = make_uint4(bf16x2_rn(xh[0], xh[1]), bf16x2_rn(xh[2], xh[3]),
                                  bf16x2_rn(xh[4], xh[5]), bf16x2_rn(xh[6], xh[7]));
             *reinterpret_cast<uint4 *>((char *)a.y + oe * 2) = o;
+        } else if (y32) {  // whole 32-byte sectors
+            st32((char *)a.y + oe * 4,
+                 make_uint4(__float_as_uint(xh[0]), __float_as_uint(xh[1]), __float_as_uint(xh[2]),
+                            __float_as_uint(xh[3])),
+                 make_uint4(__float_as_uint(xh[4]), __float_as_uint(xh[5]), __float_as_uint(xh[6]),
+                            __float_as_uint(xh[7])));
         } else {
             float4 *dst = reinterpret_cast<float4 *>((char *)a.y + oe * 4);
             dst[0] = make_float4(xh[0], xh[1], xh[2], xh[3]);
@@ -53,33 +62,52 @@ __global__ void __launch_bounds__(kAuxThreads) dequant_kernel(DequantArgs a)
     }
 }
 
-// One thread = one 16-byte vector of dy.
+// Each thread takes kSteU 16-byte vectors of dy per step (kAuxThreads apart,
+// so every load is coalesced across the warp), all loads issued before any
+// is used: four vectors in flight per thread keep about 32 KB of loads in
+// flight per CTA.
+constexpr int kSteU = 4;
 template <typename T>
 __global__ void __launch_bounds__(kAuxThreads) ste_kernel(const void *__restrict__ dy,
                                                           const uint8_t *__restrict__ mask,
                                                           int64_t nch, void *__restrict__ dx)
 {
     constexpr int E = VecInfo<T>::E;
-    const int64_t stride = (int64_t)gridDim.x * kAuxThreads;
-    for (int64_t ch = (int64_t)blockIdx.x * kAuxThreads + threadIdx.x; ch < nch; ch += stride) {
-        uint4 v = ld16((const char *)dy + ch * 16);
-        uint32_t m = __ldg(mask + (ch * E) / 8);
-        if (E == 4)
-            m >>= (ch & 1) * 4;
-        uint32_t w[4] = {v.x, v.y, v.z, v.w};
-        if (E == 8) {
+    const int64_t stride = (int64_t)gridDim.x * kAuxThreads * kSteU;
+    for (int64_t base = (int64_t)blockIdx.x * kAuxThreads * kSteU; base < nch; base += stride) {
+        uint4 v[kSteU];
+        uint32_t m[kSteU];
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const uint32_t keep = ((m >> (2 * i)) & 1u ? 0x0000FFFFu : 0u) |
-                                      ((m >> (2 * i + 1)) & 1u ? 0xFFFF0000u : 0u);
-                w[i] &= keep;
+        for (int k = 0; k < kSteU; ++k) {
+            const int64_t ch = base + k * kAuxThreads + threadIdx.x;
+            if (ch < nch) {
+                v[k] = ld16((const char *)dy + ch * 16);
+                m[k] = __ldg(mask + (ch * E) / 8);
             }
-        } else {
-#pragma unroll
-            for (int i = 0; i < 4; ++i)
-                w[i] = ((m >> i) & 1u) ? w[i] : 0u;
         }
-        reinterpret_cast<uint4 *>(dx)[ch] = make_uint4(w[0], w[1], w[2], w[3]);
+#pragma unroll
+        for (int k = 0; k < kSteU; ++k) {
+            const int64_t ch = base + k * kAuxThreads + threadIdx.x;
+            if (ch >= nch)
+                continue;
+            uint32_t mk = m[k];
+            if (E == 4)
+                mk >>= (ch & 1) * 4;
+            uint32_t w[4] = {v[k].x, v[k].y, v[k].z, v[k].w};
+            if (E == 8) {
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const uint32_t keep = ((mk >> (2 * i)) & 1u ? 0x0000FFFFu : 0u) |
+                                          ((mk >> (2 * i + 1)) & 1u ? 0xFFFF0000u : 0u);
+                    w[i] &= keep;
+                }
+            } else {
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                    w[i] = ((mk >> i) & 1u) ? w[i] : 0u;
+            }
+            reinterpret_cast<uint4 *>(dx)[ch] = make_uint4(w[0], w[1], w[2], w[3]);
+        }
     }
 }
 
@@ -114,7 +142,7 @@ cudaError_t launch_ste(const void *dy, int bf16, const uint8_t *mask, int64_t n,
     if (n == 0)
         return cudaSuccess;
     const int64_t nch = n / (bf16 ? 8 : 4);
-    const int grid = grid_for(nch, 8);
+    const int grid = grid_for((nch + kSteU - 1) / kSteU, 4);
     if (bf16)
         ste_kernel<__nv_bfloat16><<<grid, kAuxThreads, 0, s>>>(dy, mask, nch, dx);
     else

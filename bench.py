@@ -72,14 +72,14 @@ LAUNCHES_PER_STEP = {"nvfp4_small": 2, "mxfp4_weight": 1, "nvfp4_act": 2, "ste_b
 # DRAM traffic per call of the OsciReset steps from an ncu capture, valid only
 # for the kernel sources it was taken on (sha256 of the OsciReset sources).
 # Captured on the 2-expert case (66.4 M weights; pass A + pass B read + write:
-# 2227.2 MB for the ordinary step, 2824.2 MB for the window-end step) and
+# 2228.0 MB for the ordinary step, 2823.6 MB for the window-end step) and
 # scaled by the weights processed to the 32-expert call (traffic is linear in
 # the number of weights).
 _OSCI_SCALE = 1061683200 / 66355200
-NCU_TRAFFIC = {"osci_update": {"bytes": int((1270196480 + 957032704) * _OSCI_SCALE),
-                               "src_sha256": "bd356cd28a000929f6bd2ea87c7f3e48747ead30794f9d5527514e9a4affe524"},
-               "osci_update_reset": {"bytes": int((1267570688 + 1556631296) * _OSCI_SCALE),
-                                     "src_sha256": "bd356cd28a000929f6bd2ea87c7f3e48747ead30794f9d5527514e9a4affe524"}}
+NCU_TRAFFIC = {"osci_update": {"bytes": int((1270751488 + 957224960) * _OSCI_SCALE),
+                               "src_sha256": "e90bdd1e2ecf7cc6e38986de7bf7b9ff7693a6b1cd87f7bc7423558fce02aa53"},
+               "osci_update_reset": {"bytes": int((1267193856 + 1556393216) * _OSCI_SCALE),
+                                     "src_sha256": "e90bdd1e2ecf7cc6e38986de7bf7b9ff7693a6b1cd87f7bc7423558fce02aa53"}}
 
 
 def log(*a):

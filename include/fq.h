@@ -64,7 +64,10 @@
  * Conventions:
  *  - Every pointer argument to tensor data is a DEVICE pointer unless said
  *    otherwise; the caller allocates all of them.  Pointers to tensor data
- *    must be 16-byte aligned (FQ_ERR_ALIGN otherwise).
+ *    must be 16-byte aligned (FQ_ERR_ALIGN otherwise).  Where x, xhat, y or
+ *    the GEMM's C (and its row pitch) are 32-byte aligned as well, the
+ *    kernels move whole 32-byte sectors per access; the results are the same
+ *    either way.
  *  - `stream` is a cudaStream_t passed as void*; NULL is the legacy default
  *    stream.  Calls are asynchronous on that stream: they never synchronise,
  *    never allocate device memory, and may return before the GPU finishes.

@@ -67,9 +67,7 @@ struct VecInfo<__nv_bfloat16> {
         return d;                                                                           \
     }
 FQK_F32X2_TERNARY(fma2, "fma.rn.f32x2")
-FQK_F32X2_TERNARY(fma2_rz, "fma.rz.f32x2")
 FQK_F32X2_BINARY(add2, "add.rn.f32x2")
-FQK_F32X2_BINARY(add2_ru, "add.rp.f32x2")
 FQK_F32X2_BINARY(sub2, "sub.rn.f32x2")
 FQK_F32X2_BINARY(mul2, "mul.rn.f32x2")
 #undef FQK_F32X2_TERNARY
@@ -525,9 +523,12 @@ __device__ __forceinline__ void e2m1_decode8(uint32_t q, float *out)
 // The sign of y is copied (a zero result keeps it).
 __device__ __forceinline__ float e2m1_sr_value(float y, float c)
 {
-    // q = 1 for |y| < 1, else 0 (one set instruction)
+    // q = 1 for |y| < 1, else 0, on the FMA pipe: 2^24 (1 - |y|) is at least 1
+    // for every FP32 |y| < 1 (the largest is 1 - 2^-24) and at most 0 from 1 on,
+    // so clamping it to [0, 1] gives q exactly (a NaN clamps to 0, as a compare
+    // would give)
     float q;
-    asm("set.lt.f32.f32 %0, %1, 0f3F800000;" : "=f"(q) : "f"(fabsf(y)));
+    asm("fma.rn.sat.f32 %0, %1, 0fCB800000, 0f4B800000;" : "=f"(q) : "f"(fabsf(y)));
     const float z = __fadd_ru(fabsf(y), q);                              // |y| + 1 or |y|
     const float p = __uint_as_float(__float_as_uint(z) & 0x7F800000u);   // 2^e of z
     const float t = __fmaf_rz(c, p, z);
@@ -549,23 +550,6 @@ __device__ __forceinline__ float2 sr_operand2(uint32_t word)
     const float2 u = sub2(b, make_float2(8388608.0f, 8388608.0f));  // exact
     return fma2(u, make_float2(-7.62939453125e-06f, -7.62939453125e-06f),
                 make_float2(0.49999988079071044921875f, 0.49999988079071044921875f));
-}
-
-// e2m1_sr_value on a pair, the floating-point steps in packed form.
-__device__ __forceinline__ float2 e2m1_sr_value2(float2 y, float2 c)
-{
-    const float2 a = make_float2(fabsf(y.x), fabsf(y.y));
-    const float2 q = make_float2(a.x < 1.0f ? 1.0f : 0.0f, a.y < 1.0f ? 1.0f : 0.0f);
-    const float2 z = add2_ru(a, q);
-    const float2 p = make_float2(__uint_as_float(__float_as_uint(z.x) & 0x7F800000u),
-                                 __uint_as_float(__float_as_uint(z.y) & 0x7F800000u));
-    const float2 t = fma2_rz(c, p, z);
-    const float2 m = make_float2(__uint_as_float(__float_as_uint(t.x) & 0xFFC00000u),
-                                 __uint_as_float(__float_as_uint(t.y) & 0xFFC00000u));
-    const float2 r = sub2(m, q);
-    return make_float2(
-        __uint_as_float(__float_as_uint(r.x) | (__float_as_uint(y.x) & 0x80000000u)),
-        __uint_as_float(__float_as_uint(r.y) | (__float_as_uint(y.y) & 0x80000000u)));
 }
 
 // One 32-byte store (st.global.v8.b32): a whole sector per lane, where two

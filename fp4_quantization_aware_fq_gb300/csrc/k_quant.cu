@@ -455,44 +455,46 @@ __global__ void __launch_bounds__(kThreads, tile_min_ctas<T, FMT>())
     // Phase 2: column blocks (BC rows x 1 column) out of shared memory.  BF16
     // NVFP4 tiles are read two columns at a time (one 32-bit word per row).
     const uint32_t *tile32 = reinterpret_cast<const uint32_t *>(tile);
-    auto col_amax = [&](float *w) {  // double block: inner amax for the outer scale
-        if (rht) {
-#pragma unroll
-            for (int j = 0; j < BC / 16; ++j)
-                rht16(w + 16 * j, signs);
-        }
+    auto abs_max = [&](const float *v) {
         float m = 0.0f;
 #pragma unroll
         for (int i = 0; i < BC; ++i)
-            m = fmaxf(m, fabsf(w[i]));
+            m = fmaxf(m, fabsf(v[i]));
         return m;
     };
+    // column c, rows rb * BC .. rb * BC + BC - 1 of the tile, widened to FP32
+    // (and Hadamard-transformed, if asked: not for NVFP4)
+    auto load_col = [&](int c, int rb, float *v) {
+#pragma unroll
+        for (int i = 0; i < BC; ++i)
+            v[i] = static_cast<float>(tile[(rb * BC + i) * TCP + c]);
+        if (FMT != NVFP4 && rht) {
+#pragma unroll
+            for (int j = 0; j < BC / 16; ++j)
+                rht16(v + 16 * j, signs);
+        }
+    };
+    // Double block: a first sweep stores the amax of every 16 x 1 block, for
+    // the 128-row outer scales.  In both sweeps a thread's column is the same
+    // for each of its tasks (TC divides the thread count), so the quantize
+    // sweep derives its outer scale once per tile and takes each block's
+    // amax from the first sweep.
+    static_assert(FMT != NV2L || kThreads % TC == 0, "a thread's column must not change");
     if (FMT == NV2L) {
         for (int task = threadIdx.x; task < TC * NRB; task += kThreads) {
             const int c = task % TC, rb = task / TC;
-            float w[BC];
-#pragma unroll
-            for (int i = 0; i < BC; ++i)
-                w[i] = static_cast<float>(tile[(rb * BC + i) * TCP + c]);
-            am16[rb * TC + c] = col_amax(w);
+            float v[BC];
+            load_col(c, rb, v);
+            am16[rb * TC + c] = abs_max(v);
         }
         __syncthreads();
     }
     // quantize column block (c, rb) of the tile into the staging buffers: v
     // holds the block (after the Hadamard transform, if any), m its amax
-    auto col_quant = [&](int c, int rb, float *v, float m) {
+    auto col_quant = [&](int c, int rb, float *v, float m, float s_o, float inv6c) {
         const int64_t gc = c0 + c, gr0 = r0 + (int64_t)rb * BC;
-        float s_o = s_g, inv6c = inv6;
-        if (FMT == NV2L) {
-            float mo = 0.0f;
-#pragma unroll
-            for (int j = 0; j < NRB; ++j)
-                mo = fmaxf(mo, am16[j * TC + c]);
-            s_o = outer_scale(mo);
-            inv6c = nv_inv6(s_o);
-            if (rb == 0)
-                a.ctscale[gc * (rows / 128) + r0 / 128] = s_o;
-        }
+        if (FMT == NV2L && rb == 0)
+            a.ctscale[gc * (rows / 128) + r0 / 128] = s_o;
         const Scale sc = block_scale<FMT>(m, s_o, inv6c, &tab);
         uint32_t q[BC / 8];
         // flat index in X^T of the block's first element
@@ -520,11 +522,28 @@ __global__ void __launch_bounds__(kThreads, tile_min_ctas<T, FMT>())
 #pragma unroll
             for (int i = 0; i < BC; ++i)
                 v[i] = __uint_as_float(wd[i] << 16);
-            col_quant(c, rb, v, bf16_lo_abs(mw));
+            col_quant(c, rb, v, bf16_lo_abs(mw), s_g, inv6);
 #pragma unroll
             for (int i = 0; i < BC; ++i)
                 v[i] = __uint_as_float(wd[i] & 0xFFFF0000u);
-            col_quant(c + 1, rb, v, bf16_hi_abs(mw));
+            col_quant(c + 1, rb, v, bf16_hi_abs(mw), s_g, inv6);
+        }
+    } else if constexpr (FMT == NV2L) {
+        // the outer scale of this thread's column: the largest inner amax of
+        // the column over the tile's 128 rows
+        const int c = threadIdx.x % TC;
+        float mo = 0.0f;
+#pragma unroll
+        for (int j = 0; j < NRB; ++j)
+            mo = fmaxf(mo, am16[j * TC + c]);
+        const float s_o = outer_scale(mo), inv6c = nv_inv6(s_o);
+        for (int task = threadIdx.x; task < TC * NRB; task += kThreads) {
+            const int rb = task / TC;
+            if (c0 + c >= cols || r0 + (int64_t)rb * BC >= rows)
+                continue;
+            float v[BC];
+            load_col(c, rb, v);  // the same values as in the amax sweep
+            col_quant(c, rb, v, am16[rb * TC + c], s_o, inv6c);
         }
     } else {
         for (int task = threadIdx.x; task < TC * NRB; task += kThreads) {
@@ -532,19 +551,8 @@ __global__ void __launch_bounds__(kThreads, tile_min_ctas<T, FMT>())
             if (c0 + c >= cols || r0 + (int64_t)rb * BC >= rows)
                 continue;
             float v[BC];
-#pragma unroll
-            for (int i = 0; i < BC; ++i)
-                v[i] = static_cast<float>(tile[(rb * BC + i) * TCP + c]);
-            if (FMT != NVFP4 && rht) {
-#pragma unroll
-                for (int j = 0; j < BC / 16; ++j)
-                    rht16(v + 16 * j, signs);
-            }
-            float m = 0.0f;
-#pragma unroll
-            for (int i = 0; i < BC; ++i)
-                m = fmaxf(m, fabsf(v[i]));
-            col_quant(c, rb, v, m);
+            load_col(c, rb, v);
+            col_quant(c, rb, v, abs_max(v), s_g, inv6);
         }
     }
     __syncthreads();

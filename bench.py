@@ -72,14 +72,14 @@ LAUNCHES_PER_STEP = {"nvfp4_small": 2, "mxfp4_weight": 1, "nvfp4_act": 2, "ste_b
 # DRAM traffic per call of the OsciReset steps from an ncu capture, valid only
 # for the kernel sources it was taken on (sha256 of the OsciReset sources).
 # Captured on the 2-expert case (66.4 M weights; pass A + pass B read + write:
-# 2228.0 MB for the ordinary step, 2823.6 MB for the window-end step) and
+# 2227.2 MB for the ordinary step, 2824.4 MB for the window-end step) and
 # scaled by the weights processed to the 32-expert call (traffic is linear in
 # the number of weights).
 _OSCI_SCALE = 1061683200 / 66355200
-NCU_TRAFFIC = {"osci_update": {"bytes": int((1270751488 + 957224960) * _OSCI_SCALE),
-                               "src_sha256": "e90bdd1e2ecf7cc6e38986de7bf7b9ff7693a6b1cd87f7bc7423558fce02aa53"},
-               "osci_update_reset": {"bytes": int((1267193856 + 1556393216) * _OSCI_SCALE),
-                                     "src_sha256": "e90bdd1e2ecf7cc6e38986de7bf7b9ff7693a6b1cd87f7bc7423558fce02aa53"}}
+NCU_TRAFFIC = {"osci_update": {"bytes": int((1270093824 + 957093888) * _OSCI_SCALE),
+                               "src_sha256": "77eccac8680c362de9c2a40e9b8bda7658e29741b4fc3dd99c9293d23ca5a730"},
+               "osci_update_reset": {"bytes": int((1267671296 + 1556755968) * _OSCI_SCALE),
+                                     "src_sha256": "77eccac8680c362de9c2a40e9b8bda7658e29741b4fc3dd99c9293d23ca5a730"}}
 
 
 def log(*a):

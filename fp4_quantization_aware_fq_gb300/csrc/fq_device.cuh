@@ -5,10 +5,14 @@
 // Definitions follow the library header (include/fq.h): NVFP4 and MXFP4 as
 // named on "Aprimorando gpt-oss para Precisão e Desempenho com Treinamento
 // Consciente à Quantização" ("O que há de novo"), the double block and
-// stochastic rounding of "Resumo Técnico: TetraJet-v2" §2A.  All scale and
-// product arithmetic uses explicit round-to-nearest intrinsics (__fdiv_rn,
-// __fmul_rn, __frcp_rn) so that no FMA contraction or approximate division
-// can change a stored bit.
+// stochastic rounding of "Resumo Técnico: TetraJet-v2" §2A.  Every operation
+// that decides a stored bit has an explicit rounding (round-to-nearest
+// intrinsics such as __fdiv_rn and __fmul_rn, or PTX with its rounding mode:
+// the packed f32x2 forms, the round-up and round-toward-zero steps of
+// stochastic rounding), so no FMA contraction can change one.  The one
+// approximate operation, the reciprocal estimate of the scale-code search,
+// works inside a guard band: near an E4M3 rounding boundary the code is taken
+// from the exact divisions instead.
 #pragma once
 
 #include <cuda_bf16.h>

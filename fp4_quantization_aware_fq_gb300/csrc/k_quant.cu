@@ -2,16 +2,18 @@
 // column-wise quantization kernels.
 //
 // Row-wise ("Resumo Técnico: TetraJet-v2" §2A, 1x16 groups; MXFP4 1x32 as
-// named on "Aprimorando gpt-oss ...", "O que há de novo"): each thread owns
-// one 16-byte vector of the input (8 BF16 or 4 FP32 values); the lanes that
-// share a block combine their partial amax with warp shuffles, derive the
-// scale in registers, and write packed codes, scales, the fake-quantized
-// values and the STE mask with coalesced stores.
+// named on "Aprimorando gpt-oss ...", "O que há de novo"): one thread per
+// block.  The thread loads the block's 16-byte vectors, takes its amax (for
+// BF16 1x16 blocks from a max tree over the packed pairs), derives the scale
+// once and writes the packed codes, the scale, the fake-quantized values and
+// the STE mask bits of its block.  The double block's 8 inner blocks of a
+// 1x128 outer block sit on 8 consecutive lanes, which share the outer amax
+// by shuffles.
 //
 // Column-wise (§2A, the transposed 1x16 groups of the backward pass): a CTA
 // stages a tile of x in shared memory while doing the row-wise pass on it,
-// then quantizes 16x1 column blocks out of shared memory and writes the
-// transposed codes through a shared-memory staging buffer.
+// then quantizes column blocks (16x1; 32x1 for MXFP4) out of shared memory
+// and writes the transposed codes through a shared-memory staging buffer.
 #include "fq_device.cuh"
 #include "fq_internal.h"
 

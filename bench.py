@@ -77,9 +77,9 @@ LAUNCHES_PER_STEP = {"nvfp4_small": 2, "mxfp4_weight": 1, "nvfp4_act": 2, "ste_b
 # the number of weights).
 _OSCI_SCALE = 1061683200 / 66355200
 NCU_TRAFFIC = {"osci_update": {"bytes": int((1270093824 + 957093888) * _OSCI_SCALE),
-                               "src_sha256": "d2c0a5d5d221240aca20c781756bd0adf19730dbf2c98778e1bb50f12f738fe6"},
+                               "src_sha256": "6cb22632f8f08604d603377791a1b27f2dc5c97241e85ba33939fdb8a6b65569"},
                "osci_update_reset": {"bytes": int((1267671296 + 1556755968) * _OSCI_SCALE),
-                                     "src_sha256": "d2c0a5d5d221240aca20c781756bd0adf19730dbf2c98778e1bb50f12f738fe6"}}
+                                     "src_sha256": "6cb22632f8f08604d603377791a1b27f2dc5c97241e85ba33939fdb8a6b65569"}}
 
 
 def log(*a):

@@ -19,8 +19,8 @@ namespace fqk {
 
 constexpr int kOsciThreads = 256;
 constexpr int kOsciU = 4;   // chunks in flight per thread: the reset pass
-// Pass A: eight chunks in flight per thread (one CTA per SM at its register
-// count) measured 1% faster on the 32-expert step than four.
+// Pass A: eight chunks in flight per thread (128 registers: two CTAs per SM)
+// measured 1% faster on the 32-expert step than four.
 constexpr int kOsciAU = 8;
 // Pass B, four CTAs per SM (at most 64 registers).  With the window-end reset
 // (eleven streams per chunk) one chunk per thread at a time measured fastest

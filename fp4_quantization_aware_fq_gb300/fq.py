@@ -506,8 +506,8 @@ def fq_gemm_workspace_size(m: int, n: int, k: int) -> int:
 def fq_gemm(a: QTensor, b: QTensor, m: int, n: int, k: int, cfg: Optional[Config] = None,
             c: Optional[torch.Tensor] = None, c_dtype=torch.float32,
             ws: Optional[torch.Tensor] = None, err: Optional[torch.Tensor] = None, stream=None):
-    """C[m, n] = deq(A) deq(B)^T for row-wise NVFP4 A [m, k] and B [n, k] on
-    the tensor cores.  Returns (C, err); err is a device int32 that is
+    """C[m, n] = deq(A) deq(B)^T for row-wise NVFP4 or MXFP4 (cfg.format) A
+    [m, k] and B [n, k] on the tensor cores.  Returns (C, err); err is a device int32 that is
     non-zero if a pipeline wait timed out (read it after synchronising)."""
     cfg = cfg or Config(NVFP4)
     dev = a.codes.device

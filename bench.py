@@ -617,6 +617,42 @@ def run_osci_window(suite, windows=2):
                     "suite step"}
 
 
+def run_osci_reset(suite, reps=5):
+    """The standalone window-end reset (fq_osci_reset) over the MoE group: each
+    rep runs one ordinary QAT step (untimed, so the accumulators hold a step's
+    statistics), then the reset alone between CUDA events.  20.5625
+    algorithmic bytes per weight, the reset pass counted as if every weight
+    were reset: dist_Q and dist_M read and written back as zero (16), the
+    current codes and scales read (0.5625) and the master weight written (4).
+    Not part of the suite step: the step fuses the reset into its last update
+    (fq_osci_update_reset), at 8 more bytes per weight than an update."""
+    import torch
+    fq = suite.fq
+    stream = torch.cuda.current_stream()
+    times = []
+    for _ in range(reps):
+        suite.osci_update()
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        t0.record(stream)
+        # after osci_update's swap, prev holds the step's codes: the current bin
+        fq.fq_osci_reset(suite.cfg5, suite.master, suite.dq, suite.dm, suite.prev, 4.0,
+                         n_reset=suite.nreset)
+        t1.record(stream)
+        torch.cuda.synchronize()
+        times.append(t0.elapsed_time(t1))
+    times.sort()
+    ms = times[len(times) // 2]
+    nbytes = (16 + 0.5 + 1 / 16 + 4) * suite.elems["osci_update"]
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    peak, kind = measured_peaks()
+    return {"weights": suite.elems["osci_update"], "ms_median": round(ms, 4),
+            "ms_min": round(times[0], 4), "gbs": round(gbs, 1), "frac_hbm": round(gbs / peak, 3),
+            "frac_spec": round(gbs / SPEC_HBM_GBS, 3), "peak_kind": kind, "reps": reps,
+            "launches_per_call": 1,
+            "note": "fq_osci_reset alone after an ordinary step; not part of the suite step"}
+
+
 def run_quant_dequant(reps=20, warmup=3):
     """The MXFP4 weight workload as two separate calls, fq_quantize (codes and
     E8M0 scales) then fq_dequantize (BF16), on the same [4096, 4096] BF16
@@ -1041,6 +1077,7 @@ def main():
             line["gemm_nvfp4"] = run_gemm(fmt_name="nvfp4")
             line["gemm_mxfp4"] = run_gemm(fmt_name="mxfp4")
             line["osci_window"] = run_osci_window(suite)
+            line["osci_reset"] = run_osci_reset(suite)
             line["mxfp4_quant_dequant"] = run_quant_dequant()
             line["quant_diagnostics"] = quant_diagnostics(suite)
         if not args.no_cpu_baseline and world == 1 and not reduced:

@@ -111,6 +111,22 @@ __global__ void __launch_bounds__(kOutThreads) channel_amax_kernel(const void *_
 constexpr int kSelThreads = 1024;
 constexpr int kMaxOutWords = 4096;  // channels up to 131072
 constexpr int64_t kFastKept = 8192;  // retained channels listed in shared memory (12 B each)
+constexpr int64_t kKeepImageCols = 16384;  // BF16 keep-mask image: 2 B per column (32 KB)
+
+__host__ __device__ constexpr size_t align16(size_t n) { return (n + 15) & ~(size_t)15; }
+
+// Dynamic shared memory of outlier_row_kernel: the prefix, the sorted list
+// (fast), the keep-mask image (fast == 2).
+static size_t outlier_smem(int64_t cols, int64_t k, int fast)
+{
+    const int64_t nwords = (cols + 31) / 32;
+    size_t n = align16((size_t)nwords * 4);
+    if (fast)
+        n += align16((size_t)k * 12);
+    if (fast == 2)
+        n += (size_t)nwords * 64;
+    return n;
+}
 
 __device__ __forceinline__ uint64_t channel_key(const float *amax, int c)
 {
@@ -269,16 +285,24 @@ __global__ void __launch_bounds__(kOutThreads) outlier_row_kernel(const __grid_c
 {
     constexpr int B = FmtInfo<FMT>::B;
     __shared__ NvTables tab;
-    __shared__ int pre[kMaxOutWords];
     __shared__ uint32_t mstage[kOutThreads];
-    // fast: the retained columns in ascending order, then 1 / s_j and s_j for each
-    extern __shared__ int kcols[];
     __shared__ float e4m3v[128];  // E4M3 magnitudes by code (0x7F unused)
     const int64_t cols = a.cols, rows = a.rows;
     const int nwords = (int)((cols + 31) / 32);
     const int kk = (int)a.k;
+    // Dynamic shared memory (sizes from outlier_smem): the bitmap's popcount
+    // prefix (one int per word); with fast, the retained columns in ascending
+    // order, then 1 / s_j and s_j for each; with fast == 2 (BF16), a keep-mask
+    // image of one row, one 16-bit half per column (0 for a retained column,
+    // 0xFFFF otherwise), with which a block's retained elements are zeroed by
+    // ANDing its raw words.  Each part starts on a 16-byte boundary.
+    extern __shared__ __align__(16) unsigned char osm[];
+    int *pre = reinterpret_cast<int *>(osm);
+    int *kcols = reinterpret_cast<int *>(osm + align16((size_t)nwords * 4));
     float *krcp = reinterpret_cast<float *>(kcols + kk);
     float *ksj = krcp + kk;
+    uint32_t *keep = reinterpret_cast<uint32_t *>(reinterpret_cast<char *>(kcols) +
+                                                  align16((size_t)kk * 12));
     wait_prior_grid();
     popc_prefix<kOutThreads>(a.bitmap, nwords, pre);
     if (fast) {
@@ -295,6 +319,16 @@ __global__ void __launch_bounds__(kOutThreads) outlier_row_kernel(const __grid_c
         }
         for (int c = threadIdx.x; c < 128; c += kOutThreads)
             e4m3v[c] = c < 0x7F ? e4m3_value((uint32_t)c) : 0.0f;
+        if (fast == 2) {
+            // one bitmap word (32 columns) per thread: 16 image words
+            for (int w = threadIdx.x; w < nwords; w += kOutThreads) {
+                const uint32_t wd = __ldg(a.bitmap + w);
+#pragma unroll
+                for (int j = 0; j < 16; ++j)
+                    keep[16 * w + j] = (((wd >> (2 * j)) & 1u) ? 0u : 0x0000FFFFu) |
+                                       (((wd >> (2 * j + 1)) & 1u) ? 0u : 0xFFFF0000u);
+            }
+        }
         __syncthreads();
     }
     float s_g = 0.0f, inv6 = 0.0f;
@@ -330,7 +364,28 @@ __global__ void __launch_bounds__(kOutThreads) outlier_row_kernel(const __grid_c
         }
         float v[B];
         uint32_t ret = 0u;
-        {
+        float am = 0.0f;
+        if (sizeof(T) == 2 && fast == 2) {
+            // BF16 with the keep-mask image: retained elements zeroed in the
+            // raw words, the amax from a tree over the packed pairs
+            constexpr int NV = B / 8;
+            uint4 raw[NV];
+            const char *src = (const char *)a.x + blk * B * (int64_t)sizeof(T);
+            const uint4 *km = reinterpret_cast<const uint4 *>(keep + c0 / 2);
+#pragma unroll
+            for (int k = 0; k < NV; ++k) {
+                raw[k] = valid ? ld16(src + 16 * k) : make_uint4(0, 0, 0, 0);
+                const uint4 m = km[k];
+                raw[k].x &= m.x;
+                raw[k].y &= m.y;
+                raw[k].z &= m.z;
+                raw[k].w &= m.w;
+            }
+            am = block_amax<T, B>(raw);
+#pragma unroll
+            for (int k = 0; k < NV; ++k)
+                unpack16<T>(raw[k], v + 8 * k);
+        } else {
             float x[B];
             if (valid)
                 load_block<T, B>((const char *)a.x + blk * B * (int64_t)sizeof(T), x);
@@ -343,11 +398,10 @@ __global__ void __launch_bounds__(kOutThreads) outlier_row_kernel(const __grid_c
 #pragma unroll
             for (int i = 0; i < B; ++i)
                 v[i] = ((ret >> i) & 1u) ? 0.0f : x[i];
-        }
-        float am = 0.0f;
 #pragma unroll
-        for (int i = 0; i < B; ++i)
-            am = fmaxf(am, fabsf(v[i]));
+            for (int i = 0; i < B; ++i)
+                am = fmaxf(am, fabsf(v[i]));
+        }
         float s_o = s_g, inv6b = inv6;
         if (FMT == NV2L) {
             s_o = outer_scale(group_max<8>(am));
@@ -605,9 +659,14 @@ static cudaError_t outlier_go(const OutlierArgs &a, cudaStream_t s)
         return cudaSuccess;
     // the sorted-list path: the list fits in shared memory and every row is a
     // whole number of 32-block warp spans
-    const int fast = a.k > 0 && a.k <= kFastKept && (a.cols / B) % 32 == 0;
-    const size_t smem = fast ? (size_t)a.k * (sizeof(int) + 2 * sizeof(float)) : 0;
-    if (smem) {
+    int fast = a.k > 0 && a.k <= kFastKept && (a.cols / B) % 32 == 0;
+    // BF16 rows of up to 16384 columns also get the keep-mask image: 16 words
+    // per bitmap word (cols is a multiple of 512 on this path, so the bitmap
+    // words are whole)
+    if (fast && sizeof(T) == 2 && a.cols <= kKeepImageCols)
+        fast = 2;
+    const size_t smem = outlier_smem(a.cols, a.k, fast);
+    if (smem > 48 * 1024) {
         const cudaError_t e = cudaFuncSetAttribute(outlier_row_kernel<T, FMT, RND>,
                                                    cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                    (int)smem);

@@ -160,6 +160,19 @@ def test_quantize_outliers_long_channel_lists(k):
     _outlier_parity(x, sel, fq.NVFP4)
 
 
+@pytest.mark.parametrize("cols", [16384, 16896])
+@pytest.mark.parametrize("fmt", [fq.NVFP4, fq.NVFP4_2LEVEL])
+def test_quantize_outliers_both_sides_of_the_keep_mask_image(cols, fmt):
+    """BF16 rows of up to 16384 columns zero their retained elements with a
+    keep-mask image of the row held in shared memory; longer rows test the
+    bitmap bit by bit.  One row length on each side, 10% of channels kept."""
+    rows = 8
+    x = W.channel_act((rows, cols), seed=22, channel_seed=23,
+                      n_outlier_cols=64).to(torch.bfloat16).to(DEV)
+    sel, _ = _select_parity(fq.fq_channel_amax(x), cols // 10)
+    _outlier_parity(x, sel, fmt)
+
+
 @pytest.mark.parametrize("fmt", [fq.NVFP4, fq.MXFP4, fq.NVFP4_2LEVEL])
 def test_quantize_outliers_k_zero_matches_plain_fakequant(fmt):
     rows, cols = 64, 256

@@ -653,6 +653,53 @@ def run_osci_reset(suite, reps=5):
             "note": "fq_osci_reset alone after an ordinary step; not part of the suite step"}
 
 
+def run_osci_mxfp4(suite, steps=10, warmup=2):
+    """The ordinary OsciReset step of the same 32-expert group with MXFP4 weight
+    quantization (the format the gpt-oss QAT page trains back to): block-local
+    E8M0 scales need no tensor amax, so the step is one pass over the weights.
+    31.1875 algorithmic bytes per weight: master, delta, dist_M and dist_Q read
+    (16), the previous codes and scales read (0.53125), master, dist_M and
+    dist_Q written (12), the new codes and scales, BF16 xhat and mask written
+    (2.65625).  Runs after the suite's own measurements, on its master weights
+    and accumulators.  Not part of the suite step."""
+    import torch
+    fq = suite.fq
+    cfg = fq.Config(fq.MXFP4)
+    dev = suite.master[0].device
+    prev = [fq.alloc_qtensor(*m.shape, fq.MXFP4, dev) for m in suite.master]
+    nxt = [fq.alloc_qtensor(*m.shape, fq.MXFP4, dev) for m in suite.master]
+    for m, q in zip(suite.master, prev):
+        fq.fq_quantize(m, cfg, row_out=q)
+
+    def step():
+        nonlocal prev, nxt
+        fq.fq_osci_update(cfg, suite.master, suite.delta_u, suite.dq, suite.dm, prev, nxt,
+                          xhat=suite.xh5, mask=suite.m5, ws=suite.ws5)
+        prev, nxt = nxt, prev
+
+    for _ in range(warmup):
+        step()
+    stream = torch.cuda.current_stream()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    t0.record(stream)
+    for _ in range(steps):
+        step()
+    t1.record(stream)
+    torch.cuda.synchronize()
+    ms = t0.elapsed_time(t1) / steps
+    nbytes = (16 + 0.5 + 1 / 32 + 12 + 0.5 + 1 / 32 + 2 + 1 / 8) * suite.elems["osci_update"]
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    peak, kind = measured_peaks()
+    return {"weights": suite.elems["osci_update"], "ms_per_step": round(ms, 4),
+            "gbs": round(gbs, 1), "frac_hbm": round(gbs / peak, 3),
+            "frac_spec": round(gbs / SPEC_HBM_GBS, 3), "peak_kind": kind, "steps": steps,
+            "launches_per_step": 1,
+            "note": "ordinary OsciReset step with MXFP4 weights, one pass; not part of the suite "
+                    "step"}
+
+
 def run_quant_dequant(reps=20, warmup=3):
     """The MXFP4 weight workload as two separate calls, fq_quantize (codes and
     E8M0 scales) then fq_dequantize (BF16), on the same [4096, 4096] BF16
@@ -1078,6 +1125,7 @@ def main():
             line["gemm_mxfp4"] = run_gemm(fmt_name="mxfp4")
             line["osci_window"] = run_osci_window(suite)
             line["osci_reset"] = run_osci_reset(suite)
+            line["osci_update_mxfp4"] = run_osci_mxfp4(suite)
             line["mxfp4_quant_dequant"] = run_quant_dequant()
             line["quant_diagnostics"] = quant_diagnostics(suite)
         if not args.no_cpu_baseline and world == 1 and not reduced:

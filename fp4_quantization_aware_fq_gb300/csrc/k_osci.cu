@@ -4,14 +4,16 @@
 // weights whose risk exceeds a threshold are moved to the quantized value of
 // their current bin.
 //
-// One optimizer step is two passes over a group of tensors (e.g. all expert
-// matrices of an MoE layer), each a persistent grid walking 16-byte chunks of
-// FP32 master weights tile by tile across the whole group:
+// An NVFP4 optimizer step is two passes over a group of tensors (e.g. all
+// expert matrices of an MoE layer), each a persistent grid walking 16-byte
+// chunks of FP32 master weights tile by tile across the whole group:
 //   A: w += delta, dist_M += |w_t - w_{t-1}|, per-tensor amax of w_t (atomic);
 //   B: fake-quantize w_t under the new tensor scale, decode w_{t-1}'s stored
 //      codes, dist_Q += |xhat_t - xhat_{t-1}|, write codes/scales/xhat/mask
 //      (one lane per 16-byte chunk; the lanes of a block share its scale).
 // The tensor amax is the only dependency between the passes, hence the split.
+// MXFP4 and the double block scale each block from its own values, so their
+// step is pass B alone with pass A's update done in its registers (FUSED).
 #include "fq_device.cuh"
 #include "fq_internal.h"
 
@@ -27,10 +29,10 @@ constexpr int kOsciAU = 8;
 // on the 32-expert step: 7.10 ms, against 7.22 with two chunks and 7.84 with
 // four.  The ordinary step's pass B (nine streams) holds two chunks per
 // thread: 5.61 ms against 5.88 with one.
-template <bool RESET>
+template <bool RESET, bool FUSED = false>
 __host__ __device__ constexpr int osci_bu()
 {
-    return RESET ? 1 : 2;
+    return (RESET || FUSED) ? 1 : 2;
 }
 constexpr int kOsciBMinCtas = 4;
 
@@ -173,7 +175,11 @@ __device__ __forceinline__ uint32_t lanes_or(uint32_t v)
 // dist_Q exceeds threshold * dist_M, the master weight becomes xhat_t, and
 // both accumulators are written back as zero (the same bits as the separate
 // reset pass after this update).
-template <int FMT, int RND, bool RESET>
+// FUSED (block-local scales: MXFP4 and the double block, which need no tensor
+// amax): pass A's update is done here too, in the same registers -- w_t =
+// w_{t-1} + delta and dist_M += |w_t - w_{t-1}| with the same FP32 operations
+// -- so the step is one pass that reads the master weights once.
+template <int FMT, int RND, bool RESET, bool FUSED>
 __global__ void __launch_bounds__(kOsciThreads, kOsciBMinCtas)
     osci_pass_b(const __grid_constant__ OsciArgs a)
 {
@@ -206,9 +212,9 @@ __global__ void __launch_bounds__(kOsciThreads, kOsciBMinCtas)
             if (cbeg == 0 && threadIdx.x == 0)
                 T.ntscale[0] = s_g;
         }
-        constexpr int BU = osci_bu<RESET>();
+        constexpr int BU = osci_bu<RESET, FUSED>();
         for (int k0 = 0; k0 < kOsciTileChunks; k0 += kOsciThreads * BU) {
-            float4 w[BU], dq[BU], dm[BU];
+            float4 w[BU], dq[BU], dm[BU], dl[BU];
             uint32_t qp[BU], scp[BU];
             float so_p[BU];
 #pragma unroll
@@ -216,14 +222,16 @@ __global__ void __launch_bounds__(kOsciThreads, kOsciBMinCtas)
                 const int64_t ch = cbeg + k0 + k * kOsciThreads + threadIdx.x;
                 if (ch < nch) {
                     w[k] = ldf4_rw(T.master + ch * 4);
+                    if (FUSED)
+                        dl[k] = ldf4(T.delta + ch * 4);
                     dq[k] = ldf4_rw(T.dist_q + ch * 4);
-                    if (RESET)
-                        dm[k] = ldf4_rw(T.dist_m + ch * 4);
+                    dm[k] = (RESET || FUSED) ? ldf4_rw(T.dist_m + ch * 4)
+                                             : make_float4(0.f, 0.f, 0.f, 0.f);
                     qp[k] = __ldg(reinterpret_cast<const uint16_t *>(T.pcodes) + ch);
                     scp[k] = __ldg(T.pscales + ch / L);
                     so_p[k] = (FMT == NV2L) ? __ldg(T.ptscale + ch / 32) : 0.0f;
                 } else {
-                    w[k] = dq[k] = dm[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+                    w[k] = dq[k] = dm[k] = dl[k] = make_float4(0.f, 0.f, 0.f, 0.f);
                     qp[k] = scp[k] = 0;
                     so_p[k] = 0.0f;
                 }
@@ -233,7 +241,18 @@ __global__ void __launch_bounds__(kOsciThreads, kOsciBMinCtas)
                 const int64_t ch = cbeg + k0 + k * kOsciThreads + threadIdx.x;
                 const bool valid = ch < nch;  // uniform over a block's lanes (nch % L == 0)
                 const int64_t blk = ch / L;
-                const float v[4] = {w[k].x, w[k].y, w[k].z, w[k].w};
+                float v[4] = {w[k].x, w[k].y, w[k].z, w[k].w};
+                float m4[4] = {dm[k].x, dm[k].y, dm[k].z, dm[k].w};
+                if (FUSED) {
+                    // pass A in registers: the same operations as osci_pass_a
+                    const float d4[4] = {dl[k].x, dl[k].y, dl[k].z, dl[k].w};
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const float wn = __fadd_rn(v[i], d4[i]);
+                        m4[i] = __fadd_rn(m4[i], fabsf(__fsub_rn(wn, v[i])));
+                        v[i] = wn;
+                    }
+                }
                 float am = fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3])));
                 am = lanes_max<L>(am);
                 float s_o = s_g, inv6b = inv6;
@@ -267,7 +286,6 @@ __global__ void __launch_bounds__(kOsciThreads, kOsciBMinCtas)
                 e2m1_decode4(q, xh);
                 e2m1_decode4(qp[k], xp);
                 const float q4[4] = {dq[k].x, dq[k].y, dq[k].z, dq[k].w};
-                const float m4[4] = {dm[k].x, dm[k].y, dm[k].z, dm[k].w};
                 float dn[4];
                 uint32_t hit = 0;
 #pragma unroll
@@ -276,10 +294,15 @@ __global__ void __launch_bounds__(kOsciThreads, kOsciBMinCtas)
                     xp[i] = __fmul_rn(xp[i], seff_p);
                     dn[i] = __fadd_rn(q4[i], fabsf(__fsub_rn(xh[i], xp[i])));
                     if (RESET && dn[i] > __fmul_rn(a.threshold, m4[i])) {
-                        T.master[ch * 4 + i] = xh[i];
+                        if (!FUSED)
+                            T.master[ch * 4 + i] = xh[i];
                         hit |= 1u << i;
                     }
                 }
+                if (FUSED)  // w_t, or xhat_t where the window-end reset moves it
+                    stf4(T.master + ch * 4,
+                         make_float4((hit & 1u) ? xh[0] : v[0], (hit & 2u) ? xh[1] : v[1],
+                                     (hit & 4u) ? xh[2] : v[2], (hit & 8u) ? xh[3] : v[3]));
                 if (T.xhat) {
                     if (a.xhat_bf16)
                         *reinterpret_cast<uint2 *>((char *)T.xhat + ch * 8) =
@@ -294,6 +317,8 @@ __global__ void __launch_bounds__(kOsciThreads, kOsciBMinCtas)
                     cnt += __popc(hit);
                 } else {
                     stf4(T.dist_q + ch * 4, make_float4(dn[0], dn[1], dn[2], dn[3]));
+                    if (FUSED)
+                        stf4(T.dist_m + ch * 4, make_float4(m4[0], m4[1], m4[2], m4[3]));
                 }
                 reinterpret_cast<uint16_t *>(T.ncodes)[ch] = (uint16_t)q;
                 if (sub == 0) {
@@ -391,30 +416,40 @@ static int osci_grid(int64_t ntiles)
     return (int)(ntiles < cap ? (ntiles > 0 ? ntiles : 1) : cap);
 }
 
+template <int FMT, int RND, bool RESET, bool FUSED>
+static void pass_b(const OsciArgs &a, int grid, cudaStream_t s)
+{
+    osci_pass_b<FMT, RND, RESET, FUSED><<<grid, kOsciThreads, 0, s>>>(a);
+}
+
+template <int FMT, bool FUSED>
+static void pass_b_fmt(const OsciArgs &a, int rnd, int grid, cudaStream_t s)
+{
+    if (rnd == RNE)
+        a.reset ? pass_b<FMT, RNE, true, FUSED>(a, grid, s) : pass_b<FMT, RNE, false, FUSED>(a, grid, s);
+    else
+        a.reset ? pass_b<FMT, SR, true, FUSED>(a, grid, s) : pass_b<FMT, SR, false, FUSED>(a, grid, s);
+}
+
 cudaError_t launch_osci_update(const OsciArgs &a, int fmt, int rnd, cudaStream_t s)
 {
     const int64_t ntiles = a.tile_start[a.ntensors];
-    cudaError_t e = cudaMemsetAsync(a.amax, 0, sizeof(float) * (size_t)a.ntensors, s);
-    if (e != cudaSuccess || ntiles == 0)
-        return e;
+    if (ntiles == 0)
+        return cudaSuccess;
     const int grid = osci_grid(ntiles);
-    osci_pass_a<<<grid, kOsciThreads, 0, s>>>(a);
-    if ((e = cudaGetLastError()) != cudaSuccess)
-        return e;
-    const int key = (fmt * 2 + rnd) * 2 + (a.reset ? 1 : 0);
-    switch (key) {
-    case (NVFP4 * 2 + RNE) * 2: osci_pass_b<NVFP4, RNE, false><<<grid, kOsciThreads, 0, s>>>(a); break;
-    case (NVFP4 * 2 + RNE) * 2 + 1: osci_pass_b<NVFP4, RNE, true><<<grid, kOsciThreads, 0, s>>>(a); break;
-    case (NVFP4 * 2 + SR) * 2: osci_pass_b<NVFP4, SR, false><<<grid, kOsciThreads, 0, s>>>(a); break;
-    case (NVFP4 * 2 + SR) * 2 + 1: osci_pass_b<NVFP4, SR, true><<<grid, kOsciThreads, 0, s>>>(a); break;
-    case (MXFP4 * 2 + RNE) * 2: osci_pass_b<MXFP4, RNE, false><<<grid, kOsciThreads, 0, s>>>(a); break;
-    case (MXFP4 * 2 + RNE) * 2 + 1: osci_pass_b<MXFP4, RNE, true><<<grid, kOsciThreads, 0, s>>>(a); break;
-    case (MXFP4 * 2 + SR) * 2: osci_pass_b<MXFP4, SR, false><<<grid, kOsciThreads, 0, s>>>(a); break;
-    case (MXFP4 * 2 + SR) * 2 + 1: osci_pass_b<MXFP4, SR, true><<<grid, kOsciThreads, 0, s>>>(a); break;
-    case (NV2L * 2 + RNE) * 2: osci_pass_b<NV2L, RNE, false><<<grid, kOsciThreads, 0, s>>>(a); break;
-    case (NV2L * 2 + RNE) * 2 + 1: osci_pass_b<NV2L, RNE, true><<<grid, kOsciThreads, 0, s>>>(a); break;
-    case (NV2L * 2 + SR) * 2: osci_pass_b<NV2L, SR, false><<<grid, kOsciThreads, 0, s>>>(a); break;
-    default: osci_pass_b<NV2L, SR, true><<<grid, kOsciThreads, 0, s>>>(a); break;
+    if (fmt == NVFP4) {
+        // the tensor scale of w_t needs all of w_t first: two passes
+        cudaError_t e = cudaMemsetAsync(a.amax, 0, sizeof(float) * (size_t)a.ntensors, s);
+        if (e != cudaSuccess)
+            return e;
+        osci_pass_a<<<grid, kOsciThreads, 0, s>>>(a);
+        if ((e = cudaGetLastError()) != cudaSuccess)
+            return e;
+        pass_b_fmt<NVFP4, false>(a, rnd, grid, s);
+    } else if (fmt == MXFP4) {
+        pass_b_fmt<MXFP4, true>(a, rnd, grid, s);  // block-local scales: one pass
+    } else {
+        pass_b_fmt<NV2L, true>(a, rnd, grid, s);
     }
     return cudaGetLastError();
 }

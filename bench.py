@@ -72,14 +72,14 @@ LAUNCHES_PER_STEP = {"nvfp4_small": 2, "mxfp4_weight": 1, "nvfp4_act": 2, "ste_b
 # DRAM traffic per call of the OsciReset steps from an ncu capture, valid only
 # for the kernel sources it was taken on (sha256 of the OsciReset sources).
 # Captured on the 2-expert case (66.4 M weights; pass A + pass B read + write:
-# 2227.2 MB for the ordinary step, 2824.4 MB for the window-end step) and
+# 2227.5 MB for the ordinary step, 2824.0 MB for the window-end step) and
 # scaled by the weights processed to the 32-expert call (traffic is linear in
 # the number of weights).
 _OSCI_SCALE = 1061683200 / 66355200
-NCU_TRAFFIC = {"osci_update": {"bytes": int((1270093824 + 957093888) * _OSCI_SCALE),
-                               "src_sha256": "6cb22632f8f08604d603377791a1b27f2dc5c97241e85ba33939fdb8a6b65569"},
-               "osci_update_reset": {"bytes": int((1267671296 + 1556755968) * _OSCI_SCALE),
-                                     "src_sha256": "6cb22632f8f08604d603377791a1b27f2dc5c97241e85ba33939fdb8a6b65569"}}
+NCU_TRAFFIC = {"osci_update": {"bytes": int((1270458368 + 957048576) * _OSCI_SCALE),
+                               "src_sha256": "c05d65f721f01046713f95db6ee83ed6f99794b57a90bc688d6f2dad1c5ac5d7"},
+               "osci_update_reset": {"bytes": int((1267530752 + 1556487168) * _OSCI_SCALE),
+                                     "src_sha256": "c05d65f721f01046713f95db6ee83ed6f99794b57a90bc688d6f2dad1c5ac5d7"}}
 
 
 def log(*a):

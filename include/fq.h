@@ -211,7 +211,9 @@ FQ_API fq_status fq_ste_backward(const void *dy, int32_t dtype, const uint8_t *m
  *   mask[i]     STE mask of w_t (NULL array or entry: skip)
  * Quantization follows cfg (NVFP4 takes s_g from amax(w_t)).  cols must be a
  * multiple of the block length.  The workspace holds one float per tensor
- * (fq_osci_workspace_size). */
+ * (fq_osci_workspace_size): the NVFP4 step keeps amax(w_t) there between its
+ * two passes over the weights; MXFP4 and the double block, whose scales are
+ * block-local, make one pass and leave it untouched. */
 FQ_API fq_status fq_osci_update(const fq_config *cfg, int32_t ntensors, const int64_t *rows,
                          const int64_t *cols, float *const *master, const float *const *delta,
                          float *const *dist_q, float *const *dist_m, const fq_qtensor *prev,

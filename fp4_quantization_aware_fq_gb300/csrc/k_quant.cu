@@ -665,13 +665,14 @@ static cudaError_t row_go(const RowArgs &a, cudaStream_t s)
     const int64_t nblk = a.n / B;
     if (nblk == 0)
         return cudaSuccess;
-    // Stochastic rounding is bound by its arithmetic: a grid of eight CTAs per
-    // SM walks the tensor (69.7 us for the double-block SR gradient, 71.7 us
-    // with one CTA per 256 x BPT blocks).  Nearest-even rounding is bound by
+    // Stochastic rounding is bound by its arithmetic: a grid of sixteen CTAs
+    // per SM walks the tensor, four of them resident at a time (68.4-68.5 us
+    // for the double-block SR gradient with 12 to 32 per SM, 69.3 us with 8,
+    // 72.7 us with 4, 71.7 us with one CTA per 256 x BPT blocks).  Nearest-even rounding is bound by
     // memory: one CTA per 256 x BPT blocks, handed out in address order, keeps
     // the reads sequential (MXFP4 weight [32768, 4096]: 98 us against 118 us
     // for the grid-stride walk).
-    const int grid = persistent_grid(nblk, kThreads * BPT, RND == SR ? 8 : 1 << 20);
+    const int grid = persistent_grid(nblk, kThreads * BPT, RND == SR ? 16 : 1 << 20);
     if (a.ld != a.cols)
         return launch_dependent(row_kernel<T, FMT, RND, true>, dim3(grid), dim3(kThreads), 0, s, a);
     return launch_dependent(row_kernel<T, FMT, RND, false>, dim3(grid), dim3(kThreads), 0, s, a);

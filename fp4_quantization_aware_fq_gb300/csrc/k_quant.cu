@@ -720,7 +720,13 @@ static cudaError_t tile_go(const TileArgs &a, cudaStream_t s)
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads,
                                                       smem) != cudaSuccess || per_sm < 1)
         per_sm = 1;
-    const int64_t cap = (int64_t)sm_count() * per_sm;
+    // Nearest-even tiles are bound by memory: one wave of resident CTAs walks
+    // them.  Stochastic rounding is bound by arithmetic: three CTAs for each
+    // resident slot, the later ones starting as the first finish, even out
+    // the walk's tail (Hadamard + SR both orientations on [16384, 4096]:
+    // 181.5 us against 190.3 with one wave, 183.4 with two, 183.0 with four;
+    // two waves took the NVFP4 row + column call from 98.9 to 100.5 us).
+    const int64_t cap = (int64_t)sm_count() * per_sm * (RND == SR ? 3 : 1);
     const unsigned grid = (unsigned)(ntiles < cap ? ntiles : cap);
     return launch_dependent(kern, dim3(grid), dim3(kThreads), smem, s, a);
 }

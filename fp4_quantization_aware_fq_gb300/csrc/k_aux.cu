@@ -142,7 +142,10 @@ cudaError_t launch_ste(const void *dy, int bf16, const uint8_t *mask, int64_t n,
     if (n == 0)
         return cudaSuccess;
     const int64_t nch = n / (bf16 ? 8 : 4);
-    const int grid = grid_for((nch + kSteU - 1) / kSteU, 4);
+    // a grid-stride walk by 32 CTAs per SM, the later ones starting as the
+    // first finish (BF16 [8192, 8192] in the step: 45.5 us against 47.2 with
+    // 4 per SM and 47.5 with 8; 16 to 64 measure the same)
+    const int grid = grid_for((nch + kSteU - 1) / kSteU, 32);
     if (bf16)
         ste_kernel<__nv_bfloat16><<<grid, kAuxThreads, 0, s>>>(dy, mask, nch, dx);
     else

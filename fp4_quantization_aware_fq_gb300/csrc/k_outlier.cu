@@ -666,7 +666,9 @@ static cudaError_t outlier_go(const OutlierArgs &a, cudaStream_t s)
     if (fast && sizeof(T) == 2 && a.cols <= kKeepImageCols)
         fast = 2;
     const size_t smem = outlier_smem(a.cols, a.k, fast);
-    if (smem > 48 * 1024) {
+    // the kernel's static shared memory counts against the default 48 KB too,
+    // so the dynamic size is declared for every launch
+    {
         const cudaError_t e = cudaFuncSetAttribute(outlier_row_kernel<T, FMT, RND>,
                                                    cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                    (int)smem);

@@ -160,16 +160,18 @@ def test_quantize_outliers_long_channel_lists(k):
     _outlier_parity(x, sel, fq.NVFP4)
 
 
-@pytest.mark.parametrize("cols", [16384, 16896])
+@pytest.mark.parametrize("cols,k", [(16384, 1638), (16896, 1689), (16384, 1100)])
 @pytest.mark.parametrize("fmt", [fq.NVFP4, fq.NVFP4_2LEVEL])
-def test_quantize_outliers_both_sides_of_the_keep_mask_image(cols, fmt):
+def test_quantize_outliers_both_sides_of_the_keep_mask_image(cols, k, fmt):
     """BF16 rows of up to 16384 columns zero their retained elements with a
     keep-mask image of the row held in shared memory; longer rows test the
-    bitmap bit by bit.  One row length on each side, 10% of channels kept."""
+    bitmap bit by bit.  One row length on each side with 10% of channels
+    kept, and 1100 kept channels on 16384 columns, whose list and image just
+    fit in 48 KB of dynamic shared memory beside the kernel's static part."""
     rows = 8
     x = W.channel_act((rows, cols), seed=22, channel_seed=23,
                       n_outlier_cols=64).to(torch.bfloat16).to(DEV)
-    sel, _ = _select_parity(fq.fq_channel_amax(x), cols // 10)
+    sel, _ = _select_parity(fq.fq_channel_amax(x), k)
     _outlier_parity(x, sel, fmt)
 
 
